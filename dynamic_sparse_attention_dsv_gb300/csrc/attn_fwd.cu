@@ -1,0 +1,339 @@
+// Query-grouped sparse attention, forward pass.
+//
+// "DSV: Exploiting Dynamic Sparsity to Accelerate Large-Scale Video DiT
+// Training" (gist.science technical summary): section 2.1 computes full
+// attention on the critical KV pairs only; section 2.2 groups adjacent
+// queries so a group shares one key index set. The dense case (FlashAttention
+// in stage 1, or a head the dispatcher keeps dense) is the same kernel over
+// all S keys.
+//
+// One CTA per (query group, problem). The group's G (64 or 128) queries form
+// the M = 128 rows of every MMA (G = 64 leaves rows 64..127 zero). Per
+// 128-key tile:
+//   TMA row gather of the selected K and V rows into swizzled shared memory
+//   S  = Q K^T        tcgen05.mma kind::f16 (smem x smem) -> TMEM
+//   P  = exp2(S*scale*log2e - m) in registers, written back to TMEM as bf16
+//   O += P V          tcgen05.mma with A = P in TMEM, B = V (MN-major) -> TMEM
+// The running max m is raised lazily (only when it grows by more than 8 in
+// log2 units, which bounds P by 2^8), so O is rescaled rarely.
+//
+// Warps 0-3: softmax and epilogue (thread = query row = TMEM lane).
+// Warp 4: TMA producer (all lanes issue row gathers). Warp 5: MMA issuer.
+#include "attn_common.cuh"
+
+namespace dsv {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kStages = D == 128 ? 2 : 3;
+  static constexpr int kTile = 128 * D * 2;            // bytes of one 128-row bf16 tile
+  static constexpr int kOffK = kTile;                  // Q first
+  static constexpr int kOffV = kOffK + kStages * kTile;
+  static constexpr int kOffBar = kOffV + kStages * kTile;
+  static constexpr int kSmemUsed = kOffBar + 256 + 1024;
+  // at least half the SM's shared memory, so one CTA owns the SM's TMEM
+  static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
+  static constexpr int kThreads = 192;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 256;               // S buffers at 0 and 128
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    k_attn_fwd(const __grid_constant__ AttnMaps maps, const AttnParams prm, const ProblemTable tab) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm;
+  uint8_t* sK = sm + C::kOffK;
+  uint8_t* sV = sm + C::kOffV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;                  // [kStages]
+  uint64_t* v_full = bars + 4;                  // [kStages]
+  uint64_t* kv_empty = bars + 7;                // [kStages]
+  uint64_t* s_full = bars + 10;                 // [2]
+  uint64_t* p_full = bars + 12;                 // [2]
+  uint64_t* o_ready = bars + 14;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.x, lp = blockIdx.y;
+  const int p = tab.p[lp];
+  const Geometry& geo = prm.geo;
+  const bool dense = (prm.idx == nullptr) || (tab.off[lp] < 0);
+  const int k = dense ? geo.S : tab.k[lp];
+  const int nt = (k + 127) / 128;
+  const int32_t* idx_row = dense ? nullptr : prm.idx + tab.off[lp] + (int64_t)g * k;
+  const int G = geo.G;
+
+  // rows G..127 of Q stay zero (G = 64)
+  if (G < 128) {
+    for (int i = tid; i < (128 - G) * (D / 64) * 8; i += blockDim.x) {
+      const int a = i / ((128 - G) * 8), rem = i % ((128 - G) * 8);
+      reinterpret_cast<uint4*>(sQ + a * 16384 + G * 128)[rem] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == 5) {
+    tmem_alloc(tslot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(k_full + i, 1);
+      mbar_init(v_full + i, 1);
+      mbar_init(kv_empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(p_full + i, 4);
+    }
+    mbar_init(o_ready, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA
+    const int ct = g / (geo.ncy * geo.ncx), cy = (g / geo.ncx) % geo.ncy, cx = g % geo.ncx;
+    if (lane == 0) {
+      prefetch_tmap(&maps.q_cube);
+      mbar_arrive_expect_tx(q_full, G * D * 2);
+      for (int a = 0; a < D / 64; ++a)
+        tma_load_4d(sQ + a * 16384, &maps.q_cube, q_full, a * 64, cx * geo.gx, cy * geo.gy, p * geo.T + ct * geo.gt);
+    }
+    const int prow0 = p * geo.S;
+    for (int t = 0; t < nt; ++t) {
+      const int s = t % C::kStages;
+      if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, kWaitLimitNs)) {
+        if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(k_full + s, C::kTile);
+      __syncwarp();
+      load_kv_tile<D>(sK + s * C::kTile, &maps.k_rows, &maps.k_tile, k_full + s, idx_row, k, t, prow0, lane);
+      if (lane == 0) mbar_arrive_expect_tx(v_full + s, C::kTile);
+      __syncwarp();
+      load_kv_tile<D>(sV + s * C::kTile, &maps.v_rows, &maps.v_tile, v_full + s, idx_row, k, t, prow0, lane);
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = instr_desc(128, 128, 1, 0, 0);
+      constexpr uint32_t idesc_pv = instr_desc(128, D, 1, 0, 1);
+      const uint32_t q_addr = smem_u32(sQ);
+      bool ok = mbar_wait(q_full, 0, kWaitLimitNs);
+      auto issue_pv = [&](int t) -> bool {
+        const int s = t % C::kStages, b = t & 1;
+        if (!mbar_wait(p_full + b, (t >> 1) & 1, kWaitLimitNs)) return false;
+        if (!mbar_wait(v_full + s, (t / C::kStages) & 1, kWaitLimitNs)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sV + s * C::kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd = smem_desc(v_addr + kk * 2048, 16384, 1024);
+          mma_f16_ts(tbase + C::kColO, tbase + b * 128 + kk * 8, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(kv_empty + s);
+        mma_commit(o_ready);
+        return true;
+      };
+      for (int t = 0; ok && t < nt; ++t) {
+        const int s = t % C::kStages, b = t & 1;
+        if (!mbar_wait(k_full + s, (t / C::kStages) & 1, kWaitLimitNs)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sK + s * C::kTile);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_f16_ss(tbase + b * 128, smem_desc(q_addr + off, 16, 1024), smem_desc(k_addr + off, 16, 1024),
+                     idesc_qk, kk > 0);
+        }
+        mma_commit(s_full + b);
+        if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
+      }
+      if (ok && nt > 0) ok = issue_pv(nt - 1);
+      if (!ok) raise_status(prm.status, DSV_ERR_TIMEOUT);
+    }
+  } else {
+    // ----------------------------------------------------- softmax (warps 0-3)
+    const int row = warp * 32 + lane;
+    const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+    const float sc = prm.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < nt; ++t) {
+      const int b = t & 1;
+      if (!mbar_wait_warp(s_full + b, (t >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + b * 128 + c * 32, r[c]);
+      tmem_ld_wait(r[0]);
+      reg_fence(r[1]);
+      reg_fence(r[2]);
+      reg_fence(r[3]);
+      const int nvalid = min(128, k - t * 128);
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (c * 32 + e < nvalid) mt = fmaxf(mt, __uint_as_float(r[c][e]) * sc);
+      bool waited = false;
+      const bool want = t > 0 && mt > m + 8.f;
+      if (t == 0) {
+        m = mt;
+      } else if (__any_sync(0xffffffffu, want)) {
+        // O must be quiescent: wait for PV(t-1), then rescale the rows whose
+        // max grew (warp-collective TMEM access; other rows use factor 1)
+        if (!mbar_wait_warp(o_ready, (t - 1) & 1, kWaitLimitNs)) { ok = false; break; }
+        waited = true;
+        tc_fence_after();
+        const float f = want ? ex2_fast(m - mt) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + C::kColO + c * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+          tmem_st32(lane_addr + C::kColO + c * 32, o);
+        }
+        tmem_st_wait();
+        l *= f;
+        if (want) m = mt;
+      }
+      uint32_t pk[64];
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int j = c * 32 + e;
+          const float p0 = j < nvalid ? ex2_fast(__uint_as_float(r[c][e]) * sc - m) : 0.f;
+          const float p1 = j + 1 < nvalid ? ex2_fast(__uint_as_float(r[c][e + 1]) * sc - m) : 0.f;
+          lsum += p0 + p1;
+          pk[j >> 1] = pack_bf16x2(p0, p1);
+        }
+      l += lsum;
+      tmem_st32(lane_addr + b * 128, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(lane_addr + b * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st_wait();
+      if (t >= 1 && !waited) {
+        if (!mbar_wait_warp(o_ready, (t - 1) & 1, kWaitLimitNs)) { ok = false; break; }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full + b);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok && nt > 0 && !mbar_wait_warp(o_ready, (nt - 1) & 1, kWaitLimitNs)) ok = false;
+    if (!ok) {
+      if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
+    } else if (row < G) {
+      tc_fence_after();
+      const int tok = token_of(geo, g, row);
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = prm.out + ((int64_t)p * geo.S + tok) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(lane_addr + C::kColO + c * 32, o);
+        tmem_ld_wait(o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+      }
+      prm.lse_out[(int64_t)p * geo.S + tok] = (m + __log2f(l)) * 0.69314718055994531f;
+    } else {
+      // padded rows still take part in the TMEM loads (warp-collective)
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(lane_addr + C::kColO + c * 32, o);
+        tmem_ld_wait(o);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) tmem_dealloc(tbase, C::kTmemCols);
+}
+
+template <int D>
+static cudaError_t launch_fwd(const AttnMaps& maps, const AttnParams& prm, const ProblemTable& tab, int n_groups,
+                              cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(k_attn_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  k_attn_fwd<D><<<dim3(n_groups, tab.n), FwdCfg<D>::kThreads, FwdCfg<D>::kSmem, st>>>(maps, prm, tab);
+  return cudaGetLastError();
+}
+
+}  // namespace dsv
+
+using namespace dsv;
+
+extern "C" size_t dsv_sparse_attn_fwd_workspace_size(dsv_shape shape, dsv_group group) {
+  (void)shape;
+  (void)group;
+  return 0;
+}
+
+extern "C" dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx,
+                                          const int32_t* k_per_head, const int64_t* idx_offset, dsv_shape shape,
+                                          dsv_group group, float scale, void* O, float* LSE, void* workspace,
+                                          size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  dsv_status v = validate_common(shape, group, true);
+  if (v != DSV_OK) return v;
+  if (!Q || !K || !V || !O || !LSE || !(scale > 0.f)) return DSV_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(LSE, 4))
+    return DSV_ERR_INVALID_ARG;
+  if (idx && (!k_per_head || !idx_offset || !aligned(idx, 4))) return DSV_ERR_INVALID_ARG;
+  const Geometry geo = make_geometry(shape, group);
+  const int P = (int)(shape.B * shape.H);
+  const int d = (int)shape.d;
+  ProblemTable tab;
+  memset(&tab, 0, sizeof(tab));
+  tab.n = P;
+  for (int i = 0; i < P; ++i) {
+    tab.p[i] = i;
+    const bool dense = !idx || idx_offset[i] < 0;
+    tab.k[i] = dense ? geo.S : k_per_head[i];
+    tab.off[i] = dense ? -1 : idx_offset[i];
+    if (!dense && (tab.k[i] < 1 || tab.k[i] > geo.S)) return DSV_ERR_INVALID_ARG;
+  }
+  AttnMaps maps;
+  if (!make_attn_maps(&maps, Q, K, V, geo, d, P)) return DSV_ERR_CUDA;
+  AttnParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.geo = geo;
+  prm.d = d;
+  prm.scale = scale;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.idx = idx;
+  prm.out = static_cast<__nv_bfloat16*>(O);
+  prm.lse_out = LSE;
+  prm.status = dev_status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = d == 128 ? launch_fwd<128>(maps, prm, tab, geo.n_groups, st)
+                                 : launch_fwd<64>(maps, prm, tab, geo.n_groups, st);
+  return e == cudaSuccess ? DSV_OK : DSV_ERR_CUDA;
+}

@@ -1,0 +1,936 @@
+// Fused low-rank score + per-group top-k selection and predicted-mass coverage.
+//
+// Follows "DSV: Exploiting Dynamic Sparsity to Accelerate Large-Scale Video
+// DiT Training" (gist.science technical summary): section 2.1 (per-head
+// low-rank predictors W_lr^Q, W_lr^K approximating QK^T; critical KV = the
+// keys holding 90% of the attention mass) and section 2.2 (fused low-rank
+// MatMul + Top-K that never stores the S x S scores; adjacent queries grouped
+// to share one key set).
+//
+// Score of key j for group g: s_gj = qbar_g . k_lr,j with qbar_g the group
+// mean of q_lr (equal to the mean of q_lr,i . k_lr,j by linearity). Scores are
+// formed tile by tile on the tensor cores (tcgen05, kind::tf32, three products
+// hi*hi + hi*lo + lo*hi of a tf32 hi/lo split: about 2^-21 relative error) into
+// TMEM and consumed in registers; they are never written to memory.
+//
+// Exact top-k per group row, ties to the lower key, in four streaming passes
+// over the same score tiles plus two small kernels:
+//   MINMAX  per-row score range
+//   HIST    256 (128 for r=64) linear bins over the range; bracket kernel
+//           finds the bin b* holding the k-th largest score
+//   COLLECT scores in bin b* -> candidate list; per key-chunk counts
+//   resolve sorts the candidates (score desc, key asc): exact threshold tau,
+//           tie budget and output offset of every key chunk
+//   EMIT    writes every key with s > tau (and the budgeted s == tau keys)
+//           in ascending key order.
+// Coverage reuses MINMAX and a COV pass that bins exp(scale*(s - max)) by
+// log-probability (count and mass per bin); a reduce kernel searches k.
+#include <algorithm>
+#include <cmath>
+#include <vector>
+
+#include "common.cuh"
+
+namespace dsv {
+
+constexpr int kSelThreads = 320;   // warps 0-7 consume scores, 8 loads tiles, 9 issues MMAs
+constexpr int kCandCap = 4096;     // candidates kept per group row
+constexpr int kMaxChunks = 64;     // key chunks per row
+constexpr int kTargetCtas = 304;   // 2 x 152 SMs
+constexpr size_t kL2Budget = 48ull << 20;
+
+enum SelMode { kMinMax = 0, kHist = 1, kCollect = 2, kEmit = 3, kCov = 4 };
+
+template <int RP>
+struct SelCfg {
+  static constexpr int kAtoms = RP / 32;               // 128-byte atoms per fp32 row
+  static constexpr int kTileBytes = 128 * RP * 4;      // one [128][RP] fp32 tile
+  static constexpr int kStages = (RP == 32) ? 2 : 1;
+  static constexpr int kHistBins = (RP == 32) ? 256 : 128;
+  static constexpr int kCovBins = (RP == 32) ? 128 : 64;
+  static constexpr int kHistBytes = 128 * 1024 / (RP / 32);
+  static constexpr int kOffAlo = kTileBytes;
+  static constexpr int kOffB = 2 * kTileBytes;
+  static constexpr int kOffHist = kOffB + kStages * 2 * kTileBytes;
+  static constexpr int kOffMisc = kOffHist + kHistBytes;
+  static constexpr int kSmem = kOffMisc + 256 + 1024;  // + barriers, + alignment slack
+};
+
+struct SelParams {
+  Geometry geo;
+  int32_t g_pad, n_chunks, chunk_tiles, n_tiles;
+  float scale;
+  uint32_t* mmax;        // [n][g_pad] orderable max
+  uint32_t* mmin;        // [n][g_pad] orderable min
+  uint32_t* hist;        // HIST: [n][bins][g_pad]; COV: counts [n][chunks][bins][g_pad]
+  float* mass;           // COV: [n][chunks][bins][g_pad]
+  const int32_t* bstar;  // [n][g_pad]
+  uint32_t* cand_cnt;    // [n][g_pad]
+  uint64_t* cand;        // [n][g_pad][kCandCap]
+  int32_t* above;        // [n][chunks][g_pad]
+  int32_t* inbin;        // [n][chunks][g_pad]
+  const float* tau;      // [n][g_pad]
+  const int32_t* out_off;    // [n][chunks][g_pad]
+  const int32_t* eq_budget;  // [n][chunks][g_pad]
+  int32_t* idx;
+  int32_t* status;
+};
+
+__device__ __forceinline__ float tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+__device__ __forceinline__ void red_smem_u32(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_smem_f32(uint32_t addr, float v) {
+  asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Linear bin of score s over [lo, lo + nb/inv_w); identical arithmetic in every
+// pass that uses it (no contraction), so HIST and COLLECT agree bit for bit.
+__device__ __forceinline__ int lin_bin(float s, float lo, float inv_w, int nb) {
+  const float x = __fmul_rn(__fsub_rn(s, lo), inv_w);
+  return min(nb - 1, (int)x);
+}
+
+// ---------------------------------------------------------------------------
+// Score-tile pipeline with a per-mode consumer.
+// grid = (group tiles, key chunks, problems); block = 320 threads.
+template <int RP, int MODE>
+__global__ void __launch_bounds__(kSelThreads, 1)
+    k_select(const __grid_constant__ CUtensorMap map_qhi, const __grid_constant__ CUtensorMap map_qlo,
+             const __grid_constant__ CUtensorMap map_khi, const __grid_constant__ CUtensorMap map_klo,
+             const SelParams prm, const ProblemTable tab) {
+  using C = SelCfg<RP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sAhi = sm;
+  uint8_t* sAlo = sm + C::kOffAlo;
+  uint8_t* sB = sm + C::kOffB;
+  uint8_t* sHist = sm + C::kOffHist;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffMisc);
+  uint64_t* a_full = bars;
+  uint64_t* b_full = bars + 1;            // [kStages]
+  uint64_t* b_empty = bars + 3;           // [kStages]
+  uint64_t* s_full = bars + 5;            // [2]
+  uint64_t* s_empty = bars + 7;           // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 10);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gtile = blockIdx.x, chunk = blockIdx.y, lp = blockIdx.z;
+  const int t0 = chunk * prm.chunk_tiles;
+  const int nt = min(prm.chunk_tiles, prm.n_tiles - t0);
+  const int S = prm.geo.S;
+
+  if (warp == 9) {
+    tmem_alloc(tslot, 256);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(a_full, 1);
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(b_full + i, 1);
+      mbar_init(b_empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(s_empty + i, 8);
+    }
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && nt > 0) {
+      prefetch_tmap(&map_khi);
+      prefetch_tmap(&map_klo);
+      const int ya = lp * prm.g_pad + gtile * 128;
+      mbar_arrive_expect_tx(a_full, 2 * C::kTileBytes);
+      for (int a = 0; a < C::kAtoms; ++a) {
+        tma_load_2d(sAhi + a * 16384, &map_qhi, a_full, a * 32, ya);
+        tma_load_2d(sAlo + a * 16384, &map_qlo, a_full, a * 32, ya);
+      }
+      for (int i = 0; i < nt; ++i) {
+        const int s = i % C::kStages;
+        if (i >= C::kStages && !mbar_wait(b_empty + s, ((i / C::kStages) - 1) & 1, kWaitLimitNs)) {
+          raise_status(prm.status, DSV_ERR_TIMEOUT);
+          break;
+        }
+        uint8_t* bh = sB + s * 2 * C::kTileBytes;
+        uint8_t* bl = bh + C::kTileBytes;
+        const int yb = lp * S + (t0 + i) * 128;
+        mbar_arrive_expect_tx(b_full + s, 2 * C::kTileBytes);
+        for (int a = 0; a < C::kAtoms; ++a) {
+          tma_load_2d(bh + a * 16384, &map_khi, b_full + s, a * 32, yb);
+          tma_load_2d(bl + a * 16384, &map_klo, b_full + s, a * 32, yb);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t idesc = instr_desc(128, 128, 2, 0, 0);
+      bool ok = mbar_wait(a_full, 0, kWaitLimitNs);
+      for (int i = 0; ok && i < nt; ++i) {
+        const int s = i % C::kStages, b = i & 1;
+        if (!mbar_wait(b_full + s, (i / C::kStages) & 1, kWaitLimitNs)) { ok = false; break; }
+        if (i >= 2 && !mbar_wait(s_empty + b, ((i >> 1) - 1) & 1, kWaitLimitNs)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tbase + b * 128;
+        const uint32_t ah = smem_u32(sAhi), al = smem_u32(sAlo);
+        const uint32_t bh = smem_u32(sB + s * 2 * C::kTileBytes), bl = bh + C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < RP / 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint64_t dah = smem_desc(ah + off, 16, 1024), dal = smem_desc(al + off, 16, 1024);
+          const uint64_t dbh = smem_desc(bh + off, 16, 1024), dbl = smem_desc(bl + off, 16, 1024);
+          mma_tf32_ss(d, dah, dbh, idesc, kk > 0);
+          mma_tf32_ss(d, dah, dbl, idesc, 1);
+          mma_tf32_ss(d, dal, dbh, idesc, 1);
+        }
+        mma_commit(b_empty + s);
+        mma_commit(s_full + b);
+      }
+      if (!ok) raise_status(prm.status, DSV_ERR_TIMEOUT);
+    }
+  } else {
+    // ------------------------------------------------------- score consumers
+    const int q = warp & 3, half = warp >> 2;
+    const int row = q * 32 + lane;
+    const int g = gtile * 128 + row;
+    const bool valid = g < prm.geo.n_groups;
+    const int rid = lp * prm.g_pad + g;
+    const uint32_t taddr_lane = tbase + ((uint32_t)(q * 32) << 16);
+
+    float lo = 0.f, inv_w = 0.f, cmax = 0.f;
+    int bstar = 0;
+    float mx = -INFINITY, mn = INFINITY;
+    int n_above = 0, n_in = 0;
+    float tau = INFINITY;
+    int pos = 0, eq_left = 0, krow = 0;
+    int32_t* out_row = nullptr;
+    constexpr int NB = (MODE == kCov) ? C::kCovBins : C::kHistBins;
+    const uint32_t hist_base = smem_u32(sHist);
+
+    if constexpr (MODE == kHist || MODE == kCollect) {
+      lo = ord2f(prm.mmin[rid]);
+      const float hi = ord2f(prm.mmax[rid]);
+      inv_w = hi > lo ? (float)NB / (hi - lo) : 0.f;
+      if (MODE == kCollect) bstar = prm.bstar[rid];
+    }
+    if constexpr (MODE == kCov) {
+      cmax = ord2f(prm.mmax[rid]);
+      const float range = prm.scale * (cmax - ord2f(prm.mmin[rid]));
+      inv_w = range > 0.f ? (float)NB / range : 0.f;
+    }
+    if constexpr (MODE == kEmit) {
+      const int ci = (lp * prm.n_chunks + chunk) * prm.g_pad + g;
+      if (valid) {
+        tau = prm.tau[rid];
+        pos = prm.out_off[ci];
+        eq_left = prm.eq_budget[ci];
+        krow = tab.k[lp];
+        out_row = prm.idx + tab.off[lp] + (int64_t)g * krow;
+      }
+    }
+    if constexpr (MODE == kHist || MODE == kCov) {
+      // zero this CTA's private histograms ([bin][row] counts, then masses)
+      uint32_t* h = reinterpret_cast<uint32_t*>(sHist);
+      for (int i = tid; i < C::kHistBytes / 4; i += 256) h[i] = 0;
+      epi_barrier();
+    }
+
+    for (int i = 0; i < nt; ++i) {
+      const int b = i & 1;
+      if (!mbar_wait_warp(s_full + b, (i >> 1) & 1, kWaitLimitNs)) {
+        if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const int key0 = (t0 + i) * 128;
+      if constexpr (MODE == kEmit) {
+        if (half == 0) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld32(taddr_lane + b * 128 + c * 32, r);
+            tmem_ld_wait(r);
+            if (valid) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const float s = __uint_as_float(r[e]) + 0.0f;
+                const bool eq = (s == tau);
+                if (s > tau || (eq && eq_left > 0)) {
+                  eq_left -= eq;
+                  if (pos < krow) out_row[pos] = key0 + c * 32 + e;
+                  ++pos;
+                }
+              }
+            }
+          }
+        }
+      } else {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(taddr_lane + b * 128 + half * 64, r0);
+        tmem_ld32(taddr_lane + b * 128 + half * 64 + 32, r1);
+        tmem_ld_wait(r0);
+        reg_fence(r1);
+        const int kb = key0 + half * 64;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const float s = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]) + 0.0f;
+          if constexpr (MODE == kMinMax) {
+            mx = fmaxf(mx, s);
+            mn = fminf(mn, s);
+          } else if constexpr (MODE == kHist) {
+            const int bin = lin_bin(s, lo, inv_w, NB);
+            red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
+          } else if constexpr (MODE == kCollect) {
+            const int bin = lin_bin(s, lo, inv_w, NB);
+            if (bin > bstar) {
+              ++n_above;
+            } else if (bin == bstar && valid) {
+              ++n_in;
+              const uint32_t slot = atomicAdd(prm.cand_cnt + rid, 1u);
+              if (slot < (uint32_t)kCandCap)
+                prm.cand[(size_t)rid * kCandCap + slot] =
+                    ((uint64_t)(~f2ord(s)) << 32) | (uint32_t)(kb + e);
+            }
+          } else if constexpr (MODE == kCov) {
+            const float u = __fmul_rn(prm.scale, __fsub_rn(cmax, s));
+            const int bin = min(NB - 1, (int)__fmul_rn(u, inv_w));
+            const float p = ex2_fast(-u * 1.4426950408889634f);
+            red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
+            red_smem_f32(hist_base + (uint32_t)(NB * 128 + bin * 128 + row) * 4u, p);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty + b);
+    }
+
+    // ----------------------------------------------------- per-row results
+    if constexpr (MODE == kMinMax || MODE == kCollect) {
+      float* ex = reinterpret_cast<float*>(sHist);   // [2][2][128], the histogram area is unused here
+      if (MODE == kMinMax) {
+        ex[(half * 2 + 0) * 128 + row] = mx;
+        ex[(half * 2 + 1) * 128 + row] = mn;
+      } else {
+        reinterpret_cast<int*>(ex)[(half * 2 + 0) * 128 + row] = n_above;
+        reinterpret_cast<int*>(ex)[(half * 2 + 1) * 128 + row] = n_in;
+      }
+      epi_barrier();
+      if (half == 0 && valid) {
+        if (MODE == kMinMax) {
+          const float m2 = fmaxf(mx, ex[(2 + 0) * 128 + row]);
+          const float n2 = fminf(mn, ex[(2 + 1) * 128 + row]);
+          if (nt > 0) {
+            atomicMax(prm.mmax + rid, f2ord(m2));
+            atomicMin(prm.mmin + rid, f2ord(n2));
+          }
+        } else {
+          const int* exi = reinterpret_cast<int*>(ex);
+          const int ci = (lp * prm.n_chunks + chunk) * prm.g_pad + g;
+          prm.above[ci] = n_above + exi[(2 + 0) * 128 + row];
+          prm.inbin[ci] = n_in + exi[(2 + 1) * 128 + row];
+        }
+      }
+    } else if constexpr (MODE == kHist) {
+      epi_barrier();
+      const uint32_t* h = reinterpret_cast<const uint32_t*>(sHist);
+      for (int bin = half * (NB / 2); bin < (half + 1) * (NB / 2); ++bin) {
+        const uint32_t v = h[bin * 128 + row];
+        if (v) atomicAdd(prm.hist + ((size_t)lp * NB + bin) * prm.g_pad + g, v);
+      }
+    } else if constexpr (MODE == kCov) {
+      epi_barrier();
+      const uint32_t* h = reinterpret_cast<const uint32_t*>(sHist);
+      const float* m = reinterpret_cast<const float*>(sHist) + NB * 128;
+      for (int bin = half * (NB / 2); bin < (half + 1) * (NB / 2); ++bin) {
+        const size_t o = (((size_t)lp * prm.n_chunks + chunk) * NB + bin) * prm.g_pad + g;
+        prm.hist[o] = h[bin * 128 + row];
+        prm.mass[o] = m[bin * 128 + row];
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) tmem_dealloc(tbase, 256);
+}
+
+// ---------------------------------------------------------------------------
+// Low-rank projections.
+// k_lr of every key, split into tf32 hi and lo parts; rows padded to RP.
+template <int R>
+__global__ void __launch_bounds__(128) k_key_proj(const __nv_bfloat16* __restrict__ K,
+                                                  const __nv_bfloat16* __restrict__ Wk, int64_t H, int d, int S,
+                                                  float* __restrict__ khi, float* __restrict__ klo,
+                                                  const ProblemTable tab) {
+  constexpr int RP = R < 32 ? 32 : R;
+  __shared__ float Ws[128 * R];
+  const int lp = blockIdx.y, p = tab.p[lp], h = p % H;
+  const __nv_bfloat16* W = Wk + (size_t)h * d * R;
+  for (int i = threadIdx.x; i < d * R; i += 128) Ws[i] = __bfloat162float(W[i]);
+  __syncthreads();
+  const int j = blockIdx.x * 128 + threadIdx.x;
+  const uint4* row = reinterpret_cast<const uint4*>(K + ((size_t)p * S + j) * d);
+  float acc[R];
+#pragma unroll
+  for (int c = 0; c < R; ++c) acc[c] = 0.f;
+  for (int c8 = 0; c8 < d / 8; ++c8) {
+    const uint4 v = row[c8];
+    const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float xv = __bfloat162float(x[e]);
+      const float* w = Ws + (c8 * 8 + e) * R;
+#pragma unroll
+      for (int c = 0; c < R; ++c) acc[c] = fmaf(xv, w[c], acc[c]);
+    }
+  }
+  float* oh = khi + ((size_t)lp * S + j) * RP;
+  float* ol = klo + ((size_t)lp * S + j) * RP;
+#pragma unroll
+  for (int c = 0; c < RP; ++c) {
+    const float v = c < R ? acc[c < R ? c : 0] : 0.f;
+    const float hi = tf32_rna(v);
+    oh[c] = hi;
+    ol[c] = tf32_rna(v - hi);
+  }
+}
+
+// qbar_g = (mean over the group's queries of Q_i) . W_lr^Q, split into tf32
+// hi and lo parts. One block per (group, problem).
+template <int R>
+__global__ void __launch_bounds__(128) k_group_mean_proj(const __nv_bfloat16* __restrict__ Q,
+                                                         const __nv_bfloat16* __restrict__ Wq, int64_t H, int d,
+                                                         Geometry geo, int g_pad, float* __restrict__ qhi,
+                                                         float* __restrict__ qlo, const ProblemTable tab) {
+  constexpr int RP = R < 32 ? 32 : R;
+  __shared__ float part[128 * 8];
+  __shared__ float mean[128];
+  const int g = blockIdx.x, lp = blockIdx.y, p = tab.p[lp], h = p % H;
+  const int tid = threadIdx.x;
+  const int lanes_per_row = d / 8, rows_per_pass = 128 / lanes_per_row;
+  const int col8 = tid % lanes_per_row, rsub = tid / lanes_per_row;
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  const __nv_bfloat16* Qp = Q + (size_t)p * geo.S * d;
+  for (int i = rsub; i < geo.G; i += rows_per_pass) {
+    const int tok = token_of(geo, g, i);
+    const uint4 v = *reinterpret_cast<const uint4*>(Qp + (size_t)tok * d + col8 * 8);
+    const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += __bfloat162float(x[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) part[tid * 8 + e] = acc[e];
+  __syncthreads();
+  if (tid < d) {
+    const int c8 = tid / 8, e = tid % 8;
+    float s = 0.f;
+    for (int rs = 0; rs < rows_per_pass; ++rs) s += part[(rs * lanes_per_row + c8) * 8 + e];
+    mean[tid] = s / (float)geo.G;
+  }
+  __syncthreads();
+  if (tid < RP) {
+    float v = 0.f;
+    if (tid < R) {
+      const __nv_bfloat16* W = Wq + (size_t)h * d * R;
+      for (int c = 0; c < d; ++c) v = fmaf(mean[c], __bfloat162float(W[c * R + tid]), v);
+    }
+    const float hi = tf32_rna(v);
+    qhi[((size_t)lp * g_pad + g) * RP + tid] = hi;
+    qlo[((size_t)lp * g_pad + g) * RP + tid] = tf32_rna(v - hi);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Bracket: per row, the bin b* holding the k-th largest score.
+__global__ void k_bracket(const uint32_t* __restrict__ hist, int nb, int g_pad, int n_groups, int32_t* bstar,
+                          int32_t* n_above_out, const ProblemTable tab) {
+  const int lp = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n_groups) return;
+  const int k = tab.k[lp];
+  int above = 0, b = 0;
+  for (b = nb - 1; b >= 0; --b) {
+    const int c = (int)hist[((size_t)lp * nb + b) * g_pad + g];
+    if (above + c >= k) break;
+    above += c;
+  }
+  if (b < 0) b = 0;
+  bstar[lp * g_pad + g] = b;
+  n_above_out[lp * g_pad + g] = above;
+}
+
+// Resolve: exact threshold, per-chunk output offsets and tie budgets.
+__global__ void __launch_bounds__(256) k_resolve(const uint64_t* __restrict__ cand, const uint32_t* cand_cnt,
+                                                 const uint32_t* mmax, const uint32_t* mmin,
+                                                 const int32_t* n_above_all, const int32_t* above,
+                                                 const int32_t* inbin, int g_pad, int n_chunks, int chunk_keys,
+                                                 float* tau_out, int32_t* out_off, int32_t* eq_budget,
+                                                 int32_t* status, const ProblemTable tab) {
+  __shared__ uint64_t keys[kCandCap];
+  __shared__ int sel_cnt[kMaxChunks], eq_cnt[kMaxChunks];
+  __shared__ float s_tau;
+  const int g = blockIdx.x, lp = blockIdx.y, tid = threadIdx.x;
+  const int rid = lp * g_pad + g;
+  const int k = tab.k[lp];
+  const int need = k - n_above_all[rid];
+  const uint32_t ncand = cand_cnt[rid];
+  const bool all_equal = mmax[rid] == mmin[rid];
+  for (int c = tid; c < kMaxChunks; c += blockDim.x) sel_cnt[c] = eq_cnt[c] = 0;
+  if (tid == 0) s_tau = INFINITY;
+  __syncthreads();
+  if (all_equal) {
+    if (tid == 0) {
+      int rem = need;
+      for (int c = 0; c < n_chunks; ++c) {
+        const int e = min(rem, inbin[(lp * n_chunks + c) * g_pad + g]);
+        sel_cnt[c] = e;
+        eq_cnt[c] = e;
+        rem -= e;
+      }
+      s_tau = ord2f(mmax[rid]);
+    }
+  } else if (ncand > (uint32_t)kCandCap || need < 1 || (uint32_t)need > ncand) {
+    if (tid == 0) raise_status(status, DSV_ERR_CANDIDATES);
+  } else {
+    int n2 = 1;
+    while (n2 < (int)ncand) n2 <<= 1;
+    for (int i = tid; i < n2; i += blockDim.x) keys[i] = i < (int)ncand ? cand[(size_t)rid * kCandCap + i] : ~0ull;
+    __syncthreads();
+    for (int size = 2; size <= n2; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < n2 / 2; i += blockDim.x) {
+          const int a = 2 * i - (i & (stride - 1));
+          const int b = a + stride;
+          const bool asc = (a & size) == 0;
+          const uint64_t x = keys[a], y = keys[b];
+          if ((x > y) == asc) {
+            keys[a] = y;
+            keys[b] = x;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    const uint32_t tkey = (uint32_t)(keys[need - 1] >> 32);
+    const float tau = ord2f(~tkey);
+    for (int i = tid; i < need; i += blockDim.x) {
+      const uint32_t j = (uint32_t)keys[i];
+      const int c = (int)(j / (uint32_t)chunk_keys);
+      atomicAdd(&sel_cnt[c], 1);
+      if ((uint32_t)(keys[i] >> 32) == tkey) atomicAdd(&eq_cnt[c], 1);
+    }
+    if (tid == 0) s_tau = tau;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int off = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int ci = (lp * n_chunks + c) * g_pad + g;
+      out_off[ci] = off;
+      eq_budget[ci] = eq_cnt[c];
+      off += above[ci] + sel_cnt[c];
+    }
+    tau_out[rid] = s_tau;
+  }
+}
+
+// Rows with k == S select every key.
+__global__ void k_fill_all(int32_t* idx, int64_t off, int S, int64_t total) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
+    idx[off + i] = (int32_t)(i % S);
+}
+
+// ---------------------------------------------------------------------------
+// Coverage reduce: per problem, merge chunk partials, then binary search k.
+__global__ void __launch_bounds__(1024) k_cov_reduce(const uint32_t* __restrict__ cnt, const float* __restrict__ mass,
+                                                     const uint32_t* mmax, const uint32_t* mmin, int nb, int n_chunks,
+                                                     int g_pad, int n_groups, int S, float scale, float target,
+                                                     int32_t* cum_cnt, double* cum_mass, float* width,
+                                                     int32_t* k_cov, float* curve, int n_curve,
+                                                     const ProblemTable tab) {
+  const int lp = blockIdx.x, tid = threadIdx.x;
+  __shared__ double red[32];
+  // stage 1: per group cumulative counts and normalised masses, top bin first
+  for (int g = tid; g < n_groups; g += blockDim.x) {
+    const int rid = lp * g_pad + g;
+    int c_acc = 0;
+    double m_acc = 0.0;
+    for (int b = 0; b < nb; ++b) {
+      int c = 0;
+      double m = 0.0;
+      for (int ch = 0; ch < n_chunks; ++ch) {
+        const size_t o = (((size_t)lp * n_chunks + ch) * nb + b) * g_pad + g;
+        c += (int)cnt[o];
+        m += (double)mass[o];
+      }
+      c_acc += c;
+      m_acc += m;
+      cum_cnt[(size_t)rid * nb + b] = c_acc;
+      cum_mass[(size_t)rid * nb + b] = m_acc;
+    }
+    for (int b = 0; b < nb; ++b) cum_mass[(size_t)rid * nb + b] /= m_acc;
+    width[rid] = scale * (ord2f(mmax[rid]) - ord2f(mmin[rid])) / (float)nb;
+  }
+  __syncthreads();
+  auto C_of = [&](int k) -> double {
+    double acc = 0.0;
+    for (int g = tid; g < n_groups; g += blockDim.x) {
+      const int rid = lp * g_pad + g;
+      const int32_t* cc = cum_cnt + (size_t)rid * nb;
+      const double* cm = cum_mass + (size_t)rid * nb;
+      int lo = 0, hi = nb - 1;  // first bin with cumulative count >= k
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (cc[mid] >= k) hi = mid; else lo = mid + 1;
+      }
+      const int pc = lo > 0 ? cc[lo - 1] : 0;
+      const double pm = lo > 0 ? cm[lo - 1] : 0.0;
+      const int n = cc[lo] - pc;
+      const double mb = cm[lo] - pm;
+      const double f = n > 0 ? (double)(k - pc) / (double)n : 1.0;
+      const double dw = (double)width[rid];
+      const double part = dw > 1e-12 ? mb * (1.0 - exp(-f * dw)) / (1.0 - exp(-dw)) : mb * f;
+      acc += pm + part;
+    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    __syncthreads();
+    if ((tid & 31) == 0) red[tid >> 5] = acc;
+    __syncthreads();
+    double tot = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
+    return tot / (double)n_groups;
+  };
+  int lo = 1, hi = S;
+  while (lo < hi) {
+    const int mid = lo + (hi - lo) / 2;
+    if (C_of(mid) >= (double)target) hi = mid; else lo = mid + 1;
+  }
+  if (tid == 0) k_cov[tab.p[lp]] = lo;
+  if (curve) {
+    for (int i = 0; i < n_curve; ++i) {
+      const int k = (int)(((int64_t)(i + 1) * S + n_curve - 1) / n_curve);
+      const double c = C_of(k);
+      if (tid == 0) curve[(size_t)tab.p[lp] * n_curve + i] = (float)c;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host orchestration.
+struct TopkPlan {
+  Geometry geo;
+  int RP, n_gt, g_pad, n_tiles, pc;
+  int hist_bins, cov_bins;
+};
+
+static TopkPlan make_plan(const dsv_shape& s, int32_t r, const dsv_group& g) {
+  TopkPlan p;
+  p.geo = make_geometry(s, g);
+  p.RP = (r == 64) ? 64 : 32;
+  p.n_gt = (p.geo.n_groups + 127) / 128;
+  p.g_pad = p.n_gt * 128;
+  p.n_tiles = p.geo.S / 128;
+  const size_t per = (size_t)p.geo.S * p.RP * 8;
+  const int P = (int)(s.B * s.H);
+  p.pc = (int)std::max<size_t>(1, std::min<size_t>((size_t)P, kL2Budget / per));
+  p.hist_bins = p.RP == 32 ? SelCfg<32>::kHistBins : SelCfg<64>::kHistBins;
+  p.cov_bins = p.RP == 32 ? SelCfg<32>::kCovBins : SelCfg<64>::kCovBins;
+  return p;
+}
+
+static void chunking(const TopkPlan& pl, int n_local, int* n_chunks, int* chunk_tiles) {
+  int nc = (kTargetCtas + pl.n_gt * n_local - 1) / (pl.n_gt * n_local);
+  nc = std::max(1, std::min(nc, std::min(kMaxChunks, pl.n_tiles)));
+  const int ct = (pl.n_tiles + nc - 1) / nc;
+  *chunk_tiles = ct;
+  *n_chunks = (pl.n_tiles + ct - 1) / ct;
+}
+
+struct TopkWs {
+  float *khi, *klo, *qhi, *qlo;
+  uint32_t *mmax, *mmin, *hist, *cand_cnt;
+  float* mass;
+  int32_t *bstar, *nabove, *above, *inbin, *out_off, *eqb;
+  uint64_t* cand;
+  float* tau;
+  int32_t* cum_cnt;
+  double* cum_mass;
+  float* width;
+};
+
+// Carves the workspace (base == nullptr: sizing only). `cov` selects the
+// coverage buffers instead of the top-k ones.
+static size_t carve(void* base, const TopkPlan& pl, bool cov, TopkWs* w) {
+  Carver c(base);
+  const size_t pc = pl.pc, S = pl.geo.S, gp = pl.g_pad, RP = pl.RP;
+  w->khi = c.take<float>(pc * S * RP);
+  w->klo = c.take<float>(pc * S * RP);
+  w->qhi = c.take<float>(pc * gp * RP);
+  w->qlo = c.take<float>(pc * gp * RP);
+  w->mmax = c.take<uint32_t>(pc * gp);
+  w->mmin = c.take<uint32_t>(pc * gp);
+  if (!cov) {
+    w->hist = c.take<uint32_t>(pc * pl.hist_bins * gp);
+    w->bstar = c.take<int32_t>(pc * gp);
+    w->nabove = c.take<int32_t>(pc * gp);
+    w->cand_cnt = c.take<uint32_t>(pc * gp);
+    w->cand = c.take<uint64_t>(pc * gp * kCandCap);
+    w->above = c.take<int32_t>(pc * kMaxChunks * gp);
+    w->inbin = c.take<int32_t>(pc * kMaxChunks * gp);
+    w->out_off = c.take<int32_t>(pc * kMaxChunks * gp);
+    w->eqb = c.take<int32_t>(pc * kMaxChunks * gp);
+    w->tau = c.take<float>(pc * gp);
+  } else {
+    w->hist = c.take<uint32_t>(pc * kMaxChunks * pl.cov_bins * gp);
+    w->mass = c.take<float>(pc * kMaxChunks * pl.cov_bins * gp);
+    w->cum_cnt = c.take<int32_t>(pc * gp * pl.cov_bins);
+    w->cum_mass = c.take<double>(pc * gp * pl.cov_bins);
+    w->width = c.take<float>(pc * gp);
+  }
+  return c.used + 256;
+}
+
+template <int RP, int MODE>
+static cudaError_t launch_select(dim3 grid, cudaStream_t st, const CUtensorMap* maps, const SelParams& prm,
+                                 const ProblemTable& tab) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_select<RP, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SelCfg<RP>::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  k_select<RP, MODE><<<grid, kSelThreads, SelCfg<RP>::kSmem, st>>>(maps[0], maps[1], maps[2], maps[3], prm, tab);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+static cudaError_t select_pass(int RP, dim3 grid, cudaStream_t st, const CUtensorMap* maps, const SelParams& prm,
+                               const ProblemTable& tab) {
+  return RP == 32 ? launch_select<32, MODE>(grid, st, maps, prm, tab)
+                  : launch_select<64, MODE>(grid, st, maps, prm, tab);
+}
+
+static cudaError_t launch_proj(int r, const void* Q, const void* K, const void* Wq, const void* Wk,
+                               const dsv_shape& s, const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab,
+                               cudaStream_t st) {
+  const int n = tab.n, d = (int)s.d;
+  const size_t qbytes = (size_t)n * pl.g_pad * pl.RP * sizeof(float);
+  cudaError_t e = cudaMemsetAsync(w.qhi, 0, qbytes, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w.qlo, 0, qbytes, st);
+  if (e != cudaSuccess) return e;
+  dim3 gk(pl.geo.S / 128, n), gq(pl.geo.n_groups, n);
+  auto Kp = static_cast<const __nv_bfloat16*>(K);
+  auto Qp = static_cast<const __nv_bfloat16*>(Q);
+  auto Wkp = static_cast<const __nv_bfloat16*>(Wk);
+  auto Wqp = static_cast<const __nv_bfloat16*>(Wq);
+  switch (r) {
+    case 16:
+      k_key_proj<16><<<gk, 128, 0, st>>>(Kp, Wkp, s.H, d, pl.geo.S, w.khi, w.klo, tab);
+      k_group_mean_proj<16><<<gq, 128, 0, st>>>(Qp, Wqp, s.H, d, pl.geo, pl.g_pad, w.qhi, w.qlo, tab);
+      break;
+    case 32:
+      k_key_proj<32><<<gk, 128, 0, st>>>(Kp, Wkp, s.H, d, pl.geo.S, w.khi, w.klo, tab);
+      k_group_mean_proj<32><<<gq, 128, 0, st>>>(Qp, Wqp, s.H, d, pl.geo, pl.g_pad, w.qhi, w.qlo, tab);
+      break;
+    default:
+      k_key_proj<64><<<gk, 128, 0, st>>>(Kp, Wkp, s.H, d, pl.geo.S, w.khi, w.klo, tab);
+      k_group_mean_proj<64><<<gq, 128, 0, st>>>(Qp, Wqp, s.H, d, pl.geo, pl.g_pad, w.qhi, w.qlo, tab);
+      break;
+  }
+  return cudaGetLastError();
+}
+
+static bool make_score_maps(CUtensorMap* maps, const TopkPlan& pl, const TopkWs& w, int n) {
+  const uint64_t RP = pl.RP;
+  return make_map_2d(&maps[0], w.qhi, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, RP, (uint64_t)n * pl.g_pad, 32, 128) &&
+         make_map_2d(&maps[1], w.qlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, RP, (uint64_t)n * pl.g_pad, 32, 128) &&
+         make_map_2d(&maps[2], w.khi, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, RP, (uint64_t)n * pl.geo.S, 32, 128) &&
+         make_map_2d(&maps[3], w.klo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, RP, (uint64_t)n * pl.geo.S, 32, 128);
+}
+
+static dsv_status validate_lowrank(const void* Q, const void* K, const void* Wq, const void* Wk, const dsv_shape& s,
+                                   int32_t r, const dsv_group& g) {
+  dsv_status v = validate_common(s, g, true);
+  if (v != DSV_OK) return v;
+  if (!Q || !K || !Wq || !Wk) return DSV_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(Wq, 2) || !aligned(Wk, 2)) return DSV_ERR_INVALID_ARG;
+  if (r != 16 && r != 32 && r != 64) return DSV_ERR_UNSUPPORTED;
+  return DSV_OK;
+}
+
+}  // namespace dsv
+
+using namespace dsv;
+
+extern "C" size_t dsv_lowrank_topk_workspace_size(dsv_shape shape, int32_t r, dsv_group group) {
+  if (validate_common(shape, group, true) != DSV_OK || (r != 16 && r != 32 && r != 64)) return 0;
+  TopkPlan pl = make_plan(shape, r, group);
+  TopkWs w;
+  return carve(nullptr, pl, false, &w);
+}
+
+extern "C" size_t dsv_coverage_workspace_size(dsv_shape shape, int32_t r, dsv_group group) {
+  if (validate_common(shape, group, true) != DSV_OK || (r != 16 && r != 32 && r != 64)) return 0;
+  TopkPlan pl = make_plan(shape, r, group);
+  TopkWs w;
+  return carve(nullptr, pl, true, &w);
+}
+
+extern "C" dsv_status dsv_lowrank_topk(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr,
+                                       dsv_shape shape, int32_t r, dsv_group group, const int32_t* k_per_head,
+                                       const int64_t* idx_offset, int32_t* idx, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  dsv_status v = validate_lowrank(Q, K, Wq_lr, Wk_lr, shape, r, group);
+  if (v != DSV_OK) return v;
+  if (!k_per_head || !idx_offset || !idx || !aligned(idx, 4)) return DSV_ERR_INVALID_ARG;
+  const TopkPlan pl = make_plan(shape, r, group);
+  const int P = (int)(shape.B * shape.H);
+  const int S = pl.geo.S;
+  for (int p = 0; p < P; ++p)
+    if (idx_offset[p] >= 0 && (k_per_head[p] < 1 || k_per_head[p] > S)) return DSV_ERR_INVALID_ARG;
+  TopkWs w;
+  const size_t need = carve(nullptr, pl, false, &w);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DSV_ERR_WORKSPACE;
+  carve(workspace, pl, false, &w);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  std::vector<int> active;
+  for (int p = 0; p < P; ++p) {
+    if (idx_offset[p] < 0) continue;
+    if (k_per_head[p] == S) {
+      const int64_t total = (int64_t)pl.geo.n_groups * S;
+      k_fill_all<<<1216, 256, 0, st>>>(idx, idx_offset[p], S, total);
+      if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
+      continue;
+    }
+    active.push_back(p);
+  }
+  for (size_t c0 = 0; c0 < active.size(); c0 += pl.pc) {
+    ProblemTable tab;
+    memset(&tab, 0, sizeof(tab));
+    tab.n = (int)std::min<size_t>(pl.pc, active.size() - c0);
+    for (int i = 0; i < tab.n; ++i) {
+      const int p = active[c0 + i];
+      tab.p[i] = p;
+      tab.k[i] = k_per_head[p];
+      tab.off[i] = idx_offset[p];
+    }
+    const int n = tab.n;
+    if (launch_proj(r, Q, K, Wq_lr, Wk_lr, shape, pl, w, tab, st) != cudaSuccess) return DSV_ERR_CUDA;
+    CUtensorMap maps[4];
+    if (!make_score_maps(maps, pl, w, n)) return DSV_ERR_CUDA;
+    int n_chunks, chunk_tiles;
+    chunking(pl, n, &n_chunks, &chunk_tiles);
+    SelParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.geo = pl.geo;
+    prm.g_pad = pl.g_pad;
+    prm.n_chunks = n_chunks;
+    prm.chunk_tiles = chunk_tiles;
+    prm.n_tiles = pl.n_tiles;
+    prm.mmax = w.mmax;
+    prm.mmin = w.mmin;
+    prm.hist = w.hist;
+    prm.bstar = w.bstar;
+    prm.cand_cnt = w.cand_cnt;
+    prm.cand = w.cand;
+    prm.above = w.above;
+    prm.inbin = w.inbin;
+    prm.tau = w.tau;
+    prm.out_off = w.out_off;
+    prm.eq_budget = w.eqb;
+    prm.idx = idx;
+    prm.status = dev_status;
+    const dim3 grid(pl.n_gt, n_chunks, n);
+    const size_t rows = (size_t)n * pl.g_pad;
+    if (cudaMemsetAsync(w.mmax, 0, rows * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
+    if (cudaMemsetAsync(w.mmin, 0xFF, rows * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
+    if (select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
+    if (cudaMemsetAsync(w.hist, 0, rows * pl.hist_bins * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
+    if (select_pass<kHist>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
+    k_bracket<<<dim3(pl.n_gt, n), 128, 0, st>>>(w.hist, pl.hist_bins, pl.g_pad, pl.geo.n_groups, w.bstar,
+                                                 w.nabove, tab);
+    if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
+    if (cudaMemsetAsync(w.cand_cnt, 0, rows * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
+    if (select_pass<kCollect>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
+    k_resolve<<<dim3(pl.geo.n_groups, n), 256, 0, st>>>(w.cand, w.cand_cnt, w.mmax, w.mmin, w.nabove, w.above,
+                                                          w.inbin, pl.g_pad, n_chunks, chunk_tiles * 128, w.tau,
+                                                          w.out_off, w.eqb, dev_status, tab);
+    if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
+    if (select_pass<kEmit>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
+  }
+  return DSV_OK;
+}
+
+extern "C" dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr,
+                                   dsv_shape shape, int32_t r, dsv_group group, float scale, float mass,
+                                   int32_t* k_cov, float* curve, int32_t n_curve, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  dsv_status v = validate_lowrank(Q, K, Wq_lr, Wk_lr, shape, r, group);
+  if (v != DSV_OK) return v;
+  if (!k_cov || !(scale > 0.f) || !(mass > 0.f && mass <= 1.f)) return DSV_ERR_INVALID_ARG;
+  if (curve && n_curve < 1) return DSV_ERR_INVALID_ARG;
+  const TopkPlan pl = make_plan(shape, r, group);
+  TopkWs w;
+  const size_t need = carve(nullptr, pl, true, &w);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DSV_ERR_WORKSPACE;
+  carve(workspace, pl, true, &w);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int P = (int)(shape.B * shape.H);
+  for (int c0 = 0; c0 < P; c0 += pl.pc) {
+    ProblemTable tab;
+    memset(&tab, 0, sizeof(tab));
+    tab.n = std::min(pl.pc, P - c0);
+    for (int i = 0; i < tab.n; ++i) {
+      tab.p[i] = c0 + i;
+      tab.k[i] = 1;
+      tab.off[i] = 0;
+    }
+    const int n = tab.n;
+    if (launch_proj(r, Q, K, Wq_lr, Wk_lr, shape, pl, w, tab, st) != cudaSuccess) return DSV_ERR_CUDA;
+    CUtensorMap maps[4];
+    if (!make_score_maps(maps, pl, w, n)) return DSV_ERR_CUDA;
+    int n_chunks, chunk_tiles;
+    chunking(pl, n, &n_chunks, &chunk_tiles);
+    SelParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.geo = pl.geo;
+    prm.g_pad = pl.g_pad;
+    prm.n_chunks = n_chunks;
+    prm.chunk_tiles = chunk_tiles;
+    prm.n_tiles = pl.n_tiles;
+    prm.scale = scale;
+    prm.mmax = w.mmax;
+    prm.mmin = w.mmin;
+    prm.hist = w.hist;
+    prm.mass = w.mass;
+    prm.status = dev_status;
+    const dim3 grid(pl.n_gt, n_chunks, n);
+    const size_t rows = (size_t)n * pl.g_pad;
+    if (cudaMemsetAsync(w.mmax, 0, rows * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
+    if (cudaMemsetAsync(w.mmin, 0xFF, rows * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
+    if (select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
+    if (select_pass<kCov>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
+    k_cov_reduce<<<n, 1024, 0, st>>>(w.hist, w.mass, w.mmax, w.mmin, pl.cov_bins, n_chunks, pl.g_pad,
+                                     pl.geo.n_groups, pl.geo.S, scale, mass, w.cum_cnt, w.cum_mass, w.width, k_cov,
+                                     curve, n_curve, tab);
+    if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
+  }
+  return DSV_OK;
+}

@@ -1,0 +1,182 @@
+/*
+ * libdsv -- C ABI of the DSV hot path on one GB300 (sm_103a).
+ *
+ * DSV ("DSV: Exploiting Dynamic Sparsity to Accelerate Large-Scale Video DiT
+ * Training", summarised on gist.science, arXiv 2502.07590) trains video DiTs
+ * with per-head, per-step sparse attention: a rank-r predictor (W_lr^Q,
+ * W_lr^K) approximates QK^T, a fused low-rank MatMul + Top-K picks each query
+ * group's critical keys without ever storing the S x S scores, and attention
+ * (forward and backward) runs on the selected keys only.
+ *
+ * Conventions shared by every call:
+ *  - Tensors Q, K, V, O, dO, dQ, dK, dV are bf16, layout [B][H][S][d],
+ *    contiguous, device memory, 16-byte aligned. S = T*Y*X tokens of a
+ *    T x Y x X latent grid, token s = (t*Y + y)*X + x.
+ *  - W_lr^Q, W_lr^K are bf16 [H][d][r] (row-major d x r per head), device.
+ *  - A query group is one gt x gy x gx cube of the grid; groups are numbered
+ *    row-major over the (T/gt, Y/gy, X/gx) grid of cubes. n_groups = S/G.
+ *  - "Problem" p = b*H + h indexes the B*H independent (batch, head) pairs.
+ *  - Index sets: row (p, g) holds k_p ascending int32 key positions at
+ *    idx + idx_offset[p] + g*k_p (device memory).
+ *  - Every buffer is owned by the caller; libdsv allocates nothing and keeps
+ *    no state between calls. Scratch space is the caller's `workspace`
+ *    (device, 256-byte aligned) of at least the size the matching
+ *    dsv_*_workspace_size() call reports.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*).
+ *    Argument errors are returned synchronously before anything is launched.
+ *    Launch failures return DSV_ERR_CUDA. Conditions found on the device
+ *    (a wait that ran out, a fixed-point overflow, a candidate buffer
+ *    overflow) are written to the caller's device word `dev_status`
+ *    (int32, zero it before the call; libdsv only ever raises it), which the
+ *    caller reads after synchronising (dsv_read_status does both).
+ *  - Supported sizes: d in {64, 128}; r in {16, 32, 64}; G = gt*gy*gx in
+ *    {64, 128}; S a multiple of 128 and < 2^31; 1 <= k <= S; B*H <= 256.
+ */
+#ifndef LIBDSV_H
+#define LIBDSV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSV_OK = 0,
+  DSV_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or shape */
+  DSV_ERR_UNSUPPORTED = 2,   /* valid request outside the supported sizes */
+  DSV_ERR_WORKSPACE = 3,     /* workspace missing or too small */
+  DSV_ERR_CUDA = 4,          /* a CUDA launch or API call failed */
+  DSV_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out */
+  DSV_ERR_OVERFLOW = 6,      /* device: dK/dV fixed-point accumulator range exceeded */
+  DSV_ERR_CANDIDATES = 7     /* device: a top-k boundary bin exceeded its candidate buffer */
+} dsv_status;
+
+/* Problem shape: B batches x H heads, latent grid T x Y x X, head dim d. */
+typedef struct {
+  int64_t B, H, T, Y, X, d;
+} dsv_shape;
+
+/* Query-group cube gt x gy x gx; it must divide the grid. */
+typedef struct {
+  int32_t gt, gy, gx;
+} dsv_group;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* dsv_status_string(dsv_status s);
+
+/* Synchronises `stream`, then copies the device status word to *host_out.
+ * Returns DSV_ERR_CUDA if either step fails. */
+dsv_status dsv_read_status(const int32_t* dev_status, int32_t* host_out, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsv_lowrank_topk -- fused low-rank MatMul + per-group Top-K.
+ * Passage: technical summary section 2.2 ("efficient kernels": the low-rank
+ * MatMul and the Top-K selection are fused so the O(S^2) score matrix is
+ * never stored) with section 2.1 (per-head low-rank predictors W_lr^Q,
+ * W_lr^K approximating QK^T; critical KV estimation) and the query grouping
+ * of section 2.2.
+ *
+ * For every problem p with idx_offset[p] >= 0 and every group g:
+ *   q_lr = Q W_lr^Q, k_lr = K W_lr^K (fp32 accumulate of exact bf16 products)
+ *   s_gj = mean over the group's queries i of q_lr,i . k_lr,j
+ *   idx row (p, g) = the k_p keys j with the largest s_gj, ties to the lower
+ *   j, written in ascending order.
+ * Problems with idx_offset[p] < 0 are skipped (dense heads).
+ * k_per_head, idx_offset: HOST arrays of B*H entries (read during the call).
+ * Device errors: DSV_ERR_CANDIDATES if a row's boundary bin held more
+ * candidates than the workspace provides for (the row is then left
+ * incomplete); DSV_ERR_TIMEOUT on a stalled pipeline.
+ * ---------------------------------------------------------------------- */
+size_t dsv_lowrank_topk_workspace_size(dsv_shape shape, int32_t r, dsv_group group);
+dsv_status dsv_lowrank_topk(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr, dsv_shape shape,
+                            int32_t r, dsv_group group, const int32_t* k_per_head, const int64_t* idx_offset,
+                            int32_t* idx, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsv_coverage -- smallest k per problem covering `mass` of the predicted
+ * softmax mass.
+ * Passage: technical summary section 2.1 (critical KV are the pairs that
+ * carry over 90% of the attention score; the OP dispatcher decides per block
+ * from the current sparsity level).
+ *
+ * With the group scores s_gj of dsv_lowrank_topk and logits scale*s_gj, let
+ * m_g(k) be the total softmax probability of group g's k most probable keys
+ * and C(k) the mean of m_g(k) over all groups. k_cov[p] = min{k : C(k) >=
+ * mass}. Per group the probabilities are binned (128 bins of width
+ * range/128 over the group's logit range, 64 bins when r = 64) and m_g is
+ * interpolated inside a bin assuming log-probabilities spread evenly across
+ * it.
+ * k_cov: DEVICE int32 [B*H]. curve (optional, may be NULL): DEVICE float
+ * [B*H][n_curve], C(k) sampled at k = ceil((i+1)*S/n_curve), i < n_curve.
+ * ---------------------------------------------------------------------- */
+size_t dsv_coverage_workspace_size(dsv_shape shape, int32_t r, dsv_group group);
+dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr, dsv_shape shape,
+                        int32_t r, dsv_group group, float scale, float mass, int32_t* k_cov, float* curve,
+                        int32_t n_curve, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsv_plan_heads -- the OP dispatcher, per head (host only, no GPU).
+ * Passage: technical summary section 2.1 (the OP dispatcher activates sparse
+ * attention per block according to the current sparsity level).
+ *
+ * For each of n entries: dense[p] = k_cov[p] > dense_frac*S (then k_h[p] = S
+ * and idx_offset[p] = -1); otherwise k_h[p] = clamp(k_cov[p], lo, hi) with
+ * lo = round-half-up(lo_frac*S), hi = round-half-up(hi_frac*S), and the
+ * sparse rows are packed back to back: idx_offset[p] = sum over earlier
+ * sparse p' of n_groups*k_h[p']. *idx_total = total int32 entries needed.
+ * All pointers are HOST memory.
+ * ---------------------------------------------------------------------- */
+dsv_status dsv_plan_heads(const int32_t* k_cov, int32_t n, int64_t S, int64_t n_groups, double lo_frac,
+                          double hi_frac, double dense_frac, int32_t* k_h, uint8_t* dense, int64_t* idx_offset,
+                          int64_t* idx_total);
+
+/* ------------------------------------------------------------------------
+ * dsv_sparse_attn_fwd -- query-grouped sparse attention, forward.
+ * Passage: technical summary section 2.1 (full attention computed on the
+ * critical KV pairs only) and section 2.2 (query grouping: a group of
+ * adjacent queries shares one key index set).
+ *
+ * For query i of group g of problem p, with I = idx row (p, g) (or all S keys
+ * when idx == NULL or idx_offset[p] < 0, the dense case):
+ *   O_i = sum_{j in I} softmax_j(scale q_i.k_j) v_j      (bf16 out)
+ *   LSE_i = ln sum_{j in I} exp(scale q_i.k_j)           (fp32 [B][H][S])
+ * k_per_head, idx_offset: HOST arrays of B*H entries, or NULL with idx NULL.
+ * ---------------------------------------------------------------------- */
+size_t dsv_sparse_attn_fwd_workspace_size(dsv_shape shape, dsv_group group);
+dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx,
+                               const int32_t* k_per_head, const int64_t* idx_offset, dsv_shape shape,
+                               dsv_group group, float scale, void* O, float* LSE, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsv_sparse_attn_bwd -- query-grouped sparse attention, backward.
+ * Passage: technical summary section 2.1 (stage 2 trains with sparse
+ * attention over the critical KV, so gradients flow through the selected
+ * pairs only; the index sets are constants of the step).
+ *
+ * Given O, LSE from the forward and dO: P = exp(scale q.k - LSE),
+ * dP = dO v^T, Delta_i = sum_c dO_ic O_ic, dS = P (dP - Delta):
+ *   dQ_i = scale sum_{j in I} dS_ij k_j
+ *   dK_j = scale sum over (group, query i) pairs that selected j of dS_ij q_i
+ *   dV_j = sum over the same pairs of P_ij dO_i
+ * dK and dV are accumulated in fixed point (int64, 2^-32 units), so the
+ * result does not depend on the order of accumulation; then rounded to bf16.
+ * dQ, dK, dV are fully overwritten. Device error DSV_ERR_OVERFLOW if a
+ * partial sum leaves the fixed-point range (|value| >= 2^30 / n_groups).
+ * ---------------------------------------------------------------------- */
+size_t dsv_sparse_attn_bwd_workspace_size(dsv_shape shape, dsv_group group);
+dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                               const void* dO, const int32_t* idx, const int32_t* k_per_head,
+                               const int64_t* idx_offset, dsv_shape shape, dsv_group group, float scale, void* dQ,
+                               void* dK, void* dV, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                               void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBDSV_H */

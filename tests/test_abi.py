@@ -1,0 +1,120 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol the
+header declares, validates arguments before launching anything, and its host
+logic (dispatcher, workspace sizing) matches the oracle and the O(S*k) claim."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from dynamic_sparse_attention_dsv_gb300 import api, native
+from oracle import dsv_oracle as ora
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "libdsv.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"\b(dsv_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return native.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "dsv_lowrank_topk" in names and "dsv_sparse_attn_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    # the binding declares exactly the header's entry points
+    assert sorted(n for n, _, _ in native.SIGNATURES) == names
+
+
+def test_status_strings(lib):
+    for code, name in native.DSV_STATUS.items():
+        assert lib.dsv_status_string(code).decode().startswith(name)
+
+
+@pytest.mark.parametrize("S,kcovs", [(262144, [1, 2621, 50000, 65536, 70000, 131072, 131073, 262144]),
+                                     (16384, [1, 163, 164, 2000, 4096, 4097, 8192, 8193]),
+                                     (1024, [1, 10, 11, 256, 257, 512, 513])])
+def test_plan_heads_matches_oracle(S, kcovs):
+    n_groups = S // 128
+    k_h, dense, offs, total = api.plan_heads(kcovs, S, n_groups)
+    ok, od = ora.plan_heads(kcovs, S)
+    assert k_h == ok and dense == od
+    run = 0
+    for k, dn, off in zip(k_h, dense, offs):
+        if dn:
+            assert off == -1
+        else:
+            assert off == run
+            run += n_groups * k
+    assert total == run
+
+
+def test_plan_heads_rejects_bad_input(lib):
+    kc = (ctypes.c_int32 * 1)(0)
+    out_k = (ctypes.c_int32 * 1)()
+    out_d = (ctypes.c_uint8 * 1)()
+    out_o = (ctypes.c_int64 * 1)()
+    tot = ctypes.c_int64()
+    assert lib.dsv_plan_heads(kc, 1, 1024, 8, 0.01, 0.25, 0.5, out_k, out_d, out_o, ctypes.byref(tot)) == 1
+
+
+def _shape(B, H, T, Y, X, d):
+    return native.dsv_shape(B, H, T, Y, X, d)
+
+
+def test_workspace_is_linear_in_S_not_quadratic(lib):
+    g = native.dsv_group(2, 8, 8)
+    sizes = []
+    for T in (8, 16, 32, 64):
+        s = _shape(1, 1, T, 64, 64, 128)
+        sizes.append(lib.dsv_lowrank_topk_workspace_size(s, 32, g) + lib.dsv_coverage_workspace_size(s, 32, g) +
+                     lib.dsv_sparse_attn_bwd_workspace_size(s, g))
+    S = np.array([8, 16, 32, 64]) * 4096
+    ratio = np.array(sizes) / S
+    # bytes per token stay bounded as S grows 8x (an S^2 term would grow 8x)
+    assert ratio.max() / ratio.min() < 1.5, ratio
+
+
+def test_argument_validation_before_launch(lib):
+    g = native.dsv_group(2, 8, 8)
+    s = _shape(1, 1, 16, 64, 64, 128)
+    fake = ctypes.c_void_p(256)
+    ks = (ctypes.c_int32 * 1)(10)
+    offs = (ctypes.c_int64 * 1)(0)
+    # group does not divide the grid
+    assert lib.dsv_lowrank_topk(fake, fake, fake, fake, s, 32, native.dsv_group(3, 8, 8), ks, offs, fake, fake, 1 << 30,
+                                None, None) == 1
+    # unsupported rank / head dim / group size
+    assert lib.dsv_lowrank_topk(fake, fake, fake, fake, s, 48, g, ks, offs, fake, fake, 1 << 30, None, None) == 2
+    assert lib.dsv_sparse_attn_fwd(fake, fake, fake, None, None, None, _shape(1, 1, 16, 64, 64, 96), g,
+                                   ctypes.c_float(0.1), fake, fake, None, 0, None, None) == 2
+    assert lib.dsv_sparse_attn_fwd(fake, fake, fake, None, None, None, s, native.dsv_group(1, 4, 8),
+                                   ctypes.c_float(0.1), fake, fake, None, 0, None, None) == 2
+    # null / misaligned pointers
+    assert lib.dsv_sparse_attn_fwd(None, fake, fake, None, None, None, s, g, ctypes.c_float(0.1), fake, fake, None, 0,
+                                   None, None) == 1
+    assert lib.dsv_sparse_attn_fwd(ctypes.c_void_p(258), fake, fake, None, None, None, s, g, ctypes.c_float(0.1), fake,
+                                   fake, None, 0, None, None) == 1
+    # k out of range
+    bad = (ctypes.c_int32 * 1)(s.T * s.Y * s.X + 1)
+    assert lib.dsv_lowrank_topk(fake, fake, fake, fake, s, 32, g, bad, offs, fake, fake, 1 << 40, None, None) == 1
+    # missing or short workspace
+    assert lib.dsv_lowrank_topk(fake, fake, fake, fake, s, 32, g, ks, offs, fake, None, 0, None, None) == 3
+    assert lib.dsv_sparse_attn_bwd(fake, fake, fake, fake, fake, fake, None, None, None, s, g, ctypes.c_float(0.1),
+                                   fake, fake, fake, fake, 16, None, None) == 3
+    # S not a multiple of 128
+    assert lib.dsv_coverage(fake, fake, fake, fake, _shape(1, 1, 1, 8, 8, 64), 16, native.dsv_group(1, 8, 8),
+                            ctypes.c_float(0.1), ctypes.c_float(0.9), fake, None, 0, fake, 1 << 30, None, None) == 2
+
+
+def test_topk_layout_packs_rows():
+    ks, offs, total = api.topk_layout(3, 16, [5, 7, 9], skip=[False, True, False])
+    assert offs == [0, -1, 80] and total == 80 + 16 * 9
