@@ -1,0 +1,409 @@
+"""Benchmark of the DSV hot path on one GB300.
+
+One step = the whole hot path on the S=64K video-DiT attention layer (H=24,
+16x64x64 latent grid, d=128, r=32, 2x8x8 query groups of 128, k=6554 = 10% of
+S): predicted-mass coverage (k_cov per head), fused low-rank top-k, sparse
+attention forward and backward. Inputs are seeded synthetic bf16 tensors
+(larger than L2: Q, K, V, dO are 403 MB each) resident in HBM.
+
+Prints ONE JSON line. `value` is the effective attention TFLOP/s of the whole
+step (algorithmic fwd+bwd FLOPs 14*H*S*k*d over the step time). Breakdown keys
+give each phase's time, the top-k Gscore/s and the attention TFLOP/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import dynamic_sparse_attention_dsv_gb300 as dsv  # noqa: E402
+from dynamic_sparse_attention_dsv_gb300 import api, synthetic as syn  # noqa: E402
+
+METRIC = "sparse attn fwd+bwd ms & TFLOP/s at S=64K; lowrank top-k Gscore/s; % roofline"
+CFG = 2
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p.get("bf16_tflops_sustained"),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def workload_dict(w):
+    return {"workload": f"cfg{w.cfg}: " + w.name, "B": 1, "H": w.H, "grid": [w.T, w.Y, w.X], "S": w.S, "d": w.d,
+            "r": w.r, "group": [w.gt, w.gy, w.gx], "k": w.k, "l2": "inputs larger than L2 (1.6 GB of Q/K/V/dO)"}
+
+
+def attn_flops(w, ks):
+    return 14.0 * w.S * w.d * sum(ks)
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self, dev_index: int):
+        self.proc = None
+        self.path = tempfile.mktemp(suffix=".csv")
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(dev_index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- GPU step
+class Step:
+    """Preallocated buffers and the calls of one hot-path step."""
+
+    def __init__(self, w, inp, device):
+        self.w = w
+        self.grid, self.group = (w.T, w.Y, w.X), (w.gt, w.gy, w.gx)
+        dev = lambda t: t.to(device) if t is not None else None
+        self.Q, self.K, self.V, self.dO = dev(inp["Q"]), dev(inp["K"]), dev(inp["V"]), dev(inp["dO"])
+        self.Wq, self.Wk = dev(inp["Wq"]), dev(inp["Wk"])
+        self.ks, self.offs, total = dsv.topk_layout(w.H, w.n_groups, w.k)
+        self.idx = torch.empty(total, dtype=torch.int32, device=device)
+        self.O = torch.empty_like(self.Q)
+        self.LSE = torch.empty(self.Q.shape[:-1], dtype=torch.float32, device=device)
+        self.dQ, self.dK, self.dV = torch.empty_like(self.Q), torch.empty_like(self.K), torch.empty_like(self.V)
+        nb = max(api.lowrank_topk_workspace_size(self.Q, self.grid, self.group, w.r),
+                 int(dsv.native.load().dsv_coverage_workspace_size(api.make_shape(self.Q, self.grid), w.r,
+                                                                   api.make_group(self.group))),
+                 api.sparse_attn_bwd_workspace_size(self.Q, self.grid, self.group))
+        self.ws = torch.empty(nb, dtype=torch.uint8, device=device)
+        self.status = dsv.new_status(device)
+        self.k_cov = None
+
+    def coverage(self):
+        self.k_cov, _ = dsv.coverage(self.Q, self.K, self.Wq, self.Wk, self.grid, self.group, workspace=self.ws,
+                                     status=self.status)
+
+    def topk(self):
+        dsv.lowrank_topk(self.Q, self.K, self.Wq, self.Wk, self.grid, self.group, self.ks, idx_offset=self.offs,
+                         idx=self.idx, workspace=self.ws, status=self.status)
+
+    def fwd(self):
+        dsv.sparse_attn_fwd(self.Q, self.K, self.V, self.idx, self.ks, self.offs, self.grid, self.group, O=self.O,
+                            LSE=self.LSE, status=self.status)
+
+    def bwd(self):
+        dsv.sparse_attn_bwd(self.Q, self.K, self.V, self.O, self.LSE, self.dO, self.idx, self.ks, self.offs,
+                            self.grid, self.group, dQ=self.dQ, dK=self.dK, dV=self.dV, workspace=self.ws,
+                            status=self.status)
+
+    def phases(self):
+        return [("coverage", self.coverage), ("lowrank_topk", self.topk), ("attn_fwd", self.fwd),
+                ("attn_bwd", self.bwd)]
+
+    def run(self):
+        for _, f in self.phases():
+            f()
+
+
+def count_kernel_launches(step: Step) -> int:
+    """Captures one step into a CUDA graph and counts its kernel nodes."""
+    cudart = None
+    for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+        try:
+            cudart = ctypes.CDLL(name)
+            break
+        except OSError:
+            continue
+    if cudart is None:
+        return -1
+    s = torch.cuda.Stream()
+    graph = ctypes.c_void_p()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        h = ctypes.c_void_p(s.cuda_stream)
+        if cudart.cudaStreamBeginCapture(h, 2) != 0:   # relaxed
+            return -1
+        step.run()
+        if cudart.cudaStreamEndCapture(h, ctypes.byref(graph)) != 0:
+            return -1
+    n = ctypes.c_size_t(0)
+    cudart.cudaGraphGetNodes(graph, None, ctypes.byref(n))
+    nodes = (ctypes.c_void_p * n.value)()
+    cudart.cudaGraphGetNodes(graph, nodes, ctypes.byref(n))
+    kernels = 0
+    for i in range(n.value):
+        t = ctypes.c_int(-1)
+        cudart.cudaGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t))
+        kernels += t.value == 0
+    cudart.cudaGraphDestroy(graph)
+    return kernels
+
+
+# --------------------------------------------------------- CPU baseline
+def cpu_baseline(w, inp, budget_s: float = 12.0, max_groups: int = 1 << 30):
+    """The oracle (as it stands) on a bounded sample of the step: top-k scores,
+    predicted-mass curve and attention fwd+bwd for m groups of head 0."""
+    from oracle import dsv_oracle as ora
+    mem = ora.group_members(w.T, w.Y, w.X, w.gt, w.gy, w.gx)
+    scale = 1.0 / math.sqrt(w.d)
+    Q, K, V, dO = (ora.as_f64(inp[n][0]) for n in ("Q", "K", "V", "dO"))
+    q_lr, k_lr = ora.lowrank_project(inp["Q"][0], inp["Wq"][0]), ora.lowrank_project(inp["K"][0], inp["Wk"][0])
+
+    def one(gs):
+        s = ora.group_scores(q_lr, k_lr, mem, gs)
+        idx = np.stack([ora.topk_ascending(row, w.k) for row in s])
+        ora.coverage_curve(s, scale)
+        ora.sparse_attn_bwd(Q, K, V, dO, idx, mem[gs], scale)   # recomputes the forward per group
+
+    t0 = time.perf_counter()
+    one([0])
+    t1 = time.perf_counter() - t0
+    m = int(max(1, min(max_groups, w.n_groups - 1, budget_s / max(t1, 1e-3))))
+    gs = list(range(1, 1 + m))
+    t0 = time.perf_counter()
+    one(gs)
+    dt = time.perf_counter() - t0
+    flops = 14.0 * w.G * w.k * w.d * m
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"head 0, {m} of {w.n_groups} groups: group scores, top-k, predicted-mass curve, sparse "
+                      f"attention fwd+bwd (fp64 numpy), {dt:.1f} s"}, dt
+
+
+# ------------------------------------------------------------------- main
+def dist_setup(n):
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+        rank = tdist.get_rank()
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+        return tdist, rank, tdist.get_world_size()
+    torch.cuda.set_device(0)
+    return None, 0, 1
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="dsv", choices=["dsv", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    w = syn.workload(CFG)
+
+    if args.impl == "reference":
+        return reference_arm(args, w)
+
+    tdist, rank, world = dist_setup(args.gpus)
+    device = torch.device("cuda", torch.cuda.current_device())
+    inp = syn.make_inputs(w)
+    step = Step(w, inp, device)
+    pk = peaks()
+
+    for _ in range(max(args.warmup, 1)):
+        step.run()
+    torch.cuda.synchronize()
+    code = dsv.read_status(step.status)
+    if code:
+        raise SystemExit(f"device status {dsv.native.DSV_STATUS.get(code, code)} during warm-up")
+    launches = count_kernel_launches(step)
+
+    # timed region: per-phase CUDA events on the launching stream
+    stream = torch.cuda.current_stream()
+    names = [n for n, _ in step.phases()]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
+    clocks = ClockSampler(device.index)
+    if tdist:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        for j, (_, f) in enumerate(step.phases()):
+            f()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    if tdist:
+        tdist.barrier()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    code = dsv.read_status(step.status)
+    if code:
+        raise SystemExit(f"device status {dsv.native.DSV_STATUS.get(code, code)} in the timed region")
+
+    per_phase = {n: [] for n in names}
+    total_ms = 0.0
+    for i in range(args.steps):
+        for j, n in enumerate(names):
+            per_phase[n].append(ev[i][j].elapsed_time(ev[i][j + 1]))
+        total_ms += ev[i][0].elapsed_time(ev[i][-1])
+    ms = total_ms / args.steps
+    if tdist:
+        t = torch.tensor([ms], device=device)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms = float(t.item())
+    ph = {n: statistics.mean(v) for n, v in per_phase.items()}
+    flops = attn_flops(w, step.ks)
+    value = world * flops / (ms * 1e-3) / 1e12
+    fb_ms = ph["attn_fwd"] + ph["attn_bwd"]
+    scores = w.H * w.n_groups * w.S
+    fwd_flops = 4.0 * w.S * w.d * sum(step.ks)
+    bwd_flops = 10.0 * w.S * w.d * sum(step.ks)
+    # roofline of the dominant phase (largest share of the step). Attention
+    # phases are tensor-bound (algorithmic FLOPs); the low-rank phases are
+    # graded against HBM (algorithmic bytes: read Q and K, write idx).
+    topk_bytes = w.H * (4.0 * w.S * w.d + 4.0 * w.n_groups * w.k)
+    cov_bytes = w.H * 4.0 * w.S * w.d
+    work = {"attn_bwd": ("tensor", bwd_flops / 1e12, "TFLOP/s", "k_attn_bwd_q + k_fix_to_bf16 (dsv_sparse_attn_bwd)"),
+            "attn_fwd": ("tensor", fwd_flops / 1e12, "TFLOP/s", "k_attn_fwd (dsv_sparse_attn_fwd)"),
+            "lowrank_topk": ("hbm", topk_bytes / 1e9, "GB/s", "k_select passes (dsv_lowrank_topk)"),
+            "coverage": ("hbm", cov_bytes / 1e9, "GB/s", "k_select passes (dsv_coverage)")}
+    dom = max(work, key=lambda n: ph[n])
+    bound, amount, unit, kname = work[dom]
+    achieved = amount / (ph[dom] * 1e-3)
+    peak = (pk["bf16_sus"] or pk["bf16"]) if bound == "tensor" else pk["hbm"]
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e and rank == 0:
+        e2e = end_to_end(w, inp, device, args)
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded video-latent-shaped Q/K/V/dO)",
+        "config": workload_dict(w),
+        "breakdown": {
+            "coverage_ms": round(ph["coverage"], 3), "lowrank_topk_ms": round(ph["lowrank_topk"], 3),
+            "lowrank_topk_gscore_s": round(scores / (ph["lowrank_topk"] * 1e-3) / 1e9, 2),
+            "attn_fwd_ms": round(ph["attn_fwd"], 3), "attn_bwd_ms": round(ph["attn_bwd"], 3),
+            "attn_fwd_bwd_ms": round(fb_ms, 3),
+            "attn_fwd_bwd_tflops": round(flops / (fb_ms * 1e-3) / 1e12, 2),
+            "attn_fwd_tflops": round(fwd_flops / (ph["attn_fwd"] * 1e-3) / 1e12, 2),
+            "attn_fwd_bwd_frac_of_bf16_peak": round(flops / (fb_ms * 1e-3) / 1e12 / (pk["bf16_sus"] or pk["bf16"]), 4),
+            "lowrank_topk_hbm_gbs": round(w.H * (4.0 * w.S * w.d + 4.0 * w.n_groups * w.k) /
+                                          (ph["lowrank_topk"] * 1e-3) / 1e9, 1),
+            "wall_s": round(wall, 3),
+        },
+        "roofline": {"kernel": kname, "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": pk["source"] + (" bf16 sustained" if bound == "tensor" else " HBM copy")},
+        "gpu_launches": launches * args.steps if launches >= 0 else None,
+        "clocks": clk,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp)[0]
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if tdist:
+        tdist.destroy_process_group()
+
+
+def end_to_end(w, inp, device, args):
+    """Same metric through the public API with pinned host buffers: every step
+    copies the inputs host->device and reads O, dQ, dK, dV back."""
+    host_in = {n: inp[n].pin_memory() for n in ("Q", "K", "V", "dO", "Wq", "Wk")}
+    step = Step(w, inp, device)
+    outs = {n: torch.empty(step.Q.shape, dtype=torch.bfloat16).pin_memory() for n in ("O", "dQ", "dK", "dV")}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+
+    def once():
+        for n, dst in (("Q", step.Q), ("K", step.K), ("V", step.V), ("dO", step.dO), ("Wq", step.Wq),
+                       ("Wk", step.Wk)):
+            dst.copy_(host_in[n], non_blocking=True)
+        step.run()
+        for n, src in (("O", step.O), ("dQ", step.dQ), ("dK", step.dK), ("dV", step.dV)):
+            outs[n].copy_(src, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        once()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        once()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    return {"value": round(attn_flops(w, step.ks) / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def reference_arm(args, w):
+    """The oracle timed on the host cores, one bounded sample of the workload
+    per step (rank 0 only; other ranks exit without work)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    inp = syn.make_inputs(w, heads=1)
+    for _ in range(args.warmup):
+        cpu_baseline(w, inp, budget_s=0.0, max_groups=1)
+    vals, secs = [], 0.0
+    for _ in range(args.steps):
+        cb, dt = cpu_baseline(w, inp, budget_s=5.0, max_groups=8)
+        vals.append(cb["value"])
+        secs += dt
+    v = statistics.mean(vals)
+    cb["value"] = round(v, 6)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded video-latent-shaped Q/K/V/dO)", "config": workload_dict(w),
+            "cpu_baseline": cb, "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
