@@ -27,6 +27,7 @@
 // log-probability (count and mass per bin); a reduce kernel searches k.
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <vector>
 
 #include "common.cuh"
@@ -933,4 +934,56 @@ extern "C" dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_
     if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
   }
   return DSV_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of dsv_lowrank_topk.
+//
+// Some callers cannot allocate device memory at the point where they need a
+// top-k: a plugin whose enqueue step may not allocate, a serving loop whose
+// device memory budget is fixed at start-up, or an embedding runtime that owns
+// every allocation itself. For them the scratch lives in the fixed array below,
+// reserved in the library's own device image: every GPU that loads this code
+// holds kStaticScratchBytes of it until the process exits.
+namespace dsv {
+
+constexpr size_t kStaticScratchBytes = 64ull << 20;   // 64 MiB
+static __device__ __align__(256) uint8_t g_topk_scratch[kStaticScratchBytes];
+
+// Device address of g_topk_scratch for the current device. The host-side name
+// is only a stand-in, so the address is looked up (once per device, with that
+// device current) through the runtime; the first lookup also loads this
+// module on that device.
+static void* static_scratch_address(cudaError_t* err) {
+  static std::mutex mu;
+  static void* addr[128] = {};
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_topk_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace dsv
+
+extern "C" dsv_status dsv_lowrank_topk_noalloc(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr,
+                                               dsv_shape shape, int32_t r, dsv_group group,
+                                               const int32_t* k_per_head, const int64_t* idx_offset, int32_t* idx,
+                                               int32_t* dev_status, void* stream) {
+  dsv_status v = validate_lowrank(Q, K, Wq_lr, Wk_lr, shape, r, group);
+  if (v != DSV_OK) return v;
+  const size_t need = dsv_lowrank_topk_workspace_size(shape, r, group);
+  if (need == 0) return DSV_ERR_INVALID_ARG;
+  if (need > kStaticScratchBytes) return DSV_ERR_WORKSPACE;   // shape needs more than the fixed scratch
+  cudaError_t err = cudaSuccess;
+  void* scratch = static_scratch_address(&err);
+  if (!scratch) return DSV_ERR_CUDA;
+  return dsv_lowrank_topk(Q, K, Wq_lr, Wk_lr, shape, r, group, k_per_head, idx_offset, idx, scratch,
+                          kStaticScratchBytes, dev_status, stream);
 }

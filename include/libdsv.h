@@ -19,7 +19,8 @@
  *  - Index sets: row (p, g) holds k_p ascending int32 key positions at
  *    idx + idx_offset[p] + g*k_p (device memory).
  *  - Every buffer is owned by the caller; libdsv allocates nothing and keeps
- *    no state between calls. Scratch space is the caller's `workspace`
+ *    no state between calls (dsv_lowrank_topk_noalloc, below, instead uses a
+ *    fixed array inside the library). Scratch space is the caller's `workspace`
  *    (device, 256-byte aligned) of at least the size the matching
  *    dsv_*_workspace_size() call reports.
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*).
@@ -94,6 +95,31 @@ dsv_status dsv_lowrank_topk(const void* Q, const void* K, const void* Wq_lr, con
                             int32_t r, dsv_group group, const int32_t* k_per_head, const int64_t* idx_offset,
                             int32_t* idx, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                             void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsv_lowrank_topk_noalloc -- dsv_lowrank_topk for callers that cannot
+ * allocate device memory.
+ * The DSV pages have no counterpart to this call; it exists for callers such
+ * as a plugin whose enqueue step may not allocate, a serving loop with a
+ * device memory budget fixed at start-up, or a host runtime that owns every
+ * allocation and cannot lend a workspace.
+ *
+ * Same inputs, outputs and results as dsv_lowrank_topk, but the scratch space
+ * is a fixed 64 MiB array compiled into libdsv (reserved on every GPU that
+ * loads this part of the library, until the process exits). No workspace is
+ * passed and nothing is allocated: the call makes no cudaMalloc/cudaFree and
+ * no allocating library call.
+ *  - Shapes whose dsv_lowrank_topk_workspace_size() exceeds 64 MiB are
+ *    rejected with DSV_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address (and
+ *    loads the module there); make that first call before any stream capture.
+ *  - Every call uses the same array. The call clears what must start at zero
+ *    itself, but calls whose work overlaps on the GPU (different streams, or
+ *    several host threads) race on it: serialise them.
+ * ---------------------------------------------------------------------- */
+dsv_status dsv_lowrank_topk_noalloc(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr,
+                                    dsv_shape shape, int32_t r, dsv_group group, const int32_t* k_per_head,
+                                    const int64_t* idx_offset, int32_t* idx, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
  * dsv_coverage -- smallest k per problem covering `mass` of the predicted
