@@ -121,7 +121,7 @@ class Step:
         nb = max(api.lowrank_topk_workspace_size(self.Q, self.grid, self.group, w.r),
                  int(dsv.native.load().dsv_coverage_workspace_size(api.make_shape(self.Q, self.grid), w.r,
                                                                    api.make_group(self.group))),
-                 api.sparse_attn_bwd_workspace_size(self.Q, self.grid, self.group))
+                 api.sparse_attn_bwd_workspace_size(self.Q, self.grid, self.group, self.ks, self.offs))
         self.ws = torch.empty(nb, dtype=torch.uint8, device=device)
         self.status = dsv.new_status(device)
         self.k_cov = None
@@ -302,7 +302,7 @@ def main():
     # graded against HBM (algorithmic bytes: read Q and K, write idx).
     topk_bytes = w.H * (4.0 * w.S * w.d + 4.0 * w.n_groups * w.k)
     cov_bytes = w.H * 4.0 * w.S * w.d
-    work = {"attn_bwd": ("tensor", bwd_flops / 1e12, "TFLOP/s", "k_attn_bwd_q + k_fix_to_bf16 (dsv_sparse_attn_bwd)"),
+    work = {"attn_bwd": ("tensor", bwd_flops / 1e12, "TFLOP/s", "k_attn_bwd_q + k_csc_reduce (dsv_sparse_attn_bwd)"),
             "attn_fwd": ("tensor", fwd_flops / 1e12, "TFLOP/s", "k_attn_fwd (dsv_sparse_attn_fwd)"),
             "lowrank_topk": ("hbm", topk_bytes / 1e9, "GB/s", "k_select passes (dsv_lowrank_topk)"),
             "coverage": ("hbm", cov_bytes / 1e9, "GB/s", "k_select passes (dsv_coverage)")}

@@ -183,8 +183,10 @@ def sparse_attn_fwd(Q, K, V, idx, k_per_head, idx_offset, grid, group, scale: Op
     return O, LSE
 
 
-def sparse_attn_bwd_workspace_size(x, grid, group) -> int:
-    return int(N.load().dsv_sparse_attn_bwd_workspace_size(make_shape(x, grid), make_group(group)))
+def sparse_attn_bwd_workspace_size(x, grid, group, k_per_head=None, idx_offset=None) -> int:
+    kp = _i32(k_per_head) if k_per_head is not None else None
+    op = _i64(idx_offset) if k_per_head is not None else None
+    return int(N.load().dsv_sparse_attn_bwd_workspace_size(make_shape(x, grid), make_group(group), kp, op))
 
 
 def sparse_attn_bwd(Q, K, V, O, LSE, dO, idx, k_per_head, idx_offset, grid, group, scale: Optional[float] = None,
@@ -197,10 +199,10 @@ def sparse_attn_bwd(Q, K, V, O, LSE, dO, idx, k_per_head, idx_offset, grid, grou
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
-    ws = _workspace(int(lib.dsv_sparse_attn_bwd_workspace_size(shape, grp)), Q.device, workspace)
-    st = status if status is not None else new_status(Q.device)
     kp = _i32(k_per_head) if idx is not None else None
     op = _i64(idx_offset) if idx is not None else None
+    ws = _workspace(int(lib.dsv_sparse_attn_bwd_workspace_size(shape, grp, kp, op)), Q.device, workspace)
+    st = status if status is not None else new_status(Q.device)
     code = lib.dsv_sparse_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(dO), _ptr(idx), kp, op, shape,
                                    grp, ctypes.c_float(scale), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(),
                                    _ptr(st), _stream())

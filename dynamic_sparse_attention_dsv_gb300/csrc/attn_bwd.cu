@@ -12,10 +12,13 @@
 //   S = Q K^T, dP = dO V^T                        tcgen05 (smem x smem) -> TMEM
 //   P = exp2(S*scale*log2e - LSE*log2e), dS = P (dP - Delta)   registers
 //   dQ += dS K                                    accumulated in TMEM, written once
-//   sparse problems only: dV_tile = P^T dO, dK_tile = dS^T Q -> TMEM, then
-//   converted to int64 fixed point (2^-32 units) and added into per-key
-//   accumulators. Integer addition is associative, so dK/dV do not depend on
-//   the order in which groups arrive.
+//   sparse problems only: dV_tile = P^T dO, dK_tile = scale dS^T Q -> TMEM,
+//   written as bf16 partial rows, one per (group, selected key) pair.
+// Ordered dK/dV reduction (no atomics on the data): a bitmap of which groups
+// selected each key gives every (key, group) pair a slot, off[key] + the
+// number of lower groups that selected the key, so the partials of one key
+// lie contiguously in ascending group order; a reduce kernel sums each key's
+// slots in that order in fp32. The result is the same bits on every run.
 // Key-major kernel (dense problems): one CTA per (128-key tile, problem),
 // looping over all 128-token query tiles with dV, dK accumulated in TMEM;
 // no cross-CTA reduction at all.
@@ -27,7 +30,34 @@
 namespace dsv {
 
 constexpr int kBwdThreads = 192;
-constexpr int kBwdChunkProblems = 4;   // sparse problems per accumulator chunk
+constexpr int kMaxUnits = 48;                       // work units per group-major launch
+constexpr size_t kPartialBudget = 8ull << 30;       // bytes of bf16 dK/dV partials in flight
+
+// A unit is a range of groups of one problem whose dK/dV partials are
+// produced and reduced by one launch.
+struct UnitTable {
+  int32_t n;
+  int32_t p[kMaxUnits];        // problem (b*H + h)
+  int32_t k[kMaxUnits];        // keys per group (S for dense problems)
+  int32_t g0[kMaxUnits];       // first group of the unit
+  int32_t ng[kMaxUnits];       // groups in the unit
+  int32_t nwords[kMaxUnits];   // bitmap words per key (ceil(ng / 32))
+  int32_t flags[kMaxUnits];    // bit 0: first unit of its problem, bit 1: last unit
+  int64_t off[kMaxUnits];      // idx offset of row (p, 0); -1 = dense
+  int64_t part_base[kMaxUnits];   // first partial slot of the unit
+  int64_t bits_base[kMaxUnits];   // first bitmap word of the unit
+};
+
+struct CscParams {
+  uint32_t* bits;              // per unit [S][nwords]: bit (key, group) set if the group selected the key
+  int32_t* off;                // per unit [S + 1]: first slot of each key
+  __nv_bfloat16* part_v;       // [slots][d]
+  __nv_bfloat16* part_k;       // [slots][d]
+  float* acc_v;                // [S][d] fp32 running sums of a problem split over several units
+  float* acc_k;
+  __nv_bfloat16* dK;
+  __nv_bfloat16* dV;
+};
 
 template <int D>
 struct BwdCfg {
@@ -38,25 +68,10 @@ struct BwdCfg {
   static constexpr int kOffV = kOffK + kStages * kTile;
   static constexpr int kOffP = kOffV + kStages * kTile;   // [128 q][128 keys] bf16 = 32 KB
   static constexpr int kOffDS = kOffP + 32768;
-  static constexpr int kOffBar = kOffDS + 32768;   // barriers at +0, key slots at +128
+  static constexpr int kOffBar = kOffDS + 32768;
   static constexpr int kSmemUsed = kOffBar + 1024 + 1024;
   static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
 };
-
-// round(v * 2^32) as int64 for |v| < 2^30, from the float's bits (no FP64).
-__device__ __forceinline__ int64_t f2fix(float v) {
-  const uint32_t b = __float_as_uint(v);
-  const int e = (int)((b >> 23) & 0xFF) - 127;
-  if (e < -33) return 0;
-  const uint64_t m = (b & 0x7FFFFFu) | 0x800000u;   // v = m * 2^(e-23)
-  const int sh = e + 9;                              // v * 2^32 = m * 2^(e+9)
-  const uint64_t mag = sh >= 0 ? (m << sh) : ((m + (1ull << (-sh - 1))) >> (-sh));
-  return (b >> 31) ? -(int64_t)mag : (int64_t)mag;
-}
-
-__device__ __forceinline__ void red_global_u64(int64_t* addr, int64_t v) {
-  asm volatile("red.global.add.u64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
-}
 
 __device__ __forceinline__ void compute_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -71,7 +86,7 @@ __device__ __forceinline__ void st_sw128_chunk(uint8_t* tile, int row, int chunk
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     k_attn_bwd_q(const __grid_constant__ AttnMaps maps, const __grid_constant__ CUtensorMap do_cube,
-                 const AttnParams prm, const ProblemTable tab) {
+                 const AttnParams prm, const CscParams csc, const UnitTable tab) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -93,10 +108,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 12);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = blockIdx.x, lp = blockIdx.y, p = tab.p[lp];
+  const int u = blockIdx.y;
+  if ((int)blockIdx.x >= tab.ng[u]) return;   // units of a launch may hold fewer groups than the grid
+  const int g = tab.g0[u] + blockIdx.x, p = tab.p[u], lp = u;
   const Geometry& geo = prm.geo;
   const bool dense = (prm.idx == nullptr) || (tab.off[lp] < 0);
-  const bool partials = !dense && prm.dK_acc != nullptr;
+  const bool partials = !dense && csc.part_v != nullptr;
   const int k = dense ? geo.S : tab.k[lp];
   const int nt = (k + 127) / 128;
   const int32_t* idx_row = dense ? nullptr : prm.idx + tab.off[lp] + (int64_t)g * k;
@@ -280,45 +297,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       if (partials) {
         // Drain dV_tile (cols 0..D) and dK_tile (cols 128..128+D): TMEM lane =
-        // key slot. Rows are staged as int64 in the P/dS area (64 rows per
-        // round), then added with consecutive threads on consecutive columns.
-        int64_t* stage = reinterpret_cast<int64_t*>(sP);
+        // key slot of the tile. Each selected key's two bf16 rows go to its
+        // slot: off[key] + number of lower groups (of this unit) that chose it.
         const int slot_key = t * 128 + row;
-        const int krow = slot_key < k ? __ldg(idx_row + slot_key) : -1;
-        int* keys = reinterpret_cast<int*>(sm + C::kOffBar + 128);   // [128] key of each slot
-        keys[row] = krow;
+        const bool kvalid = slot_key < k;
+        int64_t pos = 0;
+        if (kvalid) {
+          const int j = __ldg(idx_row + slot_key);
+          const int gl = g - tab.g0[u];
+          const uint32_t* b = csc.bits + tab.bits_base[u] + (int64_t)j * tab.nwords[u];
+          int r = 0;
+          for (int w = 0; w < (gl >> 5); ++w) r += __popc(__ldg(b + w));
+          r += __popc(__ldg(b + (gl >> 5)) & ((1u << (gl & 31)) - 1u));
+          pos = tab.part_base[u] + csc.off[(int64_t)u * (geo.S + 1) + j] + r;
+        }
+#pragma unroll 1
         for (int tensor = 0; tensor < 2; ++tensor) {
           const uint32_t col = tensor == 0 ? kColS : kColDP;
           const float mul = tensor == 0 ? 1.f : prm.scale;
-          int64_t* acc = tensor == 0 ? prm.dV_acc : prm.dK_acc;
-          for (int half = 0; half < 2; ++half) {
-            compute_barrier();   // staging area free; keys[] visible
+          __nv_bfloat16* dst_row = (tensor == 0 ? csc.part_v : csc.part_k) + pos * D;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t v[32];
-              tmem_ld32(lane_addr + col + c * 32, v);
-              tmem_ld_wait(v);
-              if ((row >> 6) == half) {
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(lane_addr + col + c * 32, v);
+            tmem_ld_wait(v);
+            if (kvalid) {
+              uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                  const float x = __uint_as_float(v[e]) * mul;
-                  int64_t fx = 0;
-                  if (fabsf(x) < prm.overflow_limit) fx = f2fix(x);
-                  else raise_status(prm.status, DSV_ERR_OVERFLOW);
-                  stage[(row & 63) * D + c * 32 + e] = fx;
-                }
-              }
-            }
-            compute_barrier();
-            for (int i = tid; i < 64 * D; i += 128) {
-              const int r = i / D, cc = i % D;
-              const int kr = keys[half * 64 + r];
-              const int64_t val = stage[i];
-              if (kr >= 0 && val != 0) red_global_u64(acc + ((int64_t)lp * geo.S + kr) * D + cc, val);
+              for (int e = 0; e < 16; ++e)
+                pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+              uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
             }
           }
         }
-        compute_barrier();
       }
       tc_fence_before();
       __syncwarp();
@@ -575,15 +588,120 @@ __global__ void k_bwd_delta(const __nv_bfloat16* __restrict__ O, const __nv_bflo
   delta[(int64_t)p * S + s] = acc;
 }
 
-// Fixed-point accumulators (local problem lp) -> bf16 dK, dV of problem p.
-__global__ void k_fix_to_bf16(const int64_t* __restrict__ acc_k, const int64_t* __restrict__ acc_v, int64_t per,
-                              __nv_bfloat16* dK, __nv_bfloat16* dV, const ProblemTable tab) {
-  const int lp = blockIdx.y, p = tab.p[lp];
-  const int64_t base_l = (int64_t)lp * per, base_p = (int64_t)p * per;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < per; i += (int64_t)gridDim.x * blockDim.x) {
-    dK[base_p + i] = __float2bfloat16_rn((float)acc_k[base_l + i] * 2.3283064365386963e-10f);
-    dV[base_p + i] = __float2bfloat16_rn((float)acc_v[base_l + i] * 2.3283064365386963e-10f);
+// ---------------------------------------------------------------------------
+// Ordered dK/dV reduction.
+// Sets bit (key, group) for every selected pair of every unit.
+__global__ void k_sel_bitmap(const int32_t* __restrict__ idx, uint32_t* bits, const UnitTable tab) {
+  const int u = blockIdx.y, gl = blockIdx.x;
+  if (gl >= tab.ng[u]) return;
+  const int k = tab.k[u];
+  const int32_t* row = idx + tab.off[u] + (int64_t)(tab.g0[u] + gl) * k;
+  uint32_t* b = bits + tab.bits_base[u] + (gl >> 5);
+  const uint32_t bit = 1u << (gl & 31);
+  const int nw = tab.nwords[u];
+  for (int s = threadIdx.x; s < k; s += blockDim.x) atomicOr(b + (int64_t)__ldg(row + s) * nw, bit);
+}
+
+// off[key] = number of pairs of lower keys (exclusive scan of the bit counts).
+__global__ void __launch_bounds__(1024) k_csc_offsets(const uint32_t* __restrict__ bits, int S, int32_t* off,
+                                                      const UnitTable tab) {
+  __shared__ int wsum[32];
+  const int u = blockIdx.x, tid = threadIdx.x;
+  const int nw = tab.nwords[u];
+  const uint32_t* b = bits + tab.bits_base[u];
+  int32_t* o = off + (int64_t)u * (S + 1);
+  const int per = (S + blockDim.x - 1) / blockDim.x;
+  const int j0 = min(S, tid * per), j1 = min(S, j0 + per);
+  int local = 0;
+  for (int j = j0; j < j1; ++j)
+    for (int w = 0; w < nw; ++w) local += __popc(b[(int64_t)j * nw + w]);
+  // block-wide exclusive scan of `local`
+  int x = local;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, d);
+    if ((tid & 31) >= d) x += y;
   }
+  if ((tid & 31) == 31) wsum[tid >> 5] = x;
+  __syncthreads();
+  if (tid < 32) {
+    int v = tid < (int)(blockDim.x >> 5) ? wsum[tid] : 0;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, d);
+      if (tid >= d) v += y;
+    }
+    wsum[tid] = v;   // inclusive over warps
+  }
+  __syncthreads();
+  int run = x - local + ((tid >> 5) ? wsum[(tid >> 5) - 1] : 0);
+  for (int j = j0; j < j1; ++j) {
+    o[j] = run;
+    for (int w = 0; w < nw; ++w) run += __popc(b[(int64_t)j * nw + w]);
+  }
+  if (j1 == S && j0 < j1) o[S] = run;
+  if (S == 0 && tid == 0) o[0] = 0;
+}
+
+// Per key: dV = sum of its partial rows in slot (= group) order, same for dK;
+// fp32 sums. A problem split over several units carries fp32 running sums.
+template <int D>
+__global__ void __launch_bounds__(256) k_csc_reduce(const CscParams csc, int S, const UnitTable tab) {
+  constexpr int E = D / 32;                          // elements per lane
+  const int u = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.x * 8 + warp;
+  if (j >= S) return;
+  const int32_t* o = csc.off + (int64_t)u * (S + 1);
+  const int64_t a = tab.part_base[u] + o[j], b = tab.part_base[u] + o[j + 1];
+  const bool first = tab.flags[u] & 1, last = tab.flags[u] & 2;
+  float sv[E], sk[E];
+  const int64_t arow = (int64_t)j * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    sv[e] = first ? 0.f : csc.acc_v[arow + e];
+    sk[e] = first ? 0.f : csc.acc_k[arow + e];
+  }
+  for (int64_t s = a; s < b; ++s) {
+    const __nv_bfloat16* pv = csc.part_v + s * D + lane * E;
+    const __nv_bfloat16* pk = csc.part_k + s * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(pv + e));
+      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(pk + e));
+      sv[e] += x.x;
+      sv[e + 1] += x.y;
+      sk[e] += y.x;
+      sk[e + 1] += y.y;
+    }
+  }
+  if (last) {
+    const int64_t orow = ((int64_t)tab.p[u] * S + j) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      *reinterpret_cast<__nv_bfloat162*>(csc.dV + orow + e) = __floats2bfloat162_rn(sv[e], sv[e + 1]);
+      *reinterpret_cast<__nv_bfloat162*>(csc.dK + orow + e) = __floats2bfloat162_rn(sk[e], sk[e + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      csc.acc_v[arow + e] = sv[e];
+      csc.acc_k[arow + e] = sk[e];
+    }
+  }
+}
+
+template <int D>
+static cudaError_t launch_bwd_q(const AttnMaps& maps, const CUtensorMap& do_cube, const AttnParams& prm,
+                                const CscParams& csc, const UnitTable& tab, int max_ng, cudaStream_t st) {
+  k_attn_bwd_q<D><<<dim3(max_ng, tab.n), kBwdThreads, BwdCfg<D>::kSmem, st>>>(maps, do_cube, prm, csc, tab);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_bwd_kv(const AttnMaps& maps, const CUtensorMap& q_tile, const CUtensorMap& do_tile,
+                                 const AttnParams& prm, const float* delta, __nv_bfloat16* dK, __nv_bfloat16* dV,
+                                 const ProblemTable& tab, int S, cudaStream_t st) {
+  k_attn_bwd_kv<D><<<dim3(S / 128, tab.n), kBwdThreads, KvCfg<D>::kSmem, st>>>(maps, q_tile, do_tile, prm, delta,
+                                                                                dK, dV, tab);
+  return cudaGetLastError();
 }
 
 template <int D>
@@ -597,35 +715,104 @@ static cudaError_t configure_bwd() {
   return e;
 }
 
-template <int D>
-static cudaError_t launch_bwd_q(const AttnMaps& maps, const CUtensorMap& do_cube, const AttnParams& prm,
-                                const ProblemTable& tab, int n_groups, cudaStream_t st) {
-  k_attn_bwd_q<D><<<dim3(n_groups, tab.n), kBwdThreads, BwdCfg<D>::kSmem, st>>>(maps, do_cube, prm, tab);
-  return cudaGetLastError();
-}
+// ---------------------------------------------------------------------------
+// Host planning: units, launches and workspace.
+struct BwdPlan {
+  std::vector<UnitTable> launches;   // sparse problems (partials)
+  UnitTable dense;                   // dense problems (dQ only)
+  int max_ng = 1;                    // largest unit (grid x of the group-major launches)
+  size_t slots = 0;                  // partial slots needed by the largest launch
+  size_t bits_words = 0;             // bitmap words needed by the largest launch
+  bool split = false;                // some problem spans several units
+};
 
-template <int D>
-static cudaError_t launch_bwd_kv(const AttnMaps& maps, const CUtensorMap& q_tile, const CUtensorMap& do_tile,
-                                 const AttnParams& prm, const float* delta, __nv_bfloat16* dK, __nv_bfloat16* dV,
-                                 const ProblemTable& tab, int S, cudaStream_t st) {
-  k_attn_bwd_kv<D><<<dim3(S / 128, tab.n), kBwdThreads, KvCfg<D>::kSmem, st>>>(maps, q_tile, do_tile, prm, delta,
-                                                                                dK, dV, tab);
-  return cudaGetLastError();
+static BwdPlan plan_bwd(const dsv_shape& shape, const Geometry& geo, bool any_sparse, const int32_t* k_per_head,
+                        const int64_t* idx_offset) {
+  BwdPlan pl;
+  memset(&pl.dense, 0, sizeof(pl.dense));
+  const int P = (int)(shape.B * shape.H);
+  const size_t slot_bytes = (size_t)shape.d * 2 * sizeof(__nv_bfloat16);
+  const size_t cap = std::max<size_t>(1, kPartialBudget / slot_bytes);
+  UnitTable cur;
+  memset(&cur, 0, sizeof(cur));
+  size_t cur_slots = 0, cur_words = 0;
+  auto flush = [&]() {
+    if (cur.n == 0) return;
+    pl.launches.push_back(cur);
+    pl.slots = std::max(pl.slots, cur_slots);
+    pl.bits_words = std::max(pl.bits_words, cur_words);
+    memset(&cur, 0, sizeof(cur));
+    cur_slots = cur_words = 0;
+  };
+  auto add = [&](int p, int k, int64_t off, int g0, int ng, int flags) {
+    const size_t slots = (size_t)ng * k;
+    const int nw = (ng + 31) / 32;
+    const size_t words = (size_t)geo.S * nw;
+    if (cur.n == kMaxUnits || cur_slots + slots > cap || (flags != 3 && cur.n > 0)) flush();
+    const int i = cur.n++;
+    cur.p[i] = p;
+    cur.k[i] = k;
+    cur.g0[i] = g0;
+    cur.ng[i] = ng;
+    cur.nwords[i] = nw;
+    cur.flags[i] = flags;
+    cur.off[i] = off;
+    cur.part_base[i] = (int64_t)cur_slots;
+    cur.bits_base[i] = (int64_t)cur_words;
+    cur_slots += slots;
+    cur_words += words;
+    pl.max_ng = std::max(pl.max_ng, ng);
+    if (flags != 3) flush();   // a unit of a split problem runs alone
+  };
+  for (int p = 0; p < P; ++p) {
+    const bool dense = !any_sparse || idx_offset[p] < 0;
+    if (dense) {
+      const int i = pl.dense.n++;
+      pl.dense.p[i] = p;
+      pl.dense.k[i] = geo.S;
+      pl.dense.g0[i] = 0;
+      pl.dense.ng[i] = geo.n_groups;
+      pl.dense.off[i] = -1;
+      pl.dense.flags[i] = 3;
+      continue;
+    }
+    const int k = k_per_head[p];
+    const size_t pairs = (size_t)geo.n_groups * k;
+    if (pairs <= cap) {
+      add(p, k, idx_offset[p], 0, geo.n_groups, 3);
+    } else {
+      pl.split = true;
+      const int per = (int)std::max<size_t>(1, cap / (size_t)k);
+      for (int g0 = 0; g0 < geo.n_groups; g0 += per) {
+        const int ng = std::min(per, geo.n_groups - g0);
+        add(p, k, idx_offset[p], g0, ng, (g0 == 0 ? 1 : 0) | (g0 + ng == geo.n_groups ? 2 : 0));
+      }
+    }
+  }
+  flush();
+  return pl;
 }
 
 struct BwdWs {
-  int64_t* acc_k;
-  int64_t* acc_v;
+  __nv_bfloat16* part_v;
+  __nv_bfloat16* part_k;
+  uint32_t* bits;
+  int32_t* off;
+  float* acc_v;
+  float* acc_k;
   float* delta;
 };
 
-static size_t carve_bwd(void* base, const dsv_shape& s, BwdWs* w) {
+static size_t carve_bwd(void* base, const dsv_shape& s, const BwdPlan& pl, BwdWs* w) {
   Carver c(base);
   const size_t S = (size_t)(s.T * s.Y * s.X), P = (size_t)(s.B * s.H);
-  const size_t hc = std::min<size_t>(P, kBwdChunkProblems);
-  w->acc_k = c.take<int64_t>(hc * S * s.d);
-  w->acc_v = c.take<int64_t>(hc * S * s.d);
-  w->delta = c.take<float>(P * S);
+  w->part_v = c.take<__nv_bfloat16>(pl.slots * s.d);
+  w->part_k = c.take<__nv_bfloat16>(pl.slots * s.d);
+  w->bits = c.take<uint32_t>(pl.bits_words);
+  w->off = c.take<int32_t>((size_t)kMaxUnits * (S + 1));
+  w->acc_v = c.take<float>(pl.split ? S * s.d : 0);
+  w->acc_k = c.take<float>(pl.split ? S * s.d : 0);
+  w->delta = c.take<float>(pl.dense.n ? P * S : 0);
   return c.used + 256;
 }
 
@@ -633,10 +820,19 @@ static size_t carve_bwd(void* base, const dsv_shape& s, BwdWs* w) {
 
 using namespace dsv;
 
-extern "C" size_t dsv_sparse_attn_bwd_workspace_size(dsv_shape shape, dsv_group group) {
+extern "C" size_t dsv_sparse_attn_bwd_workspace_size(dsv_shape shape, dsv_group group, const int32_t* k_per_head,
+                                                     const int64_t* idx_offset) {
   if (validate_common(shape, group, true) != DSV_OK) return 0;
+  const Geometry geo = make_geometry(shape, group);
+  const int P = (int)(shape.B * shape.H);
+  const bool any_sparse = k_per_head != nullptr;
+  if (any_sparse && !idx_offset) return 0;
+  if (any_sparse)
+    for (int i = 0; i < P; ++i)
+      if (idx_offset[i] >= 0 && (k_per_head[i] < 1 || k_per_head[i] > geo.S)) return 0;
+  const BwdPlan pl = plan_bwd(shape, geo, any_sparse, k_per_head, idx_offset);
   BwdWs w;
-  return carve_bwd(nullptr, shape, &w);
+  return carve_bwd(nullptr, shape, pl, &w);
 }
 
 extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, const void* O,
@@ -651,21 +847,16 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
   for (const void* ptr : {Q, K, V, O, dO, (const void*)dQ, (const void*)dK, (const void*)dV})
     if (!aligned(ptr, 16)) return DSV_ERR_INVALID_ARG;
   if (idx && (!k_per_head || !idx_offset || !aligned(idx, 4))) return DSV_ERR_INVALID_ARG;
-  BwdWs w;
-  const size_t need = carve_bwd(nullptr, shape, &w);
-  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DSV_ERR_WORKSPACE;
-  carve_bwd(workspace, shape, &w);
   const Geometry geo = make_geometry(shape, group);
   const int P = (int)(shape.B * shape.H), d = (int)shape.d;
-  std::vector<int> sparse, dense;
-  for (int i = 0; i < P; ++i) {
-    if (!idx || idx_offset[i] < 0) {
-      dense.push_back(i);
-    } else {
-      if (k_per_head[i] < 1 || k_per_head[i] > geo.S) return DSV_ERR_INVALID_ARG;
-      sparse.push_back(i);
-    }
-  }
+  if (idx)
+    for (int i = 0; i < P; ++i)
+      if (idx_offset[i] >= 0 && (k_per_head[i] < 1 || k_per_head[i] > geo.S)) return DSV_ERR_INVALID_ARG;
+  const BwdPlan pl = plan_bwd(shape, geo, idx != nullptr, k_per_head, idx_offset);
+  BwdWs w;
+  const size_t need = carve_bwd(nullptr, shape, pl, &w);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DSV_ERR_WORKSPACE;
+  carve_bwd(workspace, shape, pl, &w);
   AttnMaps maps;
   CUtensorMap do_cube, q_tile, do_tile;
   if (!make_attn_maps(&maps, Q, K, V, geo, d, P) || !make_cube_map(&do_cube, dO, geo, d, P) ||
@@ -686,55 +877,67 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
   prm.dO = static_cast<const __nv_bfloat16*>(dO);
   prm.LSE = LSE;
   prm.out = static_cast<__nv_bfloat16*>(dQ);
-  prm.overflow_limit = 1073741824.0f / (float)geo.n_groups;
   prm.status = dev_status;
-  auto* dKp = static_cast<__nv_bfloat16*>(dK);
-  auto* dVp = static_cast<__nv_bfloat16*>(dV);
-  const int64_t per = (int64_t)geo.S * d;
+  CscParams csc;
+  memset(&csc, 0, sizeof(csc));
+  csc.bits = w.bits;
+  csc.off = w.off;
+  csc.part_v = w.part_v;
+  csc.part_k = w.part_k;
+  csc.acc_v = w.acc_v;
+  csc.acc_k = w.acc_k;
+  csc.dK = static_cast<__nv_bfloat16*>(dK);
+  csc.dV = static_cast<__nv_bfloat16*>(dV);
 
-  // sparse problems: dQ + fixed-point dK/dV, in chunks of accumulators
-  for (size_t c0 = 0; c0 < sparse.size(); c0 += kBwdChunkProblems) {
-    ProblemTable tab;
-    memset(&tab, 0, sizeof(tab));
-    tab.n = (int)std::min<size_t>(kBwdChunkProblems, sparse.size() - c0);
+  // sparse problems: dQ + ordered dK/dV
+  for (const UnitTable& tab : pl.launches) {
+    size_t words = 0;
+    int max_ng = 1;
     for (int i = 0; i < tab.n; ++i) {
-      const int p = sparse[c0 + i];
-      tab.p[i] = p;
-      tab.k[i] = k_per_head[p];
-      tab.off[i] = idx_offset[p];
+      words += (size_t)geo.S * tab.nwords[i];
+      max_ng = std::max(max_ng, tab.ng[i]);
     }
-    const size_t bytes = (size_t)tab.n * per * sizeof(int64_t);
-    if (cudaMemsetAsync(w.acc_k, 0, bytes, st) != cudaSuccess || cudaMemsetAsync(w.acc_v, 0, bytes, st) != cudaSuccess)
-      return DSV_ERR_CUDA;
-    AttnParams pc = prm;
-    pc.dK_acc = w.acc_k;
-    pc.dV_acc = w.acc_v;
-    const cudaError_t e = d == 128 ? launch_bwd_q<128>(maps, do_cube, pc, tab, geo.n_groups, st)
-                                   : launch_bwd_q<64>(maps, do_cube, pc, tab, geo.n_groups, st);
+    if (cudaMemsetAsync(w.bits, 0, words * sizeof(uint32_t), st) != cudaSuccess) return DSV_ERR_CUDA;
+    k_sel_bitmap<<<dim3(max_ng, tab.n), 256, 0, st>>>(idx, w.bits, tab);
+    k_csc_offsets<<<tab.n, 1024, 0, st>>>(w.bits, geo.S, w.off, tab);
+    cudaError_t e = d == 128 ? launch_bwd_q<128>(maps, do_cube, prm, csc, tab, max_ng, st)
+                             : launch_bwd_q<64>(maps, do_cube, prm, csc, tab, max_ng, st);
     if (e != cudaSuccess) return DSV_ERR_CUDA;
-    k_fix_to_bf16<<<dim3(592, tab.n), 256, 0, st>>>(w.acc_k, w.acc_v, per, dKp, dVp, tab);
+    if (d == 128) k_csc_reduce<128><<<dim3((geo.S + 7) / 8, tab.n), 256, 0, st>>>(csc, geo.S, tab);
+    else k_csc_reduce<64><<<dim3((geo.S + 7) / 8, tab.n), 256, 0, st>>>(csc, geo.S, tab);
     if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
   }
   // dense problems: dQ group-major, dK/dV key-major
-  if (!dense.empty()) {
-    ProblemTable tab;
-    memset(&tab, 0, sizeof(tab));
-    tab.n = (int)dense.size();
-    for (int i = 0; i < tab.n; ++i) {
-      tab.p[i] = dense[i];
-      tab.k[i] = geo.S;
-      tab.off[i] = -1;
+  if (pl.dense.n) {
+    ProblemTable ptab;
+    memset(&ptab, 0, sizeof(ptab));
+    ptab.n = pl.dense.n;
+    for (int i = 0; i < ptab.n; ++i) {
+      ptab.p[i] = pl.dense.p[i];
+      ptab.k[i] = geo.S;
+      ptab.off[i] = -1;
     }
-    k_bwd_delta<<<dim3((geo.S + 255) / 256, tab.n), 256, 0, st>>>(prm.O, prm.dO, geo.S, d, w.delta, tab);
+    for (int c0 = 0; c0 < pl.dense.n; c0 += kMaxUnits) {
+      UnitTable dt = pl.dense;
+      dt.n = std::min(kMaxUnits, pl.dense.n - c0);
+      for (int i = 0; i < dt.n; ++i) {
+        dt.p[i] = pl.dense.p[c0 + i];
+        dt.k[i] = geo.S;
+        dt.g0[i] = 0;
+        dt.ng[i] = geo.n_groups;
+        dt.off[i] = -1;
+      }
+      CscParams none;
+      memset(&none, 0, sizeof(none));
+      cudaError_t e = d == 128 ? launch_bwd_q<128>(maps, do_cube, prm, none, dt, geo.n_groups, st)
+                               : launch_bwd_q<64>(maps, do_cube, prm, none, dt, geo.n_groups, st);
+      if (e != cudaSuccess) return DSV_ERR_CUDA;
+    }
+    k_bwd_delta<<<dim3((geo.S + 255) / 256, ptab.n), 256, 0, st>>>(prm.O, prm.dO, geo.S, d, w.delta, ptab);
     if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
-    AttnParams pd = prm;
-    pd.dK_acc = nullptr;
-    pd.dV_acc = nullptr;
-    cudaError_t e = d == 128 ? launch_bwd_q<128>(maps, do_cube, pd, tab, geo.n_groups, st)
-                             : launch_bwd_q<64>(maps, do_cube, pd, tab, geo.n_groups, st);
-    if (e == cudaSuccess)
-      e = d == 128 ? launch_bwd_kv<128>(maps, q_tile, do_tile, pd, w.delta, dKp, dVp, tab, geo.S, st)
-                   : launch_bwd_kv<64>(maps, q_tile, do_tile, pd, w.delta, dKp, dVp, tab, geo.S, st);
+    const cudaError_t e =
+        d == 128 ? launch_bwd_kv<128>(maps, q_tile, do_tile, prm, w.delta, csc.dK, csc.dV, ptab, geo.S, st)
+                 : launch_bwd_kv<64>(maps, q_tile, do_tile, prm, w.delta, csc.dK, csc.dV, ptab, geo.S, st);
     if (e != cudaSuccess) return DSV_ERR_CUDA;
   }
   return DSV_OK;

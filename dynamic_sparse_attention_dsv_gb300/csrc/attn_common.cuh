@@ -28,9 +28,6 @@ struct AttnParams {
   const float* LSE;          // bwd
   __nv_bfloat16* out;        // fwd: O; bwd: dQ
   float* lse_out;            // fwd
-  int64_t* dK_acc;           // bwd: fixed-point accumulators [P][S][d] (sparse problems)
-  int64_t* dV_acc;
-  float overflow_limit;      // bwd: |partial| bound that keeps the fixed-point sums in range
   int32_t* status;
 };
 

@@ -26,8 +26,7 @@
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*).
  *    Argument errors are returned synchronously before anything is launched.
  *    Launch failures return DSV_ERR_CUDA. Conditions found on the device
- *    (a wait that ran out, a fixed-point overflow, a candidate buffer
- *    overflow) are written to the caller's device word `dev_status`
+ *    (a wait that ran out, a candidate buffer overflow) are written to the caller's device word `dev_status`
  *    (int32, zero it before the call; libdsv only ever raises it), which the
  *    caller reads after synchronising (dsv_read_status does both).
  *  - Supported sizes: d in {64, 128}; r in {16, 32, 64}; G = gt*gy*gx in
@@ -50,7 +49,7 @@ typedef enum {
   DSV_ERR_WORKSPACE = 3,     /* workspace missing or too small */
   DSV_ERR_CUDA = 4,          /* a CUDA launch or API call failed */
   DSV_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out */
-  DSV_ERR_OVERFLOW = 6,      /* device: dK/dV fixed-point accumulator range exceeded */
+  DSV_ERR_OVERFLOW = 6,      /* reserved (no current call raises it) */
   DSV_ERR_CANDIDATES = 7     /* device: a top-k boundary bin exceeded its candidate buffer */
 } dsv_status;
 
@@ -189,12 +188,19 @@ dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const void* V, cons
  *   dQ_i = scale sum_{j in I} dS_ij k_j
  *   dK_j = scale sum over (group, query i) pairs that selected j of dS_ij q_i
  *   dV_j = sum over the same pairs of P_ij dO_i
- * dK and dV are accumulated in fixed point (int64, 2^-32 units), so the
- * result does not depend on the order of accumulation; then rounded to bf16.
- * dQ, dK, dV are fully overwritten. Device error DSV_ERR_OVERFLOW if a
- * partial sum leaves the fixed-point range (|value| >= 2^30 / n_groups).
+ * dK and dV are reduced in a fixed order: every (group, key) pair writes its
+ * bf16 partial rows to a slot ordered by (key, group), and each key's slots
+ * are summed in ascending group order in fp32, so the result does not depend
+ * on scheduling. dQ, dK, dV are fully overwritten.
+ * k_per_head, idx_offset: HOST arrays (NULL with idx NULL: every problem
+ * dense). The workspace size depends on the plan: pass the same k_per_head
+ * and idx_offset to dsv_sparse_attn_bwd_workspace_size (it holds the bf16
+ * partials of up to 8 GiB worth of (group, key) pairs at a time, a key x group
+ * selection bitmap and per-key slot offsets; a head with more pairs is split
+ * over several launches with fp32 running sums).
  * ---------------------------------------------------------------------- */
-size_t dsv_sparse_attn_bwd_workspace_size(dsv_shape shape, dsv_group group);
+size_t dsv_sparse_attn_bwd_workspace_size(dsv_shape shape, dsv_group group, const int32_t* k_per_head,
+                                          const int64_t* idx_offset);
 dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
                                const void* dO, const int32_t* idx, const int32_t* k_per_head,
                                const int64_t* idx_offset, dsv_shape shape, dsv_group group, float scale, void* dQ,

@@ -70,17 +70,28 @@ def _shape(B, H, T, Y, X, d):
     return native.dsv_shape(B, H, T, Y, X, d)
 
 
-def test_workspace_is_linear_in_S_not_quadratic(lib):
+def test_workspace_is_order_S_k_not_S_squared(lib):
+    """At a fixed k, scratch bytes per token stay bounded as S grows 8x (an
+    S x S term would grow 8x); the backward's grows with k as O(S k)."""
     g = native.dsv_group(2, 8, 8)
     sizes = []
     for T in (8, 16, 32, 64):
         s = _shape(1, 1, T, 64, 64, 128)
+        k = (ctypes.c_int32 * 1)(2048)
+        off = (ctypes.c_int64 * 1)(0)
         sizes.append(lib.dsv_lowrank_topk_workspace_size(s, 32, g) + lib.dsv_coverage_workspace_size(s, 32, g) +
-                     lib.dsv_sparse_attn_bwd_workspace_size(s, g))
+                     lib.dsv_sparse_attn_bwd_workspace_size(s, g, k, off))
     S = np.array([8, 16, 32, 64]) * 4096
     ratio = np.array(sizes) / S
-    # bytes per token stay bounded as S grows 8x (an S^2 term would grow 8x)
-    assert ratio.max() / ratio.min() < 1.5, ratio
+    assert ratio.max() / ratio.min() < 1.6, ratio
+    # backward scratch: O(n_groups * k) partial rows
+    s = _shape(1, 1, 16, 64, 64, 128)
+    small = lib.dsv_sparse_attn_bwd_workspace_size(s, g, (ctypes.c_int32 * 1)(1000), (ctypes.c_int64 * 1)(0))
+    big = lib.dsv_sparse_attn_bwd_workspace_size(s, g, (ctypes.c_int32 * 1)(4000), (ctypes.c_int64 * 1)(0))
+    n_groups = 16 * 64 * 64 // 128
+    assert big - small >= n_groups * 3000 * 128 * 4 * 0.99
+    # dense-only problems need almost nothing
+    assert lib.dsv_sparse_attn_bwd_workspace_size(s, g, None, None) < 64 << 20
 
 
 def test_argument_validation_before_launch(lib):
