@@ -29,7 +29,8 @@
 
 namespace dsv {
 
-constexpr int kBwdThreads = 192;
+constexpr int kBwdThreads = 192;                       // key-major kernel
+constexpr int kBwdQThreads = 32 * (5 + kGatherWarps);   // group-major kernel
 constexpr int kMaxUnits = 48;                       // work units per group-major launch
 constexpr size_t kPartialBudget = 8ull << 30;       // bytes of bf16 dK/dV partials in flight
 
@@ -84,7 +85,7 @@ __device__ __forceinline__ void st_sw128_chunk(uint8_t* tile, int row, int chunk
 
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kBwdQThreads, 1)
     k_attn_bwd_q(const __grid_constant__ AttnMaps maps, const __grid_constant__ CUtensorMap do_cube,
                  const AttnParams prm, const CscParams csc, const UnitTable tab) {
   using C = BwdCfg<D>;
@@ -128,15 +129,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     fence_proxy_async_smem();
   }
-  if (warp == 5) {
+  constexpr int kMmaWarp = 4 + kGatherWarps;
+  if (warp == kMmaWarp) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
   if (tid == 0) {
     mbar_init(q_full, 1);
+    const uint32_t fills = dense ? 1u : 32u * kGatherWarps;   // TMA tx arrival, or one per gathering lane
     for (int i = 0; i < 2; ++i) {
-      mbar_init(k_full + i, 1);
-      mbar_init(v_full + i, 1);
+      mbar_init(k_full + i, fills);
+      mbar_init(v_full + i, fills);
       mbar_init(kv_empty + i, 1);
     }
     mbar_init(sdp_full, 1);
@@ -150,10 +153,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp == 4) {
-    // ---------------------------------------------------------------- TMA
+  if (warp >= 4 && warp < kMmaWarp) {
+    // ----------------------------------------------------------- producers
+    const int pw = warp - 4;
     const int ct = g / (geo.ncy * geo.ncx), cy = (g / geo.ncx) % geo.ncy, cx = g % geo.ncx;
-    if (lane == 0) {
+    if (pw == 0 && lane == 0) {
       mbar_arrive_expect_tx(q_full, 2 * G * D * 2);
       for (int a = 0; a < D / 64; ++a) {
         tma_load_4d(sQ + a * 16384, &maps.q_cube, q_full, a * 64, cx * geo.gx, cy * geo.gy, p * geo.T + ct * geo.gt);
@@ -161,20 +165,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     const int prow0 = p * geo.S;
-    for (int t = 0; t < nt; ++t) {
-      const int s = t % C::kStages;
-      if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, kWaitLimitNs)) {
-        if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
-        break;
+    if (idx_row) {
+      int rows[Gather<D>::kIters], nxt[Gather<D>::kIters];
+      gather_rows<D>(nxt, idx_row, k, 0, prow0, pw, lane);
+      for (int t = 0; t < nt; ++t) {
+        const int s = t % C::kStages;
+#pragma unroll
+        for (int i = 0; i < Gather<D>::kIters; ++i) rows[i] = nxt[i];
+        if (t + 1 < nt) gather_rows<D>(nxt, idx_row, k, t + 1, prow0, pw, lane);
+        if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, kWaitLimitNs)) {
+          if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
+          break;
+        }
+        gather_tile<D>(sK + s * C::kTile, prm.K, rows, pw, lane);
+        cp_async_arrive_noinc(k_full + s);
+        gather_tile<D>(sV + s * C::kTile, prm.V, rows, pw, lane);
+        cp_async_arrive_noinc(v_full + s);
       }
-      if (lane == 0) mbar_arrive_expect_tx(k_full + s, C::kTile);
-      __syncwarp();
-      load_kv_tile<D>(sK + s * C::kTile, &maps.k_rows, &maps.k_tile, k_full + s, idx_row, k, t, prow0, lane);
-      if (lane == 0) mbar_arrive_expect_tx(v_full + s, C::kTile);
-      __syncwarp();
-      load_kv_tile<D>(sV + s * C::kTile, &maps.v_rows, &maps.v_tile, v_full + s, idx_row, k, t, prow0, lane);
+    } else if (pw == 0) {
+      for (int t = 0; t < nt; ++t) {
+        const int s = t % C::kStages;
+        if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, kWaitLimitNs)) {
+          if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(k_full + s, C::kTile);
+          load_dense_tile<D>(sK + s * C::kTile, &maps.k_tile, k_full + s, t, prow0);
+          mbar_arrive_expect_tx(v_full + s, C::kTile);
+          load_dense_tile<D>(sV + s * C::kTile, &maps.v_tile, v_full + s, t, prow0);
+        }
+      }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t id_sdp = instr_desc(128, 128, 1, 0, 0);   // Q K^T, dO V^T
@@ -190,6 +213,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = false;
           break;
         }
+        fence_proxy_async_smem();   // rows written by cp.async (generic proxy) -> tensor core reads
         tc_fence_after();
         const uint32_t ak = smem_u32(sK + s * C::kTile), av = smem_u32(sV + s * C::kTile);
 #pragma unroll
@@ -362,7 +386,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) tmem_dealloc(tbase, 512);
+  if (warp == kMmaWarp) tmem_dealloc(tbase, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -691,7 +715,7 @@ __global__ void __launch_bounds__(256) k_csc_reduce(const CscParams csc, int S, 
 template <int D>
 static cudaError_t launch_bwd_q(const AttnMaps& maps, const CUtensorMap& do_cube, const AttnParams& prm,
                                 const CscParams& csc, const UnitTable& tab, int max_ng, cudaStream_t st) {
-  k_attn_bwd_q<D><<<dim3(max_ng, tab.n), kBwdThreads, BwdCfg<D>::kSmem, st>>>(maps, do_cube, prm, csc, tab);
+  k_attn_bwd_q<D><<<dim3(max_ng, tab.n), kBwdQThreads, BwdCfg<D>::kSmem, st>>>(maps, do_cube, prm, csc, tab);
   return cudaGetLastError();
 }
 
@@ -873,6 +897,8 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
   prm.scale = scale;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.idx = idx;
+  prm.K = static_cast<const __nv_bfloat16*>(K);
+  prm.V = static_cast<const __nv_bfloat16*>(V);
   prm.O = static_cast<const __nv_bfloat16*>(O);
   prm.dO = static_cast<const __nv_bfloat16*>(dO);
   prm.LSE = LSE;

@@ -55,30 +55,55 @@ inline bool make_attn_maps(AttnMaps* m, const void* Q, const void* K, const void
          make_map_2d(&m->v_tile, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, rows, 64, 128);
 }
 
-// Issues the loads of one 128-row key (or value) tile into `dst` (K-major,
-// 128-byte swizzle, d/64 atoms of 16 KB). Called by all 32 lanes of a warp;
-// lane 0 has already posted the expected byte count on `bar`.
-// Sparse: rows idx_row[t*128 + i] (padded with the row's last key past k).
-// Dense: rows t*128 .. t*128+127.
+// ---------------------------------------------------------------------------
+// Row gather of selected K/V rows with cp.async by kGatherWarps producer
+// warps. A warp instruction copies whole rows (d*2 bytes = d/8 16-byte
+// chunks, consecutive lanes on consecutive chunks) into the K-major 128-byte
+// swizzled tile layout the tensor cores read. Per tile and tensor each lane
+// copies kGatherIters chunks.
+constexpr int kGatherWarps = 2;
+
 template <int D>
-__device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* rows_map, const CUtensorMap* tile_map,
-                                             uint64_t* bar, const int32_t* idx_row, int k, int t, int prow0,
-                                             int lane) {
-  constexpr int kAtoms = D / 64;
-  if (idx_row) {
-    int r[4];
+struct Gather {
+  static constexpr int kChunksPerRow = D / 8;                      // 16-byte chunks per row
+  static constexpr int kRowsPerInstr = 32 / kChunksPerRow;         // rows per warp instruction
+  static constexpr int kRowsPerWarp = 128 / kGatherWarps;
+  static constexpr int kIters = kRowsPerWarp / kRowsPerInstr;      // instructions per lane per tensor
+};
+
+// Key rows (absolute row in the [P*S][d] tensor) this lane copies for tile t.
+// Slots past k repeat the row's last key, so every copied row is a real key.
+template <int D>
+__device__ __forceinline__ void gather_rows(int (&rows)[Gather<D>::kIters], const int32_t* idx_row, int k, int t,
+                                            int prow0, int pw, int lane) {
+  using Gt = Gather<D>;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int j = t * 128 + lane * 4 + i;
-      r[i] = prow0 + __ldg(idx_row + (j < k ? j : k - 1));
-    }
-#pragma unroll
-    for (int a = 0; a < kAtoms; ++a)
-      tma_gather4(dst + a * 16384 + lane * 512, rows_map, bar, a * 64, r[0], r[1], r[2], r[3]);
-  } else if (lane == 0) {
-#pragma unroll
-    for (int a = 0; a < kAtoms; ++a) tma_load_2d(dst + a * 16384, tile_map, bar, a * 64, prow0 + t * 128);
+  for (int i = 0; i < Gt::kIters; ++i) {
+    const int slot = t * 128 + pw * Gt::kRowsPerWarp + i * Gt::kRowsPerInstr + lane / Gt::kChunksPerRow;
+    rows[i] = prow0 + __ldg(idx_row + (slot < k ? slot : k - 1));
   }
+}
+
+template <int D>
+__device__ __forceinline__ void gather_tile(uint8_t* dst, const __nv_bfloat16* src, const int (&rows)[Gather<D>::kIters],
+                                            int pw, int lane) {
+  using Gt = Gather<D>;
+  const int chunk = lane % Gt::kChunksPerRow;
+  const uint32_t base = smem_u32(dst) + (chunk >> 3) * 16384;
+#pragma unroll
+  for (int i = 0; i < Gt::kIters; ++i) {
+    const int row = pw * Gt::kRowsPerWarp + i * Gt::kRowsPerInstr + lane / Gt::kChunksPerRow;
+    cp_async_16(base + row * 128 + (((chunk & 7) ^ (row & 7)) << 4), src + (int64_t)rows[i] * D + chunk * 8);
+  }
+}
+
+// Dense tiles (rows t*128 .. t*128+127 of the problem) by one TMA box per
+// 64-column atom, issued by one thread that has posted the byte count.
+template <int D>
+__device__ __forceinline__ void load_dense_tile(uint8_t* dst, const CUtensorMap* tile_map, uint64_t* bar, int t,
+                                                int prow0) {
+#pragma unroll
+  for (int a = 0; a < D / 64; ++a) tma_load_2d(dst + a * 16384, tile_map, bar, a * 64, prow0 + t * 128);
 }
 
 }  // namespace dsv

@@ -18,14 +18,15 @@
 // log2 units, which bounds P by 2^8), so O is rescaled rarely.
 //
 // Warps 0-3: softmax and epilogue (thread = query row = TMEM lane).
-// Warp 4: TMA producer (all lanes issue row gathers). Warp 5: MMA issuer.
+// Warps 4-5: producers (cp.async row gather of the selected K/V rows; TMA
+// boxes for dense tiles and the query cube). Warp 6: MMA issuer.
 #include "attn_common.cuh"
 
 namespace dsv {
 
 template <int D>
 struct FwdCfg {
-  static constexpr int kStages = D == 128 ? 2 : 3;
+  static constexpr int kStages = D == 128 ? 3 : 4;
   static constexpr int kTile = 128 * D * 2;            // bytes of one 128-row bf16 tile
   static constexpr int kOffK = kTile;                  // Q first
   static constexpr int kOffV = kOffK + kStages * kTile;
@@ -33,13 +34,13 @@ struct FwdCfg {
   static constexpr int kSmemUsed = kOffBar + 256 + 1024;
   // at least half the SM's shared memory, so one CTA owns the SM's TMEM
   static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 32 * (5 + kGatherWarps);
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;               // S buffers at 0 and 128
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     k_attn_fwd(const __grid_constant__ AttnMaps maps, const AttnParams prm, const ProblemTable tab) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -49,13 +50,13 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sV = sm + C::kOffV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;                  // [kStages]
-  uint64_t* v_full = bars + 4;                  // [kStages]
-  uint64_t* kv_empty = bars + 7;                // [kStages]
-  uint64_t* s_full = bars + 10;                 // [2]
-  uint64_t* p_full = bars + 12;                 // [2]
-  uint64_t* o_ready = bars + 14;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* k_full = bars + 1;                  // [kStages <= 4]
+  uint64_t* v_full = bars + 5;                  // [kStages]
+  uint64_t* kv_empty = bars + 9;                // [kStages]
+  uint64_t* s_full = bars + 13;                 // [2]
+  uint64_t* p_full = bars + 15;                 // [2]
+  uint64_t* o_ready = bars + 17;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 18);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x, lp = blockIdx.y;
@@ -75,15 +76,17 @@ __global__ void __launch_bounds__(192, 1)
     }
     fence_proxy_async_smem();
   }
-  if (warp == 5) {
+  constexpr int kMmaWarp = 4 + kGatherWarps;
+  if (warp == kMmaWarp) {
     tmem_alloc(tslot, C::kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
     mbar_init(q_full, 1);
+    const uint32_t fills = dense ? 1u : 32u * kGatherWarps;   // TMA tx arrival, or one per gathering lane
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(k_full + i, 1);
-      mbar_init(v_full + i, 1);
+      mbar_init(k_full + i, fills);
+      mbar_init(v_full + i, fills);
       mbar_init(kv_empty + i, 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -98,30 +101,50 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp == 4) {
-    // ---------------------------------------------------------------- TMA
+  if (warp >= 4 && warp < kMmaWarp) {
+    // ----------------------------------------------------------- producers
+    const int pw = warp - 4;
     const int ct = g / (geo.ncy * geo.ncx), cy = (g / geo.ncx) % geo.ncy, cx = g % geo.ncx;
-    if (lane == 0) {
+    if (pw == 0 && lane == 0) {
       prefetch_tmap(&maps.q_cube);
       mbar_arrive_expect_tx(q_full, G * D * 2);
       for (int a = 0; a < D / 64; ++a)
         tma_load_4d(sQ + a * 16384, &maps.q_cube, q_full, a * 64, cx * geo.gx, cy * geo.gy, p * geo.T + ct * geo.gt);
     }
     const int prow0 = p * geo.S;
-    for (int t = 0; t < nt; ++t) {
-      const int s = t % C::kStages;
-      if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, kWaitLimitNs)) {
-        if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
-        break;
+    if (idx_row) {
+      int rows[Gather<D>::kIters], nxt[Gather<D>::kIters];
+      gather_rows<D>(nxt, idx_row, k, 0, prow0, pw, lane);
+      for (int t = 0; t < nt; ++t) {
+        const int s = t % C::kStages;
+#pragma unroll
+        for (int i = 0; i < Gather<D>::kIters; ++i) rows[i] = nxt[i];
+        if (t + 1 < nt) gather_rows<D>(nxt, idx_row, k, t + 1, prow0, pw, lane);
+        if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, kWaitLimitNs)) {
+          if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
+          break;
+        }
+        gather_tile<D>(sK + s * C::kTile, prm.K, rows, pw, lane);
+        cp_async_arrive_noinc(k_full + s);
+        gather_tile<D>(sV + s * C::kTile, prm.V, rows, pw, lane);
+        cp_async_arrive_noinc(v_full + s);
       }
-      if (lane == 0) mbar_arrive_expect_tx(k_full + s, C::kTile);
-      __syncwarp();
-      load_kv_tile<D>(sK + s * C::kTile, &maps.k_rows, &maps.k_tile, k_full + s, idx_row, k, t, prow0, lane);
-      if (lane == 0) mbar_arrive_expect_tx(v_full + s, C::kTile);
-      __syncwarp();
-      load_kv_tile<D>(sV + s * C::kTile, &maps.v_rows, &maps.v_tile, v_full + s, idx_row, k, t, prow0, lane);
+    } else if (pw == 0) {
+      for (int t = 0; t < nt; ++t) {
+        const int s = t % C::kStages;
+        if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, kWaitLimitNs)) {
+          if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(k_full + s, C::kTile);
+          load_dense_tile<D>(sK + s * C::kTile, &maps.k_tile, k_full + s, t, prow0);
+          mbar_arrive_expect_tx(v_full + s, C::kTile);
+          load_dense_tile<D>(sV + s * C::kTile, &maps.v_tile, v_full + s, t, prow0);
+        }
+      }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t idesc_qk = instr_desc(128, 128, 1, 0, 0);
@@ -132,6 +155,7 @@ __global__ void __launch_bounds__(192, 1)
         const int s = t % C::kStages, b = t & 1;
         if (!mbar_wait(p_full + b, (t >> 1) & 1, kWaitLimitNs)) return false;
         if (!mbar_wait(v_full + s, (t / C::kStages) & 1, kWaitLimitNs)) return false;
+        fence_proxy_async_smem();   // rows written by cp.async (generic proxy) -> tensor core reads
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sV + s * C::kTile);
 #pragma unroll
@@ -146,6 +170,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int t = 0; ok && t < nt; ++t) {
         const int s = t % C::kStages, b = t & 1;
         if (!mbar_wait(k_full + s, (t / C::kStages) & 1, kWaitLimitNs)) { ok = false; break; }
+        fence_proxy_async_smem();
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sK + s * C::kTile);
 #pragma unroll
@@ -268,7 +293,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) tmem_dealloc(tbase, C::kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tbase, C::kTmemCols);
 }
 
 template <int D>
@@ -329,6 +354,8 @@ extern "C" dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const vo
   prm.scale = scale;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.idx = idx;
+  prm.K = static_cast<const __nv_bfloat16*>(K);
+  prm.V = static_cast<const __nv_bfloat16*>(V);
   prm.out = static_cast<__nv_bfloat16*>(O);
   prm.lse_out = LSE;
   prm.status = dev_status;

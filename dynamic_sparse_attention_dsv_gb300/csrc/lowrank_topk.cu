@@ -557,43 +557,58 @@ __global__ void k_fill_all(int32_t* idx, int64_t off, int S, int64_t total) {
 }
 
 // ---------------------------------------------------------------------------
-// Coverage reduce: per problem, merge chunk partials, then binary search k.
-__global__ void __launch_bounds__(1024) k_cov_reduce(const uint32_t* __restrict__ cnt, const float* __restrict__ mass,
-                                                     const uint32_t* mmax, const uint32_t* mmin, int nb, int n_chunks,
-                                                     int g_pad, int n_groups, int S, float scale, float target,
-                                                     int32_t* cum_cnt, double* cum_mass, float* width,
-                                                     int32_t* k_cov, float* curve, int n_curve,
+// Coverage reduce, in three steps:
+//   k_cov_merge   (group, bin) totals over key chunks, one thread per pair
+//   k_cov_scan    per group: cumulative counts and normalised masses over bins
+//   k_cov_search  per problem: binary search of the smallest k with C(k) >= mass
+__global__ void k_cov_merge(const uint32_t* __restrict__ cnt, const float* __restrict__ mass, int nb, int n_chunks,
+                            int g_pad, int n_groups, int32_t* cum_cnt, double* cum_mass) {
+  const int lp = blockIdx.z, b = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n_groups) return;
+  int c = 0;
+  double m = 0.0;
+  for (int ch = 0; ch < n_chunks; ++ch) {
+    const size_t o = (((size_t)lp * n_chunks + ch) * nb + b) * g_pad + g;
+    c += (int)cnt[o];
+    m += (double)mass[o];
+  }
+  const size_t rid = (size_t)lp * g_pad + g;
+  cum_cnt[rid * nb + b] = c;
+  cum_mass[rid * nb + b] = m;
+}
+
+__global__ void k_cov_scan(const uint32_t* mmax, const uint32_t* mmin, int nb, int g_pad, int n_groups, float scale,
+                           int32_t* cum_cnt, double* cum_mass, float* width) {
+  const int lp = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n_groups) return;
+  const size_t rid = (size_t)lp * g_pad + g;
+  int32_t* cc = cum_cnt + rid * nb;
+  double* cm = cum_mass + rid * nb;
+  int c_acc = 0;
+  double m_acc = 0.0;
+  for (int b = 0; b < nb; ++b) {
+    c_acc += cc[b];
+    m_acc += cm[b];
+    cc[b] = c_acc;
+    cm[b] = m_acc;
+  }
+  const double inv = m_acc > 0.0 ? 1.0 / m_acc : 0.0;
+  for (int b = 0; b < nb; ++b) cm[b] *= inv;
+  width[rid] = scale * (ord2f(mmax[rid]) - ord2f(mmin[rid])) / (float)nb;
+}
+
+__global__ void __launch_bounds__(1024) k_cov_search(int nb, int g_pad, int n_groups, int S, float target,
+                                                     const int32_t* cum_cnt, const double* cum_mass,
+                                                     const float* width, int32_t* k_cov, float* curve, int n_curve,
                                                      const ProblemTable tab) {
   const int lp = blockIdx.x, tid = threadIdx.x;
   __shared__ double red[32];
-  // stage 1: per group cumulative counts and normalised masses, top bin first
-  for (int g = tid; g < n_groups; g += blockDim.x) {
-    const int rid = lp * g_pad + g;
-    int c_acc = 0;
-    double m_acc = 0.0;
-    for (int b = 0; b < nb; ++b) {
-      int c = 0;
-      double m = 0.0;
-      for (int ch = 0; ch < n_chunks; ++ch) {
-        const size_t o = (((size_t)lp * n_chunks + ch) * nb + b) * g_pad + g;
-        c += (int)cnt[o];
-        m += (double)mass[o];
-      }
-      c_acc += c;
-      m_acc += m;
-      cum_cnt[(size_t)rid * nb + b] = c_acc;
-      cum_mass[(size_t)rid * nb + b] = m_acc;
-    }
-    for (int b = 0; b < nb; ++b) cum_mass[(size_t)rid * nb + b] /= m_acc;
-    width[rid] = scale * (ord2f(mmax[rid]) - ord2f(mmin[rid])) / (float)nb;
-  }
-  __syncthreads();
   auto C_of = [&](int k) -> double {
     double acc = 0.0;
     for (int g = tid; g < n_groups; g += blockDim.x) {
-      const int rid = lp * g_pad + g;
-      const int32_t* cc = cum_cnt + (size_t)rid * nb;
-      const double* cm = cum_mass + (size_t)rid * nb;
+      const size_t rid = (size_t)lp * g_pad + g;
+      const int32_t* cc = cum_cnt + rid * nb;
+      const double* cm = cum_mass + rid * nb;
       int lo = 0, hi = nb - 1;  // first bin with cumulative count >= k
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
@@ -928,9 +943,13 @@ extern "C" dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_
     if (cudaMemsetAsync(w.mmin, 0xFF, rows * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
     if (select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
     if (select_pass<kCov>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
-    k_cov_reduce<<<n, 1024, 0, st>>>(w.hist, w.mass, w.mmax, w.mmin, pl.cov_bins, n_chunks, pl.g_pad,
-                                     pl.geo.n_groups, pl.geo.S, scale, mass, w.cum_cnt, w.cum_mass, w.width, k_cov,
-                                     curve, n_curve, tab);
+    const int gb = (pl.geo.n_groups + 127) / 128;
+    k_cov_merge<<<dim3(gb, pl.cov_bins, n), 128, 0, st>>>(w.hist, w.mass, pl.cov_bins, n_chunks, pl.g_pad,
+                                                           pl.geo.n_groups, w.cum_cnt, w.cum_mass);
+    k_cov_scan<<<dim3(gb, n), 128, 0, st>>>(w.mmax, w.mmin, pl.cov_bins, pl.g_pad, pl.geo.n_groups, scale,
+                                            w.cum_cnt, w.cum_mass, w.width);
+    k_cov_search<<<n, 1024, 0, st>>>(pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.geo.S, mass, w.cum_cnt, w.cum_mass,
+                                     w.width, k_cov, curve, n_curve, tab);
     if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
   }
   return DSV_OK;
