@@ -30,7 +30,7 @@
 namespace dsv {
 
 constexpr int kBwdThreads = 192;                       // key-major kernel
-constexpr int kBwdQThreads = 32 * (5 + kGatherWarps);   // group-major kernel
+constexpr int kBwdQThreads = 32 * (9 + kGatherWarps);   // group-major kernel
 constexpr int kMaxUnits = 48;                       // work units per group-major launch
 constexpr size_t kPartialBudget = 8ull << 30;       // bytes of bf16 dK/dV partials in flight
 
@@ -63,16 +63,22 @@ struct CscParams {
 template <int D>
 struct BwdCfg {
   static constexpr int kTile = 128 * D * 2;      // one [128][D] bf16 tile
-  static constexpr int kStages = D == 128 ? 1 : 2;
+  static constexpr int kKStages = 2;
+  static constexpr int kVStages = D == 128 ? 1 : 2;
+  static constexpr int kHalves = D / 64;         // dV/dK are produced 64 columns at a time
   static constexpr int kOffDO = kTile;           // Q at 0
   static constexpr int kOffK = 2 * kTile;
-  static constexpr int kOffV = kOffK + kStages * kTile;
-  static constexpr int kOffP = kOffV + kStages * kTile;   // [128 q][128 keys] bf16 = 32 KB
+  static constexpr int kOffV = kOffK + kKStages * kTile;
+  static constexpr int kOffP = kOffV + kVStages * kTile;  // [128 q][128 keys] bf16 = 32 KB
   static constexpr int kOffDS = kOffP + 32768;
   static constexpr int kOffBar = kOffDS + 32768;
   static constexpr int kSmemUsed = kOffBar + 1024 + 1024;
   static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
+  // TMEM columns: S, dP, dQ accumulator, then one 64-column half of dV and of dK
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDV = 256 + D, kColDK = 320 + D;
 };
+static_assert(BwdCfg<128>::kSmemUsed <= 232448, "group-major backward exceeds shared memory");
+static_assert(BwdCfg<128>::kColDK + 64 <= 512 && BwdCfg<64>::kColDK + 64 <= 512, "TMEM budget");
 
 __device__ __forceinline__ void compute_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -84,6 +90,13 @@ __device__ __forceinline__ void st_sw128_chunk(uint8_t* tile, int row, int chunk
 }
 
 // ---------------------------------------------------------------------------
+// Group-major backward. Warps 0-3 turn S, dP into P, dS (shared memory);
+// warps 4-7 drain the dV/dK partial halves to their slots and write dQ at
+// the end; warps 8-9 load (cp.async row gather or TMA boxes); warp 10 issues
+// the MMAs. Per 128-key tile t:
+//   S, dP (TMEM) -> P, dS (smem) -> dQ += dS K; then for each 64-column half
+//   h: dV_h = P^T dO_h, dK_h = dS^T Q_h into one TMEM half-region, drained
+//   while the next tile's S, dP are computed.
 template <int D>
 __global__ void __launch_bounds__(kBwdQThreads, 1)
     k_attn_bwd_q(const __grid_constant__ AttnMaps maps, const __grid_constant__ CUtensorMap do_cube,
@@ -100,26 +113,29 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;       // [2]
-  uint64_t* v_full = bars + 3;       // [2]
-  uint64_t* kv_empty = bars + 5;     // [2]
-  uint64_t* sdp_full = bars + 7;
-  uint64_t* ps_full = bars + 8;
-  uint64_t* part_full = bars + 9;
-  uint64_t* part_empty = bars + 10;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* k_empty = bars + 3;      // [2]
+  uint64_t* v_full = bars + 5;       // [2]
+  uint64_t* v_empty = bars + 7;      // [2]
+  uint64_t* sdp_full = bars + 9;
+  uint64_t* ps_full = bars + 10;
+  uint64_t* p_free = bars + 11;
+  uint64_t* part_full = bars + 12;
+  uint64_t* part_free = bars + 13;
+  uint64_t* dq_done = bars + 14;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int u = blockIdx.y;
   if ((int)blockIdx.x >= tab.ng[u]) return;   // units of a launch may hold fewer groups than the grid
-  const int g = tab.g0[u] + blockIdx.x, p = tab.p[u], lp = u;
+  const int g = tab.g0[u] + blockIdx.x, p = tab.p[u];
   const Geometry& geo = prm.geo;
-  const bool dense = (prm.idx == nullptr) || (tab.off[lp] < 0);
+  const bool dense = (prm.idx == nullptr) || (tab.off[u] < 0);
   const bool partials = !dense && csc.part_v != nullptr;
-  const int k = dense ? geo.S : tab.k[lp];
+  const int k = dense ? geo.S : tab.k[u];
   const int nt = (k + 127) / 128;
-  const int32_t* idx_row = dense ? nullptr : prm.idx + tab.off[lp] + (int64_t)g * k;
+  const int32_t* idx_row = dense ? nullptr : prm.idx + tab.off[u] + (int64_t)g * k;
   const int G = geo.G;
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  constexpr int kProdWarp = 8, kMmaWarp = 8 + kGatherWarps;
 
   if (G < 128) {
     for (int i = tid; i < (128 - G) * (D / 64) * 8; i += blockDim.x) {
@@ -129,7 +145,6 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     }
     fence_proxy_async_smem();
   }
-  constexpr int kMmaWarp = 4 + kGatherWarps;
   if (warp == kMmaWarp) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
@@ -140,12 +155,15 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(k_full + i, fills);
       mbar_init(v_full + i, fills);
-      mbar_init(kv_empty + i, 1);
+      mbar_init(k_empty + i, 1);
+      mbar_init(v_empty + i, 1);
     }
     mbar_init(sdp_full, 1);
     mbar_init(ps_full, 4);
+    mbar_init(p_free, 1);
     mbar_init(part_full, 1);
-    mbar_init(part_empty, 4);
+    mbar_init(part_free, 4);
+    mbar_init(dq_done, 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -153,9 +171,9 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp >= 4 && warp < kMmaWarp) {
+  if (warp >= kProdWarp && warp < kMmaWarp) {
     // ----------------------------------------------------------- producers
-    const int pw = warp - 4;
+    const int pw = warp - kProdWarp;
     const int ct = g / (geo.ncy * geo.ncx), cy = (g / geo.ncx) % geo.ncy, cx = g % geo.ncx;
     if (pw == 0 && lane == 0) {
       mbar_arrive_expect_tx(q_full, 2 * G * D * 2);
@@ -165,36 +183,36 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       }
     }
     const int prow0 = p * geo.S;
-    if (idx_row) {
-      int rows[Gather<D>::kIters], nxt[Gather<D>::kIters];
-      gather_rows<D>(nxt, idx_row, k, 0, prow0, pw, lane);
-      for (int t = 0; t < nt; ++t) {
-        const int s = t % C::kStages;
+    int rows[Gather<D>::kIters], nxt[Gather<D>::kIters];
+    if (idx_row) gather_rows<D>(nxt, idx_row, k, 0, prow0, pw, lane);
+    for (int t = 0; t < nt; ++t) {
+      const int ks = t % C::kKStages, vs = t % C::kVStages;
+      if (idx_row) {
 #pragma unroll
         for (int i = 0; i < Gather<D>::kIters; ++i) rows[i] = nxt[i];
         if (t + 1 < nt) gather_rows<D>(nxt, idx_row, k, t + 1, prow0, pw, lane);
-        if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, kWaitLimitNs)) {
-          if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
-          break;
-        }
-        gather_tile<D>(sK + s * C::kTile, prm.K, rows, pw, lane);
-        cp_async_arrive_noinc(k_full + s);
-        gather_tile<D>(sV + s * C::kTile, prm.V, rows, pw, lane);
-        cp_async_arrive_noinc(v_full + s);
       }
-    } else if (pw == 0) {
-      for (int t = 0; t < nt; ++t) {
-        const int s = t % C::kStages;
-        if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, kWaitLimitNs)) {
-          if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
-          break;
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(k_full + s, C::kTile);
-          load_dense_tile<D>(sK + s * C::kTile, &maps.k_tile, k_full + s, t, prow0);
-          mbar_arrive_expect_tx(v_full + s, C::kTile);
-          load_dense_tile<D>(sV + s * C::kTile, &maps.v_tile, v_full + s, t, prow0);
-        }
+      if (t >= C::kKStages && !mbar_wait_warp(k_empty + ks, ((t / C::kKStages) - 1) & 1, kWaitLimitNs)) {
+        if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
+        break;
+      }
+      if (idx_row) {
+        gather_tile<D>(sK + ks * C::kTile, prm.K, rows, pw, lane);
+        cp_async_arrive_noinc(k_full + ks);
+      } else if (pw == 0 && lane == 0) {
+        mbar_arrive_expect_tx(k_full + ks, C::kTile);
+        load_dense_tile<D>(sK + ks * C::kTile, &maps.k_tile, k_full + ks, t, prow0);
+      }
+      if (t >= C::kVStages && !mbar_wait_warp(v_empty + vs, ((t / C::kVStages) - 1) & 1, kWaitLimitNs)) {
+        if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
+        break;
+      }
+      if (idx_row) {
+        gather_tile<D>(sV + vs * C::kTile, prm.V, rows, pw, lane);
+        cp_async_arrive_noinc(v_full + vs);
+      } else if (pw == 0 && lane == 0) {
+        mbar_arrive_expect_tx(v_full + vs, C::kTile);
+        load_dense_tile<D>(sV + vs * C::kTile, &maps.v_tile, v_full + vs, t, prow0);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -202,68 +220,83 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_sdp = instr_desc(128, 128, 1, 0, 0);   // Q K^T, dO V^T
       constexpr uint32_t id_dq = instr_desc(128, D, 1, 0, 1);      // dS K (B = K, MN-major)
-      constexpr uint32_t id_kv = instr_desc(128, D, 1, 1, 1);      // P^T dO, dS^T Q (A, B MN-major)
+      constexpr uint32_t id_kv = instr_desc(128, 64, 1, 1, 1);     // P^T dO_h, dS^T Q_h (A, B MN-major)
       const uint32_t aq = smem_u32(sQ), ado = smem_u32(sDO), ap = smem_u32(sP), ads = smem_u32(sDS);
       bool ok = mbar_wait(q_full, 0, kWaitLimitNs);
-      for (int t = 0; ok && t < nt; ++t) {
-        const int s = t % C::kStages;
-        if (!mbar_wait(k_full + s, (t / C::kStages) & 1, kWaitLimitNs) ||
-            !mbar_wait(v_full + s, (t / C::kStages) & 1, kWaitLimitNs) ||
-            (t >= 1 && !mbar_wait(part_empty, (t - 1) & 1, kWaitLimitNs))) {
-          ok = false;
-          break;
-        }
+      auto issue_sdp = [&](int t) -> bool {
+        const int ks = t % C::kKStages, vs = t % C::kVStages;
+        if (!mbar_wait(k_full + ks, (t / C::kKStages) & 1, kWaitLimitNs) ||
+            !mbar_wait(v_full + vs, (t / C::kVStages) & 1, kWaitLimitNs))
+          return false;
         fence_proxy_async_smem();   // rows written by cp.async (generic proxy) -> tensor core reads
         tc_fence_after();
-        const uint32_t ak = smem_u32(sK + s * C::kTile), av = smem_u32(sV + s * C::kTile);
+        const uint32_t ak = smem_u32(sK + ks * C::kTile), av = smem_u32(sV + vs * C::kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tbase + kColS, smem_desc(aq + off, 16, 1024), smem_desc(ak + off, 16, 1024), id_sdp, kk > 0);
+          mma_f16_ss(tbase + C::kColS, smem_desc(aq + off, 16, 1024), smem_desc(ak + off, 16, 1024), id_sdp, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tbase + kColDP, smem_desc(ado + off, 16, 1024), smem_desc(av + off, 16, 1024), id_sdp,
+          mma_f16_ss(tbase + C::kColDP, smem_desc(ado + off, 16, 1024), smem_desc(av + off, 16, 1024), id_sdp,
                      kk > 0);
         }
         mma_commit(sdp_full);
+        mma_commit(v_empty + vs);
+        return true;
+      };
+      int job = 0;   // dV/dK half-jobs issued so far
+      auto issue_half = [&](int h) -> bool {
+        if (job >= 1 && !mbar_wait(part_free, (job - 1) & 1, kWaitLimitNs)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_f16_ss(tbase + C::kColDV, smem_desc(ap + kk * 2048, 16384, 1024),
+                     smem_desc(ado + h * 16384 + kk * 2048, 16384, 1024), id_kv, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_f16_ss(tbase + C::kColDK, smem_desc(ads + kk * 2048, 16384, 1024),
+                     smem_desc(aq + h * 16384 + kk * 2048, 16384, 1024), id_kv, kk > 0);
+        }
+        mma_commit(part_full);
+        ++job;
+        return true;
+      };
+      if (ok && nt > 0) ok = issue_sdp(0);
+      for (int t = 0; ok && t < nt; ++t) {
+        const int ks = t % C::kKStages;
         if (!mbar_wait(ps_full, t & 1, kWaitLimitNs)) { ok = false; break; }
         tc_fence_after();
-        // dQ += dS K   (K over the 128 keys of the tile)
+        const uint32_t ak = smem_u32(sK + ks * C::kTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t offa = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tbase + kColDQ, smem_desc(ads + offa, 16, 1024), smem_desc(ak + kk * 2048, 16384, 1024), id_dq,
+          mma_f16_ss(tbase + C::kColDQ, smem_desc(ads + offa, 16, 1024), smem_desc(ak + kk * 2048, 16384, 1024), id_dq,
                      (t > 0 || kk > 0) ? 1u : 0u);
         }
+        mma_commit(k_empty + ks);
+        if (partials && !issue_half(0)) { ok = false; break; }
+        if (t + 1 < nt && !issue_sdp(t + 1)) { ok = false; break; }
         if (partials) {
-          // dV_tile = P^T dO, dK_tile = dS^T Q   (K over the 128 queries)
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            mma_f16_ss(tbase + kColS, smem_desc(ap + kk * 2048, 16384, 1024), smem_desc(ado + kk * 2048, 16384, 1024),
-                       id_kv, kk > 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            mma_f16_ss(tbase + kColDP, smem_desc(ads + kk * 2048, 16384, 1024), smem_desc(aq + kk * 2048, 16384, 1024),
-                       id_kv, kk > 0);
-          }
+          for (int h = 1; h < C::kHalves; ++h)
+            if (!issue_half(h)) { ok = false; break; }
+          if (!ok) break;
         }
-        mma_commit(kv_empty + s);
-        mma_commit(part_full);
+        mma_commit(p_free);
       }
-      if (!ok) raise_status(prm.status, DSV_ERR_TIMEOUT);
+      if (ok) mma_commit(dq_done);
+      else raise_status(prm.status, DSV_ERR_TIMEOUT);
     }
-  } else {
-    // ------------------------------------------------ compute (warps 0-3)
+  } else if (warp < 4) {
+    // ------------------------------------------- S, dP -> P, dS (warps 0-3)
     const int row = warp * 32 + lane;
     const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
     const float sc = prm.scale_log2;
     float lse2 = INFINITY, delta = 0.f;
-    int tok = 0;
     if (row < G) {
-      tok = token_of(geo, g, row);
+      const int tok = token_of(geo, g, row);
       const int64_t o = ((int64_t)p * geo.S + tok) * D;
       const uint4* orow = reinterpret_cast<const uint4*>(prm.O + o);
       const uint4* drow = reinterpret_cast<const uint4*>(prm.dO + o);
@@ -282,21 +315,19 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       delta = acc;
       lse2 = prm.LSE[(int64_t)p * geo.S + tok] * 1.4426950408889634f;
     }
-    // A wait that runs out clears `ok`; later waits are skipped but every
-    // warp still passes every named barrier, so the CTA always terminates.
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
       ok = ok && mbar_wait_warp(sdp_full, t & 1, kWaitLimitNs);
       tc_fence_after();
       const int nvalid = min(128, k - t * 128);
-#pragma unroll 1
+      uint32_t pw[64], dw[64];
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t sr[32], dr[32];
-        tmem_ld32(lane_addr + kColS + c * 32, sr);
-        tmem_ld32(lane_addr + kColDP + c * 32, dr);
+        tmem_ld32(lane_addr + C::kColS + c * 32, sr);
+        tmem_ld32(lane_addr + C::kColDP + c * 32, dr);
         tmem_ld_wait(sr);
         reg_fence(dr);
-        uint32_t pw[16], dw[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int j = c * 32 + e;
@@ -304,44 +335,53 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
           const float p1 = j + 1 < nvalid ? ex2_fast(__uint_as_float(sr[e + 1]) * sc - lse2) : 0.f;
           const float d0 = p0 * (__uint_as_float(dr[e]) - delta);
           const float d1 = p1 * (__uint_as_float(dr[e + 1]) - delta);
-          pw[e >> 1] = pack_bf16x2(p0, p1);
-          dw[e >> 1] = pack_bf16x2(d0, d1);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          st_sw128_chunk(sP, row, c * 4 + q, make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]));
-          st_sw128_chunk(sDS, row, c * 4 + q, make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]));
+          pw[j >> 1] = pack_bf16x2(p0, p1);
+          dw[j >> 1] = pack_bf16x2(d0, d1);
         }
       }
-      fence_proxy_async_smem();
       tc_fence_before();
+      // P/dS of the previous tile must no longer be read by the tensor cores
+      if (t >= 1) ok = ok && mbar_wait_warp(p_free, (t - 1) & 1, kWaitLimitNs);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        st_sw128_chunk(sP, row, q, make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]));
+        st_sw128_chunk(sDS, row, q, make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]));
+      }
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(ps_full);
-      ok = ok && mbar_wait_warp(part_full, t & 1, kWaitLimitNs);
-      tc_fence_after();
-      if (partials) {
-        // Drain dV_tile (cols 0..D) and dK_tile (cols 128..128+D): TMEM lane =
-        // key slot of the tile. Each selected key's two bf16 rows go to its
-        // slot: off[key] + number of lower groups (of this unit) that chose it.
-        const int slot_key = t * 128 + row;
-        const bool kvalid = slot_key < k;
-        int64_t pos = 0;
-        if (kvalid) {
-          const int j = __ldg(idx_row + slot_key);
-          const int gl = g - tab.g0[u];
-          const uint32_t* b = csc.bits + tab.bits_base[u] + (int64_t)j * tab.nwords[u];
-          int r = 0;
-          for (int w = 0; w < (gl >> 5); ++w) r += __popc(__ldg(b + w));
-          r += __popc(__ldg(b + (gl >> 5)) & ((1u << (gl & 31)) - 1u));
-          pos = tab.part_base[u] + csc.off[(int64_t)u * (geo.S + 1) + j] + r;
-        }
+    }
+    if (!ok && lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
+  } else if (warp < 8) {
+    // -------------------------------- dV/dK partial drain, then dQ (warps 4-7)
+    const int q = warp - 4;
+    const int row = q * 32 + lane;   // key slot of the tile for the partials; query row for dQ
+    const uint32_t lane_addr = tbase + ((uint32_t)(q * 32) << 16);
+    bool ok = true;
+    int job = 0;
+    for (int t = 0; partials && t < nt; ++t) {
+      const int slot_key = t * 128 + row;
+      const bool kvalid = slot_key < k;
+      int64_t pos = 0;
+      if (kvalid) {
+        const int j = __ldg(idx_row + slot_key);
+        const int gl = g - tab.g0[u];
+        const uint32_t* b = csc.bits + tab.bits_base[u] + (int64_t)j * tab.nwords[u];
+        int r = 0;
+        for (int w = 0; w < (gl >> 5); ++w) r += __popc(__ldg(b + w));
+        r += __popc(__ldg(b + (gl >> 5)) & ((1u << (gl & 31)) - 1u));
+        pos = tab.part_base[u] + csc.off[(int64_t)u * (geo.S + 1) + j] + r;
+      }
+      for (int h = 0; h < C::kHalves; ++h, ++job) {
+        ok = ok && mbar_wait_warp(part_full, job & 1, kWaitLimitNs);
+        tc_fence_after();
 #pragma unroll 1
         for (int tensor = 0; tensor < 2; ++tensor) {
-          const uint32_t col = tensor == 0 ? kColS : kColDP;
+          const uint32_t col = tensor == 0 ? C::kColDV : C::kColDK;
           const float mul = tensor == 0 ? 1.f : prm.scale;
-          __nv_bfloat16* dst_row = (tensor == 0 ? csc.part_v : csc.part_k) + pos * D;
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          __nv_bfloat16* dst_row = (tensor == 0 ? csc.part_v : csc.part_k) + pos * D + h * 64;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
             uint32_t v[32];
             tmem_ld32(lane_addr + col + c * 32, v);
             tmem_ld_wait(v);
@@ -356,21 +396,23 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(part_free);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(part_empty);
     }
     // ----------------------------------------------------------- dQ out
+    ok = ok && mbar_wait_warp(dq_done, 0, kWaitLimitNs);
     if (!ok) {
       if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
     } else {
       tc_fence_after();
+      const int tok = row < G ? token_of(geo, g, row) : 0;
       __nv_bfloat16* qrow = prm.out + ((int64_t)p * geo.S + tok) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(lane_addr + kColDQ + c * 32, o);
+        tmem_ld32(lane_addr + C::kColDQ + c * 32, o);
         tmem_ld_wait(o);
         if (row < G) {
           uint32_t pk[16];
@@ -626,20 +668,27 @@ __global__ void k_sel_bitmap(const int32_t* __restrict__ idx, uint32_t* bits, co
   for (int s = threadIdx.x; s < k; s += blockDim.x) atomicOr(b + (int64_t)__ldg(row + s) * nw, bit);
 }
 
-// off[key] = number of pairs of lower keys (exclusive scan of the bit counts).
-__global__ void __launch_bounds__(1024) k_csc_offsets(const uint32_t* __restrict__ bits, int S, int32_t* off,
-                                                      const UnitTable tab) {
+// Number of groups that selected each key (popcount of its bitmap row).
+__global__ void k_csc_count(const uint32_t* __restrict__ bits, int S, int32_t* off, const UnitTable tab) {
+  const int u = blockIdx.y, j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= S) return;
+  const int nw = tab.nwords[u];
+  const uint32_t* b = bits + tab.bits_base[u] + (int64_t)j * nw;
+  int c = 0;
+  for (int w = 0; w < nw; ++w) c += __popc(__ldg(b + w));
+  off[(int64_t)u * (S + 1) + j] = c;
+}
+
+// In place: counts -> exclusive offsets, off[S] = total. One CTA per unit,
+// each thread scanning a contiguous run of S/1024 keys (S is a multiple of 128).
+__global__ void __launch_bounds__(1024) k_csc_scan(int S, int32_t* off) {
   __shared__ int wsum[32];
   const int u = blockIdx.x, tid = threadIdx.x;
-  const int nw = tab.nwords[u];
-  const uint32_t* b = bits + tab.bits_base[u];
   int32_t* o = off + (int64_t)u * (S + 1);
   const int per = (S + blockDim.x - 1) / blockDim.x;
   const int j0 = min(S, tid * per), j1 = min(S, j0 + per);
   int local = 0;
-  for (int j = j0; j < j1; ++j)
-    for (int w = 0; w < nw; ++w) local += __popc(b[(int64_t)j * nw + w]);
-  // block-wide exclusive scan of `local`
+  for (int j = j0; j < j1; ++j) local += o[j];
   int x = local;
   for (int d = 1; d < 32; d <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, x, d);
@@ -653,16 +702,16 @@ __global__ void __launch_bounds__(1024) k_csc_offsets(const uint32_t* __restrict
       const int y = __shfl_up_sync(0xffffffffu, v, d);
       if (tid >= d) v += y;
     }
-    wsum[tid] = v;   // inclusive over warps
+    wsum[tid] = v;
   }
   __syncthreads();
   int run = x - local + ((tid >> 5) ? wsum[(tid >> 5) - 1] : 0);
   for (int j = j0; j < j1; ++j) {
+    const int c = o[j];
     o[j] = run;
-    for (int w = 0; w < nw; ++w) run += __popc(b[(int64_t)j * nw + w]);
+    run += c;
   }
   if (j1 == S && j0 < j1) o[S] = run;
-  if (S == 0 && tid == 0) o[0] = 0;
 }
 
 // Per key: dV = sum of its partial rows in slot (= group) order, same for dK;
@@ -925,7 +974,8 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
     }
     if (cudaMemsetAsync(w.bits, 0, words * sizeof(uint32_t), st) != cudaSuccess) return DSV_ERR_CUDA;
     k_sel_bitmap<<<dim3(max_ng, tab.n), 256, 0, st>>>(idx, w.bits, tab);
-    k_csc_offsets<<<tab.n, 1024, 0, st>>>(w.bits, geo.S, w.off, tab);
+    k_csc_count<<<dim3((geo.S + 255) / 256, tab.n), 256, 0, st>>>(w.bits, geo.S, w.off, tab);
+    k_csc_scan<<<tab.n, 1024, 0, st>>>(geo.S, w.off);
     cudaError_t e = d == 128 ? launch_bwd_q<128>(maps, do_cube, prm, csc, tab, max_ng, st)
                              : launch_bwd_q<64>(maps, do_cube, prm, csc, tab, max_ng, st);
     if (e != cudaSuccess) return DSV_ERR_CUDA;
