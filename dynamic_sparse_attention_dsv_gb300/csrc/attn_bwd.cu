@@ -16,7 +16,8 @@
 //   written as bf16 partial rows, one per (group, selected key) pair.
 // Ordered dK/dV reduction (no atomics on the data): a bitmap of which groups
 // selected each key gives every (key, group) pair a slot, off[key] + the
-// number of lower groups that selected the key, so the partials of one key
+// number of lower groups that selected the key (each 32-group bitmap word
+// carries the count of the key's lower words), so the partials of one key
 // lie contiguously in ascending group order; a reduce kernel sums each key's
 // slots in that order in fp32. The result is the same bits on every run.
 // Key-major kernel (dense problems): one CTA per (128-key tile, problem),
@@ -50,7 +51,8 @@ struct UnitTable {
 };
 
 struct CscParams {
-  uint32_t* bits;              // per unit [S][nwords]: bit (key, group) set if the group selected the key
+  uint64_t* bits;              // per unit [S][nwords]: low 32 bits: bit (key, group) set if the group selected
+                               // the key; high 32 bits: number of set bits in the key's lower words
   int32_t* off;                // per unit [S + 1]: first slot of each key
   __nv_bfloat16* part_v;       // [slots][d]
   __nv_bfloat16* part_k;       // [slots][d]
@@ -359,19 +361,22 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     const uint32_t lane_addr = tbase + ((uint32_t)(q * 32) << 16);
     bool ok = true;
     int job = 0;
+    // Slot of this key row for tile t: off[key] + groups below ours that chose it.
+    const int gl = g - tab.g0[u];
+    const uint64_t* bits_u = partials ? csc.bits + tab.bits_base[u] : nullptr;
+    const int32_t* off_u = partials ? csc.off + (int64_t)u * (geo.S + 1) : nullptr;
+    auto slot_of = [&](int j) -> int64_t {
+      const uint64_t x = __ldg(bits_u + (int64_t)j * tab.nwords[u] + (gl >> 5));
+      const int r = (int)(x >> 32) + __popc((uint32_t)x & ((1u << (gl & 31)) - 1u));
+      return tab.part_base[u] + __ldg(off_u + j) + r;
+    };
+    int j_next = (partials && row < k) ? __ldg(idx_row + row) : -1;
+    int64_t pos_next = j_next >= 0 ? slot_of(j_next) : 0;
     for (int t = 0; partials && t < nt; ++t) {
-      const int slot_key = t * 128 + row;
-      const bool kvalid = slot_key < k;
-      int64_t pos = 0;
-      if (kvalid) {
-        const int j = __ldg(idx_row + slot_key);
-        const int gl = g - tab.g0[u];
-        const uint32_t* b = csc.bits + tab.bits_base[u] + (int64_t)j * tab.nwords[u];
-        int r = 0;
-        for (int w = 0; w < (gl >> 5); ++w) r += __popc(__ldg(b + w));
-        r += __popc(__ldg(b + (gl >> 5)) & ((1u << (gl & 31)) - 1u));
-        pos = tab.part_base[u] + csc.off[(int64_t)u * (geo.S + 1) + j] + r;
-      }
+      const bool kvalid = t * 128 + row < k;
+      const int64_t pos = pos_next;
+      const int nslot = (t + 1) * 128 + row;
+      j_next = (t + 1 < nt && nslot < k) ? __ldg(idx_row + nslot) : -1;   // next tile's key, loaded early
       for (int h = 0; h < C::kHalves; ++h, ++job) {
         ok = ok && mbar_wait_warp(part_full, job & 1, kWaitLimitNs);
         tc_fence_after();
@@ -390,15 +395,15 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
 #pragma unroll
               for (int e = 0; e < 16; ++e)
                 pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-              uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+              st_global_v8(dst_row + c * 32, pk);
+              st_global_v8(dst_row + c * 32 + 16, pk + 8);
             }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(part_free);
+        if (h == 0) pos_next = j_next >= 0 ? slot_of(j_next) : 0;   // overlaps the next half's MMAs
       }
     }
     // ----------------------------------------------------------- dQ out
@@ -657,26 +662,31 @@ __global__ void k_bwd_delta(const __nv_bfloat16* __restrict__ O, const __nv_bflo
 // ---------------------------------------------------------------------------
 // Ordered dK/dV reduction.
 // Sets bit (key, group) for every selected pair of every unit.
-__global__ void k_sel_bitmap(const int32_t* __restrict__ idx, uint32_t* bits, const UnitTable tab) {
+__global__ void k_sel_bitmap(const int32_t* __restrict__ idx, uint64_t* bits, const UnitTable tab) {
   const int u = blockIdx.y, gl = blockIdx.x;
   if (gl >= tab.ng[u]) return;
   const int k = tab.k[u];
   const int32_t* row = idx + tab.off[u] + (int64_t)(tab.g0[u] + gl) * k;
-  uint32_t* b = bits + tab.bits_base[u] + (gl >> 5);
-  const uint32_t bit = 1u << (gl & 31);
+  unsigned long long* b = reinterpret_cast<unsigned long long*>(bits + tab.bits_base[u] + (gl >> 5));
+  const unsigned long long bit = 1ull << (gl & 31);
   const int nw = tab.nwords[u];
   for (int s = threadIdx.x; s < k; s += blockDim.x) atomicOr(b + (int64_t)__ldg(row + s) * nw, bit);
 }
 
-// Number of groups that selected each key (popcount of its bitmap row).
-__global__ void k_csc_count(const uint32_t* __restrict__ bits, int S, int32_t* off, const UnitTable tab) {
+// Number of groups that selected each key (popcount of its bitmap row); also
+// stores, in each word's high half, the count of the key's lower words.
+__global__ void k_csc_count(uint64_t* bits, int S, int32_t* off, const UnitTable tab) {
   const int u = blockIdx.y, j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= S) return;
   const int nw = tab.nwords[u];
-  const uint32_t* b = bits + tab.bits_base[u] + (int64_t)j * nw;
-  int c = 0;
-  for (int w = 0; w < nw; ++w) c += __popc(__ldg(b + w));
-  off[(int64_t)u * (S + 1) + j] = c;
+  uint64_t* b = bits + tab.bits_base[u] + (int64_t)j * nw;
+  uint32_t c = 0;
+  for (int w = 0; w < nw; ++w) {
+    const uint32_t word = (uint32_t)b[w];
+    b[w] = ((uint64_t)c << 32) | word;
+    c += __popc(word);
+  }
+  off[(int64_t)u * (S + 1) + j] = (int32_t)c;
 }
 
 // In place: counts -> exclusive offsets, off[S] = total. One CTA per unit,
@@ -869,7 +879,7 @@ static BwdPlan plan_bwd(const dsv_shape& shape, const Geometry& geo, bool any_sp
 struct BwdWs {
   __nv_bfloat16* part_v;
   __nv_bfloat16* part_k;
-  uint32_t* bits;
+  uint64_t* bits;
   int32_t* off;
   float* acc_v;
   float* acc_k;
@@ -881,7 +891,7 @@ static size_t carve_bwd(void* base, const dsv_shape& s, const BwdPlan& pl, BwdWs
   const size_t S = (size_t)(s.T * s.Y * s.X), P = (size_t)(s.B * s.H);
   w->part_v = c.take<__nv_bfloat16>(pl.slots * s.d);
   w->part_k = c.take<__nv_bfloat16>(pl.slots * s.d);
-  w->bits = c.take<uint32_t>(pl.bits_words);
+  w->bits = c.take<uint64_t>(pl.bits_words);
   w->off = c.take<int32_t>((size_t)kMaxUnits * (S + 1));
   w->acc_v = c.take<float>(pl.split ? S * s.d : 0);
   w->acc_k = c.take<float>(pl.split ? S * s.d : 0);
@@ -972,7 +982,7 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
       words += (size_t)geo.S * tab.nwords[i];
       max_ng = std::max(max_ng, tab.ng[i]);
     }
-    if (cudaMemsetAsync(w.bits, 0, words * sizeof(uint32_t), st) != cudaSuccess) return DSV_ERR_CUDA;
+    if (cudaMemsetAsync(w.bits, 0, words * sizeof(uint64_t), st) != cudaSuccess) return DSV_ERR_CUDA;
     k_sel_bitmap<<<dim3(max_ng, tab.n), 256, 0, st>>>(idx, w.bits, tab);
     k_csc_count<<<dim3((geo.S + 255) / 256, tab.n), 256, 0, st>>>(w.bits, geo.S, w.off, tab);
     k_csc_scan<<<tab.n, 1024, 0, st>>>(geo.S, w.off);
