@@ -234,3 +234,40 @@ def sparse_attn_group_dq(Q, K, V, dO, idx_row: Optional[np.ndarray], mem: np.nda
     delta = (dOg * Og).sum(axis=1, keepdims=True)
     dS = P * (dOg @ V[I].T - delta)
     return Og, lse, scale * (dS @ K[I])
+
+
+# ------------------------------------------------- full-size check helpers
+def group_scores_via_mean(q_lr: np.ndarray, k_lr: np.ndarray, members: np.ndarray,
+                          groups: Optional[Sequence[int]] = None) -> np.ndarray:
+    """Same group scores as `group_scores`, formed as (mean of q_lr over the
+    group) . k_lr, which equals the mean of q_lr . k_lr by linearity. Used
+    where the literal form is too slow (all groups of a 64K-262K token head)."""
+    gs = range(members.shape[0]) if groups is None else groups
+    qbar = np.stack([q_lr[members[g]].mean(axis=0) for g in gs])
+    return qbar @ k_lr.T
+
+
+def sparse_attn_key_grads(Q, K, V, dO, idx: np.ndarray, members: np.ndarray, scale: float, key: int):
+    """dK and dV of one key only: sum over the groups whose index set holds the
+    key of that group's contribution (each group's softmax over its own
+    selected keys). Returns (dK_key [d], dV_key [d], number of groups)."""
+    Q, K, V, dO = as_f64(Q), as_f64(K), as_f64(V), as_f64(dO)
+    dk = np.zeros(K.shape[1])
+    dv = np.zeros(V.shape[1])
+    hits = 0
+    for g in range(members.shape[0]):
+        row = idx[g]
+        pos = np.searchsorted(row, key)
+        if pos >= row.shape[0] or row[pos] != key:
+            continue
+        hits += 1
+        mem = members[g]
+        P, Og, _ = _group_forward(Q[mem], K[row], V[row], scale)
+        dOg = dO[mem]
+        delta = (dOg * Og).sum(axis=1)
+        pj = P[:, pos]
+        dpj = dOg @ V[key]
+        dsj = pj * (dpj - delta)
+        dv += pj @ dOg
+        dk += scale * (dsj @ Q[mem])
+    return dk, dv, hits

@@ -77,6 +77,8 @@ def test_mean_of_dots_equals_dot_of_mean():
     s = ora.group_scores(q, k, mem)
     alt = np.stack([q[m].mean(axis=0) for m in mem]) @ k.T
     np.testing.assert_allclose(s, alt, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ora.group_scores_via_mean(q, k, mem), s, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ora.group_scores_via_mean(q, k, mem, [3, 1]), s[[3, 1]], rtol=0, atol=1e-12)
 
 
 def test_identity_predictor_gives_true_group_topk():
@@ -285,6 +287,26 @@ def test_backward_equals_torch_autograd():
     for g in (0, 3):
         Og, lse, dq = ora.sparse_attn_group_dq(Q, K, V, dO, idx[g], mem[g], scale)
         np.testing.assert_allclose(dq, dQ[mem[g]], atol=1e-12)
+
+
+def test_key_grads_equal_full_backward_rows():
+    mem, Q, K, V, dO, idx = _tiny_problem(17, k=9)
+    scale = 0.41
+    _, dK, dV = ora.sparse_attn_bwd(Q, K, V, dO, idx, mem, scale)
+    for key in range(Q.shape[0]):
+        dk, dv, hits = ora.sparse_attn_key_grads(Q, K, V, dO, idx, mem, scale, key)
+        assert hits == int(sum(key in row for row in idx))
+        np.testing.assert_allclose(dk, dK[key], atol=1e-12)
+        np.testing.assert_allclose(dv, dV[key], atol=1e-12)
+
+
+def test_backward_column_sums_identities():
+    """sum_j dV_j = sum_i dO_i (softmax rows sum to 1) and sum_j dK_j = 0
+    (sum_j P_ij dP_ij = Delta_i); both hold for any index sets."""
+    mem, Q, K, V, dO, idx = _tiny_problem(18, k=7)
+    _, dK, dV = ora.sparse_attn_bwd(Q, K, V, dO, idx, mem, 0.5)
+    np.testing.assert_allclose(dV.sum(axis=0), dO.sum(axis=0), atol=1e-12)
+    np.testing.assert_allclose(dK.sum(axis=0), 0.0, atol=1e-12)
 
 
 def test_backward_dense_equals_all_keys():
