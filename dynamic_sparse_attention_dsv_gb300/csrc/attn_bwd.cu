@@ -698,6 +698,7 @@ __global__ void __launch_bounds__(1024) k_csc_scan(int S, int32_t* off) {
   const int per = (S + blockDim.x - 1) / blockDim.x;
   const int j0 = min(S, tid * per), j1 = min(S, j0 + per);
   int local = 0;
+#pragma unroll 8
   for (int j = j0; j < j1; ++j) local += o[j];
   int x = local;
   for (int d = 1; d < 32; d <<= 1) {
@@ -716,10 +717,16 @@ __global__ void __launch_bounds__(1024) k_csc_scan(int S, int32_t* off) {
   }
   __syncthreads();
   int run = x - local + ((tid >> 5) ? wsum[(tid >> 5) - 1] : 0);
-  for (int j = j0; j < j1; ++j) {
-    const int c = o[j];
-    o[j] = run;
-    run += c;
+  for (int j = j0; j < j1; j += 8) {
+    int c[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) c[e] = j + e < j1 ? o[j + e] : 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (j + e < j1) {
+        o[j + e] = run;
+        run += c[e];
+      }
   }
   if (j1 == S && j0 < j1) o[S] = run;
 }

@@ -217,6 +217,9 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     int n_above = 0, n_in = 0;
     float tau = INFINITY;
     int pos = 0, eq_left = 0, krow = 0;
+    // COLLECT stages up to kStage candidates per (row, half) in the unused histogram area
+    constexpr int kStage = C::kHistBytes / (256 * 8);
+    uint64_t* stage = reinterpret_cast<uint64_t*>(sHist) + (size_t)(half * 128 + row) * kStage;
     int32_t* out_row = nullptr;
     constexpr int NB = (MODE == kCov) ? C::kCovBins : C::kHistBins;
     const uint32_t hist_base = smem_u32(sHist);
@@ -299,11 +302,14 @@ __global__ void __launch_bounds__(kSelThreads, 1)
             if (bin > bstar) {
               ++n_above;
             } else if (bin == bstar && valid) {
+              const uint64_t key = ((uint64_t)(~f2ord(s)) << 32) | (uint32_t)(kb + e);
+              if (n_in < kStage) {
+                stage[n_in] = key;
+              } else {   // staging full: reserve a slot directly
+                const uint32_t slot = atomicAdd(prm.cand_cnt + rid, 1u);
+                if (slot < (uint32_t)kCandCap) prm.cand[(size_t)rid * kCandCap + slot] = key;
+              }
               ++n_in;
-              const uint32_t slot = atomicAdd(prm.cand_cnt + rid, 1u);
-              if (slot < (uint32_t)kCandCap)
-                prm.cand[(size_t)rid * kCandCap + slot] =
-                    ((uint64_t)(~f2ord(s)) << 32) | (uint32_t)(kb + e);
             }
           } else if constexpr (MODE == kCov) {
             const float u = __fmul_rn(prm.scale, __fsub_rn(cmax, s));
@@ -320,6 +326,17 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     }
 
     // ----------------------------------------------------- per-row results
+    if constexpr (MODE == kCollect) {
+      // flush this (row, half)'s staged candidates with one slot reservation,
+      // before the exchange below reuses the start of the staging area
+      const int ns = min(n_in, kStage);
+      if (valid && ns > 0) {
+        const uint32_t slot0 = atomicAdd(prm.cand_cnt + rid, (uint32_t)ns);
+        for (int i = 0; i < ns; ++i)
+          if (slot0 + i < (uint32_t)kCandCap) prm.cand[(size_t)rid * kCandCap + slot0 + i] = stage[i];
+      }
+      epi_barrier();
+    }
     if constexpr (MODE == kMinMax || MODE == kCollect) {
       float* ex = reinterpret_cast<float*>(sHist);   // [2][2][128], the histogram area is unused here
       if (MODE == kMinMax) {
@@ -345,6 +362,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
           prm.inbin[ci] = n_in + exi[(2 + 1) * 128 + row];
         }
       }
+
     } else if constexpr (MODE == kHist) {
       epi_barrier();
       const uint32_t* h = reinterpret_cast<const uint32_t*>(sHist);
@@ -464,13 +482,26 @@ __global__ void k_bracket(const uint32_t* __restrict__ hist, int nb, int g_pad, 
   const int lp = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= n_groups) return;
   const int k = tab.k[lp];
-  int above = 0, b = 0;
-  for (b = nb - 1; b >= 0; --b) {
-    const int c = (int)hist[((size_t)lp * nb + b) * g_pad + g];
-    if (above + c >= k) break;
-    above += c;
+  const uint32_t* h = hist + (size_t)lp * nb * g_pad + g;
+  int above = 0, b = nb - 1;
+  bool found = false;
+  for (int top = nb - 1; top >= 0 && !found; top -= 8) {
+    uint32_t c[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) c[e] = top - e >= 0 ? __ldg(h + (size_t)(top - e) * g_pad) : 0u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (!found && top - e >= 0) {
+        if (above + (int)c[e] >= k) {
+          b = top - e;
+          found = true;
+        } else {
+          above += (int)c[e];
+        }
+      }
+    }
   }
-  if (b < 0) b = 0;
+  if (!found) b = 0;
   bstar[lp * g_pad + g] = b;
   n_above_out[lp * g_pad + g] = above;
 }
@@ -577,71 +608,135 @@ __global__ void k_cov_merge(const uint32_t* __restrict__ cnt, const float* __res
   cum_mass[rid * nb + b] = m;
 }
 
+// One warp per group: lane l owns bins [4l, 4l+4) of the (at most 128) bins.
 __global__ void k_cov_scan(const uint32_t* mmax, const uint32_t* mmin, int nb, int g_pad, int n_groups, float scale,
                            int32_t* cum_cnt, double* cum_mass, float* width) {
-  const int lp = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
+  const int lp = blockIdx.y, lane = threadIdx.x & 31;
+  const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (g >= n_groups) return;
   const size_t rid = (size_t)lp * g_pad + g;
   int32_t* cc = cum_cnt + rid * nb;
   double* cm = cum_mass + rid * nb;
-  int c_acc = 0;
-  double m_acc = 0.0;
-  for (int b = 0; b < nb; ++b) {
-    c_acc += cc[b];
-    m_acc += cm[b];
-    cc[b] = c_acc;
-    cm[b] = m_acc;
+  const int per = nb / 32;   // 4 (nb = 128) or 2 (nb = 64)
+  int c[4] = {0, 0, 0, 0};
+  double m[4] = {0.0, 0.0, 0.0, 0.0};
+  int csum = 0;
+  double msum = 0.0;
+  for (int e = 0; e < per; ++e) {
+    c[e] = cc[lane * per + e];
+    m[e] = cm[lane * per + e];
+    csum += c[e];
+    msum += m[e];
   }
-  const double inv = m_acc > 0.0 ? 1.0 / m_acc : 0.0;
-  for (int b = 0; b < nb; ++b) cm[b] *= inv;
-  width[rid] = scale * (ord2f(mmax[rid]) - ord2f(mmin[rid])) / (float)nb;
+  int ci = csum;   // inclusive warp scans of the lane totals
+  double mi = msum;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int cy = __shfl_up_sync(0xffffffffu, ci, d);
+    const double my = __shfl_up_sync(0xffffffffu, mi, d);
+    if (lane >= d) {
+      ci += cy;
+      mi += my;
+    }
+  }
+  const double total = __shfl_sync(0xffffffffu, mi, 31);
+  const double inv = total > 0.0 ? 1.0 / total : 0.0;
+  int crun = ci - csum;
+  double mrun = mi - msum;
+  for (int e = 0; e < per; ++e) {
+    crun += c[e];
+    mrun += m[e];
+    cc[lane * per + e] = crun;
+    cm[lane * per + e] = mrun * inv;
+  }
+  if (lane == 0) width[rid] = scale * (ord2f(mmax[rid]) - ord2f(mmin[rid])) / (float)nb;
 }
 
+// k-ary search (15 probes per round, about five rounds for S = 2^18) of the
+// smallest k with C(k) >= target; per-group terms in fp32, sums in fp64.
+constexpr int kProbes = 15;
 __global__ void __launch_bounds__(1024) k_cov_search(int nb, int g_pad, int n_groups, int S, float target,
                                                      const int32_t* cum_cnt, const double* cum_mass,
                                                      const float* width, int32_t* k_cov, float* curve, int n_curve,
                                                      const ProblemTable tab) {
-  const int lp = blockIdx.x, tid = threadIdx.x;
-  __shared__ double red[32];
-  auto C_of = [&](int k) -> double {
-    double acc = 0.0;
+  const int lp = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  __shared__ double red[32][kProbes];
+  __shared__ double tot[kProbes];
+  __shared__ int s_lo, s_hi;
+  // mass of group g's k most probable keys (interpolated inside the boundary bin)
+  auto m_of = [&](size_t rid, int k) -> float {
+    const int32_t* cc = cum_cnt + rid * nb;
+    const double* cm = cum_mass + rid * nb;
+    int lo = 0, hi = nb - 1;  // first bin with cumulative count >= k
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (cc[mid] >= k) hi = mid; else lo = mid + 1;
+    }
+    const int pc = lo > 0 ? cc[lo - 1] : 0;
+    const float pm = lo > 0 ? (float)cm[lo - 1] : 0.f;
+    const int n = cc[lo] - pc;
+    const float mb = (float)cm[lo] - pm;
+    const float f = n > 0 ? (float)(k - pc) / (float)n : 1.f;
+    const float dw = width[rid];
+    const float part = dw > 1e-6f ? mb * (1.f - __expf(-f * dw)) / (1.f - __expf(-dw)) : mb * f;
+    return pm + part;
+  };
+  // C at up to kProbes points, result in tot[]
+  auto eval = [&](const int* ks, int np) {
+    double acc[kProbes];
+    for (int i = 0; i < kProbes; ++i) acc[i] = 0.0;
     for (int g = tid; g < n_groups; g += blockDim.x) {
       const size_t rid = (size_t)lp * g_pad + g;
-      const int32_t* cc = cum_cnt + rid * nb;
-      const double* cm = cum_mass + rid * nb;
-      int lo = 0, hi = nb - 1;  // first bin with cumulative count >= k
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (cc[mid] >= k) hi = mid; else lo = mid + 1;
-      }
-      const int pc = lo > 0 ? cc[lo - 1] : 0;
-      const double pm = lo > 0 ? cm[lo - 1] : 0.0;
-      const int n = cc[lo] - pc;
-      const double mb = cm[lo] - pm;
-      const double f = n > 0 ? (double)(k - pc) / (double)n : 1.0;
-      const double dw = (double)width[rid];
-      const double part = dw > 1e-12 ? mb * (1.0 - exp(-f * dw)) / (1.0 - exp(-dw)) : mb * f;
-      acc += pm + part;
+      for (int i = 0; i < np; ++i) acc[i] += (double)m_of(rid, ks[i]);
     }
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    for (int i = 0; i < np; ++i) {
+      double a = acc[i];
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      if (lane == 0) red[wid][i] = a;
+    }
     __syncthreads();
-    if ((tid & 31) == 0) red[tid >> 5] = acc;
+    if (tid < np) {
+      double t = 0.0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w][tid];
+      tot[tid] = t / (double)n_groups;
+    }
     __syncthreads();
-    double tot = 0.0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
-    return tot / (double)n_groups;
   };
-  int lo = 1, hi = S;
-  while (lo < hi) {
-    const int mid = lo + (hi - lo) / 2;
-    if (C_of(mid) >= (double)target) hi = mid; else lo = mid + 1;
+  if (tid == 0) {
+    s_lo = 1;
+    s_hi = S;
   }
-  if (tid == 0) k_cov[tab.p[lp]] = lo;
+  __syncthreads();
+  int ks[kProbes];
+  while (true) {
+    const int lo = s_lo, hi = s_hi;   // answer in [lo, hi]; C(hi) >= target or hi == S
+    if (lo >= hi) break;
+    const int span = hi - lo;
+    int np = 0;
+    for (int i = 1; i <= kProbes; ++i) {
+      const int kp = lo + (int)(((int64_t)span * i) / (kProbes + 1));
+      if (kp >= lo && kp < hi && (np == 0 || kp > ks[np - 1])) ks[np++] = kp;
+    }
+    if (np == 0) ks[np++] = lo;
+    eval(ks, np);
+    if (tid == 0) {
+      int nlo = lo, nhi = hi;
+      for (int i = 0; i < np; ++i) {
+        if (tot[i] >= (double)target) { nhi = ks[i]; break; }
+        nlo = ks[i] + 1;
+      }
+      s_lo = nlo;
+      s_hi = nhi;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) k_cov[tab.p[lp]] = s_lo;
   if (curve) {
-    for (int i = 0; i < n_curve; ++i) {
-      const int k = (int)(((int64_t)(i + 1) * S + n_curve - 1) / n_curve);
-      const double c = C_of(k);
-      if (tid == 0) curve[(size_t)tab.p[lp] * n_curve + i] = (float)c;
+    for (int c0 = 0; c0 < n_curve; c0 += kProbes) {
+      const int np = min(kProbes, n_curve - c0);
+      for (int i = 0; i < np; ++i) ks[i] = (int)(((int64_t)(c0 + i + 1) * S + n_curve - 1) / n_curve);
+      eval(ks, np);
+      if (tid < np) curve[(size_t)tab.p[lp] * n_curve + c0 + tid] = (float)tot[tid];
+      __syncthreads();
     }
   }
 }
@@ -946,8 +1041,9 @@ extern "C" dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_
     const int gb = (pl.geo.n_groups + 127) / 128;
     k_cov_merge<<<dim3(gb, pl.cov_bins, n), 128, 0, st>>>(w.hist, w.mass, pl.cov_bins, n_chunks, pl.g_pad,
                                                            pl.geo.n_groups, w.cum_cnt, w.cum_mass);
-    k_cov_scan<<<dim3(gb, n), 128, 0, st>>>(w.mmax, w.mmin, pl.cov_bins, pl.g_pad, pl.geo.n_groups, scale,
-                                            w.cum_cnt, w.cum_mass, w.width);
+    k_cov_scan<<<dim3((pl.geo.n_groups + 7) / 8, n), 256, 0, st>>>(w.mmax, w.mmin, pl.cov_bins, pl.g_pad,
+                                                                    pl.geo.n_groups, scale, w.cum_cnt, w.cum_mass,
+                                                                    w.width);
     k_cov_search<<<n, 1024, 0, st>>>(pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.geo.S, mass, w.cum_cnt, w.cum_mass,
                                      w.width, k_cov, curve, n_curve, tab);
     if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
