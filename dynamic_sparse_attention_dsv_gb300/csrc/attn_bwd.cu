@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
   uint64_t* part_full = bars + 12;
   uint64_t* part_free = bars + 13;
   uint64_t* dq_done = bars + 14;
+  uint64_t* sdp_free = bars + 15;    // S, dP of the current tile read out of TMEM
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     mbar_init(part_full, 1);
     mbar_init(part_free, 4);
     mbar_init(dq_done, 1);
+    mbar_init(sdp_free, 4);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -269,6 +271,8 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       if (ok && nt > 0) ok = issue_sdp(0);
       for (int t = 0; ok && t < nt; ++t) {
         const int ks = t % C::kKStages;
+        // the next tile's S and dP may overwrite TMEM once tile t's are read out
+        if (t + 1 < nt && (!mbar_wait(sdp_free, t & 1, kWaitLimitNs) || !issue_sdp(t + 1))) { ok = false; break; }
         if (!mbar_wait(ps_full, t & 1, kWaitLimitNs)) { ok = false; break; }
         tc_fence_after();
         const uint32_t ak = smem_u32(sK + ks * C::kTile);
@@ -280,7 +284,6 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         }
         mma_commit(k_empty + ks);
         if (partials && !issue_half(0)) { ok = false; break; }
-        if (t + 1 < nt && !issue_sdp(t + 1)) { ok = false; break; }
         if (partials) {
           for (int h = 1; h < C::kHalves; ++h)
             if (!issue_half(h)) { ok = false; break; }
@@ -342,6 +345,8 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         }
       }
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sdp_free);
       // P/dS of the previous tile must no longer be read by the tensor cores
       if (t >= 1) ok = ok && mbar_wait_warp(p_free, (t - 1) & 1, kWaitLimitNs);
 #pragma unroll
