@@ -11,6 +11,9 @@ step (algorithmic fwd+bwd FLOPs 14*H*S*k*d over the step time). Breakdown keys
 give each phase's time, the top-k Gscore/s and the attention TFLOP/s.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+`--heads N` (profiling aid, used for ncu captures of single kernels) runs the
+same workload with N heads instead of 24.
 """
 from __future__ import annotations
 
@@ -50,7 +53,8 @@ def peaks():
 
 def workload_dict(w):
     return {"workload": f"cfg{w.cfg}: " + w.name, "B": 1, "H": w.H, "grid": [w.T, w.Y, w.X], "S": w.S, "d": w.d,
-            "r": w.r, "group": [w.gt, w.gy, w.gx], "k": w.k, "l2": "inputs larger than L2 (1.6 GB of Q/K/V/dO)"}
+            "r": w.r, "group": [w.gt, w.gy, w.gx], "k": w.k,
+            "l2": f"inputs larger than L2 ({4 * w.H * w.S * w.d * 2 / 1e9:.2f} GB of Q/K/V/dO)"}
 
 
 def attn_flops(w, ks):
@@ -236,8 +240,10 @@ def main():
     ap.add_argument("--impl", default="dsv", choices=["dsv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="profiling aid: run the workload with only this many heads (default: all)")
     args = ap.parse_args()
-    w = syn.workload(CFG)
+    w = syn.workload(CFG) if args.heads <= 0 else syn.workload(CFG, H=args.heads)
 
     if args.impl == "reference":
         return reference_arm(args, w)

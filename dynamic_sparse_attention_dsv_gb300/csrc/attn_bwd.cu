@@ -24,6 +24,7 @@
 // looping over all 128-token query tiles with dV, dK accumulated in TMEM;
 // no cross-CTA reduction at all.
 #include <algorithm>
+#include <type_traits>
 #include <vector>
 
 #include "attn_common.cuh"
@@ -34,6 +35,7 @@ constexpr int kBwdThreads = 192;                       // key-major kernel
 constexpr int kBwdQThreads = 32 * (9 + kGatherWarps);   // group-major kernel
 constexpr int kMaxUnits = 48;                       // work units per group-major launch
 constexpr size_t kPartialBudget = 8ull << 30;       // bytes of bf16 dK/dV partials in flight
+constexpr int kMaxBlocks = 1024;                    // 256-key blocks per problem (S <= 2^18)
 
 // A unit is a range of groups of one problem whose dK/dV partials are
 // produced and reduced by one launch.
@@ -53,7 +55,8 @@ struct UnitTable {
 struct CscParams {
   uint64_t* bits;              // per unit [S][nwords]: low 32 bits: bit (key, group) set if the group selected
                                // the key; high 32 bits: number of set bits in the key's lower words
-  int32_t* off;                // per unit [S + 1]: first slot of each key
+  int32_t* off;                // per unit [S + 1]: first slot of each key within its 256-key block
+  int32_t* bpre;               // per unit [S/256 + 1]: first slot of each 256-key block; last = total
   __nv_bfloat16* part_v;       // [slots][d]
   __nv_bfloat16* part_k;       // [slots][d]
   float* acc_v;                // [S][d] fp32 running sums of a problem split over several units
@@ -370,10 +373,11 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     const int gl = g - tab.g0[u];
     const uint64_t* bits_u = partials ? csc.bits + tab.bits_base[u] : nullptr;
     const int32_t* off_u = partials ? csc.off + (int64_t)u * (geo.S + 1) : nullptr;
+    const int32_t* bpre_u = partials ? csc.bpre + (int64_t)u * (kMaxBlocks + 1) : nullptr;
     auto slot_of = [&](int j) -> int64_t {
       const uint64_t x = __ldg(bits_u + (int64_t)j * tab.nwords[u] + (gl >> 5));
       const int r = (int)(x >> 32) + __popc((uint32_t)x & ((1u << (gl & 31)) - 1u));
-      return tab.part_base[u] + __ldg(off_u + j) + r;
+      return tab.part_base[u] + __ldg(bpre_u + (j >> 8)) + __ldg(off_u + j) + r;
     };
     int j_next = (partials && row < k) ? __ldg(idx_row + row) : -1;
     int64_t pos_next = j_next >= 0 ? slot_of(j_next) : 0;
@@ -680,60 +684,52 @@ __global__ void k_sel_bitmap(const int32_t* __restrict__ idx, uint64_t* bits, co
 
 // Number of groups that selected each key (popcount of its bitmap row); also
 // stores, in each word's high half, the count of the key's lower words.
-__global__ void k_csc_count(uint64_t* bits, int S, int32_t* off, const UnitTable tab) {
-  const int u = blockIdx.y, j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= S) return;
+// Writes each key's offset within its 256-key block and the block's total.
+__global__ void __launch_bounds__(256) k_csc_count(uint64_t* bits, int S, int32_t* off, int32_t* bsum,
+                                                   const UnitTable tab) {
+  __shared__ int wsum[8];
+  const int u = blockIdx.y, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int j = blockIdx.x * 256 + tid;
   const int nw = tab.nwords[u];
-  uint64_t* b = bits + tab.bits_base[u] + (int64_t)j * nw;
   uint32_t c = 0;
-  for (int w = 0; w < nw; ++w) {
-    const uint32_t word = (uint32_t)b[w];
-    b[w] = ((uint64_t)c << 32) | word;
-    c += __popc(word);
+  if (j < S) {
+    uint64_t* b = bits + tab.bits_base[u] + (int64_t)j * nw;
+    for (int i = 0; i < nw; ++i) {
+      const uint32_t word = (uint32_t)b[i];
+      b[i] = ((uint64_t)c << 32) | word;
+      c += __popc(word);
+    }
   }
-  off[(int64_t)u * (S + 1) + j] = (int32_t)c;
-}
-
-// In place: counts -> exclusive offsets, off[S] = total. One CTA per unit,
-// each thread scanning a contiguous run of S/1024 keys (S is a multiple of 128).
-__global__ void __launch_bounds__(1024) k_csc_scan(int S, int32_t* off) {
-  __shared__ int wsum[32];
-  const int u = blockIdx.x, tid = threadIdx.x;
-  int32_t* o = off + (int64_t)u * (S + 1);
-  const int per = (S + blockDim.x - 1) / blockDim.x;
-  const int j0 = min(S, tid * per), j1 = min(S, j0 + per);
-  int local = 0;
-#pragma unroll 8
-  for (int j = j0; j < j1; ++j) local += o[j];
-  int x = local;
+  int x = (int)c;
   for (int d = 1; d < 32; d <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, x, d);
-    if ((tid & 31) >= d) x += y;
+    if (lane >= d) x += y;
   }
-  if ((tid & 31) == 31) wsum[tid >> 5] = x;
+  if (lane == 31) wsum[w] = x;
   __syncthreads();
-  if (tid < 32) {
-    int v = tid < (int)(blockDim.x >> 5) ? wsum[tid] : 0;
-    for (int d = 1; d < 32; d <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, v, d);
-      if (tid >= d) v += y;
-    }
-    wsum[tid] = v;
+  int before = 0;
+  for (int i = 0; i < w; ++i) before += wsum[i];
+  if (j < S) off[(int64_t)u * (S + 1) + j] = before + x - (int)c;
+  if (tid == 255) bsum[(int64_t)u * (kMaxBlocks + 1) + blockIdx.x] = before + x;
+}
+
+// In place: block totals -> exclusive block offsets; entry nblk = total.
+__global__ void __launch_bounds__(1024) k_csc_bscan(int nblk, int32_t* bsum) {
+  __shared__ int wsum[32];
+  const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  int32_t* b = bsum + (int64_t)u * (kMaxBlocks + 1);
+  const int v = tid < nblk ? b[tid] : 0;
+  int x = v;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += y;
   }
+  if (lane == 31) wsum[w] = x;
   __syncthreads();
-  int run = x - local + ((tid >> 5) ? wsum[(tid >> 5) - 1] : 0);
-  for (int j = j0; j < j1; j += 8) {
-    int c[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) c[e] = j + e < j1 ? o[j + e] : 0;
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-      if (j + e < j1) {
-        o[j + e] = run;
-        run += c[e];
-      }
-  }
-  if (j1 == S && j0 < j1) o[S] = run;
+  int before = 0;
+  for (int i = 0; i < w; ++i) before += wsum[i];
+  if (tid < nblk) b[tid] = before + x - v;
+  if (tid == nblk - 1) b[nblk] = before + x;
 }
 
 // Per key: dV = sum of its partial rows in slot (= group) order, same for dK;
@@ -745,7 +741,10 @@ __global__ void __launch_bounds__(256) k_csc_reduce(const CscParams csc, int S, 
   const int j = blockIdx.x * 8 + warp;
   if (j >= S) return;
   const int32_t* o = csc.off + (int64_t)u * (S + 1);
-  const int64_t a = tab.part_base[u] + o[j], b = tab.part_base[u] + o[j + 1];
+  const int32_t* bp = csc.bpre + (int64_t)u * (kMaxBlocks + 1);
+  const int nblk = (S + 255) / 256;
+  const int64_t a = tab.part_base[u] + bp[j >> 8] + o[j];
+  const int64_t b = tab.part_base[u] + (j + 1 == S ? bp[nblk] : bp[(j + 1) >> 8] + o[j + 1]);
   const bool first = tab.flags[u] & 1, last = tab.flags[u] & 2;
   float sv[E], sk[E];
   const int64_t arow = (int64_t)j * D + lane * E;
@@ -754,7 +753,8 @@ __global__ void __launch_bounds__(256) k_csc_reduce(const CscParams csc, int S, 
     sv[e] = first ? 0.f : csc.acc_v[arow + e];
     sk[e] = first ? 0.f : csc.acc_k[arow + e];
   }
-  for (int64_t s = a; s < b; ++s) {
+  int64_t s = a;
+  for (; s < b; ++s) {
     const __nv_bfloat16* pv = csc.part_v + s * D + lane * E;
     const __nv_bfloat16* pk = csc.part_k + s * D + lane * E;
 #pragma unroll
@@ -893,6 +893,7 @@ struct BwdWs {
   __nv_bfloat16* part_k;
   uint64_t* bits;
   int32_t* off;
+  int32_t* bpre;
   float* acc_v;
   float* acc_k;
   float* delta;
@@ -905,6 +906,7 @@ static size_t carve_bwd(void* base, const dsv_shape& s, const BwdPlan& pl, BwdWs
   w->part_k = c.take<__nv_bfloat16>(pl.slots * s.d);
   w->bits = c.take<uint64_t>(pl.bits_words);
   w->off = c.take<int32_t>((size_t)kMaxUnits * (S + 1));
+  w->bpre = c.take<int32_t>((size_t)kMaxUnits * (kMaxBlocks + 1));
   w->acc_v = c.take<float>(pl.split ? S * s.d : 0);
   w->acc_k = c.take<float>(pl.split ? S * s.d : 0);
   w->delta = c.take<float>(pl.dense.n ? P * S : 0);
@@ -945,8 +947,11 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
   const Geometry geo = make_geometry(shape, group);
   const int P = (int)(shape.B * shape.H), d = (int)shape.d;
   if (idx)
-    for (int i = 0; i < P; ++i)
-      if (idx_offset[i] >= 0 && (k_per_head[i] < 1 || k_per_head[i] > geo.S)) return DSV_ERR_INVALID_ARG;
+    for (int i = 0; i < P; ++i) {
+      if (idx_offset[i] < 0) continue;
+      if (k_per_head[i] < 1 || k_per_head[i] > geo.S) return DSV_ERR_INVALID_ARG;
+      if (geo.S > 256 * kMaxBlocks) return DSV_ERR_UNSUPPORTED;   // slot map covers S <= 2^18
+    }
   const BwdPlan pl = plan_bwd(shape, geo, idx != nullptr, k_per_head, idx_offset);
   BwdWs w;
   const size_t need = carve_bwd(nullptr, shape, pl, &w);
@@ -979,6 +984,7 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
   memset(&csc, 0, sizeof(csc));
   csc.bits = w.bits;
   csc.off = w.off;
+  csc.bpre = w.bpre;
   csc.part_v = w.part_v;
   csc.part_k = w.part_k;
   csc.acc_v = w.acc_v;
@@ -996,8 +1002,8 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
     }
     if (cudaMemsetAsync(w.bits, 0, words * sizeof(uint64_t), st) != cudaSuccess) return DSV_ERR_CUDA;
     k_sel_bitmap<<<dim3(max_ng, tab.n), 256, 0, st>>>(idx, w.bits, tab);
-    k_csc_count<<<dim3((geo.S + 255) / 256, tab.n), 256, 0, st>>>(w.bits, geo.S, w.off, tab);
-    k_csc_scan<<<tab.n, 1024, 0, st>>>(geo.S, w.off);
+    k_csc_count<<<dim3((geo.S + 255) / 256, tab.n), 256, 0, st>>>(w.bits, geo.S, w.off, w.bpre, tab);
+    k_csc_bscan<<<tab.n, 1024, 0, st>>>((geo.S + 255) / 256, w.bpre);
     cudaError_t e = d == 128 ? launch_bwd_q<128>(maps, do_cube, prm, csc, tab, max_ng, st)
                              : launch_bwd_q<64>(maps, do_cube, prm, csc, tab, max_ng, st);
     if (e != cudaSuccess) return DSV_ERR_CUDA;

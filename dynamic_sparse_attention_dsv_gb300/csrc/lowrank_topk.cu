@@ -390,41 +390,73 @@ __global__ void __launch_bounds__(kSelThreads, 1)
 // ---------------------------------------------------------------------------
 // Low-rank projections.
 // k_lr of every key, split into tf32 hi and lo parts; rows padded to RP.
+// 128 keys per block: the K tile is staged in shared memory with coalesced
+// loads (rows padded by 16 bytes so a warp reading 32 rows hits 32 banks);
+// each thread computes one key's r outputs against W in shared memory and
+// stores its hi/lo rows with 32-byte stores.
+template <int R>
+struct ProjCfg {
+  static constexpr int RP = R < 32 ? 32 : R;
+  static constexpr int kRowElems = 128 + 8;                  // bf16 per staged row (d <= 128)
+  static constexpr int kSmem = 128 * R * 4 + 128 * kRowElems * 2;
+};
+
 template <int R>
 __global__ void __launch_bounds__(128) k_key_proj(const __nv_bfloat16* __restrict__ K,
                                                   const __nv_bfloat16* __restrict__ Wk, int64_t H, int d, int S,
                                                   float* __restrict__ khi, float* __restrict__ klo,
                                                   const ProblemTable tab) {
-  constexpr int RP = R < 32 ? 32 : R;
-  __shared__ float Ws[128 * R];
+  using C = ProjCfg<R>;
+  constexpr int RP = C::RP;
+  extern __shared__ __align__(16) uint8_t proj_smem[];
+  float* Ws = reinterpret_cast<float*>(proj_smem);
+  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(proj_smem + 128 * R * 4);
   const int lp = blockIdx.y, p = tab.p[lp], h = p % H;
+  const int tid = threadIdx.x, j0 = blockIdx.x * 128;
   const __nv_bfloat16* W = Wk + (size_t)h * d * R;
-  for (int i = threadIdx.x; i < d * R; i += 128) Ws[i] = __bfloat162float(W[i]);
+  for (int i = tid; i < d * R; i += 128) Ws[i] = __bfloat162float(W[i]);
+  const int cpr = d / 8;   // 16-byte chunks per key row
+  const uint4* src = reinterpret_cast<const uint4*>(K + ((size_t)p * S + j0) * d);
+  for (int i = tid; i < 128 * cpr; i += 128) {
+    const int row = i / cpr, ch = i % cpr;
+    *reinterpret_cast<uint4*>(Ks + row * C::kRowElems + ch * 8) = src[i];
+  }
   __syncthreads();
-  const int j = blockIdx.x * 128 + threadIdx.x;
-  const uint4* row = reinterpret_cast<const uint4*>(K + ((size_t)p * S + j) * d);
   float acc[R];
 #pragma unroll
   for (int c = 0; c < R; ++c) acc[c] = 0.f;
+  const __nv_bfloat16* krow = Ks + tid * C::kRowElems;
   for (int c8 = 0; c8 < d / 8; ++c8) {
-    const uint4 v = row[c8];
+    const uint4 v = *reinterpret_cast<const uint4*>(krow + c8 * 8);
     const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&v);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float xv = __bfloat162float(x[e]);
-      const float* w = Ws + (c8 * 8 + e) * R;
+      const float4* w4 = reinterpret_cast<const float4*>(Ws + (c8 * 8 + e) * R);
 #pragma unroll
-      for (int c = 0; c < R; ++c) acc[c] = fmaf(xv, w[c], acc[c]);
+      for (int c = 0; c < R / 4; ++c) {
+        const float4 wv = w4[c];
+        acc[4 * c + 0] = fmaf(xv, wv.x, acc[4 * c + 0]);
+        acc[4 * c + 1] = fmaf(xv, wv.y, acc[4 * c + 1]);
+        acc[4 * c + 2] = fmaf(xv, wv.z, acc[4 * c + 2]);
+        acc[4 * c + 3] = fmaf(xv, wv.w, acc[4 * c + 3]);
+      }
     }
   }
-  float* oh = khi + ((size_t)lp * S + j) * RP;
-  float* ol = klo + ((size_t)lp * S + j) * RP;
+  const size_t o = ((size_t)lp * S + j0 + tid) * RP;
 #pragma unroll
-  for (int c = 0; c < RP; ++c) {
-    const float v = c < R ? acc[c < R ? c : 0] : 0.f;
-    const float hi = tf32_rna(v);
-    oh[c] = hi;
-    ol[c] = tf32_rna(v - hi);
+  for (int c8 = 0; c8 < RP / 8; ++c8) {
+    uint32_t hv[8], lv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int c = c8 * 8 + e;
+      const float v = c < R ? acc[c < R ? c : 0] : 0.f;
+      const float hi = tf32_rna(v);
+      hv[e] = __float_as_uint(hi);
+      lv[e] = __float_as_uint(tf32_rna(v - hi));
+    }
+    st_global_v8(khi + o + c8 * 8, hv);
+    st_global_v8(klo + o + c8 * 8, lv);
   }
 }
 
@@ -591,7 +623,7 @@ __global__ void k_fill_all(int32_t* idx, int64_t off, int S, int64_t total) {
 // Coverage reduce, in three steps:
 //   k_cov_merge   (group, bin) totals over key chunks, one thread per pair
 //   k_cov_scan    per group: cumulative counts and normalised masses over bins
-//   k_cov_search  per problem: binary search of the smallest k with C(k) >= mass
+//   k_cov_eval/k_cov_pick  two wide rounds locating the smallest k with C(k) >= mass
 __global__ void k_cov_merge(const uint32_t* __restrict__ cnt, const float* __restrict__ mass, int nb, int n_chunks,
                             int g_pad, int n_groups, int32_t* cum_cnt, double* cum_mass) {
   const int lp = blockIdx.z, b = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
@@ -651,94 +683,112 @@ __global__ void k_cov_scan(const uint32_t* mmax, const uint32_t* mmin, int nb, i
   if (lane == 0) width[rid] = scale * (ord2f(mmax[rid]) - ord2f(mmin[rid])) / (float)nb;
 }
 
-// k-ary search (15 probes per round, about five rounds for S = 2^18) of the
-// smallest k with C(k) >= target; per-group terms in fp32, sums in fp64.
-constexpr int kProbes = 15;
-__global__ void __launch_bounds__(1024) k_cov_search(int nb, int g_pad, int n_groups, int S, float target,
-                                                     const int32_t* cum_cnt, const double* cum_mass,
-                                                     const float* width, int32_t* k_cov, float* curve, int n_curve,
-                                                     const ProblemTable tab) {
-  const int lp = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  __shared__ double red[32][kProbes];
-  __shared__ double tot[kProbes];
-  __shared__ int s_lo, s_hi;
-  // mass of group g's k most probable keys (interpolated inside the boundary bin)
-  auto m_of = [&](size_t rid, int k) -> float {
-    const int32_t* cc = cum_cnt + rid * nb;
-    const double* cm = cum_mass + rid * nb;
-    int lo = 0, hi = nb - 1;  // first bin with cumulative count >= k
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (cc[mid] >= k) hi = mid; else lo = mid + 1;
-    }
-    const int pc = lo > 0 ? cc[lo - 1] : 0;
-    const float pm = lo > 0 ? (float)cm[lo - 1] : 0.f;
-    const int n = cc[lo] - pc;
-    const float mb = (float)cm[lo] - pm;
-    const float f = n > 0 ? (float)(k - pc) / (float)n : 1.f;
-    const float dw = width[rid];
-    const float part = dw > 1e-6f ? mb * (1.f - __expf(-f * dw)) / (1.f - __expf(-dw)) : mb * f;
-    return pm + part;
-  };
-  // C at up to kProbes points, result in tot[]
-  auto eval = [&](const int* ks, int np) {
-    double acc[kProbes];
-    for (int i = 0; i < kProbes; ++i) acc[i] = 0.0;
-    for (int g = tid; g < n_groups; g += blockDim.x) {
-      const size_t rid = (size_t)lp * g_pad + g;
-      for (int i = 0; i < np; ++i) acc[i] += (double)m_of(rid, ks[i]);
-    }
-    for (int i = 0; i < np; ++i) {
-      double a = acc[i];
-      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-      if (lane == 0) red[wid][i] = a;
-    }
-    __syncthreads();
-    if (tid < np) {
-      double t = 0.0;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w][tid];
-      tot[tid] = t / (double)n_groups;
-    }
-    __syncthreads();
-  };
-  if (tid == 0) {
-    s_lo = 1;
-    s_hi = S;
+// Smallest k with C(k) >= target, in wide rounds. Each round evaluates C at
+// up to kCovPoints values of k spread evenly over the current interval
+// [lo, hi] (initially [1, S]) and keeps the sub-interval where C first
+// reaches the target; once the interval holds at most kCovPoints values,
+// every one of them is evaluated and the smallest qualifying k is the answer.
+// Each evaluation block takes kCovGroupsPerBlock groups and all points;
+// per-block partial sums are added in block order, so the result does not
+// depend on scheduling.
+constexpr int kCovPoints = 1024;
+constexpr int kCovGroupsPerBlock = 16;
+
+// C's per-group term: mass of the group's k most probable keys, interpolated
+// inside the boundary bin assuming evenly spread log-probabilities. cc / cm
+// are the group's cumulative counts and masses over its nb bins.
+__device__ __forceinline__ float cov_group_mass(const int32_t* cc, const float* cm, int nb, float dw, int k) {
+  int lo = 0, hi = nb - 1;  // first bin with cumulative count >= k
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (cc[mid] >= k) hi = mid; else lo = mid + 1;
   }
+  const int pc = lo > 0 ? cc[lo - 1] : 0;
+  const float pm = lo > 0 ? cm[lo - 1] : 0.f;
+  const int n = cc[lo] - pc;
+  const float mb = cm[lo] - pm;
+  const float f = n > 0 ? (float)(k - pc) / (float)n : 1.f;
+  const float part = dw > 1e-6f ? mb * (1.f - __expf(-f * dw)) / (1.f - __expf(-dw)) : mb * f;
+  return pm + part;
+}
+
+// The k of point p for interval [lo, hi] (search), or the curve's point p
+// (curve: k = ceil((p+1) S / n_curve)); -1 for no point.
+__device__ __forceinline__ int cov_point(bool curve, int lo, int hi, int p, int S, int n_curve) {
+  if (curve) return p < n_curve ? (int)(((int64_t)(p + 1) * S + n_curve - 1) / n_curve) : -1;
+  const int64_t span = (int64_t)hi - lo + 1;
+  if (span <= kCovPoints) return p < span ? lo + p : -1;
+  return (int)(lo - 1 + ((int64_t)(p + 1) * span + kCovPoints - 1) / kCovPoints);
+}
+
+// range[2*lp .. 2*lp+1] holds the current interval; round 0 ignores it and
+// starts from [1, S].
+__device__ __forceinline__ void cov_interval(int round, const int32_t* range, int lp, int S, int& lo, int& hi) {
+  lo = round == 0 ? 1 : range[2 * lp];
+  hi = round == 0 ? S : range[2 * lp + 1];
+}
+
+// One thread per point; the block's kCovGroupsPerBlock group tables are
+// staged in shared memory first.
+__global__ void __launch_bounds__(kCovPoints) k_cov_eval(int round, bool curve, int nb, int g_pad, int n_groups,
+                                                         int S, const int32_t* cum_cnt, const double* cum_mass,
+                                                         const float* width, const int32_t* range, int n_curve,
+                                                         double* partial) {
+  static_assert(SelCfg<32>::kCovBins <= 128 && SelCfg<64>::kCovBins <= 128, "coverage tables hold 128 bins");
+  __shared__ int32_t s_cc[kCovGroupsPerBlock * 128];
+  __shared__ float s_cm[kCovGroupsPerBlock * 128];
+  __shared__ float s_w[kCovGroupsPerBlock];
+  const int lp = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x, p = threadIdx.x;
+  const int g0 = blk * kCovGroupsPerBlock, ng = min(n_groups - g0, kCovGroupsPerBlock);
+  const size_t base = (size_t)lp * g_pad + g0;
+  for (int i = p; i < ng * nb; i += blockDim.x) {
+    s_cc[i] = cum_cnt[base * nb + i];
+    s_cm[i] = (float)cum_mass[base * nb + i];
+  }
+  if (p < ng) s_w[p] = width[base + p];
   __syncthreads();
-  int ks[kProbes];
-  while (true) {
-    const int lo = s_lo, hi = s_hi;   // answer in [lo, hi]; C(hi) >= target or hi == S
-    if (lo >= hi) break;
-    const int span = hi - lo;
-    int np = 0;
-    for (int i = 1; i <= kProbes; ++i) {
-      const int kp = lo + (int)(((int64_t)span * i) / (kProbes + 1));
-      if (kp >= lo && kp < hi && (np == 0 || kp > ks[np - 1])) ks[np++] = kp;
-    }
-    if (np == 0) ks[np++] = lo;
-    eval(ks, np);
-    if (tid == 0) {
-      int nlo = lo, nhi = hi;
-      for (int i = 0; i < np; ++i) {
-        if (tot[i] >= (double)target) { nhi = ks[i]; break; }
-        nlo = ks[i] + 1;
-      }
-      s_lo = nlo;
-      s_hi = nhi;
-    }
-    __syncthreads();
-  }
-  if (tid == 0) k_cov[tab.p[lp]] = s_lo;
+  int lo, hi;
+  cov_interval(round, range, lp, S, lo, hi);
+  const int k = cov_point(curve, lo, hi, p, S, n_curve);
+  double acc = 0.0;
+  if (k >= 1)
+    for (int g = 0; g < ng; ++g) acc += (double)cov_group_mass(s_cc + g * nb, s_cm + g * nb, nb, s_w[g], k);
+  partial[((size_t)lp * nblk + blk) * kCovPoints + p] = acc;
+}
+
+// Sums the partials of each point in block order. Search: narrow range[lp]
+// to the sub-interval where C first reaches the target, or, when every k of
+// the interval was evaluated, write k_cov. Curve: write the curve.
+__global__ void __launch_bounds__(1024) k_cov_pick(int round, bool curve, int nblk, int n_groups, int S,
+                                                   float target, const double* partial, int32_t* range,
+                                                   int32_t* k_cov, float* curve_out, int n_curve,
+                                                   const ProblemTable tab) {
+  __shared__ int first;
+  const int lp = blockIdx.x, p = threadIdx.x;
+  int lo, hi;
+  cov_interval(round, range, lp, S, lo, hi);
+  if (p == 0) first = kCovPoints;
+  __syncthreads();  // every thread has read range before thread 0 rewrites it
+  const int k = cov_point(curve, lo, hi, p, S, n_curve);
+  double c = 0.0;
+  for (int b = 0; b < nblk; ++b) c += partial[((size_t)lp * nblk + b) * kCovPoints + p];
+  c /= (double)n_groups;
   if (curve) {
-    for (int c0 = 0; c0 < n_curve; c0 += kProbes) {
-      const int np = min(kProbes, n_curve - c0);
-      for (int i = 0; i < np; ++i) ks[i] = (int)(((int64_t)(c0 + i + 1) * S + n_curve - 1) / n_curve);
-      eval(ks, np);
-      if (tid < np) curve[(size_t)tab.p[lp] * n_curve + c0 + tid] = (float)tot[tid];
-      __syncthreads();
-    }
+    if (k >= 1) curve_out[(size_t)tab.p[lp] * n_curve + p] = (float)c;
+    return;
   }
+  if (k >= 1 && c >= (double)target) atomicMin(&first, p);
+  __syncthreads();
+  if (p != 0) return;
+  const int64_t span = (int64_t)hi - lo + 1;
+  if (span <= kCovPoints) {
+    // C(S) = 1 >= target up to rounding; with no qualifying point keep hi
+    k_cov[tab.p[lp]] = first < kCovPoints ? lo + first : hi;
+    return;
+  }
+  const int f = first < kCovPoints ? first : kCovPoints - 1;  // answer in (k_{f-1}, k_f]
+  range[2 * lp] = f > 0 ? cov_point(false, lo, hi, f - 1, S, 0) + 1 : lo;
+  range[2 * lp + 1] = cov_point(false, lo, hi, f, S, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -782,6 +832,8 @@ struct TopkWs {
   int32_t* cum_cnt;
   double* cum_mass;
   float* width;
+  double* cov_partial;
+  int32_t* cov_range;
 };
 
 // Carves the workspace (base == nullptr: sizing only). `cov` selects the
@@ -812,6 +864,8 @@ static size_t carve(void* base, const TopkPlan& pl, bool cov, TopkWs* w) {
     w->cum_cnt = c.take<int32_t>(pc * gp * pl.cov_bins);
     w->cum_mass = c.take<double>(pc * gp * pl.cov_bins);
     w->width = c.take<float>(pc * gp);
+    w->cov_partial = c.take<double>(pc * ((gp + kCovGroupsPerBlock - 1) / kCovGroupsPerBlock) * kCovPoints);
+    w->cov_range = c.take<int32_t>(pc * 2);
   }
   return c.used + 256;
 }
@@ -850,17 +904,24 @@ static cudaError_t launch_proj(int r, const void* Q, const void* K, const void* 
   auto Qp = static_cast<const __nv_bfloat16*>(Q);
   auto Wkp = static_cast<const __nv_bfloat16*>(Wk);
   auto Wqp = static_cast<const __nv_bfloat16*>(Wq);
+  static bool proj_configured = false;
+  if (!proj_configured) {
+    cudaFuncSetAttribute(k_key_proj<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, ProjCfg<16>::kSmem);
+    cudaFuncSetAttribute(k_key_proj<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, ProjCfg<32>::kSmem);
+    cudaFuncSetAttribute(k_key_proj<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, ProjCfg<64>::kSmem);
+    proj_configured = true;
+  }
   switch (r) {
     case 16:
-      k_key_proj<16><<<gk, 128, 0, st>>>(Kp, Wkp, s.H, d, pl.geo.S, w.khi, w.klo, tab);
+      k_key_proj<16><<<gk, 128, ProjCfg<16>::kSmem, st>>>(Kp, Wkp, s.H, d, pl.geo.S, w.khi, w.klo, tab);
       k_group_mean_proj<16><<<gq, 128, 0, st>>>(Qp, Wqp, s.H, d, pl.geo, pl.g_pad, w.qhi, w.qlo, tab);
       break;
     case 32:
-      k_key_proj<32><<<gk, 128, 0, st>>>(Kp, Wkp, s.H, d, pl.geo.S, w.khi, w.klo, tab);
+      k_key_proj<32><<<gk, 128, ProjCfg<32>::kSmem, st>>>(Kp, Wkp, s.H, d, pl.geo.S, w.khi, w.klo, tab);
       k_group_mean_proj<32><<<gq, 128, 0, st>>>(Qp, Wqp, s.H, d, pl.geo, pl.g_pad, w.qhi, w.qlo, tab);
       break;
     default:
-      k_key_proj<64><<<gk, 128, 0, st>>>(Kp, Wkp, s.H, d, pl.geo.S, w.khi, w.klo, tab);
+      k_key_proj<64><<<gk, 128, ProjCfg<64>::kSmem, st>>>(Kp, Wkp, s.H, d, pl.geo.S, w.khi, w.klo, tab);
       k_group_mean_proj<64><<<gq, 128, 0, st>>>(Qp, Wqp, s.H, d, pl.geo, pl.g_pad, w.qhi, w.qlo, tab);
       break;
   }
@@ -996,7 +1057,7 @@ extern "C" dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_
   dsv_status v = validate_lowrank(Q, K, Wq_lr, Wk_lr, shape, r, group);
   if (v != DSV_OK) return v;
   if (!k_cov || !(scale > 0.f) || !(mass > 0.f && mass <= 1.f)) return DSV_ERR_INVALID_ARG;
-  if (curve && n_curve < 1) return DSV_ERR_INVALID_ARG;
+  if (curve && (n_curve < 1 || n_curve > 1024)) return DSV_ERR_INVALID_ARG;
   const TopkPlan pl = make_plan(shape, r, group);
   TopkWs w;
   const size_t need = carve(nullptr, pl, true, &w);
@@ -1044,8 +1105,22 @@ extern "C" dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_
     k_cov_scan<<<dim3((pl.geo.n_groups + 7) / 8, n), 256, 0, st>>>(w.mmax, w.mmin, pl.cov_bins, pl.g_pad,
                                                                     pl.geo.n_groups, scale, w.cum_cnt, w.cum_mass,
                                                                     w.width);
-    k_cov_search<<<n, 1024, 0, st>>>(pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.geo.S, mass, w.cum_cnt, w.cum_mass,
-                                     w.width, k_cov, curve, n_curve, tab);
+    const int nblk = (pl.geo.n_groups + kCovGroupsPerBlock - 1) / kCovGroupsPerBlock;
+    // rounds: the interval shrinks from S values to at most ceil(span / kCovPoints) per round
+    int rounds = 1;
+    for (int64_t span = pl.geo.S; span > kCovPoints; span = (span + kCovPoints - 1) / kCovPoints) ++rounds;
+    for (int round = 0; round < rounds; ++round) {
+      k_cov_eval<<<dim3(nblk, n), kCovPoints, 0, st>>>(round, false, pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.geo.S,
+                                                 w.cum_cnt, w.cum_mass, w.width, w.cov_range, 0, w.cov_partial);
+      k_cov_pick<<<n, kCovPoints, 0, st>>>(round, false, nblk, pl.geo.n_groups, pl.geo.S, mass, w.cov_partial,
+                                            w.cov_range, k_cov, nullptr, 0, tab);
+    }
+    if (curve) {
+      k_cov_eval<<<dim3(nblk, n), kCovPoints, 0, st>>>(0, true, pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.geo.S,
+                                                 w.cum_cnt, w.cum_mass, w.width, w.cov_range, n_curve, w.cov_partial);
+      k_cov_pick<<<n, kCovPoints, 0, st>>>(0, true, nblk, pl.geo.n_groups, pl.geo.S, mass, w.cov_partial,
+                                            w.cov_range, k_cov, curve, n_curve, tab);
+    }
     if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
   }
   return DSV_OK;

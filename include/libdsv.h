@@ -135,7 +135,7 @@ dsv_status dsv_lowrank_topk_noalloc(const void* Q, const void* K, const void* Wq
  * interpolated inside a bin assuming log-probabilities spread evenly across
  * it.
  * k_cov: DEVICE int32 [B*H]. curve (optional, may be NULL): DEVICE float
- * [B*H][n_curve], C(k) sampled at k = ceil((i+1)*S/n_curve), i < n_curve.
+ * [B*H][n_curve] (n_curve <= 1024), C(k) sampled at k = ceil((i+1)*S/n_curve).
  * ---------------------------------------------------------------------- */
 size_t dsv_coverage_workspace_size(dsv_shape shape, int32_t r, dsv_group group);
 dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr, dsv_shape shape,
@@ -197,7 +197,8 @@ dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const void* V, cons
  * and idx_offset to dsv_sparse_attn_bwd_workspace_size (it holds the bf16
  * partials of up to 8 GiB worth of (group, key) pairs at a time, a key x group
  * selection bitmap and per-key slot offsets; a head with more pairs is split
- * over several launches with fp32 running sums).
+ * over several launches with fp32 running sums). Sparse problems need
+ * S <= 262144 (DSV_ERR_UNSUPPORTED otherwise); dense problems do not.
  * ---------------------------------------------------------------------- */
 size_t dsv_sparse_attn_bwd_workspace_size(dsv_shape shape, dsv_group group, const int32_t* k_per_head,
                                           const int64_t* idx_offset);
