@@ -32,7 +32,15 @@
 namespace dsv {
 
 constexpr int kBwdThreads = 192;                       // key-major kernel
-constexpr int kBwdQThreads = 32 * (9 + kGatherWarps);   // group-major kernel
+// Group-major kernel: three warpgroups. Registers per thread at launch are
+// 16384 / (3 warps x 32 lanes) per SM sub-partition, rounded down to 8; the
+// warpgroups then rebalance them (softmax up, loaders down) so that the three
+// shares add up to exactly the launch total.
+constexpr int kBwdQThreads = 384;
+constexpr int kBwdQLaunchRegs = 168;
+constexpr int kRegsSoftmax = 232, kRegsDrain = 136, kRegsLoad = 136;
+static_assert(kRegsSoftmax + kRegsDrain + kRegsLoad == 3 * kBwdQLaunchRegs, "register split must equal the launch");
+static_assert(kGatherWarps == 2, "warps 8-9 gather, warp 10 issues MMAs, warp 11 idles");
 constexpr int kMaxUnits = 48;                       // work units per group-major launch
 constexpr size_t kPartialBudget = 8ull << 30;       // bytes of bf16 dK/dV partials in flight
 constexpr int kMaxBlocks = 1024;                    // 256-key blocks per problem (S <= 2^18)
@@ -70,7 +78,9 @@ struct BwdCfg {
   static constexpr int kTile = 128 * D * 2;      // one [128][D] bf16 tile
   static constexpr int kKStages = 2;
   static constexpr int kVStages = D == 128 ? 1 : 2;
-  static constexpr int kHalves = D / 64;         // dV/dK are produced 64 columns at a time
+  // dV/dK jobs share one 128-column TMEM region: with d = 128 a job is dV,
+  // then dK, over the full width; with d = 64 one job holds both.
+  static constexpr int kJobs = D == 128 ? 2 : 1;
   static constexpr int kOffDO = kTile;           // Q at 0
   static constexpr int kOffK = 2 * kTile;
   static constexpr int kOffV = kOffK + kKStages * kTile;
@@ -79,11 +89,11 @@ struct BwdCfg {
   static constexpr int kOffBar = kOffDS + 32768;
   static constexpr int kSmemUsed = kOffBar + 1024 + 1024;
   static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
-  // TMEM columns: S, dP, dQ accumulator, then one 64-column half of dV and of dK
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDV = 256 + D, kColDK = 320 + D;
+  // TMEM columns: S, dP, dQ accumulator, then the dV/dK job region
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColJob = 256 + D;
 };
 static_assert(BwdCfg<128>::kSmemUsed <= 232448, "group-major backward exceeds shared memory");
-static_assert(BwdCfg<128>::kColDK + 64 <= 512 && BwdCfg<64>::kColDK + 64 <= 512, "TMEM budget");
+static_assert(BwdCfg<128>::kColJob + 128 <= 512 && BwdCfg<64>::kColJob + 128 <= 512, "TMEM budget");
 
 __device__ __forceinline__ void compute_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -99,9 +109,9 @@ __device__ __forceinline__ void st_sw128_chunk(uint8_t* tile, int row, int chunk
 // warps 4-7 drain the dV/dK partial halves to their slots and write dQ at
 // the end; warps 8-9 load (cp.async row gather or TMA boxes); warp 10 issues
 // the MMAs. Per 128-key tile t:
-//   S, dP (TMEM) -> P, dS (smem) -> dQ += dS K; then for each 64-column half
-//   h: dV_h = P^T dO_h, dK_h = dS^T Q_h into one TMEM half-region, drained
-//   while the next tile's S, dP are computed.
+//   S, dP (TMEM) -> P, dS (smem) -> dQ += dS K; then dV = P^T dO and
+//   dK = dS^T Q, one after the other, in a shared 128-column TMEM region,
+//   each drained while the tensor cores move on.
 template <int D>
 __global__ void __launch_bounds__(kBwdQThreads, 1)
     k_attn_bwd_q(const __grid_constant__ AttnMaps maps, const __grid_constant__ CUtensorMap do_cube,
@@ -178,7 +188,9 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp >= kProdWarp && warp < kMmaWarp) {
+  if (warp >= kProdWarp) {
+   setmaxnreg_dec<kRegsLoad>();   // the whole warpgroup (warps 8-11) executes this one instruction
+   if (warp < kMmaWarp) {
     // ----------------------------------------------------------- producers
     const int pw = warp - kProdWarp;
     const int ct = g / (geo.ncy * geo.ncx), cy = (g / geo.ncx) % geo.ncy, cx = g % geo.ncx;
@@ -222,12 +234,12 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         load_dense_tile<D>(sV + vs * C::kTile, &maps.v_tile, v_full + vs, t, prow0);
       }
     }
-  } else if (warp == kMmaWarp) {
+   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t id_sdp = instr_desc(128, 128, 1, 0, 0);   // Q K^T, dO V^T
       constexpr uint32_t id_dq = instr_desc(128, D, 1, 0, 1);      // dS K (B = K, MN-major)
-      constexpr uint32_t id_kv = instr_desc(128, 64, 1, 1, 1);     // P^T dO_h, dS^T Q_h (A, B MN-major)
+      constexpr uint32_t id_kv = instr_desc(128, D == 128 ? 128 : 64, 1, 1, 1);   // P^T dO, dS^T Q (MN-major)
       const uint32_t aq = smem_u32(sQ), ado = smem_u32(sDO), ap = smem_u32(sP), ads = smem_u32(sDS);
       bool ok = mbar_wait(q_full, 0, kWaitLimitNs);
       auto issue_sdp = [&](int t) -> bool {
@@ -253,19 +265,21 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         mma_commit(v_empty + vs);
         return true;
       };
-      int job = 0;   // dV/dK half-jobs issued so far
-      auto issue_half = [&](int h) -> bool {
+      int job = 0;   // dV/dK jobs issued so far
+      auto issue_job = [&](int jb) -> bool {
         if (job >= 1 && !mbar_wait(part_free, (job - 1) & 1, kWaitLimitNs)) return false;
         tc_fence_after();
+        if (D == 64 || jb == 0) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          mma_f16_ss(tbase + C::kColDV, smem_desc(ap + kk * 2048, 16384, 1024),
-                     smem_desc(ado + h * 16384 + kk * 2048, 16384, 1024), id_kv, kk > 0);
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ss(tbase + C::kColJob, smem_desc(ap + kk * 2048, 16384, 1024),
+                       smem_desc(ado + kk * 2048, 16384, 1024), id_kv, kk > 0);
         }
+        if (D == 64 || jb == 1) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          mma_f16_ss(tbase + C::kColDK, smem_desc(ads + kk * 2048, 16384, 1024),
-                     smem_desc(aq + h * 16384 + kk * 2048, 16384, 1024), id_kv, kk > 0);
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ss(tbase + C::kColJob + (D == 64 ? 64 : 0), smem_desc(ads + kk * 2048, 16384, 1024),
+                       smem_desc(aq + kk * 2048, 16384, 1024), id_kv, kk > 0);
         }
         mma_commit(part_full);
         ++job;
@@ -286,10 +300,9 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
                      (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(k_empty + ks);
-        if (partials && !issue_half(0)) { ok = false; break; }
         if (partials) {
-          for (int h = 1; h < C::kHalves; ++h)
-            if (!issue_half(h)) { ok = false; break; }
+          for (int jb = 0; jb < C::kJobs; ++jb)
+            if (!issue_job(jb)) { ok = false; break; }
           if (!ok) break;
         }
         mma_commit(p_free);
@@ -297,8 +310,10 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       if (ok) mma_commit(dq_done);
       else raise_status(prm.status, DSV_ERR_TIMEOUT);
     }
+   }
   } else if (warp < 4) {
     // ------------------------------------------- S, dP -> P, dS (warps 0-3)
+    setmaxnreg_inc<kRegsSoftmax>();
     const int row = warp * 32 + lane;
     const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
     const float sc = prm.scale_log2;
@@ -362,8 +377,9 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       if (lane == 0) mbar_arrive(ps_full);
     }
     if (!ok && lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
-  } else if (warp < 8) {
+  } else if (warp >= 4 && warp < 8) {
     // -------------------------------- dV/dK partial drain, then dQ (warps 4-7)
+    setmaxnreg_dec<kRegsDrain>();
     const int q = warp - 4;
     const int row = q * 32 + lane;   // key slot of the tile for the partials; query row for dQ
     const uint32_t lane_addr = tbase + ((uint32_t)(q * 32) << 16);
@@ -386,33 +402,36 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       const int64_t pos = pos_next;
       const int nslot = (t + 1) * 128 + row;
       j_next = (t + 1 < nt && nslot < k) ? __ldg(idx_row + nslot) : -1;   // next tile's key, loaded early
-      for (int h = 0; h < C::kHalves; ++h, ++job) {
+      for (int jb = 0; jb < C::kJobs; ++jb, ++job) {
         ok = ok && mbar_wait_warp(part_full, job & 1, kWaitLimitNs);
         tc_fence_after();
 #pragma unroll 1
-        for (int tensor = 0; tensor < 2; ++tensor) {
-          const uint32_t col = tensor == 0 ? C::kColDV : C::kColDK;
-          const float mul = tensor == 0 ? 1.f : prm.scale;
-          __nv_bfloat16* dst_row = (tensor == 0 ? csc.part_v : csc.part_k) + pos * D + h * 64;
+        for (int c2 = 0; c2 < 4; c2 += 2) {
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = c2; c < c2 + 2; ++c) {
+            // 32-column chunk c of the job region: d = 128: columns c*32.. of dV (job 0) or dK (job 1);
+            // d = 64: dV columns for c < 2, dK columns for c >= 2
+            const int tensor = D == 128 ? jb : (c >> 1);
+            const int dcol = D == 128 ? c * 32 : (c & 1) * 32;
+            const float mul = tensor == 0 ? 1.f : prm.scale;
             uint32_t v[32];
-            tmem_ld32(lane_addr + col + c * 32, v);
+            tmem_ld32(lane_addr + C::kColJob + c * 32, v);
             tmem_ld_wait(v);
             if (kvalid) {
+              __nv_bfloat16* dst = (tensor == 0 ? csc.part_v : csc.part_k) + pos * D + dcol;
               uint32_t pk[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e)
                 pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-              st_global_v8(dst_row + c * 32, pk);
-              st_global_v8(dst_row + c * 32 + 16, pk + 8);
+              st_global_v8(dst, pk);
+              st_global_v8(dst + 16, pk + 8);
             }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(part_free);
-        if (h == 0) pos_next = j_next >= 0 ? slot_of(j_next) : 0;   // overlaps the next half's MMAs
+        if (jb == 0) pos_next = j_next >= 0 ? slot_of(j_next) : 0;   // overlaps the next job's MMAs
       }
     }
     // ----------------------------------------------------------- dQ out
@@ -806,6 +825,12 @@ static cudaError_t configure_bwd() {
   cudaError_t e = cudaFuncSetAttribute(k_attn_bwd_q<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_attn_bwd_kv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::kSmem);
+  // The warpgroups' register shares add up to kBwdQLaunchRegs per thread; a
+  // build that launched with any other count would never satisfy the softmax
+  // warpgroup's increase, so it is refused here instead of launched.
+  cudaFuncAttributes a;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, k_attn_bwd_q<D>);
+  if (e == cudaSuccess && a.numRegs != kBwdQLaunchRegs) e = cudaErrorInvalidConfiguration;
   if (e == cudaSuccess) done = true;
   return e;
 }

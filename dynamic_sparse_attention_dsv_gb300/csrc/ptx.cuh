@@ -178,6 +178,9 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
   asm volatile("" : DSV_P8(0), DSV_P8(8), DSV_P8(16), DSV_P8(24)::"memory");
 }
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[16]) {
+  asm volatile("" : DSV_P8(0), DSV_P8(8)::"memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
@@ -262,6 +265,18 @@ __host__ __device__ __forceinline__ uint32_t sw128_off32(uint32_t row, uint32_t 
 }
 
 // 2^x on the special-function unit (about 2 ulp; flushes denormals).
+// Per-warpgroup register reallocation. Every warp of the warpgroup executes
+// the same instruction; an increase waits until other warpgroups of the CTA
+// have released enough of the CTA's launch-time registers.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ float ex2_fast(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
