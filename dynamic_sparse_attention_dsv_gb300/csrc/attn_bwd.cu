@@ -343,28 +343,60 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       ok = ok && mbar_wait_warp(sdp_full, t & 1, kWaitLimitNs);
       tc_fence_after();
       const int nvalid = min(128, k - t * 128);
-      uint32_t pw[64], dw[64];
+      // TMEM loads complete long after they issue, so they go out in two
+      // batches: S (all 128 columns) with dP columns 0-63, then dP 64-127,
+      // whose latency hides behind the first half's arithmetic.
+      uint32_t sr[4][32], da[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(lane_addr + C::kColS + c * 32, sr);
-        tmem_ld32(lane_addr + C::kColDP + c * 32, dr);
-        tmem_ld_wait(sr);
-        reg_fence(dr);
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + C::kColS + c * 32, sr[c]);
+      tmem_ld32(lane_addr + C::kColDP, da[0]);
+      tmem_ld32(lane_addr + C::kColDP + 32, da[1]);
+      tmem_ld_wait(sr[0]);
+      reg_fence(sr[1]);
+      reg_fence(sr[2]);
+      reg_fence(sr[3]);
+      reg_fence(da[0]);
+      reg_fence(da[1]);
+      uint32_t pw[64], dw[64];
+      // columns 0-63: P and dS
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int j = c * 32 + e;
-          const float p0 = j < nvalid ? ex2_fast(__uint_as_float(sr[e]) * sc - lse2) : 0.f;
-          const float p1 = j + 1 < nvalid ? ex2_fast(__uint_as_float(sr[e + 1]) * sc - lse2) : 0.f;
-          const float d0 = p0 * (__uint_as_float(dr[e]) - delta);
-          const float d1 = p1 * (__uint_as_float(dr[e + 1]) - delta);
+          const float p0 = j < nvalid ? ex2_fast(__uint_as_float(sr[c][e]) * sc - lse2) : 0.f;
+          const float p1 = j + 1 < nvalid ? ex2_fast(__uint_as_float(sr[c][e + 1]) * sc - lse2) : 0.f;
           pw[j >> 1] = pack_bf16x2(p0, p1);
-          dw[j >> 1] = pack_bf16x2(d0, d1);
+          dw[j >> 1] = pack_bf16x2(p0 * (__uint_as_float(da[c][e]) - delta),
+                                   p1 * (__uint_as_float(da[c][e + 1]) - delta));
         }
-      }
+      // dP columns 64-127 into the registers just freed
+#pragma unroll
+      for (int c = 0; c < 2; ++c) tmem_ld32(lane_addr + C::kColDP + 64 + c * 32, da[c]);
+      // columns 64-127: P (fp32, in place of S) while the dP loads are in flight
+#pragma unroll
+      for (int c = 2; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int j = c * 32 + e;
+          const float pv = j < nvalid ? ex2_fast(__uint_as_float(sr[c][e]) * sc - lse2) : 0.f;
+          sr[c][e] = __float_as_uint(pv);
+        }
+      tmem_ld_wait(da[0]);
+      reg_fence(da[1]);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sdp_free);
+      if (lane == 0) mbar_arrive(sdp_free);   // S and dP of tile t are in registers
+#pragma unroll
+      for (int c = 2; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int j = c * 32 + e;
+          const float p0 = __uint_as_float(sr[c][e]), p1 = __uint_as_float(sr[c][e + 1]);
+          pw[j >> 1] = pack_bf16x2(p0, p1);
+          dw[j >> 1] = pack_bf16x2(p0 * (__uint_as_float(da[c - 2][e]) - delta),
+                                   p1 * (__uint_as_float(da[c - 2][e + 1]) - delta));
+        }
       // P/dS of the previous tile must no longer be read by the tensor cores
       if (t >= 1) ok = ok && mbar_wait_warp(p_free, (t - 1) & 1, kWaitLimitNs);
 #pragma unroll
