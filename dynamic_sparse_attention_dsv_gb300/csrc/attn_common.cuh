@@ -56,27 +56,28 @@ inline bool make_attn_maps(AttnMaps* m, const void* Q, const void* K, const void
 }
 
 // ---------------------------------------------------------------------------
-// Row gather of selected K/V rows with cp.async by kGatherWarps producer
-// warps. A warp instruction copies whole rows (d*2 bytes = d/8 16-byte
-// chunks, consecutive lanes on consecutive chunks) into the K-major 128-byte
-// swizzled tile layout the tensor cores read. Per tile and tensor each lane
-// copies kGatherIters chunks.
+// Row gather of selected K/V rows with cp.async by W producer warps. A warp
+// instruction copies whole rows (d*2 bytes = d/8 16-byte chunks, consecutive
+// lanes on consecutive chunks) into the K-major 128-byte swizzled tile layout
+// the tensor cores read. Per tile and tensor each lane copies kIters chunks.
+// The rate at which an SM issues these copies grows with the number of
+// issuing warps, so a kernel that is bound by its gathers uses more of them.
 constexpr int kGatherWarps = 2;
 
-template <int D>
+template <int D, int W = kGatherWarps>
 struct Gather {
   static constexpr int kChunksPerRow = D / 8;                      // 16-byte chunks per row
   static constexpr int kRowsPerInstr = 32 / kChunksPerRow;         // rows per warp instruction
-  static constexpr int kRowsPerWarp = 128 / kGatherWarps;
+  static constexpr int kRowsPerWarp = 128 / W;
   static constexpr int kIters = kRowsPerWarp / kRowsPerInstr;      // instructions per lane per tensor
 };
 
 // Key rows (absolute row in the [P*S][d] tensor) this lane copies for tile t.
 // Slots past k repeat the row's last key, so every copied row is a real key.
-template <int D>
-__device__ __forceinline__ void gather_rows(int (&rows)[Gather<D>::kIters], const int32_t* idx_row, int k, int t,
+template <int D, int W = kGatherWarps>
+__device__ __forceinline__ void gather_rows(int (&rows)[Gather<D, W>::kIters], const int32_t* idx_row, int k, int t,
                                             int prow0, int pw, int lane) {
-  using Gt = Gather<D>;
+  using Gt = Gather<D, W>;
 #pragma unroll
   for (int i = 0; i < Gt::kIters; ++i) {
     const int slot = t * 128 + pw * Gt::kRowsPerWarp + i * Gt::kRowsPerInstr + lane / Gt::kChunksPerRow;
@@ -84,10 +85,10 @@ __device__ __forceinline__ void gather_rows(int (&rows)[Gather<D>::kIters], cons
   }
 }
 
-template <int D>
-__device__ __forceinline__ void gather_tile(uint8_t* dst, const __nv_bfloat16* src, const int (&rows)[Gather<D>::kIters],
-                                            int pw, int lane) {
-  using Gt = Gather<D>;
+template <int D, int W = kGatherWarps>
+__device__ __forceinline__ void gather_tile(uint8_t* dst, const __nv_bfloat16* src,
+                                            const int (&rows)[Gather<D, W>::kIters], int pw, int lane) {
+  using Gt = Gather<D, W>;
   const int chunk = lane % Gt::kChunksPerRow;
   const uint32_t base = smem_u32(dst) + (chunk >> 3) * 16384;
 #pragma unroll

@@ -17,9 +17,13 @@
 // The running max m is raised lazily (only when it grows by more than 8 in
 // log2 units, which bounds P by 2^8), so O is rescaled rarely.
 //
-// Warps 0-3: softmax and epilogue (thread = query row = TMEM lane).
-// Warps 4-5: producers (cp.async row gather of the selected K/V rows; TMA
-// boxes for dense tiles and the query cube). Warp 6: MMA issuer.
+// Warps 0-7: softmax and epilogue, two warps per query row (TMEM lane): warp
+// w takes key columns 64*(w/4) .. +63 of the rows in lane quarter w%4 and
+// half of O's columns; the pair exchanges its partial row maxima (and row
+// sums at the end) through shared memory. Warps 8-11: producers (cp.async row
+// gather of the selected K/V rows; TMA boxes for dense tiles and the query
+// cube). Warp 12: MMA issuer; warps 13-15 idle. The four warpgroups rebalance
+// their registers after launch (softmax up, the rest down).
 #include "attn_common.cuh"
 
 namespace dsv {
@@ -30,14 +34,24 @@ struct FwdCfg {
   static constexpr int kTile = 128 * D * 2;            // bytes of one 128-row bf16 tile
   static constexpr int kOffK = kTile;                  // Q first
   static constexpr int kOffV = kOffK + kStages * kTile;
-  static constexpr int kOffBar = kOffV + kStages * kTile;
-  static constexpr int kSmemUsed = kOffBar + 256 + 1024;
+  static constexpr int kOffBar = kOffV + kStages * kTile;   // barriers; pair status flags at +192
+  static constexpr int kOffX = kOffBar + 256;                // [2 halves][128 rows] fp32 exchange
+  static constexpr int kSmemUsed = kOffX + 1024 + 1024;
   // at least half the SM's shared memory, so one CTA owns the SM's TMEM
   static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
-  static constexpr int kThreads = 32 * (5 + kGatherWarps);
+  static constexpr int kGatherW = 4;                   // producer warps
+  static constexpr int kThreads = 512;
+  static constexpr int kLaunchRegs = 128;              // 16384 / (4 warps x 32 lanes) per SM sub-partition
+  static constexpr int kRegsSoftmax = 168, kRegsLoad = 96, kRegsMma = 80;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;               // S buffers at 0 and 128
 };
+
+static_assert(FwdCfg<128>::kSmemUsed <= 232448 && FwdCfg<64>::kSmemUsed <= 232448, "forward exceeds shared memory");
+static_assert(FwdCfg<128>::kOffX == FwdCfg<128>::kOffBar + 256, "status flags live in the barrier block");
+static_assert(2 * FwdCfg<128>::kRegsSoftmax + FwdCfg<128>::kRegsLoad + FwdCfg<128>::kRegsMma ==
+                  4 * FwdCfg<128>::kLaunchRegs,
+              "register split must equal the launch");
 
 template <int D>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
@@ -76,14 +90,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
     fence_proxy_async_smem();
   }
-  constexpr int kMmaWarp = 4 + kGatherWarps;
+  constexpr int kProdWarp = 8, kMmaWarp = 12;
+  constexpr int W = C::kGatherW;
   if (warp == kMmaWarp) {
     tmem_alloc(tslot, C::kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
     mbar_init(q_full, 1);
-    const uint32_t fills = dense ? 1u : 32u * kGatherWarps;   // TMA tx arrival, or one per gathering lane
+    const uint32_t fills = dense ? 1u : 32u * W;   // TMA tx arrival, or one per gathering lane
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(k_full + i, fills);
       mbar_init(v_full + i, fills);
@@ -91,7 +106,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(p_full + i, 4);
+      mbar_init(p_full + i, 8);
     }
     mbar_init(o_ready, 1);
     fence_mbar_init();
@@ -101,9 +116,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp >= 4 && warp < kMmaWarp) {
+  if (warp >= kProdWarp && warp < kMmaWarp) {
     // ----------------------------------------------------------- producers
-    const int pw = warp - 4;
+    setmaxnreg_dec<C::kRegsLoad>();
+    const int pw = warp - kProdWarp;
     const int ct = g / (geo.ncy * geo.ncx), cy = (g / geo.ncx) % geo.ncy, cx = g % geo.ncx;
     if (pw == 0 && lane == 0) {
       prefetch_tmap(&maps.q_cube);
@@ -113,20 +129,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
     const int prow0 = p * geo.S;
     if (idx_row) {
-      int rows[Gather<D>::kIters], nxt[Gather<D>::kIters];
-      gather_rows<D>(nxt, idx_row, k, 0, prow0, pw, lane);
+      int rows[Gather<D, W>::kIters], nxt[Gather<D, W>::kIters];
+      gather_rows<D, W>(nxt, idx_row, k, 0, prow0, pw, lane);
       for (int t = 0; t < nt; ++t) {
         const int s = t % C::kStages;
 #pragma unroll
-        for (int i = 0; i < Gather<D>::kIters; ++i) rows[i] = nxt[i];
-        if (t + 1 < nt) gather_rows<D>(nxt, idx_row, k, t + 1, prow0, pw, lane);
+        for (int i = 0; i < Gather<D, W>::kIters; ++i) rows[i] = nxt[i];
+        if (t + 1 < nt) gather_rows<D, W>(nxt, idx_row, k, t + 1, prow0, pw, lane);
         if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, kWaitLimitNs)) {
           if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
           break;
         }
-        gather_tile<D>(sK + s * C::kTile, prm.K, rows, pw, lane);
+        gather_tile<D, W>(sK + s * C::kTile, prm.K, rows, pw, lane);
         cp_async_arrive_noinc(k_full + s);
-        gather_tile<D>(sV + s * C::kTile, prm.V, rows, pw, lane);
+        gather_tile<D, W>(sV + s * C::kTile, prm.V, rows, pw, lane);
         cp_async_arrive_noinc(v_full + s);
       }
     } else if (pw == 0) {
@@ -144,9 +160,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
+  } else if (warp >= kMmaWarp) {
+    // ------------------------------------------------- MMA (warp 12; 13-15 idle)
+    setmaxnreg_dec<C::kRegsMma>();
+    if (warp == kMmaWarp && lane == 0) {
       constexpr uint32_t idesc_qk = instr_desc(128, 128, 1, 0, 0);
       constexpr uint32_t idesc_pv = instr_desc(128, D, 1, 0, 1);
       const uint32_t q_addr = smem_u32(sQ);
@@ -186,30 +203,57 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       if (!ok) raise_status(prm.status, DSV_ERR_TIMEOUT);
     }
   } else {
-    // ----------------------------------------------------- softmax (warps 0-3)
-    const int row = warp * 32 + lane;
-    const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+    // ----------------------------------------------------- softmax (warps 0-7)
+    setmaxnreg_inc<C::kRegsSoftmax>();
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tbase + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t pair_bar = 1 + quarter;   // named barrier of warps quarter and quarter + 4
+    float* xch = reinterpret_cast<float*>(sm + C::kOffX);
+    volatile int* xok = reinterpret_cast<volatile int*>(sm + C::kOffBar + 192);
+    // Publishes v (and this warp's status), returns the partner's v; both warps
+    // leave with the same status. The second barrier keeps the next exchange
+    // from overwriting a value the partner has not read yet.
+    auto exchange = [&](float v, bool& ok_io) -> float {
+      xch[half * 128 + row] = v;
+      if (lane == 0) xok[half * 4 + quarter] = ok_io ? 1 : 0;
+      asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+      const float other = xch[(half ^ 1) * 128 + row];
+      ok_io = ok_io && xok[(half ^ 1) * 4 + quarter] != 0;
+      asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+      return other;
+    };
+    constexpr int kOChunks = D / 64;   // 32-column chunks of O per warp
     const float sc = prm.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
       const int b = t & 1;
-      if (!mbar_wait_warp(s_full + b, (t >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
+      ok = ok && mbar_wait_warp(s_full + b, (t >> 1) & 1, kWaitLimitNs);
       tc_fence_after();
-      uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + b * 128 + c * 32, r[c]);
+      uint32_t r[2][32];
+      tmem_ld32(lane_addr + b * 128 + half * 64, r[0]);
+      tmem_ld32(lane_addr + b * 128 + half * 64 + 32, r[1]);
       tmem_ld_wait(r[0]);
       reg_fence(r[1]);
-      reg_fence(r[2]);
-      reg_fence(r[3]);
-      const int nvalid = min(128, k - t * 128);
-      float mt = -INFINITY;
+      const int nvalid = min(128, k - t * 128) - half * 64;   // valid columns of this warp's half
+      const bool full = nvalid >= 64;   // every tile but a group's last
+      float mx = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (c * 32 + e < nvalid) mt = fmaxf(mt, __uint_as_float(r[c][e]) * sc);
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[c][e]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e < nvalid) mx = fmaxf(mx, __uint_as_float(r[c][e]));
+      }
+      float mt = mx * sc;   // sc > 0
+      mt = fmaxf(mt, exchange(mt, ok));
+      if (!ok) break;   // both warps of the pair leave at the same tile
       bool waited = false;
       const bool want = t > 0 && mt > m + 8.f;
       if (t == 0) {
@@ -217,48 +261,61 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       } else if (__any_sync(0xffffffffu, want)) {
         // O must be quiescent: wait for PV(t-1), then rescale the rows whose
         // max grew (warp-collective TMEM access; other rows use factor 1)
-        if (!mbar_wait_warp(o_ready, (t - 1) & 1, kWaitLimitNs)) { ok = false; break; }
+        ok = ok && mbar_wait_warp(o_ready, (t - 1) & 1, kWaitLimitNs);
         waited = true;
-        tc_fence_after();
         const float f = want ? ex2_fast(m - mt) : 1.f;
+        if (ok) {
+          tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_addr + C::kColO + c * 32, o);
-          tmem_ld_wait(o);
+          for (int c = half * kOChunks; c < (half + 1) * kOChunks; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_addr + C::kColO + c * 32, o);
+            tmem_ld_wait(o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-          tmem_st32(lane_addr + C::kColO + c * 32, o);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st32(lane_addr + C::kColO + c * 32, o);
+          }
+          tmem_st_wait();
         }
-        tmem_st_wait();
         l *= f;
         if (want) m = mt;
       }
-      uint32_t pk[64];
+      uint32_t pk[32];
       float lsum = 0.f;
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int j = c * 32 + e;
-          const float p0 = j < nvalid ? ex2_fast(__uint_as_float(r[c][e]) * sc - m) : 0.f;
-          const float p1 = j + 1 < nvalid ? ex2_fast(__uint_as_float(r[c][e + 1]) * sc - m) : 0.f;
-          lsum += p0 + p1;
-          pk[j >> 1] = pack_bf16x2(p0, p1);
-        }
-      l += lsum;
-      tmem_st32(lane_addr + b * 128, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(lane_addr + b * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      tmem_st_wait();
-      if (t >= 1 && !waited) {
-        if (!mbar_wait_warp(o_ready, (t - 1) & 1, kWaitLimitNs)) { ok = false; break; }
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = ex2_fast(__uint_as_float(r[c][e]) * sc - m);
+            const float p1 = ex2_fast(__uint_as_float(r[c][e + 1]) * sc - m);
+            lsum += p0 + p1;
+            pk[(c * 32 + e) >> 1] = pack_bf16x2(p0, p1);
+          }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int j = c * 32 + e;
+            const float p0 = j < nvalid ? ex2_fast(__uint_as_float(r[c][e]) * sc - m) : 0.f;
+            const float p1 = j + 1 < nvalid ? ex2_fast(__uint_as_float(r[c][e + 1]) * sc - m) : 0.f;
+            lsum += p0 + p1;
+            pk[j >> 1] = pack_bf16x2(p0, p1);
+          }
       }
+      l += lsum;
+      // P of keys 64*half .. +63, packed two per column, in place of S
+      tmem_st32(lane_addr + b * 128 + half * 32, pk);
+      tmem_st_wait();
+      if (t >= 1 && !waited) ok = ok && mbar_wait_warp(o_ready, (t - 1) & 1, kWaitLimitNs);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full + b);
     }
     // ---------------------------------------------------------- epilogue
-    if (ok && nt > 0 && !mbar_wait_warp(o_ready, (nt - 1) & 1, kWaitLimitNs)) ok = false;
+    if (nt > 0) ok = ok && mbar_wait_warp(o_ready, (nt - 1) & 1, kWaitLimitNs);
+    l += exchange(l, ok);
     if (!ok) {
       if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
     } else if (row < G) {
@@ -267,7 +324,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const float inv_l = 1.f / l;
       __nv_bfloat16* orow = prm.out + ((int64_t)p * geo.S + tok) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = half * kOChunks; c < (half + 1) * kOChunks; ++c) {
         uint32_t o[32];
         tmem_ld32(lane_addr + C::kColO + c * 32, o);
         tmem_ld_wait(o);
@@ -279,12 +336,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
       }
-      prm.lse_out[(int64_t)p * geo.S + tok] = (m + __log2f(l)) * 0.69314718055994531f;
+      if (half == 0) prm.lse_out[(int64_t)p * geo.S + tok] = (m + __log2f(l)) * 0.69314718055994531f;
     } else {
       // padded rows still take part in the TMEM loads (warp-collective)
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = half * kOChunks; c < (half + 1) * kOChunks; ++c) {
         uint32_t o[32];
         tmem_ld32(lane_addr + C::kColO + c * 32, o);
         tmem_ld_wait(o);
@@ -304,6 +361,13 @@ static cudaError_t launch_fwd(const AttnMaps& maps, const AttnParams& prm, const
     cudaError_t e =
         cudaFuncSetAttribute(k_attn_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmem);
     if (e != cudaSuccess) return e;
+    // The warpgroups' register shares add up to kLaunchRegs per thread; a build
+    // that launched with another count would stall the softmax increase, so
+    // it is refused instead of launched.
+    cudaFuncAttributes a;
+    e = cudaFuncGetAttributes(&a, k_attn_fwd<D>);
+    if (e != cudaSuccess) return e;
+    if (a.numRegs != FwdCfg<D>::kLaunchRegs) return cudaErrorInvalidConfiguration;
     configured = true;
   }
   k_attn_fwd<D><<<dim3(n_groups, tab.n), FwdCfg<D>::kThreads, FwdCfg<D>::kSmem, st>>>(maps, prm, tab);
