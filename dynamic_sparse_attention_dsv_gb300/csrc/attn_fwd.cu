@@ -240,10 +240,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const bool full = nvalid >= 64;   // every tile but a group's last
       float mx = -INFINITY;
       if (full) {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // independent chains
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[c][e]));
+          for (int e = 0; e < 32; e += 2)
+            m4[e >> 3 & 3] = max3f(m4[e >> 3 & 3], __uint_as_float(r[c][e]), __uint_as_float(r[c][e + 1]));
+        mx = fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
       } else {
 #pragma unroll
         for (int c = 0; c < 2; ++c)
@@ -283,15 +286,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       uint32_t pk[32];
       float lsum = 0.f;
       if (full) {
+        // two-wide fp32 for the exponent argument and the running sum
+        const uint64_t sc2 = f32x2(sc, sc), nm2 = f32x2(-m, -m);
+        uint64_t ls2 = f32x2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float p0 = ex2_fast(__uint_as_float(r[c][e]) * sc - m);
-            const float p1 = ex2_fast(__uint_as_float(r[c][e + 1]) * sc - m);
-            lsum += p0 + p1;
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[c][e]), __uint_as_float(r[c][e + 1])), sc2, nm2), x0, x1);
+            const float p0 = ex2_fast(x0), p1 = ex2_fast(x1);
+            ls2 = add_f32x2(ls2, f32x2(p0, p1));
             pk[(c * 32 + e) >> 1] = pack_bf16x2(p0, p1);
           }
+        float l0, l1;
+        f32x2_split(ls2, l0, l1);
+        lsum = l0 + l1;
       } else {
 #pragma unroll
         for (int c = 0; c < 2; ++c)
