@@ -288,6 +288,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         tmem_ld_wait(r0);
         reg_fence(r1);
         const int kb = key0 + half * 64;
+        uint32_t cm_lo = 0, cm_hi = 0;   // COLLECT: columns whose score lies in bin b*
 #pragma unroll
         for (int e = 0; e < 64; ++e) {
           const float s = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]) + 0.0f;
@@ -298,25 +299,41 @@ __global__ void __launch_bounds__(kSelThreads, 1)
             const int bin = lin_bin(s, lo, inv_w, NB);
             red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
           } else if constexpr (MODE == kCollect) {
+            // branch-free here; the rare candidates are handled after the loop
             const int bin = lin_bin(s, lo, inv_w, NB);
-            if (bin > bstar) {
-              ++n_above;
-            } else if (bin == bstar && valid) {
-              const uint64_t key = ((uint64_t)(~f2ord(s)) << 32) | (uint32_t)(kb + e);
-              if (n_in < kStage) {
-                stage[n_in] = key;
-              } else {   // staging full: reserve a slot directly
-                const uint32_t slot = atomicAdd(prm.cand_cnt + rid, 1u);
-                if (slot < (uint32_t)kCandCap) prm.cand[(size_t)rid * kCandCap + slot] = key;
-              }
-              ++n_in;
-            }
+            n_above += bin > bstar;
+            if (e < 32) cm_lo |= (uint32_t)(bin == bstar) << e;
+            else cm_hi |= (uint32_t)(bin == bstar) << (e - 32);
           } else if constexpr (MODE == kCov) {
             const float u = __fmul_rn(prm.scale, __fsub_rn(cmax, s));
             const int bin = min(NB - 1, (int)__fmul_rn(u, inv_w));
             const float p = ex2_fast(-u * 1.4426950408889634f);
             red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
             red_smem_f32(hist_base + (uint32_t)(NB * 128 + bin * 128 + row) * 4u, p);
+          }
+        }
+        if constexpr (MODE == kCollect) {
+          // one short loop per candidate: pick the score out of r0/r1 with a
+          // select chain (no dynamically indexed registers), stage the key
+          uint64_t cm = valid ? ((uint64_t)cm_hi << 32 | cm_lo) : 0ull;
+#pragma unroll 1
+          while (cm) {
+            const int e = __ffsll((long long)cm) - 1;
+            cm &= cm - 1;
+            const int u = e & 31;
+            const bool hi = e >= 32;
+            uint32_t v = 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v = (u == i) ? (hi ? r1[i] : r0[i]) : v;
+            const float sv = __uint_as_float(v) + 0.0f;
+            const uint64_t key = ((uint64_t)(~f2ord(sv)) << 32) | (uint32_t)(kb + e);
+            if (n_in < kStage) {
+              stage[n_in] = key;
+            } else {   // staging full: reserve a slot directly
+              const uint32_t slot = atomicAdd(prm.cand_cnt + rid, 1u);
+              if (slot < (uint32_t)kCandCap) prm.cand[(size_t)rid * kCandCap + slot] = key;
+            }
+            ++n_in;
           }
         }
       }
