@@ -261,25 +261,54 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       tc_fence_after();
       const int key0 = (t0 + i) * 128;
       if constexpr (MODE == kEmit) {
-        if (half == 0) {
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld32(taddr_lane + b * 128 + c * 32, r);
-            tmem_ld_wait(r);
-            if (valid) {
+        // Each warp writes its 64 columns, and counts the other half's
+        // strict (s > tau) and tied (s == tau) keys, so both warps of a row
+        // know the row's output position and tie budget without a barrier.
+        uint32_t r0[32], r1[32];
+        int n_gt_o = 0, n_eq_o = 0;
+        tmem_ld32(taddr_lane + b * 128 + (half ^ 1) * 64, r0);
+        tmem_ld32(taddr_lane + b * 128 + (half ^ 1) * 64 + 32, r1);
+        tmem_ld_wait(r0);
+        reg_fence(r1);
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const float s = __uint_as_float(r[e]) + 0.0f;
-                const bool eq = (s == tau);
-                if (s > tau || (eq && eq_left > 0)) {
-                  eq_left -= eq;
-                  if (pos < krow) out_row[pos] = key0 + c * 32 + e;
-                  ++pos;
-                }
-              }
-            }
+        for (int e = 0; e < 64; ++e) {
+          const float s = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]) + 0.0f;
+          n_gt_o += s > tau;
+          n_eq_o += s == tau;
+        }
+        tmem_ld32(taddr_lane + b * 128 + half * 64, r0);
+        tmem_ld32(taddr_lane + b * 128 + half * 64 + 32, r1);
+        tmem_ld_wait(r0);
+        reg_fence(r1);
+        uint64_t gtm = 0, eqm = 0;
+        {
+          uint32_t g0 = 0, g1 = 0, q0 = 0, q1 = 0;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float s0 = __uint_as_float(r0[e]) + 0.0f, s1 = __uint_as_float(r1[e]) + 0.0f;
+            g0 |= (uint32_t)(s0 > tau) << e;
+            q0 |= (uint32_t)(s0 == tau) << e;
+            g1 |= (uint32_t)(s1 > tau) << e;
+            q1 |= (uint32_t)(s1 == tau) << e;
           }
+          gtm = (uint64_t)g1 << 32 | g0;
+          eqm = (uint64_t)q1 << 32 | q0;
+        }
+        if (valid) {
+          const int n_gt_m = __popcll(gtm), n_eq_m = __popcll(eqm);
+          const int gt0 = half == 0 ? n_gt_m : n_gt_o, eq0 = half == 0 ? n_eq_m : n_eq_o;
+          const int gt1 = half == 0 ? n_gt_o : n_gt_m, eq1 = half == 0 ? n_eq_o : n_eq_m;
+          const int t0 = min(eq_left, eq0), t1 = min(eq_left - t0, eq1);   // ties taken, in key order
+          int take = half == 0 ? t0 : t1;
+          uint64_t sel = gtm;
+#pragma unroll 1
+          for (uint64_t e = eqm; take > 0 && e; e &= e - 1, --take) sel |= e & (~e + 1);
+          int p = pos + (half == 0 ? 0 : gt0 + t0);
+#pragma unroll 1
+          for (; sel; sel &= sel - 1, ++p)
+            if (p < krow) out_row[p] = key0 + half * 64 + __ffsll((long long)sel) - 1;
+          pos += gt0 + t0 + gt1 + t1;
+          eq_left -= t0 + t1;
         }
       } else {
         uint32_t r0[32], r1[32];
