@@ -86,23 +86,38 @@ __device__ __forceinline__ float tf32_rna(float x) {
 __device__ __forceinline__ void red_smem_u32(uint32_t addr, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ void red_smem_f32(uint32_t addr, float v) {
-  asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
+// COV bins count keys and sum their probabilities with 32-bit integer adds.
+// Bin b of a row holds log-probabilities u in [b w, (b+1) w) below the row
+// maximum, so each key adds q = exp(b w - u) in (exp(-w), 1] as 16.16 fixed
+// point (relative precision 2^-17 whatever the probability's size); the bin's
+// sum is scaled back by exp(-b w) afterwards. Integer sums are exact and
+// order-independent. A chunk holds at most kCovChunkKeys keys of a row, so
+// neither the count nor the fixed-point sum overflows 32 bits.
+constexpr int kCovChunkKeys = 65535;
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Bin of x >= 0 (x < 2^22): x - 1/2 rounded to the nearest integer by adding
+// 1.5 * 2^23 and reading the integer bits (no float-to-int conversion, which
+// issues at a quarter of the add rate). Equals floor(x) except at exact
+// integers (ties to even); the map is monotone, and every pass that compares
+// bins computes them with this same arithmetic, so they agree bit for bit.
+constexpr float kRoundMagic = 12582912.f;   // 1.5 * 2^23
+__device__ __forceinline__ float bin_round(float x) { return __fadd_rn(__fsub_rn(x, 0.5f), kRoundMagic); }
+__device__ __forceinline__ int bin_of(float t, int nb) {
+  return min(nb - 1, (int)(__float_as_uint(t) - __float_as_uint(kRoundMagic)));
+}
 
 // Linear bin of score s over [lo, lo + nb/inv_w); identical arithmetic in every
 // pass that uses it (no contraction), so HIST and COLLECT agree bit for bit.
 __device__ __forceinline__ int lin_bin(float s, float lo, float inv_w, int nb) {
-  const float x = __fmul_rn(__fsub_rn(s, lo), inv_w);
-  return min(nb - 1, (int)x);
+  return bin_of(bin_round(__fmul_rn(__fsub_rn(s, lo), inv_w)), nb);
 }
 
 // ---------------------------------------------------------------------------
 // Score-tile pipeline with a per-mode consumer.
 // grid = (group tiles, key chunks, problems); block = 320 threads.
 template <int RP, int MODE>
-__global__ void __launch_bounds__(kSelThreads, 1)
+__global__ void __launch_bounds__(kSelThreads, 2)
     k_select(const __grid_constant__ CUtensorMap map_qhi, const __grid_constant__ CUtensorMap map_qlo,
              const __grid_constant__ CUtensorMap map_khi, const __grid_constant__ CUtensorMap map_klo,
              const SelParams prm, const ProblemTable tab) {
@@ -230,10 +245,12 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       inv_w = hi > lo ? (float)NB / (hi - lo) : 0.f;
       if (MODE == kCollect) bstar = prm.bstar[rid];
     }
+    float w2 = 0.f;   // COV: bin width in log2 units
     if constexpr (MODE == kCov) {
       cmax = ord2f(prm.mmax[rid]);
       const float range = prm.scale * (cmax - ord2f(prm.mmin[rid]));
       inv_w = range > 0.f ? (float)NB / range : 0.f;
+      w2 = range > 0.f ? range / (float)NB * 1.4426950408889634f : 0.f;
     }
     if constexpr (MODE == kEmit) {
       const int ci = (lp * prm.n_chunks + chunk) * prm.g_pad + g;
@@ -334,11 +351,17 @@ __global__ void __launch_bounds__(kSelThreads, 1)
             if (e < 32) cm_lo |= (uint32_t)(bin == bstar) << e;
             else cm_hi |= (uint32_t)(bin == bstar) << (e - 32);
           } else if constexpr (MODE == kCov) {
+            // log-probability below the row maximum, its bin b, and q = exp(b w - u)
             const float u = __fmul_rn(prm.scale, __fsub_rn(cmax, s));
-            const int bin = min(NB - 1, (int)__fmul_rn(u, inv_w));
-            const float p = ex2_fast(-u * 1.4426950408889634f);
+            const float x = __fmul_rn(u, inv_w);
+            const float t = bin_round(x);
+            const int bin = bin_of(t, NB);
+            const float frac = x - fminf(t - kRoundMagic, (float)(NB - 1));   // in [0, 1], more when clamped
+            const float q = ex2_fast(-frac * w2);
+            // 16.16 fixed point through the same float-bits route
+            const uint32_t qf = __float_as_uint(fmaf(q, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
             red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
-            red_smem_f32(hist_base + (uint32_t)(NB * 128 + bin * 128 + row) * 4u, p);
+            red_smem_u32(hist_base + (uint32_t)(NB * 128 + bin * 128 + row) * 4u, qf);
           }
         }
         if constexpr (MODE == kCollect) {
@@ -419,11 +442,11 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     } else if constexpr (MODE == kCov) {
       epi_barrier();
       const uint32_t* h = reinterpret_cast<const uint32_t*>(sHist);
-      const float* m = reinterpret_cast<const float*>(sHist) + NB * 128;
+      const uint32_t* m = h + NB * 128;
       for (int bin = half * (NB / 2); bin < (half + 1) * (NB / 2); ++bin) {
         const size_t o = (((size_t)lp * prm.n_chunks + chunk) * NB + bin) * prm.g_pad + g;
         prm.hist[o] = h[bin * 128 + row];
-        prm.mass[o] = m[bin * 128 + row];
+        prm.mass[o] = (float)m[bin * 128 + row] * (1.f / 65536.f) * ex2_fast(-(float)bin * w2);
       }
     }
   }
@@ -781,6 +804,9 @@ __global__ void __launch_bounds__(kCovPoints) k_cov_eval(int round, bool curve, 
                                                          const float* width, const int32_t* range, int n_curve,
                                                          double* partial) {
   static_assert(SelCfg<32>::kCovBins <= 128 && SelCfg<64>::kCovBins <= 128, "coverage tables hold 128 bins");
+  static_assert(SelCfg<32>::kCovBins * 128 * 8 <= SelCfg<32>::kHistBytes &&
+                    SelCfg<64>::kCovBins * 128 * 8 <= SelCfg<64>::kHistBytes,
+                "COV counts and sums fit the histogram area");
   __shared__ int32_t s_cc[kCovGroupsPerBlock * 128];
   __shared__ float s_cm[kCovGroupsPerBlock * 128];
   __shared__ float s_w[kCovGroupsPerBlock];
@@ -860,8 +886,9 @@ static TopkPlan make_plan(const dsv_shape& s, int32_t r, const dsv_group& g) {
   return p;
 }
 
-static void chunking(const TopkPlan& pl, int n_local, int* n_chunks, int* chunk_tiles) {
+static void chunking(const TopkPlan& pl, int n_local, int* n_chunks, int* chunk_tiles, int max_tiles = 1 << 30) {
   int nc = (kTargetCtas + pl.n_gt * n_local - 1) / (pl.n_gt * n_local);
+  nc = std::max(nc, (pl.n_tiles + max_tiles - 1) / max_tiles);
   nc = std::max(1, std::min(nc, std::min(kMaxChunks, pl.n_tiles)));
   const int ct = (pl.n_tiles + nc - 1) / nc;
   *chunk_tiles = ct;
@@ -1105,6 +1132,9 @@ extern "C" dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_
   if (!k_cov || !(scale > 0.f) || !(mass > 0.f && mass <= 1.f)) return DSV_ERR_INVALID_ARG;
   if (curve && (n_curve < 1 || n_curve > 1024)) return DSV_ERR_INVALID_ARG;
   const TopkPlan pl = make_plan(shape, r, group);
+  // the COV bin words hold at most kCovChunkKeys keys of a row per chunk
+  constexpr int kCovMaxTiles = kCovChunkKeys / 128;
+  if (pl.n_tiles > kMaxChunks * kCovMaxTiles) return DSV_ERR_UNSUPPORTED;
   TopkWs w;
   const size_t need = carve(nullptr, pl, true, &w);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DSV_ERR_WORKSPACE;
@@ -1125,7 +1155,7 @@ extern "C" dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_
     CUtensorMap maps[4];
     if (!make_score_maps(maps, pl, w, n)) return DSV_ERR_CUDA;
     int n_chunks, chunk_tiles;
-    chunking(pl, n, &n_chunks, &chunk_tiles);
+    chunking(pl, n, &n_chunks, &chunk_tiles, kCovMaxTiles);
     SelParams prm;
     memset(&prm, 0, sizeof(prm));
     prm.geo = pl.geo;

@@ -136,6 +136,8 @@ dsv_status dsv_lowrank_topk_noalloc(const void* Q, const void* K, const void* Wq
  * it.
  * k_cov: DEVICE int32 [B*H]. curve (optional, may be NULL): DEVICE float
  * [B*H][n_curve] (n_curve <= 1024), C(k) sampled at k = ceil((i+1)*S/n_curve).
+ * S <= 4186112 (64 key chunks of at most 65535 keys; DSV_ERR_UNSUPPORTED
+ * otherwise).
  * ---------------------------------------------------------------------- */
 size_t dsv_coverage_workspace_size(dsv_shape shape, int32_t r, dsv_group group);
 dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr, dsv_shape shape,
