@@ -459,74 +459,107 @@ __global__ void __launch_bounds__(kSelThreads, 2)
 // ---------------------------------------------------------------------------
 // Low-rank projections.
 // k_lr of every key, split into tf32 hi and lo parts; rows padded to RP.
-// 128 keys per block: the K tile is staged in shared memory with coalesced
-// loads (rows padded by 16 bytes so a warp reading 32 rows hits 32 banks);
-// each thread computes one key's r outputs against W in shared memory and
-// stores its hi/lo rows with 32-byte stores.
-template <int R>
+// One 128-key tile per block on the tensor cores: TMA brings the K tile
+// (128-byte swizzled atoms), the block writes W^T (RP rows of d, zero rows
+// past r) in the same K-major layout, one thread issues the d/16 MMAs
+// (128 x RP x 16, bf16 in, fp32 accumulation in TMEM; bf16 products are exact
+// in fp32), and each thread reads its key's row back and stores hi/lo.
+template <int RP>
 struct ProjCfg {
-  static constexpr int RP = R < 32 ? 32 : R;
-  static constexpr int kRowElems = 128 + 8;                  // bf16 per staged row (d <= 128)
-  static constexpr int kSmem = 128 * R * 4 + 128 * kRowElems * 2;
+  static constexpr int kATile = 128 * 128 * 2;        // K tile, d <= 128
+  static constexpr int kOffB = kATile;                // W^T: RP rows x d
+  static constexpr int kOffBar = kOffB + RP * 128 * 2;
+  static constexpr int kSmem = kOffBar + 64 + 1024;   // + barriers, + alignment slack
 };
 
-template <int R>
-__global__ void __launch_bounds__(128) k_key_proj(const __nv_bfloat16* __restrict__ K,
-                                                  const __nv_bfloat16* __restrict__ Wk, int64_t H, int d, int S,
-                                                  float* __restrict__ khi, float* __restrict__ klo,
-                                                  const ProblemTable tab) {
-  using C = ProjCfg<R>;
-  constexpr int RP = C::RP;
-  extern __shared__ __align__(16) uint8_t proj_smem[];
-  float* Ws = reinterpret_cast<float*>(proj_smem);
-  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(proj_smem + 128 * R * 4);
+template <int RP>
+__global__ void __launch_bounds__(128) k_key_proj(const __grid_constant__ CUtensorMap kmap,
+                                                  const __nv_bfloat16* __restrict__ Wk, int R, int64_t H, int d,
+                                                  int S, float* __restrict__ khi, float* __restrict__ klo,
+                                                  int32_t* status, const ProblemTable tab) {
+  using C = ProjCfg<RP>;
+  extern __shared__ uint8_t proj_smem[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(proj_smem) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = sm;
+  uint8_t* sB = sm + C::kOffB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  uint64_t* a_full = bars;
+  uint64_t* d_full = bars + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
   const int lp = blockIdx.y, p = tab.p[lp], h = p % H;
-  const int tid = threadIdx.x, j0 = blockIdx.x * 128;
-  const __nv_bfloat16* W = Wk + (size_t)h * d * R;
-  for (int i = tid; i < d * R; i += 128) Ws[i] = __bfloat162float(W[i]);
-  const int cpr = d / 8;   // 16-byte chunks per key row
-  const uint4* src = reinterpret_cast<const uint4*>(K + ((size_t)p * S + j0) * d);
-  for (int i = tid; i < 128 * cpr; i += 128) {
-    const int row = i / cpr, ch = i % cpr;
-    *reinterpret_cast<uint4*>(Ks + row * C::kRowElems + ch * 8) = src[i];
+  const int tid = threadIdx.x, warp = tid >> 5, j0 = blockIdx.x * 128;
+  if (warp == 0) {
+    tmem_alloc(tslot, RP);
+    tmem_relinquish();
   }
+  if (tid == 0) {
+    mbar_init(a_full, 1);
+    mbar_init(d_full, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(a_full, 128 * d * 2);
+    for (int a = 0; a < d / 64; ++a) tma_load_2d(sA + a * 16384, &kmap, a_full, a * 64, p * S + j0);
+  }
+  // W^T into the swizzled K-major B layout: element (n, c) of row n = column n of W
+  const __nv_bfloat16* W = Wk + (size_t)h * d * R;
+  for (int i = tid; i < RP * d; i += 128) {
+    const int c = i / RP, n = i % RP;   // consecutive threads read consecutive W columns
+    const __nv_bfloat16 v = n < R ? W[c * R + n] : __float2bfloat16(0.f);
+    const int cc = c & 63;
+    *reinterpret_cast<__nv_bfloat16*>(sB + (c >> 6) * (RP * 128) + n * 128 + ((((cc >> 3) ^ (n & 7))) << 4) +
+                                      (cc & 7) * 2) = v;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
-  float acc[R];
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  bool ok = true;
+  if (tid == 0) {
+    ok = mbar_wait(a_full, 0, kWaitLimitNs);
+    if (ok) {
+      constexpr uint32_t idesc = instr_desc(128, RP, 1, 0, 0);
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      for (int kk = 0; kk < d / 16; ++kk) {
+        const uint32_t offa = (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t offb = (kk >> 2) * (RP * 128) + (kk & 3) * 32;
+        mma_f16_ss(tbase, smem_desc(a0 + offa, 16, 1024), smem_desc(b0 + offb, 16, 1024), idesc, kk > 0);
+      }
+      mma_commit(d_full);
+    } else {
+      raise_status(status, DSV_ERR_TIMEOUT);
+    }
+  }
+  // every thread waits for the accumulator (the issuing thread's failure shows as a timeout here too)
+  ok = mbar_wait_warp(d_full, 0, kWaitLimitNs);
+  if (ok) {
+    tc_fence_after();
+    const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+    const size_t o = ((size_t)lp * S + j0 + tid) * RP;
 #pragma unroll
-  for (int c = 0; c < R; ++c) acc[c] = 0.f;
-  const __nv_bfloat16* krow = Ks + tid * C::kRowElems;
-  for (int c8 = 0; c8 < d / 8; ++c8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(krow + c8 * 8);
-    const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&v);
+    for (int c32 = 0; c32 < RP / 32; ++c32) {
+      uint32_t v[32];
+      tmem_ld32(lane_addr + c32 * 32, v);
+      tmem_ld_wait(v);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float xv = __bfloat162float(x[e]);
-      const float4* w4 = reinterpret_cast<const float4*>(Ws + (c8 * 8 + e) * R);
+      for (int c8 = 0; c8 < 4; ++c8) {
+        uint32_t hv[8], lv[8];
 #pragma unroll
-      for (int c = 0; c < R / 4; ++c) {
-        const float4 wv = w4[c];
-        acc[4 * c + 0] = fmaf(xv, wv.x, acc[4 * c + 0]);
-        acc[4 * c + 1] = fmaf(xv, wv.y, acc[4 * c + 1]);
-        acc[4 * c + 2] = fmaf(xv, wv.z, acc[4 * c + 2]);
-        acc[4 * c + 3] = fmaf(xv, wv.w, acc[4 * c + 3]);
+        for (int e = 0; e < 8; ++e) {
+          const float x = __uint_as_float(v[c8 * 8 + e]);
+          const float hi = tf32_rna(x);
+          hv[e] = __float_as_uint(hi);
+          lv[e] = __float_as_uint(tf32_rna(x - hi));
+        }
+        st_global_v8(khi + o + c32 * 32 + c8 * 8, hv);
+        st_global_v8(klo + o + c32 * 32 + c8 * 8, lv);
       }
     }
+  } else if ((tid & 31) == 0) {
+    raise_status(status, DSV_ERR_TIMEOUT);
   }
-  const size_t o = ((size_t)lp * S + j0 + tid) * RP;
-#pragma unroll
-  for (int c8 = 0; c8 < RP / 8; ++c8) {
-    uint32_t hv[8], lv[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int c = c8 * 8 + e;
-      const float v = c < R ? acc[c < R ? c : 0] : 0.f;
-      const float hi = tf32_rna(v);
-      hv[e] = __float_as_uint(hi);
-      lv[e] = __float_as_uint(tf32_rna(v - hi));
-    }
-    st_global_v8(khi + o + c8 * 8, hv);
-    st_global_v8(klo + o + c8 * 8, lv);
-  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, RP);
 }
 
 // qbar_g = (mean over the group's queries of Q_i) . W_lr^Q, split into tf32
@@ -966,35 +999,37 @@ static cudaError_t select_pass(int RP, dim3 grid, cudaStream_t st, const CUtenso
 
 static cudaError_t launch_proj(int r, const void* Q, const void* K, const void* Wq, const void* Wk,
                                const dsv_shape& s, const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab,
-                               cudaStream_t st) {
+                               int32_t* status, cudaStream_t st) {
   const int n = tab.n, d = (int)s.d;
   const size_t qbytes = (size_t)n * pl.g_pad * pl.RP * sizeof(float);
   cudaError_t e = cudaMemsetAsync(w.qhi, 0, qbytes, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(w.qlo, 0, qbytes, st);
   if (e != cudaSuccess) return e;
   dim3 gk(pl.geo.S / 128, n), gq(pl.geo.n_groups, n);
-  auto Kp = static_cast<const __nv_bfloat16*>(K);
   auto Qp = static_cast<const __nv_bfloat16*>(Q);
   auto Wkp = static_cast<const __nv_bfloat16*>(Wk);
   auto Wqp = static_cast<const __nv_bfloat16*>(Wq);
   static bool proj_configured = false;
   if (!proj_configured) {
-    cudaFuncSetAttribute(k_key_proj<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, ProjCfg<16>::kSmem);
     cudaFuncSetAttribute(k_key_proj<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, ProjCfg<32>::kSmem);
     cudaFuncSetAttribute(k_key_proj<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, ProjCfg<64>::kSmem);
     proj_configured = true;
   }
+  // the key rows of the whole batch as a [B*H*S][d] tensor, 128-row boxes
+  CUtensorMap kmap;
+  if (!make_map_2d(&kmap, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d, (uint64_t)s.B * s.H * pl.geo.S, 64, 128))
+    return cudaErrorInvalidValue;
   switch (r) {
     case 16:
-      k_key_proj<16><<<gk, 128, ProjCfg<16>::kSmem, st>>>(Kp, Wkp, s.H, d, pl.geo.S, w.khi, w.klo, tab);
+      k_key_proj<32><<<gk, 128, ProjCfg<32>::kSmem, st>>>(kmap, Wkp, 16, s.H, d, pl.geo.S, w.khi, w.klo, status, tab);
       k_group_mean_proj<16><<<gq, 128, 0, st>>>(Qp, Wqp, s.H, d, pl.geo, pl.g_pad, w.qhi, w.qlo, tab);
       break;
     case 32:
-      k_key_proj<32><<<gk, 128, ProjCfg<32>::kSmem, st>>>(Kp, Wkp, s.H, d, pl.geo.S, w.khi, w.klo, tab);
+      k_key_proj<32><<<gk, 128, ProjCfg<32>::kSmem, st>>>(kmap, Wkp, 32, s.H, d, pl.geo.S, w.khi, w.klo, status, tab);
       k_group_mean_proj<32><<<gq, 128, 0, st>>>(Qp, Wqp, s.H, d, pl.geo, pl.g_pad, w.qhi, w.qlo, tab);
       break;
     default:
-      k_key_proj<64><<<gk, 128, ProjCfg<64>::kSmem, st>>>(Kp, Wkp, s.H, d, pl.geo.S, w.khi, w.klo, tab);
+      k_key_proj<64><<<gk, 128, ProjCfg<64>::kSmem, st>>>(kmap, Wkp, 64, s.H, d, pl.geo.S, w.khi, w.klo, status, tab);
       k_group_mean_proj<64><<<gq, 128, 0, st>>>(Qp, Wqp, s.H, d, pl.geo, pl.g_pad, w.qhi, w.qlo, tab);
       break;
   }
@@ -1077,7 +1112,7 @@ extern "C" dsv_status dsv_lowrank_topk(const void* Q, const void* K, const void*
       tab.off[i] = idx_offset[p];
     }
     const int n = tab.n;
-    if (launch_proj(r, Q, K, Wq_lr, Wk_lr, shape, pl, w, tab, st) != cudaSuccess) return DSV_ERR_CUDA;
+    if (launch_proj(r, Q, K, Wq_lr, Wk_lr, shape, pl, w, tab, dev_status, st) != cudaSuccess) return DSV_ERR_CUDA;
     CUtensorMap maps[4];
     if (!make_score_maps(maps, pl, w, n)) return DSV_ERR_CUDA;
     int n_chunks, chunk_tiles;
@@ -1151,7 +1186,7 @@ extern "C" dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_
       tab.off[i] = 0;
     }
     const int n = tab.n;
-    if (launch_proj(r, Q, K, Wq_lr, Wk_lr, shape, pl, w, tab, st) != cudaSuccess) return DSV_ERR_CUDA;
+    if (launch_proj(r, Q, K, Wq_lr, Wk_lr, shape, pl, w, tab, dev_status, st) != cudaSuccess) return DSV_ERR_CUDA;
     CUtensorMap maps[4];
     if (!make_score_maps(maps, pl, w, n)) return DSV_ERR_CUDA;
     int n_chunks, chunk_tiles;
