@@ -55,6 +55,13 @@ struct SelCfg {
   static constexpr int kOffHist = kOffB + kStages * 2 * kTileBytes;
   static constexpr int kOffMisc = kOffHist + kHistBytes;
   static constexpr int kSmem = kOffMisc + 256 + 1024;  // + barriers, + alignment slack
+  // MINMAX and EMIT keep no histogram: a 2 KB exchange area, then the barriers,
+  // so two blocks share an SM and one's start and finish overlap the other's work
+  static constexpr int kOffMiscSmall = kOffHist + 2048;
+  static constexpr int kSmemSmall = kOffMiscSmall + 256 + 1024;
+  __host__ __device__ static constexpr bool big(int mode) { return mode == 1 || mode == 2 || mode == 4; }   // HIST, COLLECT, COV
+  __host__ __device__ static constexpr int smem(int mode) { return big(mode) ? kSmem : kSmemSmall; }
+  __host__ __device__ static constexpr int off_misc(int mode) { return big(mode) ? kOffMisc : kOffMiscSmall; }
 };
 
 struct SelParams {
@@ -128,7 +135,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   uint8_t* sAlo = sm + C::kOffAlo;
   uint8_t* sB = sm + C::kOffB;
   uint8_t* sHist = sm + C::kOffHist;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffMisc);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::off_misc(MODE));
   uint64_t* a_full = bars;
   uint64_t* b_full = bars + 1;            // [kStages]
   uint64_t* b_empty = bars + 3;           // [kStages]
@@ -982,11 +989,11 @@ static cudaError_t launch_select(dim3 grid, cudaStream_t st, const CUtensorMap* 
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k_select<RP, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SelCfg<RP>::kSmem);
+                                         SelCfg<RP>::smem(MODE));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k_select<RP, MODE><<<grid, kSelThreads, SelCfg<RP>::kSmem, st>>>(maps[0], maps[1], maps[2], maps[3], prm, tab);
+  k_select<RP, MODE><<<grid, kSelThreads, SelCfg<RP>::smem(MODE), st>>>(maps[0], maps[1], maps[2], maps[3], prm, tab);
   return cudaGetLastError();
 }
 
