@@ -240,7 +240,11 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       constexpr uint32_t id_sdp = instr_desc(128, 128, 1, 0, 0);   // Q K^T, dO V^T
       constexpr uint32_t id_dq = instr_desc(128, D, 1, 0, 1);      // dS K (B = K, MN-major)
       constexpr uint32_t id_kv = instr_desc(128, D == 128 ? 128 : 64, 1, 1, 1);   // P^T dO, dS^T Q (MN-major)
-      const uint32_t aq = smem_u32(sQ), ado = smem_u32(sDO), ap = smem_u32(sP), ads = smem_u32(sDS);
+      // base descriptors (K-major), built once; an operand is a fixed offset from one of
+      // them, and the MN-major form differs only by a constant in the stride field
+      constexpr uint64_t kMn = (uint64_t)((16384 >> 4) - (16 >> 4)) << 16;
+      const uint64_t dq_k = smem_desc(smem_u32(sQ), 16, 1024), ddo_k = smem_desc(smem_u32(sDO), 16, 1024);
+      const uint64_t dp_k = smem_desc(smem_u32(sP), 16, 1024), dds_k = smem_desc(smem_u32(sDS), 16, 1024);
       bool ok = mbar_wait(q_full, 0, kWaitLimitNs);
       auto issue_sdp = [&](int t) -> bool {
         const int ks = t % C::kKStages, vs = t % C::kVStages;
@@ -249,17 +253,18 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
           return false;
         fence_proxy_async_smem();   // rows written by cp.async (generic proxy) -> tensor core reads
         tc_fence_after();
-        const uint32_t ak = smem_u32(sK + ks * C::kTile), av = smem_u32(sV + vs * C::kTile);
+        const uint64_t dk = smem_desc(smem_u32(sK + ks * C::kTile), 16, 1024);
+        const uint64_t dv = smem_desc(smem_u32(sV + vs * C::kTile), 16, 1024);
+        const uint64_t dq = opaque(dq_k), ddo = opaque(ddo_k);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tbase + C::kColS, smem_desc(aq + off, 16, 1024), smem_desc(ak + off, 16, 1024), id_sdp, kk > 0);
+          mma_f16_ss(tbase + C::kColS, desc_at(dq, off), desc_at(dk, off), id_sdp, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tbase + C::kColDP, smem_desc(ado + off, 16, 1024), smem_desc(av + off, 16, 1024), id_sdp,
-                     kk > 0);
+          mma_f16_ss(tbase + C::kColDP, desc_at(ddo, off), desc_at(dv, off), id_sdp, kk > 0);
         }
         mma_commit(sdp_full);
         mma_commit(v_empty + vs);
@@ -270,16 +275,17 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         if (job >= 1 && !mbar_wait(part_free, (job - 1) & 1, kWaitLimitNs)) return false;
         tc_fence_after();
         if (D == 64 || jb == 0) {
+          const uint64_t a = opaque(dp_k + kMn), b = opaque(ddo_k + kMn);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ss(tbase + C::kColJob, smem_desc(ap + kk * 2048, 16384, 1024),
-                       smem_desc(ado + kk * 2048, 16384, 1024), id_kv, kk > 0);
+            mma_f16_ss(tbase + C::kColJob, desc_at(a, kk * 2048), desc_at(b, kk * 2048), id_kv, kk > 0);
         }
         if (D == 64 || jb == 1) {
+          const uint64_t a = opaque(dds_k + kMn), b = opaque(dq_k + kMn);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ss(tbase + C::kColJob + (D == 64 ? 64 : 0), smem_desc(ads + kk * 2048, 16384, 1024),
-                       smem_desc(aq + kk * 2048, 16384, 1024), id_kv, kk > 0);
+            mma_f16_ss(tbase + C::kColJob + (D == 64 ? 64 : 0), desc_at(a, kk * 2048), desc_at(b, kk * 2048), id_kv,
+                       kk > 0);
         }
         mma_commit(part_full);
         ++job;
@@ -292,11 +298,12 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         if (t + 1 < nt && (!mbar_wait(sdp_free, t & 1, kWaitLimitNs) || !issue_sdp(t + 1))) { ok = false; break; }
         if (!mbar_wait(ps_full, t & 1, kWaitLimitNs)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t ak = smem_u32(sK + ks * C::kTile);
+        const uint64_t dk_m = smem_desc(smem_u32(sK + ks * C::kTile), 16, 1024) + kMn;
+        const uint64_t dds = opaque(dds_k);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t offa = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tbase + C::kColDQ, smem_desc(ads + offa, 16, 1024), smem_desc(ak + kk * 2048, 16384, 1024), id_dq,
+          mma_f16_ss(tbase + C::kColDQ, desc_at(dds, offa), desc_at(dk_m, kk * 2048), id_dq,
                      (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(k_empty + ks);

@@ -166,7 +166,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     if (warp == kMmaWarp && lane == 0) {
       constexpr uint32_t idesc_qk = instr_desc(128, 128, 1, 0, 0);
       constexpr uint32_t idesc_pv = instr_desc(128, D, 1, 0, 1);
-      const uint32_t q_addr = smem_u32(sQ);
+      // base descriptors, built once; per-step operands are fixed offsets from them
+      const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024);
       bool ok = mbar_wait(q_full, 0, kWaitLimitNs);
       auto issue_pv = [&](int t) -> bool {
         const int s = t % C::kStages, b = t & 1;
@@ -174,12 +175,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         if (!mbar_wait(v_full + s, (t / C::kStages) & 1, kWaitLimitNs)) return false;
         fence_proxy_async_smem();   // rows written by cp.async (generic proxy) -> tensor core reads
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(sV + s * C::kTile);
+        const uint64_t dv0 = smem_desc(smem_u32(sV + s * C::kTile), 16384, 1024);
+        const uint32_t ta = tbase + b * 128, to = tbase + C::kColO;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = smem_desc(v_addr + kk * 2048, 16384, 1024);
-          mma_f16_ts(tbase + C::kColO, tbase + b * 128 + kk * 8, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ts(to, ta + kk * 8, desc_at(dv0, kk * 2048), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit(kv_empty + s);
         mma_commit(o_ready);
         return true;
@@ -189,12 +189,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         if (!mbar_wait(k_full + s, (t / C::kStages) & 1, kWaitLimitNs)) { ok = false; break; }
         fence_proxy_async_smem();
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(sK + s * C::kTile);
+        const uint64_t dk0 = smem_desc(smem_u32(sK + s * C::kTile), 16, 1024);
+        const uint32_t ts = tbase + b * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tbase + b * 128, smem_desc(q_addr + off, 16, 1024), smem_desc(k_addr + off, 16, 1024),
-                     idesc_qk, kk > 0);
+          mma_f16_ss(ts, desc_at(dq0, off), desc_at(dk0, off), idesc_qk, kk > 0);
         }
         mma_commit(s_full + b);
         if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }

@@ -211,6 +211,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 
 // Instruction descriptor: fp32 accumulate; operand formats 0 = f16,
 // 1 = bf16, 2 = tf32; `*_mn` = 1 when that operand is MN-major in memory.
+// Descriptor of the same layout `off` bytes further on (16-byte units in the
+// 14-bit start-address field; smem addresses stay below 2^18, so no carry).
+__device__ __forceinline__ uint64_t desc_at(uint64_t desc, uint32_t off) { return desc + (off >> 4); }
+// Hides a descriptor's value from loop-invariant code motion, so a loop issues
+// one add per MMA instead of keeping every per-step descriptor live.
+__device__ __forceinline__ uint64_t opaque(uint64_t v) {
+  asm volatile("" : "+l"(v));
+  return v;
+}
+
 __host__ __device__ constexpr uint32_t instr_desc(int M, int N, int ab_fmt, int a_mn, int b_mn) {
   return (1u << 4) | (static_cast<uint32_t>(ab_fmt) << 7) | (static_cast<uint32_t>(ab_fmt) << 10) |
          (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
