@@ -201,6 +201,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idesc = instr_desc(128, 128, 2, 0, 0);
+      const uint64_t dah0 = smem_desc(smem_u32(sAhi), 16, 1024), dal0 = smem_desc(smem_u32(sAlo), 16, 1024);
       bool ok = mbar_wait(a_full, 0, kWaitLimitNs);
       for (int i = 0; ok && i < nt; ++i) {
         const int s = i % C::kStages, b = i & 1;
@@ -208,16 +209,15 @@ __global__ void __launch_bounds__(kSelThreads, 2)
         if (i >= 2 && !mbar_wait(s_empty + b, ((i >> 1) - 1) & 1, kWaitLimitNs)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tbase + b * 128;
-        const uint32_t ah = smem_u32(sAhi), al = smem_u32(sAlo);
-        const uint32_t bh = smem_u32(sB + s * 2 * C::kTileBytes), bl = bh + C::kTileBytes;
+        const uint64_t ah = opaque(dah0), al = opaque(dal0);
+        const uint64_t bh = smem_desc(smem_u32(sB + s * 2 * C::kTileBytes), 16, 1024);
+        const uint64_t bl = desc_at(bh, C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < RP / 8; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint64_t dah = smem_desc(ah + off, 16, 1024), dal = smem_desc(al + off, 16, 1024);
-          const uint64_t dbh = smem_desc(bh + off, 16, 1024), dbl = smem_desc(bl + off, 16, 1024);
-          mma_tf32_ss(d, dah, dbh, idesc, kk > 0);
-          mma_tf32_ss(d, dah, dbl, idesc, 1);
-          mma_tf32_ss(d, dal, dbh, idesc, 1);
+          mma_tf32_ss(d, desc_at(ah, off), desc_at(bh, off), idesc, kk > 0);
+          mma_tf32_ss(d, desc_at(ah, off), desc_at(bl, off), idesc, 1);
+          mma_tf32_ss(d, desc_at(al, off), desc_at(bh, off), idesc, 1);
         }
         mma_commit(b_empty + s);
         mma_commit(s_full + b);
