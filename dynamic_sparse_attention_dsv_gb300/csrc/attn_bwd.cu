@@ -10,9 +10,9 @@
 // Group-major kernel (every problem): one CTA per (query group, problem),
 // looping over the group's 128-key tiles:
 //   S = Q K^T, dP = dO V^T                        tcgen05 (smem x smem) -> TMEM
-//   P = exp2(S*scale*log2e - LSE*log2e), dS = P (dP - Delta)   registers
-//   dQ += dS K                                    accumulated in TMEM, written once
-//   sparse problems only: dV_tile = P^T dO, dK_tile = scale dS^T Q -> TMEM,
+//   P = exp2(S*scale*log2e - LSE*log2e), dS' = scale P (dP - Delta)   registers
+//   dQ += dS' K                                   accumulated in TMEM, written once
+//   sparse problems only: dV_tile = P^T dO, dK_tile = dS'^T Q -> TMEM,
 //   written as bf16 partial rows, one per (group, selected key) pair.
 // Ordered dK/dV reduction (no atomics on the data): a bitmap of which groups
 // selected each key gives every (key, group) pair a slot, off[key] + the
@@ -345,6 +345,9 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       delta = acc;
       lse2 = prm.LSE[(int64_t)p * geo.S + tok] * 1.4426950408889634f;
     }
+    // dS is produced pre-multiplied by the attention scale (scale dS = P (scale dP - scale Delta)),
+    // so dQ = (scale dS) K and dK = (scale dS)^T Q need no scaling afterwards
+    const float dsc = prm.scale, ndd = -delta * prm.scale;
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
       ok = ok && mbar_wait_warp(sdp_full, t & 1, kWaitLimitNs);
@@ -374,8 +377,8 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
           const float p0 = j < nvalid ? ex2_fast(__uint_as_float(sr[c][e]) * sc - lse2) : 0.f;
           const float p1 = j + 1 < nvalid ? ex2_fast(__uint_as_float(sr[c][e + 1]) * sc - lse2) : 0.f;
           pw[j >> 1] = pack_bf16x2(p0, p1);
-          dw[j >> 1] = pack_bf16x2(p0 * (__uint_as_float(da[c][e]) - delta),
-                                   p1 * (__uint_as_float(da[c][e + 1]) - delta));
+          dw[j >> 1] = pack_bf16x2(p0 * fmaf(__uint_as_float(da[c][e]), dsc, ndd),
+                                   p1 * fmaf(__uint_as_float(da[c][e + 1]), dsc, ndd));
         }
       // dP columns 64-127 into the registers just freed
 #pragma unroll
@@ -401,8 +404,8 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
           const int j = c * 32 + e;
           const float p0 = __uint_as_float(sr[c][e]), p1 = __uint_as_float(sr[c][e + 1]);
           pw[j >> 1] = pack_bf16x2(p0, p1);
-          dw[j >> 1] = pack_bf16x2(p0 * (__uint_as_float(da[c - 2][e]) - delta),
-                                   p1 * (__uint_as_float(da[c - 2][e + 1]) - delta));
+          dw[j >> 1] = pack_bf16x2(p0 * fmaf(__uint_as_float(da[c - 2][e]), dsc, ndd),
+                                   p1 * fmaf(__uint_as_float(da[c - 2][e + 1]), dsc, ndd));
         }
       // P/dS of the previous tile must no longer be read by the tensor cores
       if (t >= 1) ok = ok && mbar_wait_warp(p_free, (t - 1) & 1, kWaitLimitNs);
@@ -452,7 +455,6 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
             // d = 64: dV columns for c < 2, dK columns for c >= 2
             const int tensor = D == 128 ? jb : (c >> 1);
             const int dcol = D == 128 ? c * 32 : (c & 1) * 32;
-            const float mul = tensor == 0 ? 1.f : prm.scale;
             uint32_t v[32];
             tmem_ld32(lane_addr + C::kColJob + c * 32, v);
             tmem_ld_wait(v);
@@ -461,7 +463,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
               uint32_t pk[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e)
-                pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
               st_global_v8(dst, pk);
               st_global_v8(dst + 16, pk + 8);
             }
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * prm.scale, __uint_as_float(o[2 * e + 1]) * prm.scale);
+            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
           uint4* dst = reinterpret_cast<uint4*>(qrow + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
