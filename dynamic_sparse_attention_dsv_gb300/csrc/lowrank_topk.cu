@@ -21,7 +21,8 @@
 //   COLLECT scores in bin b* -> candidate list; per key-chunk counts
 //   resolve sorts the candidates (score desc, key asc): exact threshold tau,
 //           tie budget and output offset of every key chunk
-//   EMIT    writes every key with s > tau (and the budgeted s == tau keys)
+//   EMIT    marks every key with s > tau (and the budgeted s == tau keys)
+//           in a per-row bit mask; a compaction kernel writes the index row
 //           in ascending key order.
 // Coverage reuses MINMAX and a COV pass that bins exp(scale*(s - max)) by
 // log-probability (count and mass per bin); a reduce kernel searches k.
@@ -80,6 +81,8 @@ struct SelParams {
   const float* tau;      // [n][g_pad]
   const int32_t* out_off;    // [n][chunks][g_pad]
   const int32_t* eq_budget;  // [n][chunks][g_pad]
+  uint32_t* sel_bits;        // EMIT: [n][g_pad][n_tiles][4] selected-key masks, 32 keys per word
+  const int32_t* tie_cut;    // [n][g_pad] last selected key among those tied at tau (-1: none)
   int32_t* idx;
   int32_t* status;
 };
@@ -238,11 +241,10 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     float mx = -INFINITY, mn = INFINITY;
     int n_above = 0, n_in = 0;
     float tau = INFINITY;
-    int pos = 0, eq_left = 0, krow = 0;
+    int tcut = -1;
     // COLLECT stages up to kStage candidates per (row, half) in the unused histogram area
     constexpr int kStage = C::kHistBytes / (256 * 8);
     uint64_t* stage = reinterpret_cast<uint64_t*>(sHist) + (size_t)(half * 128 + row) * kStage;
-    int32_t* out_row = nullptr;
     constexpr int NB = (MODE == kCov) ? C::kCovBins : C::kHistBins;
     const uint32_t hist_base = smem_u32(sHist);
 
@@ -260,13 +262,9 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       w2 = range > 0.f ? range / (float)NB * 1.4426950408889634f : 0.f;
     }
     if constexpr (MODE == kEmit) {
-      const int ci = (lp * prm.n_chunks + chunk) * prm.g_pad + g;
       if (valid) {
         tau = prm.tau[rid];
-        pos = prm.out_off[ci];
-        eq_left = prm.eq_budget[ci];
-        krow = tab.k[lp];
-        out_row = prm.idx + tab.off[lp] + (int64_t)g * krow;
+        tcut = prm.tie_cut[rid];
       }
     }
     if constexpr (MODE == kHist || MODE == kCov) {
@@ -285,54 +283,28 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       tc_fence_after();
       const int key0 = (t0 + i) * 128;
       if constexpr (MODE == kEmit) {
-        // Each warp writes its 64 columns, and counts the other half's
-        // strict (s > tau) and tied (s == tau) keys, so both warps of a row
-        // know the row's output position and tie budget without a barrier.
-        uint32_t r0[32], r1[32];
-        int n_gt_o = 0, n_eq_o = 0;
-        tmem_ld32(taddr_lane + b * 128 + (half ^ 1) * 64, r0);
-        tmem_ld32(taddr_lane + b * 128 + (half ^ 1) * 64 + 32, r1);
-        tmem_ld_wait(r0);
-        reg_fence(r1);
+        // Each warp marks the selected keys of its 64 columns in a bit mask:
+        // s > tau, or s == tau for keys up to the row's tie cut (the tied keys
+        // are taken in ascending key order); k_sel_compact writes the index rows.
+        uint32_t r0[32];
+        uint32_t gm[2] = {0u, 0u}, qm[2] = {0u, 0u};
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const float s = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]) + 0.0f;
-          n_gt_o += s > tau;
-          n_eq_o += s == tau;
-        }
-        tmem_ld32(taddr_lane + b * 128 + half * 64, r0);
-        tmem_ld32(taddr_lane + b * 128 + half * 64 + 32, r1);
-        tmem_ld_wait(r0);
-        reg_fence(r1);
-        uint64_t gtm = 0, eqm = 0;
-        {
-          uint32_t g0 = 0, g1 = 0, q0 = 0, q1 = 0;
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld32(taddr_lane + b * 128 + half * 64 + c * 32, r0);
+          tmem_ld_wait(r0);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float s0 = __uint_as_float(r0[e]) + 0.0f, s1 = __uint_as_float(r1[e]) + 0.0f;
-            g0 |= (uint32_t)(s0 > tau) << e;
-            q0 |= (uint32_t)(s0 == tau) << e;
-            g1 |= (uint32_t)(s1 > tau) << e;
-            q1 |= (uint32_t)(s1 == tau) << e;
+            const float sv = __uint_as_float(r0[e]) + 0.0f;
+            gm[c] |= (uint32_t)(sv > tau) << e;
+            qm[c] |= (uint32_t)(sv == tau) << e;
           }
-          gtm = (uint64_t)g1 << 32 | g0;
-          eqm = (uint64_t)q1 << 32 | q0;
         }
         if (valid) {
-          const int n_gt_m = __popcll(gtm), n_eq_m = __popcll(eqm);
-          const int gt0 = half == 0 ? n_gt_m : n_gt_o, eq0 = half == 0 ? n_eq_m : n_eq_o;
-          const int gt1 = half == 0 ? n_gt_o : n_gt_m, eq1 = half == 0 ? n_eq_o : n_eq_m;
-          const int t0 = min(eq_left, eq0), t1 = min(eq_left - t0, eq1);   // ties taken, in key order
-          int take = half == 0 ? t0 : t1;
-          uint64_t sel = gtm;
-#pragma unroll 1
-          for (uint64_t e = eqm; take > 0 && e; e &= e - 1, --take) sel |= e & (~e + 1);
-          int p = pos + (half == 0 ? 0 : gt0 + t0);
-#pragma unroll 1
-          for (; sel; sel &= sel - 1, ++p)
-            if (p < krow) out_row[p] = key0 + half * 64 + __ffsll((long long)sel) - 1;
-          pos += gt0 + t0 + gt1 + t1;
-          eq_left -= t0 + t1;
+          const int lim = tcut - (key0 + half * 64);   // tied columns 0..lim are taken
+          const uint64_t keep = lim >= 63 ? ~0ull : (lim < 0 ? 0ull : (2ull << lim) - 1ull);
+          const uint64_t sel = ((uint64_t)gm[1] << 32 | gm[0]) | (((uint64_t)qm[1] << 32 | qm[0]) & keep);
+          const size_t wi = ((size_t)rid * prm.n_tiles + (t0 + i)) * 4 + half * 2;
+          *reinterpret_cast<uint2*>(prm.sel_bits + wi) = make_uint2((uint32_t)sel, (uint32_t)(sel >> 32));
         }
       } else {
         uint32_t r0[32], r1[32];
@@ -653,10 +625,11 @@ __global__ void __launch_bounds__(256) k_resolve(const uint64_t* __restrict__ ca
                                                  const int32_t* n_above_all, const int32_t* above,
                                                  const int32_t* inbin, int g_pad, int n_chunks, int chunk_keys,
                                                  float* tau_out, int32_t* out_off, int32_t* eq_budget,
-                                                 int32_t* status, const ProblemTable tab) {
+                                                 int32_t* tie_cut, int32_t* status, const ProblemTable tab) {
   __shared__ uint64_t keys[kCandCap];
   __shared__ int sel_cnt[kMaxChunks], eq_cnt[kMaxChunks];
   __shared__ float s_tau;
+  __shared__ int s_cut;
   const int g = blockIdx.x, lp = blockIdx.y, tid = threadIdx.x;
   const int rid = lp * g_pad + g;
   const int k = tab.k[lp];
@@ -664,7 +637,10 @@ __global__ void __launch_bounds__(256) k_resolve(const uint64_t* __restrict__ ca
   const uint32_t ncand = cand_cnt[rid];
   const bool all_equal = mmax[rid] == mmin[rid];
   for (int c = tid; c < kMaxChunks; c += blockDim.x) sel_cnt[c] = eq_cnt[c] = 0;
-  if (tid == 0) s_tau = INFINITY;
+  if (tid == 0) {
+    s_tau = INFINITY;
+    s_cut = -1;
+  }
   __syncthreads();
   if (all_equal) {
     if (tid == 0) {
@@ -676,6 +652,7 @@ __global__ void __launch_bounds__(256) k_resolve(const uint64_t* __restrict__ ca
         rem -= e;
       }
       s_tau = ord2f(mmax[rid]);
+      s_cut = need - 1;   // every key ties: the first `need` keys
     }
   } else if (ncand > (uint32_t)kCandCap || need < 1 || (uint32_t)need > ncand) {
     if (tid == 0) raise_status(status, DSV_ERR_CANDIDATES);
@@ -707,7 +684,10 @@ __global__ void __launch_bounds__(256) k_resolve(const uint64_t* __restrict__ ca
       atomicAdd(&sel_cnt[c], 1);
       if ((uint32_t)(keys[i] >> 32) == tkey) atomicAdd(&eq_cnt[c], 1);
     }
-    if (tid == 0) s_tau = tau;
+    if (tid == 0) {
+      s_tau = tau;
+      s_cut = (int)(uint32_t)keys[need - 1];   // sorted (score desc, key asc): the last tie taken
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -719,7 +699,73 @@ __global__ void __launch_bounds__(256) k_resolve(const uint64_t* __restrict__ ca
       off += above[ci] + sel_cnt[c];
     }
     tau_out[rid] = s_tau;
+    tie_cut[rid] = s_cut;
   }
+}
+
+// Index rows from the EMIT masks: one block per group row, its 8 warps on
+// consecutive segments of the row's mask words. Each warp counts its
+// segment's selected keys, a block scan gives each segment its first output
+// position, and each warp then writes its keys 32 output positions at a time:
+// lane j finds the word of position j by binary search over the warp's prefix
+// sums and the key inside it with __fns, so every store instruction writes 32
+// consecutive indices (selected keys cluster, so per-word loops would diverge).
+constexpr int kCompactWarps = 8;
+
+__device__ __forceinline__ int warp_incl_scan(int x, int lane) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += y;
+  }
+  return x;
+}
+
+__global__ void __launch_bounds__(32 * kCompactWarps) k_sel_compact(const uint32_t* __restrict__ bits, int g_pad,
+                                                                    int n_words, int32_t* idx, int32_t* status,
+                                                                    const ProblemTable tab) {
+  __shared__ int seg_total[kCompactWarps];
+  const int g = blockIdx.x, lp = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k = tab.k[lp];
+  int32_t* out = idx + tab.off[lp] + (int64_t)g * k;
+  const uint32_t* row = bits + ((size_t)lp * g_pad + g) * n_words;
+  const int seg = ((n_words + kCompactWarps * 32 - 1) / (kCompactWarps * 32)) * 32;   // words per warp
+  const int w_begin = min(n_words, warp * seg), w_end = min(n_words, w_begin + seg);
+  int cnt = 0;
+#pragma unroll 8
+  for (int w = w_begin + lane; w < w_end; w += 32) cnt += __popc(__ldg(row + w));
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, d);
+  if (lane == 0) seg_total[warp] = cnt;
+  __syncthreads();
+  int base = 0, row_total = 0;
+  for (int i = 0; i < kCompactWarps; ++i) {
+    base += i < warp ? seg_total[i] : 0;
+    row_total += seg_total[i];
+  }
+  for (int w0 = w_begin; w0 < w_end; w0 += 32) {
+    const uint32_t m = w0 + lane < w_end ? __ldg(row + w0 + lane) : 0u;
+    const int c = __popc(m);
+    const int incl = warp_incl_scan(c, lane);
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    for (int q0 = 0; q0 < total; q0 += 32) {
+      const int q = q0 + lane;   // this lane's position among the step's selected keys
+      int lo = 0;                // first lane (word) whose inclusive count exceeds q
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1) {
+        const int v = __shfl_sync(0xffffffffu, incl, lo + step - 1);
+        if (v <= q) lo += step;
+      }
+      const uint32_t wm = __shfl_sync(0xffffffffu, m, lo);
+      const int excl = __shfl_sync(0xffffffffu, incl - c, lo);
+      if (q < total) {
+        const int p = base + q;
+        if (p < k) out[p] = (w0 + lo) * 32 + (int)__fns(wm, 0, q - excl + 1);
+      }
+    }
+    base += total;
+  }
+  if (threadIdx.x == 0 && row_total != k) raise_status(status, DSV_ERR_CANDIDATES);
 }
 
 // Rows with k == S select every key.
@@ -940,6 +986,8 @@ struct TopkWs {
   uint32_t *mmax, *mmin, *hist, *cand_cnt;
   float* mass;
   int32_t *bstar, *nabove, *above, *inbin, *out_off, *eqb;
+  uint32_t* selb;
+  int32_t* tcut;
   uint64_t* cand;
   float* tau;
   int32_t* cum_cnt;
@@ -969,6 +1017,8 @@ static size_t carve(void* base, const TopkPlan& pl, bool cov, TopkWs* w) {
     w->above = c.take<int32_t>(pc * kMaxChunks * gp);
     w->inbin = c.take<int32_t>(pc * kMaxChunks * gp);
     w->out_off = c.take<int32_t>(pc * kMaxChunks * gp);
+    w->selb = c.take<uint32_t>(pc * gp * pl.n_tiles * 4);
+    w->tcut = c.take<int32_t>(pc * gp);
     w->eqb = c.take<int32_t>(pc * kMaxChunks * gp);
     w->tau = c.take<float>(pc * gp);
   } else {
@@ -1142,6 +1192,8 @@ extern "C" dsv_status dsv_lowrank_topk(const void* Q, const void* K, const void*
     prm.tau = w.tau;
     prm.out_off = w.out_off;
     prm.eq_budget = w.eqb;
+    prm.sel_bits = w.selb;
+    prm.tie_cut = w.tcut;
     prm.idx = idx;
     prm.status = dev_status;
     const dim3 grid(pl.n_gt, n_chunks, n);
@@ -1158,9 +1210,12 @@ extern "C" dsv_status dsv_lowrank_topk(const void* Q, const void* K, const void*
     if (select_pass<kCollect>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
     k_resolve<<<dim3(pl.geo.n_groups, n), 256, 0, st>>>(w.cand, w.cand_cnt, w.mmax, w.mmin, w.nabove, w.above,
                                                           w.inbin, pl.g_pad, n_chunks, chunk_tiles * 128, w.tau,
-                                                          w.out_off, w.eqb, dev_status, tab);
+                                                          w.out_off, w.eqb, w.tcut, dev_status, tab);
     if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
     if (select_pass<kEmit>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
+    k_sel_compact<<<dim3(pl.geo.n_groups, n), 32 * kCompactWarps, 0, st>>>(w.selb, pl.g_pad, pl.n_tiles * 4, idx,
+                                                                            dev_status, tab);
+    if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
   }
   return DSV_OK;
 }
