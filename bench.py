@@ -314,6 +314,14 @@ def main():
             "coverage": ("hbm", cov_bytes / 1e9, "GB/s", "k_select passes (dsv_coverage)")}
     dom = max(work, key=lambda n: ph[n])
     bound, amount, unit, kname = work[dom]
+    # DRAM bytes (read + write) per head of the phase's kernels from one ncu
+    # capture of this workload at 2 heads (the per-head work is independent,
+    # so traffic scales with the head count); null for other workloads
+    dram_per_head = {"attn_bwd": (287815424 + 3414817000 + 3436778000 + 70182144) / 2,   # k_attn_bwd_q, k_csc_reduce
+                     "attn_fwd": (101435136 + 17325056) / 2}                                # k_attn_fwd
+    traffic = None
+    if dom in dram_per_head and (w.S, w.d, w.k, w.gt, w.gy, w.gx) == (65536, 128, 6554, 2, 8, 8):
+        traffic = int(dram_per_head[dom] * w.H)
     achieved = amount / (ph[dom] * 1e-3)
     peak = (pk["bf16_sus"] or pk["bf16"]) if bound == "tensor" else pk["hbm"]
 
@@ -340,7 +348,7 @@ def main():
             "wall_s": round(wall, 3),
         },
         "roofline": {"kernel": kname, "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": pk["source"] + (" bf16 sustained" if bound == "tensor" else " HBM copy")},
         "gpu_launches": launches * args.steps if launches >= 0 else None,
         "clocks": clk,
