@@ -39,7 +39,11 @@ constexpr int kSelThreads = 320;   // warps 0-7 consume scores, 8 loads tiles, 9
 constexpr int kCandCap = 4096;     // candidates kept per group row
 constexpr int kMaxChunks = 64;     // key chunks per row
 constexpr int kTargetCtas = 304;   // 2 x 152 SMs
-constexpr size_t kL2Budget = 48ull << 20;
+// Problems per launch: as many as keep the projected keys within this budget.
+// Fewer, larger launches beat keeping the projections L2-resident: the score
+// passes are bound by their consumers, and every extra launch of the pass
+// chain costs its ramp-up and tail.
+constexpr size_t kProjBudget = 1ull << 30;
 
 enum SelMode { kMinMax = 0, kHist = 1, kCollect = 2, kEmit = 3, kCov = 4 };
 
@@ -955,7 +959,11 @@ struct TopkPlan {
   Geometry geo;
   int RP, n_gt, g_pad, n_tiles, pc;
   int hist_bins, cov_bins;
+  int max_chunks;   // key chunks of the largest launch (per-chunk arrays are sized by it)
 };
+constexpr int kCovMaxTiles = 65535 / 128;   // COV bin words hold at most 65535 keys of a row per chunk
+
+static int max_chunks_of(const struct TopkPlan& pl, int P);
 
 static TopkPlan make_plan(const dsv_shape& s, int32_t r, const dsv_group& g) {
   TopkPlan p;
@@ -966,9 +974,10 @@ static TopkPlan make_plan(const dsv_shape& s, int32_t r, const dsv_group& g) {
   p.n_tiles = p.geo.S / 128;
   const size_t per = (size_t)p.geo.S * p.RP * 8;
   const int P = (int)(s.B * s.H);
-  p.pc = (int)std::max<size_t>(1, std::min<size_t>((size_t)P, kL2Budget / per));
+  p.pc = (int)std::max<size_t>(1, std::min<size_t>((size_t)P, kProjBudget / per));
   p.hist_bins = p.RP == 32 ? SelCfg<32>::kHistBins : SelCfg<64>::kHistBins;
   p.cov_bins = p.RP == 32 ? SelCfg<32>::kCovBins : SelCfg<64>::kCovBins;
+  p.max_chunks = max_chunks_of(p, P);
   return p;
 }
 
@@ -979,6 +988,20 @@ static void chunking(const TopkPlan& pl, int n_local, int* n_chunks, int* chunk_
   const int ct = (pl.n_tiles + nc - 1) / nc;
   *chunk_tiles = ct;
   *n_chunks = (pl.n_tiles + ct - 1) / ct;
+}
+
+// Largest chunk count over the launches of P problems (full launches of pc
+// problems and the remainder), for both the top-k and the coverage passes.
+static int max_chunks_of(const TopkPlan& pl, int P) {
+  int m = 1, nc, ct;
+  for (int n_local : {pl.pc, P % pl.pc}) {
+    if (n_local <= 0) continue;
+    chunking(pl, n_local, &nc, &ct);
+    m = std::max(m, nc);
+    chunking(pl, n_local, &nc, &ct, kCovMaxTiles);
+    m = std::max(m, nc);
+  }
+  return m;
 }
 
 struct TopkWs {
@@ -1014,16 +1037,16 @@ static size_t carve(void* base, const TopkPlan& pl, bool cov, TopkWs* w) {
     w->nabove = c.take<int32_t>(pc * gp);
     w->cand_cnt = c.take<uint32_t>(pc * gp);
     w->cand = c.take<uint64_t>(pc * gp * kCandCap);
-    w->above = c.take<int32_t>(pc * kMaxChunks * gp);
-    w->inbin = c.take<int32_t>(pc * kMaxChunks * gp);
-    w->out_off = c.take<int32_t>(pc * kMaxChunks * gp);
+    w->above = c.take<int32_t>(pc * pl.max_chunks * gp);
+    w->inbin = c.take<int32_t>(pc * pl.max_chunks * gp);
+    w->out_off = c.take<int32_t>(pc * pl.max_chunks * gp);
     w->selb = c.take<uint32_t>(pc * gp * pl.n_tiles * 4);
     w->tcut = c.take<int32_t>(pc * gp);
-    w->eqb = c.take<int32_t>(pc * kMaxChunks * gp);
+    w->eqb = c.take<int32_t>(pc * pl.max_chunks * gp);
     w->tau = c.take<float>(pc * gp);
   } else {
-    w->hist = c.take<uint32_t>(pc * kMaxChunks * pl.cov_bins * gp);
-    w->mass = c.take<float>(pc * kMaxChunks * pl.cov_bins * gp);
+    w->hist = c.take<uint32_t>(pc * pl.max_chunks * pl.cov_bins * gp);
+    w->mass = c.take<float>(pc * pl.max_chunks * pl.cov_bins * gp);
     w->cum_cnt = c.take<int32_t>(pc * gp * pl.cov_bins);
     w->cum_mass = c.take<double>(pc * gp * pl.cov_bins);
     w->width = c.take<float>(pc * gp);
@@ -1229,8 +1252,6 @@ extern "C" dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_
   if (!k_cov || !(scale > 0.f) || !(mass > 0.f && mass <= 1.f)) return DSV_ERR_INVALID_ARG;
   if (curve && (n_curve < 1 || n_curve > 1024)) return DSV_ERR_INVALID_ARG;
   const TopkPlan pl = make_plan(shape, r, group);
-  // the COV bin words hold at most kCovChunkKeys keys of a row per chunk
-  constexpr int kCovMaxTiles = kCovChunkKeys / 128;
   if (pl.n_tiles > kMaxChunks * kCovMaxTiles) return DSV_ERR_UNSUPPORTED;
   TopkWs w;
   const size_t need = carve(nullptr, pl, true, &w);
