@@ -42,7 +42,7 @@ constexpr int kRegsSoftmax = 232, kRegsDrain = 136, kRegsLoad = 136;
 static_assert(kRegsSoftmax + kRegsDrain + kRegsLoad == 3 * kBwdQLaunchRegs, "register split must equal the launch");
 static_assert(kGatherWarps == 2, "warps 8-9 gather, warp 10 issues MMAs, warp 11 idles");
 constexpr int kMaxUnits = 48;                       // work units per group-major launch
-constexpr size_t kPartialBudget = 8ull << 30;       // bytes of bf16 dK/dV partials in flight
+constexpr size_t kPartialBudget = 48ull << 30;      // bytes of bf16 dK/dV partials in flight
 constexpr int kMaxBlocks = 1024;                    // 256-key blocks per problem (S <= 2^18)
 
 // A unit is a range of groups of one problem whose dK/dV partials are

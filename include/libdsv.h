@@ -197,7 +197,7 @@ dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const void* V, cons
  * k_per_head, idx_offset: HOST arrays (NULL with idx NULL: every problem
  * dense). The workspace size depends on the plan: pass the same k_per_head
  * and idx_offset to dsv_sparse_attn_bwd_workspace_size (it holds the bf16
- * partials of up to 8 GiB worth of (group, key) pairs at a time, a key x group
+ * partials of up to 48 GiB worth of (group, key) pairs at a time, a key x group
  * selection bitmap and per-key slot offsets; a head with more pairs is split
  * over several launches with fp32 running sums). Sparse problems need
  * S <= 262144 (DSV_ERR_UNSUPPORTED otherwise); dense problems do not.
