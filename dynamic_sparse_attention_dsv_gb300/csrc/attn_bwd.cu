@@ -729,48 +729,88 @@ __global__ void k_bwd_delta(const __nv_bfloat16* __restrict__ O, const __nv_bflo
 }
 
 // ---------------------------------------------------------------------------
-// Ordered dK/dV reduction.
-// Sets bit (key, group) for every selected pair of every unit.
-__global__ void k_sel_bitmap(const int32_t* __restrict__ idx, uint64_t* bits, const UnitTable tab) {
-  const int u = blockIdx.y, gl = blockIdx.x;
-  if (gl >= tab.ng[u]) return;
-  const int k = tab.k[u];
-  const int32_t* row = idx + tab.off[u] + (int64_t)(tab.g0[u] + gl) * k;
-  unsigned long long* b = reinterpret_cast<unsigned long long*>(bits + tab.bits_base[u] + (gl >> 5));
-  const unsigned long long bit = 1ull << (gl & 31);
-  const int nw = tab.nwords[u];
-  for (int s = threadIdx.x; s < k; s += blockDim.x) atomicOr(b + (int64_t)__ldg(row + s) * nw, bit);
-}
+// Ordered dK/dV reduction: slot map.
+// One CTA per (256-key block, unit) builds the block's part of the selection
+// bitmap in shared memory. Index rows are ascending, so each thread binary-
+// searches a group's row for the block's first key and walks the row while
+// the keys stay inside the block. The words then go out with, in each word's
+// high half, the count of the key's set bits in its lower words, and every
+// key's slot offset within the block plus the block's total are written.
+// Keys outside the block (including values outside [0, S)) are ignored.
+constexpr int kCscKeys = 256;
+constexpr int kCscStride = kCscKeys + 1;   // words per bitmap column in shared memory (bank spread)
 
-// Number of groups that selected each key (popcount of its bitmap row); also
-// stores, in each word's high half, the count of the key's lower words.
-// Writes each key's offset within its 256-key block and the block's total.
-__global__ void __launch_bounds__(256) k_csc_count(uint64_t* bits, int S, int32_t* off, int32_t* bsum,
-                                                   const UnitTable tab) {
+__global__ void __launch_bounds__(256) k_csc_build(const int32_t* __restrict__ idx, uint64_t* bits, int S,
+                                                   int32_t* off, int32_t* bsum, const UnitTable tab) {
+  extern __shared__ uint32_t sb[];                 // [nw][kCscStride]: word w of each key of the block
+  __shared__ int cnt[kCscKeys];
   __shared__ int wsum[8];
-  const int u = blockIdx.y, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int j = blockIdx.x * 256 + tid;
-  const int nw = tab.nwords[u];
-  uint32_t c = 0;
-  if (j < S) {
-    uint64_t* b = bits + tab.bits_base[u] + (int64_t)j * nw;
-    for (int i = 0; i < nw; ++i) {
-      const uint32_t word = (uint32_t)b[i];
-      b[i] = ((uint64_t)c << 32) | word;
-      c += __popc(word);
+  const int u = blockIdx.y, kb = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int j0 = kb * kCscKeys;
+  if (j0 >= S) return;
+  const int j1 = min(j0 + kCscKeys, S);
+  const int nw = tab.nwords[u], ng = tab.ng[u], k = tab.k[u];
+  for (int i = tid; i < kCscStride * nw; i += 256) sb[i] = 0u;
+  __syncthreads();
+  for (int gl = tid; gl < ng; gl += 256) {
+    const int32_t* row = idx + tab.off[u] + (int64_t)(tab.g0[u] + gl) * k;
+    int lo = 0, hi = k;                            // first position whose key is >= j0
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(row + mid) < j0) lo = mid + 1;
+      else hi = mid;
+    }
+    const uint32_t bit = 1u << (gl & 31);
+    uint32_t* col = sb + (gl >> 5) * kCscStride;
+    for (int s = lo; s < k; s += 4) {
+      int key[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) key[e] = s + e < k ? __ldg(row + s + e) : j1;
+      bool done = false;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (key[e] >= j0 && key[e] < j1) atomicOr(col + (key[e] - j0), bit);
+        done = done || key[e] >= j1;
+      }
+      if (done) break;
     }
   }
-  int x = (int)c;
-  for (int d = 1; d < 32; d <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, d);
-    if (lane >= d) x += y;
+  __syncthreads();
+  // one warp per key: words with their lower-word counts, coalesced
+  uint64_t* out = bits + tab.bits_base[u];
+  for (int jj = w; jj < kCscKeys; jj += 8) {
+    const int j = j0 + jj;
+    uint32_t carry = 0;
+    for (int i0 = 0; i0 < nw; i0 += 32) {
+      const int i = i0 + lane;
+      const uint32_t word = i < nw ? sb[i * kCscStride + jj] : 0u;
+      const uint32_t x = __popc(word);
+      uint32_t incl = x;
+#pragma unroll
+      for (int dd = 1; dd < 32; dd <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, dd);
+        if (lane >= dd) incl += y;
+      }
+      if (i < nw && j < j1) out[(int64_t)j * nw + i] = ((uint64_t)(carry + incl - x) << 32) | word;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) cnt[jj] = j < j1 ? (int)carry : 0;
+  }
+  __syncthreads();
+  // slot offsets of the block's keys and the block total
+  const int c = cnt[tid];
+  int x = c;
+#pragma unroll
+  for (int dd = 1; dd < 32; dd <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, dd);
+    if (lane >= dd) x += y;
   }
   if (lane == 31) wsum[w] = x;
   __syncthreads();
   int before = 0;
   for (int i = 0; i < w; ++i) before += wsum[i];
-  if (j < S) off[(int64_t)u * (S + 1) + j] = before + x - (int)c;
-  if (tid == 255) bsum[(int64_t)u * (kMaxBlocks + 1) + blockIdx.x] = before + x;
+  if (j0 + tid < S) off[(int64_t)u * (S + 1) + j0 + tid] = before + x - c;
+  if (tid == 255) bsum[(int64_t)u * (kMaxBlocks + 1) + kb] = before + x;
 }
 
 // In place: block totals -> exclusive block offsets; entry nblk = total.
@@ -869,6 +909,10 @@ static cudaError_t configure_bwd() {
   // The warpgroups' register shares add up to kBwdQLaunchRegs per thread; a
   // build that launched with any other count would never satisfy the softmax
   // warpgroup's increase, so it is refused here instead of launched.
+  // the slot-map bitmap of a 256-key block: up to S / 64 groups, 32 per word
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_csc_build, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kCscStride * (256 * kMaxBlocks / 64 / 32) * (int)sizeof(uint32_t));
   cudaFuncAttributes a;
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, k_attn_bwd_q<D>);
   if (e == cudaSuccess && a.numRegs != kBwdQLaunchRegs) e = cudaErrorInvalidConfiguration;
@@ -1060,15 +1104,13 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
 
   // sparse problems: dQ + ordered dK/dV
   for (const UnitTable& tab : pl.launches) {
-    size_t words = 0;
-    int max_ng = 1;
+    int max_ng = 1, max_nw = 1;
     for (int i = 0; i < tab.n; ++i) {
-      words += (size_t)geo.S * tab.nwords[i];
       max_ng = std::max(max_ng, tab.ng[i]);
+      max_nw = std::max(max_nw, tab.nwords[i]);
     }
-    if (cudaMemsetAsync(w.bits, 0, words * sizeof(uint64_t), st) != cudaSuccess) return DSV_ERR_CUDA;
-    k_sel_bitmap<<<dim3(max_ng, tab.n), 256, 0, st>>>(idx, w.bits, tab);
-    k_csc_count<<<dim3((geo.S + 255) / 256, tab.n), 256, 0, st>>>(w.bits, geo.S, w.off, w.bpre, tab);
+    k_csc_build<<<dim3((geo.S + kCscKeys - 1) / kCscKeys, tab.n), 256, (size_t)kCscStride * max_nw * sizeof(uint32_t),
+                  st>>>(idx, w.bits, geo.S, w.off, w.bpre, tab);
     k_csc_bscan<<<tab.n, 1024, 0, st>>>((geo.S + 255) / 256, w.bpre);
     cudaError_t e = d == 128 ? launch_bwd_q<128>(maps, do_cube, prm, csc, tab, max_ng, st)
                              : launch_bwd_q<64>(maps, do_cube, prm, csc, tab, max_ng, st);
