@@ -59,17 +59,21 @@ inline bool make_attn_maps(AttnMaps* m, const void* Q, const void* K, const void
 // Row gather of selected K/V rows with cp.async by W producer warps. A warp
 // instruction copies whole rows (d*2 bytes = d/8 16-byte chunks, consecutive
 // lanes on consecutive chunks) into the K-major 128-byte swizzled tile layout
-// the tensor cores read. Per tile and tensor each lane copies kIters chunks.
+// the tensor cores read. The tile's instructions are dealt round-robin to the
+// W warps (instruction pw + i*W for warp pw), so W need not divide the tile.
 // The rate at which an SM issues these copies grows with the number of
-// issuing warps, so a kernel that is bound by its gathers uses more of them.
+// issuing warps (up to ~33 B/clk per SM on random 256-byte rows from L2), so a
+// kernel that is bound by its gathers uses more of them.
 constexpr int kGatherWarps = 2;
 
 template <int D, int W = kGatherWarps>
 struct Gather {
   static constexpr int kChunksPerRow = D / 8;                      // 16-byte chunks per row
   static constexpr int kRowsPerInstr = 32 / kChunksPerRow;         // rows per warp instruction
-  static constexpr int kRowsPerWarp = 128 / W;
-  static constexpr int kIters = kRowsPerWarp / kRowsPerInstr;      // instructions per lane per tensor
+  static constexpr int kInstr = 128 / kRowsPerInstr;               // warp instructions per tile and tensor
+  static constexpr int kIters = (kInstr + W - 1) / W;              // instructions per lane per tensor
+  __device__ static bool valid(int pw, int i) { return kInstr % W == 0 || pw + i * W < kInstr; }
+  __device__ static int row(int pw, int i, int lane) { return (pw + i * W) * kRowsPerInstr + lane / kChunksPerRow; }
 };
 
 // Key rows (absolute row in the [P*S][d] tensor) this lane copies for tile t.
@@ -80,7 +84,8 @@ __device__ __forceinline__ void gather_rows(int (&rows)[Gather<D, W>::kIters], c
   using Gt = Gather<D, W>;
 #pragma unroll
   for (int i = 0; i < Gt::kIters; ++i) {
-    const int slot = t * 128 + pw * Gt::kRowsPerWarp + i * Gt::kRowsPerInstr + lane / Gt::kChunksPerRow;
+    if (!Gt::valid(pw, i)) break;
+    const int slot = t * 128 + Gt::row(pw, i, lane);
     rows[i] = prow0 + __ldg(idx_row + (slot < k ? slot : k - 1));
   }
 }
@@ -93,7 +98,8 @@ __device__ __forceinline__ void gather_tile(uint8_t* dst, const __nv_bfloat16* s
   const uint32_t base = smem_u32(dst) + (chunk >> 3) * 16384;
 #pragma unroll
   for (int i = 0; i < Gt::kIters; ++i) {
-    const int row = pw * Gt::kRowsPerWarp + i * Gt::kRowsPerInstr + lane / Gt::kChunksPerRow;
+    if (!Gt::valid(pw, i)) break;
+    const int row = Gt::row(pw, i, lane);
     cp_async_16(base + row * 128 + (((chunk & 7) ^ (row & 7)) << 4), src + (int64_t)rows[i] * D + chunk * 8);
   }
 }

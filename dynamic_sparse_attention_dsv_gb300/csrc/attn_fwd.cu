@@ -20,10 +20,11 @@
 // Warps 0-7: softmax and epilogue, two warps per query row (TMEM lane): warp
 // w takes key columns 64*(w/4) .. +63 of the rows in lane quarter w%4 and
 // half of O's columns; the pair exchanges its partial row maxima (and row
-// sums at the end) through shared memory. Warps 8-11: producers (cp.async row
-// gather of the selected K/V rows; TMA boxes for dense tiles and the query
-// cube). Warp 12: MMA issuer; warps 13-15 idle. The four warpgroups rebalance
-// their registers after launch (softmax up, the rest down).
+// sums at the end) through shared memory. Warps 8-11 and 13-15: producers
+// (cp.async row gather of the selected K/V rows, which bounds the kernel, so
+// seven warps issue them; TMA boxes for dense tiles and the query cube).
+// Warp 12: MMA issuer. The four warpgroups rebalance their registers after
+// launch (softmax up, the rest down).
 #include "attn_common.cuh"
 
 namespace dsv {
@@ -39,7 +40,7 @@ struct FwdCfg {
   static constexpr int kSmemUsed = kOffX + 1024 + 1024;
   // at least half the SM's shared memory, so one CTA owns the SM's TMEM
   static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
-  static constexpr int kGatherW = 4;                   // producer warps
+  static constexpr int kGatherW = 7;                   // producer warps: 8-11 and 13-15
   static constexpr int kThreads = 512;
   static constexpr int kLaunchRegs = 128;              // 16384 / (4 warps x 32 lanes) per SM sub-partition
   static constexpr int kRegsSoftmax = 168, kRegsLoad = 96, kRegsMma = 80;
@@ -116,10 +117,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp >= kProdWarp && warp < kMmaWarp) {
-    // ----------------------------------------------------------- producers
-    setmaxnreg_dec<C::kRegsLoad>();
-    const int pw = warp - kProdWarp;
+  // ------------------------------------------------------------- producers
+  auto produce = [&](const int pw) {
     const int ct = g / (geo.ncy * geo.ncx), cy = (g / geo.ncx) % geo.ncy, cx = g % geo.ncx;
     if (pw == 0 && lane == 0) {
       prefetch_tmap(&maps.q_cube);
@@ -160,10 +159,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
       }
     }
-  } else if (warp >= kMmaWarp) {
-    // ------------------------------------------------- MMA (warp 12; 13-15 idle)
+  };
+  if (warp >= kProdWarp && warp < kMmaWarp) {
+    setmaxnreg_dec<C::kRegsLoad>();
+    produce(warp - kProdWarp);
+  } else if (warp > kMmaWarp) {
+    setmaxnreg_dec<C::kRegsMma>();   // the same instruction as warp 12 (one warpgroup)
+    produce(warp - kMmaWarp - 1 + (kMmaWarp - kProdWarp));
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------- MMA (warp 12)
     setmaxnreg_dec<C::kRegsMma>();
-    if (warp == kMmaWarp && lane == 0) {
+    if (lane == 0) {
       constexpr uint32_t idesc_qk = instr_desc(128, 128, 1, 0, 0);
       constexpr uint32_t idesc_pv = instr_desc(128, D, 1, 0, 1);
       // base descriptors, built once; per-step operands are fixed offsets from them
