@@ -11,7 +11,8 @@
 // the M = 128 rows of every MMA (G = 64 leaves rows 64..127 zero). Per
 // 128-key tile:
 //   TMA row gather of the selected K and V rows into swizzled shared memory
-//   S  = Q K^T        tcgen05.mma kind::f16 (smem x smem) -> TMEM
+//   S  = Q K^T        tcgen05.mma kind::f16, A = Q in TMEM (copied there once
+//                     per CTA), B = K (smem) -> TMEM
 //   P  = exp2(S*scale*log2e - m) in registers, written back to TMEM as bf16
 //   O += P V          tcgen05.mma with A = P in TMEM, B = V (MN-major) -> TMEM
 // The running max m is raised lazily (only when it grows by more than 8 in
@@ -46,6 +47,7 @@ struct FwdCfg {
   static constexpr int kRegsSoftmax = 168, kRegsLoad = 96, kRegsMma = 80;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;               // S buffers at 0 and 128
+  static constexpr uint32_t kColQ = 384;               // Q as bf16 pairs, D/2 columns
 };
 
 static_assert(FwdCfg<128>::kSmemUsed <= 232448 && FwdCfg<64>::kSmemUsed <= 232448, "forward exceeds shared memory");
@@ -72,6 +74,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   uint64_t* p_full = bars + 15;                 // [2]
   uint64_t* o_ready = bars + 17;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 18);
+  uint64_t* q_tm = bars + 19;                   // Q copied into TMEM by the eight softmax warps
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x, lp = blockIdx.y;
@@ -110,6 +113,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mbar_init(p_full + i, 8);
     }
     mbar_init(o_ready, 1);
+    mbar_init(q_tm, 8);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -172,9 +176,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = instr_desc(128, 128, 1, 0, 0);
       constexpr uint32_t idesc_pv = instr_desc(128, D, 1, 0, 1);
-      // base descriptors, built once; per-step operands are fixed offsets from them
-      const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024);
-      bool ok = mbar_wait(q_full, 0, kWaitLimitNs);
+      // Q is read from TMEM: the shared-memory operand traffic of S = Q K^T halves
+      bool ok = mbar_wait(q_tm, 0, kWaitLimitNs);
+      tc_fence_after();
       auto issue_pv = [&](int t) -> bool {
         const int s = t % C::kStages, b = t & 1;
         if (!mbar_wait(p_full + b, (t >> 1) & 1, kWaitLimitNs)) return false;
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(ts, desc_at(dq0, off), desc_at(dk0, off), idesc_qk, kk > 0);
+          mma_f16_ts(ts, tbase + C::kColQ + kk * 8, desc_at(dk0, off), idesc_qk, kk > 0);
         }
         mma_commit(s_full + b);
         if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
@@ -232,7 +236,29 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     constexpr int kOChunks = D / 64;   // 32-column chunks of O per warp
     const float sc = prm.scale_log2;
     float m = -INFINITY, l = 0.f;
-    bool ok = true;
+    bool ok = mbar_wait_warp(q_full, 0, kWaitLimitNs);
+    {
+      // this warp's 32 rows of Q, half of the columns, from the swizzled tile into TMEM
+      constexpr int kQc = D / 16;   // 16-byte chunks
+      uint32_t qv[kQc * 4];
+#pragma unroll
+      for (int c = 0; c < kQc; ++c) {
+        const int cg = half * kQc + c, atom = cg >> 3, c8 = cg & 7;
+        const uint4 v = *reinterpret_cast<const uint4*>(sQ + atom * 16384 + row * 128 + ((c8 ^ (row & 7)) << 4));
+        qv[4 * c] = v.x;
+        qv[4 * c + 1] = v.y;
+        qv[4 * c + 2] = v.z;
+        qv[4 * c + 3] = v.w;
+      }
+      if (ok) {
+        if constexpr (D == 128) tmem_st32(lane_addr + C::kColQ + half * (D / 4), qv);
+        else tmem_st16(lane_addr + C::kColQ + half * (D / 4), qv);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_tm);
+    }
     for (int t = 0; t < nt; ++t) {
       const int b = t & 1;
       ok = ok && mbar_wait_warp(s_full + b, (t >> 1) & 1, kWaitLimitNs);
