@@ -2,13 +2,15 @@
 
 One step = the whole hot path on the S=64K video-DiT attention layer (H=24,
 16x64x64 latent grid, d=128, r=32, 2x8x8 query groups of 128, k=6554 = 10% of
-S): predicted-mass coverage (k_cov per head), fused low-rank top-k, sparse
-attention forward and backward. Inputs are seeded synthetic bf16 tensors
+S): predicted-mass coverage (k_cov per head) and the low-rank top-k in one
+call that shares their projections and score ranges, sparse attention
+forward and backward. Inputs are seeded synthetic bf16 tensors
 (larger than L2: Q, K, V, dO are 403 MB each) resident in HBM.
 
 Prints ONE JSON line. `value` is the effective attention TFLOP/s of the whole
 step (algorithmic fwd+bwd FLOPs 14*H*S*k*d over the step time). Breakdown keys
-give each phase's time, the top-k Gscore/s and the attention TFLOP/s.
+give each phase's time, the selection's Gscore/s (scored (group, key) pairs
+per second, coverage and top-k together) and the attention TFLOP/s.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -147,12 +149,15 @@ class Step:
             return
         self.idx = torch.empty(total, dtype=torch.int32, device=device)
         self.LSE = torch.empty(self.Q.shape[:-1], dtype=torch.float32, device=device)
-        nb = max(api.lowrank_topk_workspace_size(self.Q, self.grid, self.group, w.r),
-                 int(dsv.native.load().dsv_coverage_workspace_size(api.make_shape(self.Q, self.grid), w.r,
-                                                                   api.make_group(self.group))),
+        nb = max(api.coverage_topk_workspace_size(self.Q, self.grid, self.group, w.r),
                  api.sparse_attn_bwd_workspace_size(self.Q, self.grid, self.group, self.ks, self.offs))
         self.ws = torch.empty(nb, dtype=torch.uint8, device=device)
         self.status = dsv.new_status(device)
+
+    def select(self):
+        self.k_cov, _, _, _, _ = dsv.coverage_topk(self.Q, self.K, self.Wq, self.Wk, self.grid, self.group, self.ks,
+                                                   idx_offset=self.offs, idx=self.idx, workspace=self.ws,
+                                                   status=self.status)
 
     def coverage(self):
         self.k_cov, _ = dsv.coverage(self.Q, self.K, self.Wq, self.Wk, self.grid, self.group, workspace=self.ws,
@@ -172,7 +177,7 @@ class Step:
                             status=self.status)
 
     def phases(self):
-        return [("coverage", self.coverage), ("lowrank_topk", self.topk), ("attn_fwd", self.fwd),
+        return [("select", self.select), ("attn_fwd", self.fwd),
                 ("attn_bwd", self.bwd)]
 
     def run(self):
@@ -330,12 +335,10 @@ def main():
     # roofline of the dominant phase (largest share of the step). Attention
     # phases are tensor-bound (algorithmic FLOPs); the low-rank phases are
     # graded against HBM (algorithmic bytes: read Q and K, write idx).
-    topk_bytes = w.H * (4.0 * w.S * w.d + 4.0 * w.n_groups * w.k)
-    cov_bytes = w.H * 4.0 * w.S * w.d
+    sel_bytes = w.H * (4.0 * w.S * w.d + 4.0 * w.n_groups * w.k)
     work = {"attn_bwd": ("tensor", bwd_flops / 1e12, "TFLOP/s", "k_attn_bwd_q + k_csc_reduce (dsv_sparse_attn_bwd)"),
             "attn_fwd": ("tensor", fwd_flops / 1e12, "TFLOP/s", "k_attn_fwd (dsv_sparse_attn_fwd)"),
-            "lowrank_topk": ("hbm", topk_bytes / 1e9, "GB/s", "k_select passes (dsv_lowrank_topk)"),
-            "coverage": ("hbm", cov_bytes / 1e9, "GB/s", "k_select passes (dsv_coverage)")}
+            "select": ("hbm", sel_bytes / 1e9, "GB/s", "k_select passes (dsv_coverage_topk)")}
     dom = max(work, key=lambda n: ph[n])
     bound, amount, unit, kname = work[dom]
     # DRAM bytes (read + write) per head of the phase's kernels from one ncu
@@ -361,15 +364,14 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded video-latent-shaped Q/K/V/dO)",
         "config": workload_dict(w),
         "breakdown": {
-            "coverage_ms": round(ph["coverage"], 3), "lowrank_topk_ms": round(ph["lowrank_topk"], 3),
-            "lowrank_topk_gscore_s": round(scores / (ph["lowrank_topk"] * 1e-3) / 1e9, 2),
+            "select_ms": round(ph["select"], 3),
+            "select_gscore_s": round(scores / (ph["select"] * 1e-3) / 1e9, 2),
             "attn_fwd_ms": round(ph["attn_fwd"], 3), "attn_bwd_ms": round(ph["attn_bwd"], 3),
             "attn_fwd_bwd_ms": round(fb_ms, 3),
             "attn_fwd_bwd_tflops": round(flops / (fb_ms * 1e-3) / 1e12, 2),
             "attn_fwd_tflops": round(fwd_flops / (ph["attn_fwd"] * 1e-3) / 1e12, 2),
             "attn_fwd_bwd_frac_of_bf16_peak": round(flops / (fb_ms * 1e-3) / 1e12 / (pk["bf16_sus"] or pk["bf16"]), 4),
-            "lowrank_topk_hbm_gbs": round(w.H * (4.0 * w.S * w.d + 4.0 * w.n_groups * w.k) /
-                                          (ph["lowrank_topk"] * 1e-3) / 1e9, 1),
+            "select_hbm_gbs": round(sel_bytes / (ph["select"] * 1e-3) / 1e9, 1),
             "wall_s": round(wall, 3),
         },
         "roofline": {"kernel": kname, "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
@@ -388,7 +390,7 @@ def main():
         tdist.destroy_process_group()
 
 
-def end_to_end(w, inp, device, args, step0=None, windows=5, clocks=None):
+def end_to_end(w, inp, device, args, step0=None, windows=9, clocks=None):
     """Same metric through the public API with pinned host buffers: every step
     copies its inputs host->device and reads O, dQ, dK, dV back inside the
     timed region. Steps are pipelined as a training loop would run them: two

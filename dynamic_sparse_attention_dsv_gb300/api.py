@@ -148,6 +148,39 @@ def coverage(Q, K, Wq, Wk, grid, group, scale: Optional[float] = None, mass: flo
     return k_cov, curve
 
 
+def coverage_topk_workspace_size(x, grid, group, r) -> int:
+    return int(N.load().dsv_coverage_topk_workspace_size(make_shape(x, grid), int(r), make_group(group)))
+
+
+def coverage_topk(Q, K, Wq, Wk, grid, group, k, scale: Optional[float] = None, mass: float = 0.9,
+                  curve_points: int = 0, idx_offset: Optional[Sequence[int]] = None,
+                  idx: Optional[torch.Tensor] = None, workspace=None, status=None):
+    """dsv_coverage_topk. Returns (k_cov int32 device tensor [P], curve or None,
+    idx int32 flat tensor, k list, offset list)."""
+    _check_bf16(Q, K, Wq, Wk)
+    lib = N.load()
+    shape, grp = make_shape(Q, grid), make_group(group)
+    P = shape.B * shape.H
+    n_groups = (shape.T * shape.Y * shape.X) // (grp.gt * grp.gy * grp.gx)
+    scale = 1.0 / math.sqrt(shape.d) if scale is None else float(scale)
+    ks, offs, total = topk_layout(P, n_groups, k)
+    if idx_offset is not None:
+        offs = [int(v) for v in idx_offset]
+        total = max([o + n_groups * kk for o, kk in zip(offs, ks) if o >= 0] + [0])
+    if idx is None:
+        idx = torch.empty(max(total, 1), dtype=torch.int32, device=Q.device)
+    k_cov = torch.empty(P, dtype=torch.int32, device=Q.device)
+    curve = torch.empty((P, curve_points), dtype=torch.float32, device=Q.device) if curve_points else None
+    r = Wq.shape[-1]
+    ws = _workspace(int(lib.dsv_coverage_topk_workspace_size(shape, r, grp)), Q.device, workspace)
+    st = status if status is not None else new_status(Q.device)
+    code = lib.dsv_coverage_topk(_ptr(Q), _ptr(K), _ptr(Wq), _ptr(Wk), shape, r, grp, ctypes.c_float(scale),
+                                 ctypes.c_float(mass), _ptr(k_cov), _ptr(curve), int(curve_points), _i32(ks),
+                                 _i64(offs), _ptr(idx), _ptr(ws), ws.numel(), _ptr(st), _stream())
+    N.check(code, "dsv_coverage_topk")
+    return k_cov, curve, idx, ks, offs
+
+
 def plan_heads(k_cov: Sequence[int], S: int, n_groups: int, lo_frac: float = 0.01, hi_frac: float = 0.25,
                dense_frac: float = 0.5):
     """dsv_plan_heads (host only). Returns (k_h list, dense list, offsets list, total)."""

@@ -105,9 +105,8 @@ __device__ __forceinline__ void red_smem_u32(uint32_t addr, uint32_t v) {
 // maximum, so each key adds q = exp(b w - u) in (exp(-w), 1] as 16.16 fixed
 // point (relative precision 2^-17 whatever the probability's size); the bin's
 // sum is scaled back by exp(-b w) afterwards. Integer sums are exact and
-// order-independent. A chunk holds at most kCovChunkKeys keys of a row, so
+// order-independent. A chunk holds at most kCovMaxTiles * 128 (< 65536) keys of a row, so
 // neither the count nor the fixed-point sum overflows 32 bits.
-constexpr int kCovChunkKeys = 65535;
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Bin of x >= 0 (x < 2^22): x - 1/2 rounded to the nearest integer by adding
@@ -1007,6 +1006,7 @@ static int max_chunks_of(const TopkPlan& pl, int P) {
 struct TopkWs {
   float *khi, *klo, *qhi, *qlo;
   uint32_t *mmax, *mmin, *hist, *cand_cnt;
+  uint32_t* cov_hist;
   float* mass;
   int32_t *bstar, *nabove, *above, *inbin, *out_off, *eqb;
   uint32_t* selb;
@@ -1020,9 +1020,10 @@ struct TopkWs {
   int32_t* cov_range;
 };
 
-// Carves the workspace (base == nullptr: sizing only). `cov` selects the
-// coverage buffers instead of the top-k ones.
-static size_t carve(void* base, const TopkPlan& pl, bool cov, TopkWs* w) {
+// Carves the workspace (base == nullptr: sizing only): the projections and
+// row ranges, then the top-k buffers, the coverage buffers, or both.
+enum CarveMode { kCarveTopk = 1, kCarveCov = 2, kCarveBoth = 3 };
+static size_t carve(void* base, const TopkPlan& pl, int mode, TopkWs* w) {
   Carver c(base);
   const size_t pc = pl.pc, S = pl.geo.S, gp = pl.g_pad, RP = pl.RP;
   w->khi = c.take<float>(pc * S * RP);
@@ -1031,7 +1032,7 @@ static size_t carve(void* base, const TopkPlan& pl, bool cov, TopkWs* w) {
   w->qlo = c.take<float>(pc * gp * RP);
   w->mmax = c.take<uint32_t>(pc * gp);
   w->mmin = c.take<uint32_t>(pc * gp);
-  if (!cov) {
+  if (mode & kCarveTopk) {
     w->hist = c.take<uint32_t>(pc * pl.hist_bins * gp);
     w->bstar = c.take<int32_t>(pc * gp);
     w->nabove = c.take<int32_t>(pc * gp);
@@ -1044,8 +1045,9 @@ static size_t carve(void* base, const TopkPlan& pl, bool cov, TopkWs* w) {
     w->tcut = c.take<int32_t>(pc * gp);
     w->eqb = c.take<int32_t>(pc * pl.max_chunks * gp);
     w->tau = c.take<float>(pc * gp);
-  } else {
-    w->hist = c.take<uint32_t>(pc * pl.max_chunks * pl.cov_bins * gp);
+  }
+  if (mode & kCarveCov) {
+    w->cov_hist = c.take<uint32_t>(pc * pl.max_chunks * pl.cov_bins * gp);
     w->mass = c.take<float>(pc * pl.max_chunks * pl.cov_bins * gp);
     w->cum_cnt = c.take<int32_t>(pc * gp * pl.cov_bins);
     w->cum_mass = c.take<double>(pc * gp * pl.cov_bins);
@@ -1134,6 +1136,113 @@ static dsv_status validate_lowrank(const void* Q, const void* K, const void* Wq,
   return DSV_OK;
 }
 
+// The top-k passes of one launch of problems whose projections are in the
+// workspace; `minmax` = false when the row ranges are already there.
+static cudaError_t topk_passes(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, const CUtensorMap* maps,
+                               bool minmax, int32_t* idx, int32_t* status, cudaStream_t st) {
+  const int n = tab.n;
+  int n_chunks, chunk_tiles;
+  chunking(pl, n, &n_chunks, &chunk_tiles);
+  SelParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.geo = pl.geo;
+  prm.g_pad = pl.g_pad;
+  prm.n_chunks = n_chunks;
+  prm.chunk_tiles = chunk_tiles;
+  prm.n_tiles = pl.n_tiles;
+  prm.mmax = w.mmax;
+  prm.mmin = w.mmin;
+  prm.hist = w.hist;
+  prm.bstar = w.bstar;
+  prm.cand_cnt = w.cand_cnt;
+  prm.cand = w.cand;
+  prm.above = w.above;
+  prm.inbin = w.inbin;
+  prm.tau = w.tau;
+  prm.out_off = w.out_off;
+  prm.eq_budget = w.eqb;
+  prm.sel_bits = w.selb;
+  prm.tie_cut = w.tcut;
+  prm.idx = idx;
+  prm.status = status;
+  const dim3 grid(pl.n_gt, n_chunks, n);
+  const size_t rows = (size_t)n * pl.g_pad;
+  if (minmax) {
+    if (cudaMemsetAsync(w.mmax, 0, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
+    if (cudaMemsetAsync(w.mmin, 0xFF, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
+    if (select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  }
+  if (cudaMemsetAsync(w.hist, 0, rows * pl.hist_bins * 4, st) != cudaSuccess) return cudaErrorUnknown;
+  if (select_pass<kHist>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  k_bracket<<<dim3(pl.n_gt, n), 128, 0, st>>>(w.hist, pl.hist_bins, pl.g_pad, pl.geo.n_groups, w.bstar,
+                                               w.nabove, tab);
+  if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
+  if (cudaMemsetAsync(w.cand_cnt, 0, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
+  if (select_pass<kCollect>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  k_resolve<<<dim3(pl.geo.n_groups, n), 256, 0, st>>>(w.cand, w.cand_cnt, w.mmax, w.mmin, w.nabove, w.above,
+                                                        w.inbin, pl.g_pad, n_chunks, chunk_tiles * 128, w.tau,
+                                                        w.out_off, w.eqb, w.tcut, status, tab);
+  if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
+  if (select_pass<kEmit>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  k_sel_compact<<<dim3(pl.geo.n_groups, n), 32 * kCompactWarps, 0, st>>>(w.selb, pl.g_pad, pl.n_tiles * 4, idx,
+                                                                          status, tab);
+  return cudaGetLastError();
+}
+
+// The coverage passes of one launch of problems whose projections are in the
+// workspace; `minmax` = false when the row ranges are already there.
+static cudaError_t cov_passes(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, const CUtensorMap* maps,
+                              bool minmax, float scale, float mass, int32_t* k_cov, float* curve, int n_curve,
+                              int32_t* status, cudaStream_t st) {
+  const int n = tab.n;
+  int n_chunks, chunk_tiles;
+  chunking(pl, n, &n_chunks, &chunk_tiles, kCovMaxTiles);
+  SelParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.geo = pl.geo;
+  prm.g_pad = pl.g_pad;
+  prm.n_chunks = n_chunks;
+  prm.chunk_tiles = chunk_tiles;
+  prm.n_tiles = pl.n_tiles;
+  prm.scale = scale;
+  prm.mmax = w.mmax;
+  prm.mmin = w.mmin;
+  prm.hist = w.cov_hist;
+  prm.mass = w.mass;
+  prm.status = status;
+  const dim3 grid(pl.n_gt, n_chunks, n);
+  const size_t rows = (size_t)n * pl.g_pad;
+  if (minmax) {
+    if (cudaMemsetAsync(w.mmax, 0, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
+    if (cudaMemsetAsync(w.mmin, 0xFF, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
+    if (select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  }
+  if (select_pass<kCov>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  const int gb = (pl.geo.n_groups + 127) / 128;
+  k_cov_merge<<<dim3(gb, pl.cov_bins, n), 128, 0, st>>>(w.cov_hist, w.mass, pl.cov_bins, n_chunks, pl.g_pad,
+                                                         pl.geo.n_groups, w.cum_cnt, w.cum_mass);
+  k_cov_scan<<<dim3((pl.geo.n_groups + 7) / 8, n), 256, 0, st>>>(w.mmax, w.mmin, pl.cov_bins, pl.g_pad,
+                                                                  pl.geo.n_groups, scale, w.cum_cnt, w.cum_mass,
+                                                                  w.width);
+  const int nblk = (pl.geo.n_groups + kCovGroupsPerBlock - 1) / kCovGroupsPerBlock;
+  // rounds: the interval shrinks from S values to at most ceil(span / kCovPoints) per round
+  int rounds = 1;
+  for (int64_t span = pl.geo.S; span > kCovPoints; span = (span + kCovPoints - 1) / kCovPoints) ++rounds;
+  for (int round = 0; round < rounds; ++round) {
+    k_cov_eval<<<dim3(nblk, n), kCovPoints, 0, st>>>(round, false, pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.geo.S,
+                                               w.cum_cnt, w.cum_mass, w.width, w.cov_range, 0, w.cov_partial);
+    k_cov_pick<<<n, kCovPoints, 0, st>>>(round, false, nblk, pl.geo.n_groups, pl.geo.S, mass, w.cov_partial,
+                                          w.cov_range, k_cov, nullptr, 0, tab);
+  }
+  if (curve) {
+    k_cov_eval<<<dim3(nblk, n), kCovPoints, 0, st>>>(0, true, pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.geo.S,
+                                               w.cum_cnt, w.cum_mass, w.width, w.cov_range, n_curve, w.cov_partial);
+    k_cov_pick<<<n, kCovPoints, 0, st>>>(0, true, nblk, pl.geo.n_groups, pl.geo.S, mass, w.cov_partial,
+                                          w.cov_range, k_cov, curve, n_curve, tab);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace dsv
 
 using namespace dsv;
@@ -1142,14 +1251,21 @@ extern "C" size_t dsv_lowrank_topk_workspace_size(dsv_shape shape, int32_t r, ds
   if (validate_common(shape, group, true) != DSV_OK || (r != 16 && r != 32 && r != 64)) return 0;
   TopkPlan pl = make_plan(shape, r, group);
   TopkWs w;
-  return carve(nullptr, pl, false, &w);
+  return carve(nullptr, pl, kCarveTopk, &w);
 }
 
 extern "C" size_t dsv_coverage_workspace_size(dsv_shape shape, int32_t r, dsv_group group) {
   if (validate_common(shape, group, true) != DSV_OK || (r != 16 && r != 32 && r != 64)) return 0;
   TopkPlan pl = make_plan(shape, r, group);
   TopkWs w;
-  return carve(nullptr, pl, true, &w);
+  return carve(nullptr, pl, kCarveCov, &w);
+}
+
+extern "C" size_t dsv_coverage_topk_workspace_size(dsv_shape shape, int32_t r, dsv_group group) {
+  if (validate_common(shape, group, true) != DSV_OK || (r != 16 && r != 32 && r != 64)) return 0;
+  TopkPlan pl = make_plan(shape, r, group);
+  TopkWs w;
+  return carve(nullptr, pl, kCarveBoth, &w);
 }
 
 extern "C" dsv_status dsv_lowrank_topk(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr,
@@ -1165,9 +1281,9 @@ extern "C" dsv_status dsv_lowrank_topk(const void* Q, const void* K, const void*
   for (int p = 0; p < P; ++p)
     if (idx_offset[p] >= 0 && (k_per_head[p] < 1 || k_per_head[p] > S)) return DSV_ERR_INVALID_ARG;
   TopkWs w;
-  const size_t need = carve(nullptr, pl, false, &w);
+  const size_t need = carve(nullptr, pl, kCarveTopk, &w);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DSV_ERR_WORKSPACE;
-  carve(workspace, pl, false, &w);
+  carve(workspace, pl, kCarveTopk, &w);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   std::vector<int> active;
@@ -1191,54 +1307,10 @@ extern "C" dsv_status dsv_lowrank_topk(const void* Q, const void* K, const void*
       tab.k[i] = k_per_head[p];
       tab.off[i] = idx_offset[p];
     }
-    const int n = tab.n;
     if (launch_proj(r, Q, K, Wq_lr, Wk_lr, shape, pl, w, tab, dev_status, st) != cudaSuccess) return DSV_ERR_CUDA;
     CUtensorMap maps[4];
-    if (!make_score_maps(maps, pl, w, n)) return DSV_ERR_CUDA;
-    int n_chunks, chunk_tiles;
-    chunking(pl, n, &n_chunks, &chunk_tiles);
-    SelParams prm;
-    memset(&prm, 0, sizeof(prm));
-    prm.geo = pl.geo;
-    prm.g_pad = pl.g_pad;
-    prm.n_chunks = n_chunks;
-    prm.chunk_tiles = chunk_tiles;
-    prm.n_tiles = pl.n_tiles;
-    prm.mmax = w.mmax;
-    prm.mmin = w.mmin;
-    prm.hist = w.hist;
-    prm.bstar = w.bstar;
-    prm.cand_cnt = w.cand_cnt;
-    prm.cand = w.cand;
-    prm.above = w.above;
-    prm.inbin = w.inbin;
-    prm.tau = w.tau;
-    prm.out_off = w.out_off;
-    prm.eq_budget = w.eqb;
-    prm.sel_bits = w.selb;
-    prm.tie_cut = w.tcut;
-    prm.idx = idx;
-    prm.status = dev_status;
-    const dim3 grid(pl.n_gt, n_chunks, n);
-    const size_t rows = (size_t)n * pl.g_pad;
-    if (cudaMemsetAsync(w.mmax, 0, rows * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
-    if (cudaMemsetAsync(w.mmin, 0xFF, rows * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
-    if (select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
-    if (cudaMemsetAsync(w.hist, 0, rows * pl.hist_bins * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
-    if (select_pass<kHist>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
-    k_bracket<<<dim3(pl.n_gt, n), 128, 0, st>>>(w.hist, pl.hist_bins, pl.g_pad, pl.geo.n_groups, w.bstar,
-                                                 w.nabove, tab);
-    if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
-    if (cudaMemsetAsync(w.cand_cnt, 0, rows * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
-    if (select_pass<kCollect>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
-    k_resolve<<<dim3(pl.geo.n_groups, n), 256, 0, st>>>(w.cand, w.cand_cnt, w.mmax, w.mmin, w.nabove, w.above,
-                                                          w.inbin, pl.g_pad, n_chunks, chunk_tiles * 128, w.tau,
-                                                          w.out_off, w.eqb, w.tcut, dev_status, tab);
-    if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
-    if (select_pass<kEmit>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
-    k_sel_compact<<<dim3(pl.geo.n_groups, n), 32 * kCompactWarps, 0, st>>>(w.selb, pl.g_pad, pl.n_tiles * 4, idx,
-                                                                            dev_status, tab);
-    if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
+    if (!make_score_maps(maps, pl, w, tab.n)) return DSV_ERR_CUDA;
+    if (topk_passes(pl, w, tab, maps, true, idx, dev_status, st) != cudaSuccess) return DSV_ERR_CUDA;
   }
   return DSV_OK;
 }
@@ -1254,9 +1326,9 @@ extern "C" dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_
   const TopkPlan pl = make_plan(shape, r, group);
   if (pl.n_tiles > kMaxChunks * kCovMaxTiles) return DSV_ERR_UNSUPPORTED;
   TopkWs w;
-  const size_t need = carve(nullptr, pl, true, &w);
+  const size_t need = carve(nullptr, pl, kCarveCov, &w);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DSV_ERR_WORKSPACE;
-  carve(workspace, pl, true, &w);
+  carve(workspace, pl, kCarveCov, &w);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int P = (int)(shape.B * shape.H);
   for (int c0 = 0; c0 < P; c0 += pl.pc) {
@@ -1268,54 +1340,63 @@ extern "C" dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_
       tab.k[i] = 1;
       tab.off[i] = 0;
     }
-    const int n = tab.n;
     if (launch_proj(r, Q, K, Wq_lr, Wk_lr, shape, pl, w, tab, dev_status, st) != cudaSuccess) return DSV_ERR_CUDA;
     CUtensorMap maps[4];
-    if (!make_score_maps(maps, pl, w, n)) return DSV_ERR_CUDA;
-    int n_chunks, chunk_tiles;
-    chunking(pl, n, &n_chunks, &chunk_tiles, kCovMaxTiles);
-    SelParams prm;
-    memset(&prm, 0, sizeof(prm));
-    prm.geo = pl.geo;
-    prm.g_pad = pl.g_pad;
-    prm.n_chunks = n_chunks;
-    prm.chunk_tiles = chunk_tiles;
-    prm.n_tiles = pl.n_tiles;
-    prm.scale = scale;
-    prm.mmax = w.mmax;
-    prm.mmin = w.mmin;
-    prm.hist = w.hist;
-    prm.mass = w.mass;
-    prm.status = dev_status;
-    const dim3 grid(pl.n_gt, n_chunks, n);
-    const size_t rows = (size_t)n * pl.g_pad;
-    if (cudaMemsetAsync(w.mmax, 0, rows * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
-    if (cudaMemsetAsync(w.mmin, 0xFF, rows * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
-    if (select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
-    if (select_pass<kCov>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
-    const int gb = (pl.geo.n_groups + 127) / 128;
-    k_cov_merge<<<dim3(gb, pl.cov_bins, n), 128, 0, st>>>(w.hist, w.mass, pl.cov_bins, n_chunks, pl.g_pad,
-                                                           pl.geo.n_groups, w.cum_cnt, w.cum_mass);
-    k_cov_scan<<<dim3((pl.geo.n_groups + 7) / 8, n), 256, 0, st>>>(w.mmax, w.mmin, pl.cov_bins, pl.g_pad,
-                                                                    pl.geo.n_groups, scale, w.cum_cnt, w.cum_mass,
-                                                                    w.width);
-    const int nblk = (pl.geo.n_groups + kCovGroupsPerBlock - 1) / kCovGroupsPerBlock;
-    // rounds: the interval shrinks from S values to at most ceil(span / kCovPoints) per round
-    int rounds = 1;
-    for (int64_t span = pl.geo.S; span > kCovPoints; span = (span + kCovPoints - 1) / kCovPoints) ++rounds;
-    for (int round = 0; round < rounds; ++round) {
-      k_cov_eval<<<dim3(nblk, n), kCovPoints, 0, st>>>(round, false, pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.geo.S,
-                                                 w.cum_cnt, w.cum_mass, w.width, w.cov_range, 0, w.cov_partial);
-      k_cov_pick<<<n, kCovPoints, 0, st>>>(round, false, nblk, pl.geo.n_groups, pl.geo.S, mass, w.cov_partial,
-                                            w.cov_range, k_cov, nullptr, 0, tab);
+    if (!make_score_maps(maps, pl, w, tab.n)) return DSV_ERR_CUDA;
+    if (cov_passes(pl, w, tab, maps, true, scale, mass, k_cov, curve, n_curve, dev_status, st) != cudaSuccess)
+      return DSV_ERR_CUDA;
+  }
+  return DSV_OK;
+}
+
+extern "C" dsv_status dsv_coverage_topk(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr,
+                                        dsv_shape shape, int32_t r, dsv_group group, float scale, float mass,
+                                        int32_t* k_cov, float* curve, int32_t n_curve, const int32_t* k_per_head,
+                                        const int64_t* idx_offset, int32_t* idx, void* workspace,
+                                        size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  dsv_status v = validate_lowrank(Q, K, Wq_lr, Wk_lr, shape, r, group);
+  if (v != DSV_OK) return v;
+  if (!k_cov || !(scale > 0.f) || !(mass > 0.f && mass <= 1.f)) return DSV_ERR_INVALID_ARG;
+  if (curve && (n_curve < 1 || n_curve > 1024)) return DSV_ERR_INVALID_ARG;
+  if (!k_per_head || !idx_offset || !idx || !aligned(idx, 4)) return DSV_ERR_INVALID_ARG;
+  const TopkPlan pl = make_plan(shape, r, group);
+  if (pl.n_tiles > kMaxChunks * kCovMaxTiles) return DSV_ERR_UNSUPPORTED;
+  const int P = (int)(shape.B * shape.H);
+  const int S = pl.geo.S;
+  bool all_selected = true;   // every problem takes a proper top-k (no dense head, no k = S)
+  for (int p = 0; p < P; ++p) {
+    if (idx_offset[p] >= 0 && (k_per_head[p] < 1 || k_per_head[p] > S)) return DSV_ERR_INVALID_ARG;
+    all_selected = all_selected && idx_offset[p] >= 0 && k_per_head[p] < S;
+  }
+  TopkWs w;
+  const size_t need = carve(nullptr, pl, kCarveBoth, &w);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DSV_ERR_WORKSPACE;
+  if (!all_selected) {
+    // problem tables differ between the two: run them one after the other
+    v = dsv_coverage(Q, K, Wq_lr, Wk_lr, shape, r, group, scale, mass, k_cov, curve, n_curve, workspace,
+                     workspace_bytes, dev_status, stream);
+    if (v != DSV_OK) return v;
+    return dsv_lowrank_topk(Q, K, Wq_lr, Wk_lr, shape, r, group, k_per_head, idx_offset, idx, workspace,
+                            workspace_bytes, dev_status, stream);
+  }
+  carve(workspace, pl, kCarveBoth, &w);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int c0 = 0; c0 < P; c0 += pl.pc) {
+    ProblemTable tab;
+    memset(&tab, 0, sizeof(tab));
+    tab.n = std::min(pl.pc, P - c0);
+    for (int i = 0; i < tab.n; ++i) {
+      tab.p[i] = c0 + i;
+      tab.k[i] = k_per_head[c0 + i];
+      tab.off[i] = idx_offset[c0 + i];
     }
-    if (curve) {
-      k_cov_eval<<<dim3(nblk, n), kCovPoints, 0, st>>>(0, true, pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.geo.S,
-                                                 w.cum_cnt, w.cum_mass, w.width, w.cov_range, n_curve, w.cov_partial);
-      k_cov_pick<<<n, kCovPoints, 0, st>>>(0, true, nblk, pl.geo.n_groups, pl.geo.S, mass, w.cov_partial,
-                                            w.cov_range, k_cov, curve, n_curve, tab);
-    }
-    if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
+    // one projection and one row-range pass serve both
+    if (launch_proj(r, Q, K, Wq_lr, Wk_lr, shape, pl, w, tab, dev_status, st) != cudaSuccess) return DSV_ERR_CUDA;
+    CUtensorMap maps[4];
+    if (!make_score_maps(maps, pl, w, tab.n)) return DSV_ERR_CUDA;
+    if (cov_passes(pl, w, tab, maps, true, scale, mass, k_cov, curve, n_curve, dev_status, st) != cudaSuccess)
+      return DSV_ERR_CUDA;
+    if (topk_passes(pl, w, tab, maps, false, idx, dev_status, st) != cudaSuccess) return DSV_ERR_CUDA;
   }
   return DSV_OK;
 }

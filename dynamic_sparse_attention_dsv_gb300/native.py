@@ -49,6 +49,10 @@ SIGNATURES = [
     ("dsv_coverage_workspace_size", ctypes.c_size_t, [dsv_shape, ctypes.c_int32, dsv_group]),
     ("dsv_coverage", ctypes.c_int, [_P, _P, _P, _P, dsv_shape, ctypes.c_int32, dsv_group, ctypes.c_float,
                                     ctypes.c_float, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P, _P]),
+    ("dsv_coverage_topk_workspace_size", ctypes.c_size_t, [dsv_shape, ctypes.c_int32, dsv_group]),
+    ("dsv_coverage_topk", ctypes.c_int, [_P, _P, _P, _P, dsv_shape, ctypes.c_int32, dsv_group, ctypes.c_float,
+                                         ctypes.c_float, _P, _P, ctypes.c_int32, _I32P, _I64P, _P, _P,
+                                         ctypes.c_size_t, _P, _P]),
     ("dsv_plan_heads", ctypes.c_int, [_I32P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
                                       ctypes.c_double, ctypes.c_double, _I32P, _U8P, _I64P, _I64P]),
     ("dsv_sparse_attn_fwd_workspace_size", ctypes.c_size_t, [dsv_shape, dsv_group]),

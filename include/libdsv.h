@@ -146,6 +146,26 @@ dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_lr, const v
                         void* stream);
 
 /* ------------------------------------------------------------------------
+ * dsv_coverage_topk -- dsv_coverage and dsv_lowrank_topk in one call.
+ * Passage: technical summary sections 2.1 and 2.2, as for the two calls.
+ *
+ * Same arguments, outputs and device errors as dsv_coverage (scale, mass,
+ * k_cov, curve, n_curve) followed by dsv_lowrank_topk (k_per_head,
+ * idx_offset, idx); k_cov, curve and idx hold exactly the values the two
+ * separate calls write. When every problem takes a top-k with 1 <= k < S
+ * (no dense entry, no k = S), the key projection, the group-mean
+ * projection and the per-row score range are computed once and serve both;
+ * otherwise the two calls run one after the other. The workspace is at least
+ * dsv_coverage_topk_workspace_size() bytes (the two calls' buffers side by
+ * side); S <= 4186112 as for dsv_coverage.
+ * ---------------------------------------------------------------------- */
+size_t dsv_coverage_topk_workspace_size(dsv_shape shape, int32_t r, dsv_group group);
+dsv_status dsv_coverage_topk(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr, dsv_shape shape,
+                             int32_t r, dsv_group group, float scale, float mass, int32_t* k_cov, float* curve,
+                             int32_t n_curve, const int32_t* k_per_head, const int64_t* idx_offset, int32_t* idx,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * dsv_plan_heads -- the OP dispatcher, per head (host only, no GPU).
  * Passage: technical summary section 2.1 (the OP dispatcher activates sparse
  * attention per block according to the current sparsity level).

@@ -126,6 +126,27 @@ def test_argument_validation_before_launch(lib):
                             ctypes.c_float(0.1), ctypes.c_float(0.9), fake, None, 0, fake, 1 << 30, None, None) == 2
 
 
+def test_coverage_topk_workspace_and_validation(lib):
+    """The combined call holds both calls' buffers with the projections and
+    row ranges once, and rejects bad arguments before anything launches."""
+    g = native.dsv_group(2, 8, 8)
+    s = _shape(1, 2, 16, 64, 64, 128)
+    both = lib.dsv_coverage_topk_workspace_size(s, 32, g)
+    topk = lib.dsv_lowrank_topk_workspace_size(s, 32, g)
+    cov = lib.dsv_coverage_workspace_size(s, 32, g)
+    assert max(topk, cov) < both < topk + cov
+    fake = ctypes.c_void_p(256)
+    ks = (ctypes.c_int32 * 2)(10, 10)
+    offs = (ctypes.c_int64 * 2)(0, 10 * 512)
+    args = lambda k, mass, ws_bytes: (fake, fake, fake, fake, s, 32, g, ctypes.c_float(0.1), ctypes.c_float(mass),
+                                      fake, None, 0, k, offs, fake, fake, ws_bytes, None, None)
+    assert lib.dsv_coverage_topk(*args((ctypes.c_int32 * 2)(10, s.T * s.Y * s.X + 1), 0.9, 1 << 40)) == 1
+    assert lib.dsv_coverage_topk(*args(ks, 1.5, 1 << 40)) == 1
+    assert lib.dsv_coverage_topk(*args(ks, 0.9, both - 1)) == 3
+    assert lib.dsv_coverage_topk(fake, fake, fake, fake, s, 48, g, ctypes.c_float(0.1), ctypes.c_float(0.9), fake,
+                                 None, 0, ks, offs, fake, fake, 1 << 40, None, None) == 2
+
+
 def test_topk_layout_packs_rows():
     ks, offs, total = api.topk_layout(3, 16, [5, 7, 9], skip=[False, True, False])
     assert offs == [0, -1, 80] and total == 80 + 16 * 9

@@ -84,6 +84,19 @@ def test_coverage_matches_oracle(case):
         np.testing.assert_allclose(curve[h].cpu().numpy(), C[np.array(pts) - 1], atol=2e-4)
 
 
+def test_coverage_topk_equals_the_two_calls(case):
+    """One combined call writes exactly what dsv_coverage and dsv_lowrank_topk
+    write separately (shared projections and row ranges change no bit)."""
+    w, d = case["w"], case["dev"]
+    st = dsv.new_status()
+    k1, c1 = dsv.coverage(d["Q"], d["K"], d["Wq"], d["Wk"], _grid(w), _group(w), mass=0.9, curve_points=8, status=st)
+    i1, _, _ = dsv.lowrank_topk(d["Q"], d["K"], d["Wq"], d["Wk"], _grid(w), _group(w), w.k, status=st)
+    k2, c2, i2, ks, offs = dsv.coverage_topk(d["Q"], d["K"], d["Wq"], d["Wk"], _grid(w), _group(w), w.k, mass=0.9,
+                                             curve_points=8, status=st)
+    dsv.check_status(st, "coverage_topk")
+    assert torch.equal(k1, k2) and torch.equal(c1, c2) and torch.equal(i1, i2)
+
+
 def _oracle_attention(case, h, idx):
     inp = case["inp"]
     O, L = ora.sparse_attn_fwd(inp["Q"][h], inp["K"][h], inp["V"][h], idx, case["mem"], case["scale"])
@@ -199,6 +212,11 @@ def test_mixed_plan_sparse_and_dense_heads():
     idx = torch.empty(total, dtype=torch.int32, device="cuda")
     st = dsv.new_status()
     dsv.lowrank_topk(d["Q"], d["K"], d["Wq"], d["Wk"], _grid(w), _group(w), ks, idx_offset=offs, idx=idx, status=st)
+    # the combined call takes its two-call path on a plan with a dense head: same bits
+    kc, _, idx2, _, _ = dsv.coverage_topk(d["Q"], d["K"], d["Wq"], d["Wk"], _grid(w), _group(w), ks, idx_offset=offs,
+                                          status=st)
+    kc1, _ = dsv.coverage(d["Q"], d["K"], d["Wq"], d["Wk"], _grid(w), _group(w), status=st)
+    assert torch.equal(idx2, idx) and torch.equal(kc, kc1)
     O, L = dsv.sparse_attn_fwd(d["Q"], d["K"], d["V"], idx, ks, offs, _grid(w), _group(w), status=st)
     dQ, dK, dV = dsv.sparse_attn_bwd(d["Q"], d["K"], d["V"], O, L, d["dO"], idx, ks, offs, _grid(w), _group(w),
                                      status=st)
