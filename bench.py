@@ -66,9 +66,11 @@ def attn_flops(w, ks):
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi sampling SM clocks and throttle reasons every 100 ms. The
+    """nvidia-smi sampling SM clocks and throttle reasons every 20 ms. The
     caller marks its timed windows (wall clock); only samples taken inside a
-    window are summarised, so idle gaps between windows do not count."""
+    window are summarised. It runs over the device-timed steps only: while it
+    polls, the pinned host<->device copies of the end-to-end run were seen to
+    take up to 60% longer."""
 
     def __init__(self, dev_index: int):
         self.proc = None
@@ -80,7 +82,7 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(dev_index), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                          "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -119,8 +121,8 @@ class ClockSampler:
                 except ValueError:
                     continue
         # a sample reports the state over the preceding interval: keep those
-        # stamped inside a window or up to 100 ms after it closes
-        inside = [r for r in rows if any(t0 <= r[0] <= t1 + 0.1 for t0, t1 in self.windows)]
+        # stamped inside a window or up to 20 ms after it closes
+        inside = [r for r in rows if any(t0 <= r[0] <= t1 + 0.02 for t0, t1 in self.windows)]
         if not inside:
             return None
         return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
@@ -310,6 +312,7 @@ def main():
         tdist.barrier()
     wall = time.perf_counter() - t_wall
     clocks.mark(t_epoch, time.time())
+    clk = clocks.stop()
     code = dsv.read_status(step.status)
     if code:
         raise SystemExit(f"device status {dsv.native.DSV_STATUS.get(code, code)} in the timed region")
@@ -344,8 +347,8 @@ def main():
     # DRAM bytes (read + write) per head of the phase's kernels from one ncu
     # capture of this workload at 2 heads (the per-head work is independent,
     # so traffic scales with the head count); null for other workloads
-    dram_per_head = {"attn_bwd": (287815424 + 3414817000 + 3436778000 + 70182144) / 2,   # k_attn_bwd_q, k_csc_reduce
-                     "attn_fwd": (101435136 + 17325056) / 2}                                # k_attn_fwd
+    dram_per_head = {"attn_bwd": (287686144 + 3414548736 + 3436778000 + 70182144) / 2,   # k_attn_bwd_q, k_csc_reduce
+                     "attn_fwd": (101424896 + 17273088) / 2}                                # k_attn_fwd
     traffic = None
     if dom in dram_per_head and (w.S, w.d, w.k, w.gt, w.gy, w.gx) == (65536, 128, 6554, 2, 8, 8):
         traffic = int(dram_per_head[dom] * w.H)
@@ -355,8 +358,7 @@ def main():
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e and rank == 0:
-        e2e = end_to_end(w, inp, device, args, step, clocks=clocks)
-    clk = clocks.stop()
+        e2e = end_to_end(w, inp, device, args, step)
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
