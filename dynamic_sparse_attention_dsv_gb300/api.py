@@ -79,9 +79,13 @@ def check_status(status: torch.Tensor, where: str = "libdsv") -> None:
         raise N.DsvError(code, where + " (device)")
 
 
-def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.Tensor:
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor], any_size: bool = False) -> torch.Tensor:
+    """The caller's workspace (uint8) or a new one of nbytes. With any_size the
+    library itself decides whether a smaller workspace is enough."""
     if workspace is not None:
-        if workspace.numel() * workspace.element_size() < nbytes:
+        if workspace.dtype != torch.uint8 or workspace.device != torch.device(device):
+            raise ValueError("workspace must be a uint8 tensor on the call's device")
+        if not any_size and workspace.numel() < nbytes:
             raise ValueError("workspace too small")
         return workspace
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
@@ -222,9 +226,17 @@ def sparse_attn_bwd_workspace_size(x, grid, group, k_per_head=None, idx_offset=N
     return int(N.load().dsv_sparse_attn_bwd_workspace_size(make_shape(x, grid), make_group(group), kp, op))
 
 
+def sparse_attn_bwd_min_workspace_size(x, grid, group, k_per_head=None, idx_offset=None) -> int:
+    kp = _i32(k_per_head) if k_per_head is not None else None
+    op = _i64(idx_offset) if idx_offset is not None else None
+    return int(N.load().dsv_sparse_attn_bwd_min_workspace_size(make_shape(x, grid), make_group(group), kp, op))
+
+
 def sparse_attn_bwd(Q, K, V, O, LSE, dO, idx, k_per_head, idx_offset, grid, group, scale: Optional[float] = None,
                     dQ=None, dK=None, dV=None, workspace=None, status=None):
-    """dsv_sparse_attn_bwd. Returns (dQ, dK, dV)."""
+    """dsv_sparse_attn_bwd. Returns (dQ, dK, dV). A workspace smaller than
+    dsv_sparse_attn_bwd_workspace_size() is accepted down to the library's
+    minimum (more, smaller launches; the same result bits)."""
     _check_bf16(Q, K, V, O, dO)
     lib = N.load()
     shape, grp = make_shape(Q, grid), make_group(group)
@@ -234,7 +246,8 @@ def sparse_attn_bwd(Q, K, V, O, LSE, dO, idx, k_per_head, idx_offset, grid, grou
     dV = torch.empty_like(V) if dV is None else dV
     kp = _i32(k_per_head) if idx is not None else None
     op = _i64(idx_offset) if idx is not None else None
-    ws = _workspace(int(lib.dsv_sparse_attn_bwd_workspace_size(shape, grp, kp, op)), Q.device, workspace)
+    ws = _workspace(int(lib.dsv_sparse_attn_bwd_workspace_size(shape, grp, kp, op)), Q.device, workspace,
+                    any_size=True)
     st = status if status is not None else new_status(Q.device)
     code = lib.dsv_sparse_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(dO), _ptr(idx), kp, op, shape,
                                    grp, ctypes.c_float(scale), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(),

@@ -730,6 +730,9 @@ __global__ void k_bwd_delta(const __nv_bfloat16* __restrict__ O, const __nv_bflo
 
 // ---------------------------------------------------------------------------
 // Ordered dK/dV reduction: slot map.
+constexpr int kCscKeys = 256;
+constexpr int kCscStride = kCscKeys + 1;   // words per bitmap column in shared memory (bank spread)
+
 // One CTA per (256-key block, unit) builds the block's part of the selection
 // bitmap in shared memory. Index rows are ascending, so each thread binary-
 // searches a group's row for the block's first key and walks the row while
@@ -737,8 +740,6 @@ __global__ void k_bwd_delta(const __nv_bfloat16* __restrict__ O, const __nv_bflo
 // high half, the count of the key's set bits in its lower words, and every
 // key's slot offset within the block plus the block's total are written.
 // Keys outside the block (including values outside [0, S)) are ignored.
-constexpr int kCscKeys = 256;
-constexpr int kCscStride = kCscKeys + 1;   // words per bitmap column in shared memory (bank spread)
 
 __global__ void __launch_bounds__(256) k_csc_build(const int32_t* __restrict__ idx, uint64_t* bits, int S,
                                                    int32_t* off, int32_t* bsum, const UnitTable tab) {
@@ -931,13 +932,14 @@ struct BwdPlan {
   bool split = false;                // some problem spans several units
 };
 
+// Units and launches for a budget of bf16 partial bytes in flight per launch.
 static BwdPlan plan_bwd(const dsv_shape& shape, const Geometry& geo, bool any_sparse, const int32_t* k_per_head,
-                        const int64_t* idx_offset) {
+                        const int64_t* idx_offset, size_t budget = kPartialBudget) {
   BwdPlan pl;
   memset(&pl.dense, 0, sizeof(pl.dense));
   const int P = (int)(shape.B * shape.H);
   const size_t slot_bytes = (size_t)shape.d * 2 * sizeof(__nv_bfloat16);
-  const size_t cap = std::max<size_t>(1, kPartialBudget / slot_bytes);
+  const size_t cap = std::max<size_t>(1, budget / slot_bytes);
   UnitTable cur;
   memset(&cur, 0, sizeof(cur));
   size_t cur_slots = 0, cur_words = 0;
@@ -1042,6 +1044,30 @@ extern "C" size_t dsv_sparse_attn_bwd_workspace_size(dsv_shape shape, dsv_group 
   return carve_bwd(nullptr, shape, pl, &w);
 }
 
+extern "C" size_t dsv_sparse_attn_bwd_min_workspace_size(dsv_shape shape, dsv_group group,
+                                                         const int32_t* k_per_head, const int64_t* idx_offset) {
+  if (validate_common(shape, group, true) != DSV_OK) return 0;
+  const Geometry geo = make_geometry(shape, group);
+  const int P = (int)(shape.B * shape.H);
+  const bool any_sparse = k_per_head != nullptr;
+  if (any_sparse && !idx_offset) return 0;
+  if (any_sparse)
+    for (int i = 0; i < P; ++i)
+      if (idx_offset[i] >= 0 && (k_per_head[i] < 1 || k_per_head[i] > geo.S)) return 0;
+  // the smallest of the plans dsv_sparse_attn_bwd tries (budgets halving from
+  // kPartialBudget to one query group per launch): any workspace at least this
+  // large fits one of them
+  const size_t slot_bytes = (size_t)shape.d * 2 * sizeof(__nv_bfloat16);
+  size_t least = SIZE_MAX;
+  for (size_t budget = kPartialBudget;; budget /= 2) {
+    const BwdPlan pl = plan_bwd(shape, geo, any_sparse, k_per_head, idx_offset, budget);
+    BwdWs w;
+    least = std::min(least, carve_bwd(nullptr, shape, pl, &w));
+    if (budget < slot_bytes) break;
+  }
+  return least;
+}
+
 extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, const void* O,
                                           const float* LSE, const void* dO, const int32_t* idx,
                                           const int32_t* k_per_head, const int64_t* idx_offset, dsv_shape shape,
@@ -1062,10 +1088,24 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
       if (k_per_head[i] < 1 || k_per_head[i] > geo.S) return DSV_ERR_INVALID_ARG;
       if (geo.S > 256 * kMaxBlocks) return DSV_ERR_UNSUPPORTED;   // slot map covers S <= 2^18
     }
-  const BwdPlan pl = plan_bwd(shape, geo, idx != nullptr, k_per_head, idx_offset);
+  if (!workspace || !aligned(workspace, 256)) return DSV_ERR_WORKSPACE;
+  // The largest budget of partials in flight whose plan fits the workspace: a
+  // smaller workspace only means more, smaller launches (a problem's groups
+  // split over several, with fp32 running sums; the summation order, and so
+  // every result bit, stays the same).
+  BwdPlan pl;
   BwdWs w;
-  const size_t need = carve_bwd(nullptr, shape, pl, &w);
-  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DSV_ERR_WORKSPACE;
+  bool fits = false;
+  const size_t slot_bytes = (size_t)d * 2 * sizeof(__nv_bfloat16);
+  for (size_t budget = kPartialBudget;; budget /= 2) {
+    pl = plan_bwd(shape, geo, idx != nullptr, k_per_head, idx_offset, budget);
+    if (carve_bwd(nullptr, shape, pl, &w) <= workspace_bytes) {
+      fits = true;
+      break;
+    }
+    if (budget < slot_bytes) break;   // one group per launch already
+  }
+  if (!fits) return DSV_ERR_WORKSPACE;
   carve_bwd(workspace, shape, pl, &w);
   AttnMaps maps;
   CUtensorMap do_cube, q_tile, do_tile;

@@ -218,12 +218,21 @@ dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const void* V, cons
  * dense). The workspace size depends on the plan: pass the same k_per_head
  * and idx_offset to dsv_sparse_attn_bwd_workspace_size (it holds the bf16
  * partials of up to 48 GiB worth of (group, key) pairs at a time, a key x group
- * selection bitmap and per-key slot offsets; a head with more pairs is split
- * over several launches with fp32 running sums). Sparse problems need
- * S <= 262144 (DSV_ERR_UNSUPPORTED otherwise); dense problems do not.
+ * selection bitmap and per-key slot offsets; a head with more
+ * pairs is split over several launches with fp32 running sums). A smaller
+ * workspace is accepted: the call then keeps fewer pairs in flight per launch
+ * (the largest power-of-two fraction of 48 GiB that fits, down to one query
+ * group per launch), which changes no result bit; below that minimum it
+ * returns DSV_ERR_WORKSPACE. Sparse problems need S <= 262144
+ * (DSV_ERR_UNSUPPORTED otherwise); dense problems do not.
  * ---------------------------------------------------------------------- */
 size_t dsv_sparse_attn_bwd_workspace_size(dsv_shape shape, dsv_group group, const int32_t* k_per_head,
                                           const int64_t* idx_offset);
+/* The smallest workspace dsv_sparse_attn_bwd accepts: the least of its plans
+ * (pairs in flight per launch halving from 48 GiB down to one query group);
+ * every workspace at least this large is accepted (0 on invalid arguments). */
+size_t dsv_sparse_attn_bwd_min_workspace_size(dsv_shape shape, dsv_group group, const int32_t* k_per_head,
+                                              const int64_t* idx_offset);
 dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
                                const void* dO, const int32_t* idx, const int32_t* k_per_head,
                                const int64_t* idx_offset, dsv_shape shape, dsv_group group, float scale, void* dQ,

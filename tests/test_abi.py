@@ -90,6 +90,15 @@ def test_workspace_is_order_S_k_not_S_squared(lib):
     big = lib.dsv_sparse_attn_bwd_workspace_size(s, g, (ctypes.c_int32 * 1)(4000), (ctypes.c_int64 * 1)(0))
     n_groups = 16 * 64 * 64 // 128
     assert big - small >= n_groups * 3000 * 128 * 4 * 0.99
+    # the minimum (one query group per launch) is far below the full plan and is accepted
+    least = lib.dsv_sparse_attn_bwd_min_workspace_size(s, g, (ctypes.c_int32 * 1)(4000), (ctypes.c_int64 * 1)(0))
+    assert 0 < least < big // 8
+    fake = ctypes.c_void_p(256)
+    args = lambda nbytes: (fake, fake, fake, fake, fake, fake, fake, (ctypes.c_int32 * 1)(4000),
+                           (ctypes.c_int64 * 1)(0), s, g, ctypes.c_float(0.1), fake, fake, fake, fake, nbytes, None,
+                           None)
+    assert lib.dsv_sparse_attn_bwd(*args(least)) != 3       # past the workspace check (no GPU here: launch fails)
+    assert lib.dsv_sparse_attn_bwd(*args(least // 2)) == 3
     # dense-only problems need almost nothing
     assert lib.dsv_sparse_attn_bwd_workspace_size(s, g, None, None) < 64 << 20
 

@@ -140,6 +140,30 @@ def test_sparse_bwd_matches_oracle(case):
             assert e <= GRAD_REL_L2, (h, name, e)
 
 
+def test_small_backward_workspace_changes_no_bit(case):
+    """A backward workspace below the reported size makes the call keep fewer
+    (group, key) pairs in flight per launch. Where a head's partial rows
+    outweigh the fp32 running sums (ragged_d128, d64_r64, r16_h3), the
+    minimum size leaves one query group per launch, so every head's groups
+    are split over launches with running sums. The summation order, and so
+    every bit of dQ, dK and dV, stays the same."""
+    w, d = case["w"], case["dev"]
+    idx, ks, offs = _idx_tensor(case)
+    O, L = dsv.sparse_attn_fwd(d["Q"], d["K"], d["V"], idx, ks, offs, _grid(w), _group(w))
+    ref = dsv.sparse_attn_bwd(d["Q"], d["K"], d["V"], O, L, d["dO"], idx, ks, offs, _grid(w), _group(w))
+    need = dsv.sparse_attn_bwd_workspace_size(d["Q"], _grid(w), _group(w), ks, offs)
+    least = dsv.sparse_attn_bwd_min_workspace_size(d["Q"], _grid(w), _group(w), ks, offs)
+    assert 0 < least <= need
+    for nbytes in (least, (least + need) // 2):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        st = dsv.new_status()
+        got = dsv.sparse_attn_bwd(d["Q"], d["K"], d["V"], O, L, d["dO"], idx, ks, offs, _grid(w), _group(w),
+                                  workspace=ws, status=st)
+        dsv.check_status(st, "small workspace")
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)
+
+
 def test_dense_fwd_bwd_matches_oracle(case):
     w, d = case["w"], case["dev"]
     st = dsv.new_status()
