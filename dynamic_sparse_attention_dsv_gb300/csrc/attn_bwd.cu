@@ -854,19 +854,47 @@ __global__ void __launch_bounds__(256) k_csc_reduce(const CscParams csc, int S, 
     sv[e] = first ? 0.f : csc.acc_v[arow + e];
     sk[e] = first ? 0.f : csc.acc_k[arow + e];
   }
-  int64_t s = a;
-  for (; s < b; ++s) {
-    const __nv_bfloat16* pv = csc.part_v + s * D + lane * E;
-    const __nv_bfloat16* pk = csc.part_k + s * D + lane * E;
+  // slots are summed one after the other in ascending order; the rows of the
+  // next kBatch slots are loaded first so that more of them are in flight
+  constexpr int kBatch = 4;
+  auto add_row = [&](const uint32_t (&xv)[E / 2], const uint32_t (&xk)[E / 2]) {
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(pv + e));
-      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(pk + e));
-      sv[e] += x.x;
-      sv[e + 1] += x.y;
-      sk[e] += y.x;
-      sk[e + 1] += y.y;
+    for (int e = 0; e < E / 2; ++e) {
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv[e]));
+      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xk[e]));
+      sv[2 * e] += x.x;
+      sv[2 * e + 1] += x.y;
+      sk[2 * e] += y.x;
+      sk[2 * e + 1] += y.y;
     }
+  };
+  // one 8-byte (d = 128) or 4-byte (d = 64) load per lane and tensor
+  auto load_row = [&](int64_t slot, uint32_t (&xv)[E / 2], uint32_t (&xk)[E / 2]) {
+    const __nv_bfloat16* pv = csc.part_v + slot * D + lane * E;
+    const __nv_bfloat16* pk = csc.part_k + slot * D + lane * E;
+    if constexpr (E == 4) {
+      const uint2 a = __ldg(reinterpret_cast<const uint2*>(pv)), c = __ldg(reinterpret_cast<const uint2*>(pk));
+      xv[0] = a.x;
+      xv[1] = a.y;
+      xk[0] = c.x;
+      xk[1] = c.y;
+    } else {
+      xv[0] = __ldg(reinterpret_cast<const uint32_t*>(pv));
+      xk[0] = __ldg(reinterpret_cast<const uint32_t*>(pk));
+    }
+  };
+  int64_t s = a;
+  for (; s + kBatch <= b; s += kBatch) {
+    uint32_t xv[kBatch][E / 2], xk[kBatch][E / 2];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) load_row(s + i, xv[i], xk[i]);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) add_row(xv[i], xk[i]);
+  }
+  for (; s < b; ++s) {
+    uint32_t xv[E / 2], xk[E / 2];
+    load_row(s, xv, xk);
+    add_row(xv, xk);
   }
   if (last) {
     const int64_t orow = ((int64_t)tab.p[u] * S + j) * D + lane * E;
