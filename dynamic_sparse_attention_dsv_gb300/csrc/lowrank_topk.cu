@@ -78,6 +78,7 @@ struct SelParams {
   uint32_t* hist;        // HIST: [n][bins][g_pad]; COV: counts [n][chunks][bins][g_pad]
   float* mass;           // COV: [n][chunks][bins][g_pad]
   const int32_t* bstar;  // [n][g_pad]
+  const float* t_bin;    // COLLECT: [n][g_pad][2] least scores of bins b* and b*+1 (see k_bracket)
   uint32_t* cand_cnt;    // [n][g_pad]
   uint64_t* cand;        // [n][g_pad][kCandCap]
   int32_t* above;        // [n][chunks][g_pad]
@@ -121,9 +122,17 @@ __device__ __forceinline__ int bin_of(float t, int nb) {
 }
 
 // Linear bin of score s over [lo, lo + nb/inv_w); identical arithmetic in every
-// pass that uses it (no contraction), so HIST and COLLECT agree bit for bit.
+// place that uses it (no contraction), so the passes agree bit for bit. It is
+// monotone in s: every step (subtract, multiply by inv_w >= 0, round, read the
+// bits) preserves order.
 __device__ __forceinline__ int lin_bin(float s, float lo, float inv_w, int nb) {
   return bin_of(bin_round(__fmul_rn(__fsub_rn(s, lo), inv_w)), nb);
+}
+// The histogram range of a row from its orderable score bounds.
+__device__ __forceinline__ void lin_range(uint32_t mmin_ord, uint32_t mmax_ord, int nb, float* lo, float* inv_w) {
+  *lo = ord2f(mmin_ord);
+  const float hi = ord2f(mmax_ord);
+  *inv_w = hi > *lo ? (float)nb / __fsub_rn(hi, *lo) : 0.f;
 }
 
 // ---------------------------------------------------------------------------
@@ -240,7 +249,6 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     const uint32_t taddr_lane = tbase + ((uint32_t)(q * 32) << 16);
 
     float lo = 0.f, inv_w = 0.f, cmax = 0.f;
-    int bstar = 0;
     float mx = -INFINITY, mn = INFINITY;
     int n_above = 0, n_in = 0;
     float tau = INFINITY;
@@ -251,11 +259,13 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     constexpr int NB = (MODE == kCov) ? C::kCovBins : C::kHistBins;
     const uint32_t hist_base = smem_u32(sHist);
 
-    if constexpr (MODE == kHist || MODE == kCollect) {
-      lo = ord2f(prm.mmin[rid]);
-      const float hi = ord2f(prm.mmax[rid]);
-      inv_w = hi > lo ? (float)NB / (hi - lo) : 0.f;
-      if (MODE == kCollect) bstar = prm.bstar[rid];
+    float t_in = INFINITY, t_above = INFINITY;   // COLLECT: least scores of bins b* and b*+1
+    if constexpr (MODE == kHist) lin_range(prm.mmin[rid], prm.mmax[rid], NB, &lo, &inv_w);
+    if constexpr (MODE == kCollect) {
+      if (valid) {
+        t_in = prm.t_bin[2 * (size_t)rid];
+        t_above = prm.t_bin[2 * (size_t)rid + 1];
+      }
     }
     float w2 = 0.f;   // COV: bin width in log2 units
     if constexpr (MODE == kCov) {
@@ -327,11 +337,13 @@ __global__ void __launch_bounds__(kSelThreads, 2)
             const int bin = lin_bin(s, lo, inv_w, NB);
             red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
           } else if constexpr (MODE == kCollect) {
-            // branch-free here; the rare candidates are handled after the loop
-            const int bin = lin_bin(s, lo, inv_w, NB);
-            n_above += bin > bstar;
-            if (e < 32) cm_lo |= (uint32_t)(bin == bstar) << e;
-            else cm_hi |= (uint32_t)(bin == bstar) << (e - 32);
+            // branch-free here; the rare candidates are handled after the loop.
+            // bin(s) > b* <=> s >= t_above and bin(s) == b* <=> t_in <= s < t_above
+            // (the binning is monotone and k_bracket found the exact least scores)
+            const bool above = s >= t_above, in = s >= t_in && !above;
+            n_above += above;
+            if (e < 32) cm_lo |= (uint32_t)in << e;
+            else cm_hi |= (uint32_t)in << (e - 32);
           } else if constexpr (MODE == kCov) {
             // log-probability below the row maximum, its bin b, and q = exp(b w - u)
             const float u = __fmul_rn(prm.scale, __fsub_rn(cmax, s));
@@ -593,8 +605,21 @@ __global__ void __launch_bounds__(128) k_group_mean_proj(const __nv_bfloat16* __
 
 // ---------------------------------------------------------------------------
 // Bracket: per row, the bin b* holding the k-th largest score.
+// Least score (as an orderable key in [o_lo, o_hi]) whose bin is at least
+// `target`; o_hi when no score up to the row maximum reaches it.
+__device__ uint32_t least_with_bin(int target, uint32_t o_lo, uint32_t o_hi, float lo, float inv_w, int nb) {
+  uint32_t a = o_lo, b = o_hi;   // answer in [a, b]; the bin of ord2f(b) is >= target or b = o_hi
+  while (a < b) {
+    const uint32_t m = a + (b - a) / 2;
+    if (lin_bin(ord2f(m) + 0.0f, lo, inv_w, nb) >= target) b = m;
+    else a = m + 1;
+  }
+  return a;
+}
+
 __global__ void k_bracket(const uint32_t* __restrict__ hist, int nb, int g_pad, int n_groups, int32_t* bstar,
-                          int32_t* n_above_out, const ProblemTable tab) {
+                          int32_t* n_above_out, const uint32_t* __restrict__ mmin, const uint32_t* __restrict__ mmax,
+                          float* t_bin, const ProblemTable tab) {
   const int lp = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= n_groups) return;
   const int k = tab.k[lp];
@@ -618,8 +643,17 @@ __global__ void k_bracket(const uint32_t* __restrict__ hist, int nb, int g_pad, 
     }
   }
   if (!found) b = 0;
-  bstar[lp * g_pad + g] = b;
-  n_above_out[lp * g_pad + g] = above;
+  const int rid = lp * g_pad + g;
+  bstar[rid] = b;
+  n_above_out[rid] = above;
+  // COLLECT compares scores against the least scores of bins b and b+1: every
+  // score lies in [min, max] of its row, and past the maximum a threshold is
+  // the next float up (never reached)
+  float lo, inv_w;
+  lin_range(mmin[rid], mmax[rid], nb, &lo, &inv_w);
+  const uint32_t o_lo = mmin[rid], o_hi = mmax[rid] + 1u;
+  t_bin[2 * (size_t)rid] = ord2f(least_with_bin(b, o_lo, o_hi, lo, inv_w, nb));
+  t_bin[2 * (size_t)rid + 1] = ord2f(least_with_bin(b + 1, o_lo, o_hi, lo, inv_w, nb));
 }
 
 // Resolve: exact threshold, per-chunk output offsets and tie budgets.
@@ -1009,6 +1043,7 @@ struct TopkWs {
   uint32_t* cov_hist;
   float* mass;
   int32_t *bstar, *nabove, *above, *inbin, *out_off, *eqb;
+  float* tbin;
   uint32_t* selb;
   int32_t* tcut;
   uint64_t* cand;
@@ -1035,6 +1070,7 @@ static size_t carve(void* base, const TopkPlan& pl, int mode, TopkWs* w) {
   if (mode & kCarveTopk) {
     w->hist = c.take<uint32_t>(pc * pl.hist_bins * gp);
     w->bstar = c.take<int32_t>(pc * gp);
+    w->tbin = c.take<float>(pc * gp * 2);
     w->nabove = c.take<int32_t>(pc * gp);
     w->cand_cnt = c.take<uint32_t>(pc * gp);
     w->cand = c.take<uint64_t>(pc * gp * kCandCap);
@@ -1154,6 +1190,7 @@ static cudaError_t topk_passes(const TopkPlan& pl, const TopkWs& w, const Proble
   prm.mmin = w.mmin;
   prm.hist = w.hist;
   prm.bstar = w.bstar;
+  prm.t_bin = w.tbin;
   prm.cand_cnt = w.cand_cnt;
   prm.cand = w.cand;
   prm.above = w.above;
@@ -1175,7 +1212,7 @@ static cudaError_t topk_passes(const TopkPlan& pl, const TopkWs& w, const Proble
   if (cudaMemsetAsync(w.hist, 0, rows * pl.hist_bins * 4, st) != cudaSuccess) return cudaErrorUnknown;
   if (select_pass<kHist>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
   k_bracket<<<dim3(pl.n_gt, n), 128, 0, st>>>(w.hist, pl.hist_bins, pl.g_pad, pl.geo.n_groups, w.bstar,
-                                               w.nabove, tab);
+                                               w.nabove, w.mmin, w.mmax, w.tbin, tab);
   if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
   if (cudaMemsetAsync(w.cand_cnt, 0, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
   if (select_pass<kCollect>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
