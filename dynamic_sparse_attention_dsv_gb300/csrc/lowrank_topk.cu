@@ -38,7 +38,6 @@ namespace dsv {
 constexpr int kSelThreads = 320;   // warps 0-7 consume scores, 8 loads tiles, 9 issues MMAs
 constexpr int kCandCap = 4096;     // candidates kept per group row
 constexpr int kMaxChunks = 64;     // key chunks per row
-constexpr int kTargetCtas = 304;   // 2 x 152 SMs
 // Problems per launch: as many as keep the projected keys within this budget.
 // Fewer, larger launches beat keeping the projections L2-resident: the score
 // passes are bound by their consumers, and every extra launch of the pass
@@ -1014,13 +1013,30 @@ static TopkPlan make_plan(const dsv_shape& s, int32_t r, const dsv_group& g) {
   return p;
 }
 
+// Key chunks per row. A launch has n_gt * n_local * n_chunks blocks, each
+// scoring chunk_tiles key tiles; the count minimises the launch's waves on the
+// 152 SMs (one block per SM, as in the passes with the large histograms) times
+// the tiles per block plus a start-up of about two tiles, so the last wave is
+// not left mostly empty.
 static void chunking(const TopkPlan& pl, int n_local, int* n_chunks, int* chunk_tiles, int max_tiles = 1 << 30) {
-  int nc = (kTargetCtas + pl.n_gt * n_local - 1) / (pl.n_gt * n_local);
-  nc = std::max(nc, (pl.n_tiles + max_tiles - 1) / max_tiles);
-  nc = std::max(1, std::min(nc, std::min(kMaxChunks, pl.n_tiles)));
-  const int ct = (pl.n_tiles + nc - 1) / nc;
-  *chunk_tiles = ct;
-  *n_chunks = (pl.n_tiles + ct - 1) / ct;
+  constexpr long kSms = 152, kStartTiles = 2;
+  const long base = (long)pl.n_gt * n_local;
+  const int lo = std::max(1, (pl.n_tiles + max_tiles - 1) / max_tiles);
+  const int hi = std::max(lo, std::min(kMaxChunks, pl.n_tiles));
+  long best = -1;
+  int best_ct = pl.n_tiles;
+  for (int nc = lo; nc <= hi; ++nc) {
+    const int ct = (pl.n_tiles + nc - 1) / nc;
+    if (ct > max_tiles) continue;
+    const long used = (pl.n_tiles + ct - 1) / ct;
+    const long cost = ((base * used + kSms - 1) / kSms) * (ct + kStartTiles);
+    if (best < 0 || cost < best) {
+      best = cost;
+      best_ct = ct;
+    }
+  }
+  *chunk_tiles = best_ct;
+  *n_chunks = (pl.n_tiles + best_ct - 1) / best_ct;
 }
 
 // Largest chunk count over the launches of P problems (full launches of pc
