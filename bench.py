@@ -161,14 +161,6 @@ class Step:
                                                    idx_offset=self.offs, idx=self.idx, workspace=self.ws,
                                                    status=self.status)
 
-    def coverage(self):
-        self.k_cov, _ = dsv.coverage(self.Q, self.K, self.Wq, self.Wk, self.grid, self.group, workspace=self.ws,
-                                     status=self.status)
-
-    def topk(self):
-        dsv.lowrank_topk(self.Q, self.K, self.Wq, self.Wk, self.grid, self.group, self.ks, idx_offset=self.offs,
-                         idx=self.idx, workspace=self.ws, status=self.status)
-
     def fwd(self):
         dsv.sparse_attn_fwd(self.Q, self.K, self.V, self.idx, self.ks, self.offs, self.grid, self.group, O=self.O,
                             LSE=self.LSE, status=self.status)
