@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
   uint64_t* dq_done = bars + 14;
   uint64_t* sdp_free = bars + 15;    // S, dP of the current tile read out of TMEM
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* pv_free = bars + 17;     // P of the previous tile read by its dV MMAs (dS may still be in use)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int u = blockIdx.y;
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     mbar_init(sdp_full, 1);
     mbar_init(ps_full, 4);
     mbar_init(p_free, 1);
+    mbar_init(pv_free, 1);
     mbar_init(part_full, 1);
     mbar_init(part_free, 4);
     mbar_init(dq_done, 1);
@@ -308,9 +310,13 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         }
         mma_commit(k_empty + ks);
         if (partials) {
-          for (int jb = 0; jb < C::kJobs; ++jb)
+          for (int jb = 0; jb < C::kJobs; ++jb) {
             if (!issue_job(jb)) { ok = false; break; }
+            if (jb == 0) mma_commit(pv_free);   // P(t) read: the dV MMAs are the first job
+          }
           if (!ok) break;
+        } else {
+          mma_commit(pv_free);
         }
         mma_commit(p_free);
       }
@@ -407,13 +413,16 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
           dw[j >> 1] = pack_bf16x2(p0 * fmaf(__uint_as_float(da[c - 2][e]), dsc, ndd),
                                    p1 * fmaf(__uint_as_float(da[c - 2][e + 1]), dsc, ndd));
         }
-      // P/dS of the previous tile must no longer be read by the tensor cores
+      // P of the previous tile is free once its dV MMAs completed, dS once its
+      // dK MMAs did: P goes out while the tensor cores may still read dS
+      if (t >= 1) ok = ok && mbar_wait_warp(pv_free, (t - 1) & 1, kWaitLimitNs);
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        st_sw128_chunk(sP, row, q, make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]));
       if (t >= 1) ok = ok && mbar_wait_warp(p_free, (t - 1) & 1, kWaitLimitNs);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        st_sw128_chunk(sP, row, q, make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]));
+      for (int q = 0; q < 16; ++q)
         st_sw128_chunk(sDS, row, q, make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]));
-      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(ps_full);
