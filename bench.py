@@ -244,6 +244,20 @@ def cpu_baseline(w, inp, budget_s: float = 12.0, max_groups: int = 1 << 30):
 
 
 # ------------------------------------------------------------------- main
+def max_over_ranks(ms: float, tdist, device) -> float:
+    """The slowest rank's time per step (every rank runs its own replica)."""
+    if not tdist:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
+    """Whole-job throughput: every rank's step work over the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def dist_setup(n):
     if int(os.environ.get("WORLD_SIZE", "1")) > 1:
         import torch.distributed as tdist
@@ -315,14 +329,10 @@ def main():
         for j, n in enumerate(names):
             per_phase[n].append(ev[i][j].elapsed_time(ev[i][j + 1]))
         total_ms += ev[i][0].elapsed_time(ev[i][-1])
-    ms = total_ms / args.steps
-    if tdist:
-        t = torch.tensor([ms], device=device)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(total_ms / args.steps, tdist, device)
     ph = {n: statistics.mean(v) for n, v in per_phase.items()}
     flops = attn_flops(w, step.ks)
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_tflops(world, flops, ms)
     fb_ms = ph["attn_fwd"] + ph["attn_bwd"]
     scores = w.H * w.n_groups * w.S
     fwd_flops = 4.0 * w.S * w.d * sum(step.ks)
