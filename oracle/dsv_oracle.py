@@ -19,7 +19,7 @@ DiT Training", gist.science summaries of arXiv 2502.07590):
 * sparse attention (section 2.1): full softmax attention over the selected
   keys only; the dense case is the same computation over all keys.
 
-Readings taken where the pages are silent (all listed in the design doc):
+Readings taken where the pages are silent:
 * group score of key j = mean over the group's queries of q_lr . k_lr (a
   design choice: the pages do not fix the aggregation);
 * top-k ties go to the lower key index; each index row is returned ascending;
