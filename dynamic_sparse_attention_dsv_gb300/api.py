@@ -226,6 +226,23 @@ def sparse_attn_bwd_workspace_size(x, grid, group, k_per_head=None, idx_offset=N
     return int(N.load().dsv_sparse_attn_bwd_workspace_size(make_shape(x, grid), make_group(group), kp, op))
 
 
+def attn_mass(LSE_sel, LSE_all, per_query: bool = False):
+    """dsv_attn_mass: the share of each query's true attention mass that its
+    selected keys carry, from the forward's LSE on the index sets and dense.
+    Returns (mean per problem, shape LSE.shape[:-1]; per-query shares or None)."""
+    if LSE_sel.dtype != torch.float32 or LSE_all.dtype != torch.float32 or LSE_sel.shape != LSE_all.shape:
+        raise TypeError("LSE_sel and LSE_all must be float32 tensors of one shape")
+    if not (LSE_sel.is_contiguous() and LSE_all.is_contiguous()):
+        raise ValueError("LSE tensors must be contiguous")
+    S = LSE_sel.shape[-1]
+    P = LSE_sel.numel() // S
+    mass = torch.empty(LSE_sel.shape[:-1], dtype=torch.float32, device=LSE_sel.device)
+    pq = torch.empty_like(LSE_sel) if per_query else None
+    code = N.load().dsv_attn_mass(_ptr(LSE_sel), _ptr(LSE_all), int(S), int(P), _ptr(mass), _ptr(pq), _stream())
+    N.check(code, "dsv_attn_mass")
+    return mass, pq
+
+
 def sparse_attn_bwd_min_workspace_size(x, grid, group, k_per_head=None, idx_offset=None) -> int:
     kp = _i32(k_per_head) if k_per_head is not None else None
     op = _i64(idx_offset) if idx_offset is not None else None

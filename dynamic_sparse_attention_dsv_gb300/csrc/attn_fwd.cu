@@ -416,6 +416,36 @@ static cudaError_t launch_fwd(const AttnMaps& maps, const AttnParams& prm, const
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// True attention mass of the selected keys. For query i the selected keys'
+// share of its softmax over all keys is exp(LSE_sel,i - LSE_all,i), with both
+// LSEs from the forward (on the index sets, and dense). One block per problem;
+// the mean runs in fp64 in a fixed order (strided per-thread sums, then a
+// fixed tree), so every run gives the same bits.
+constexpr int kMassThreads = 256;
+
+__global__ void __launch_bounds__(kMassThreads) k_attn_mass(const float* __restrict__ lse_sel,
+                                                            const float* __restrict__ lse_all, int64_t S,
+                                                            float* mass, float* per_query) {
+  __shared__ double part[kMassThreads];
+  const int p = blockIdx.x, tid = threadIdx.x;
+  const float* a = lse_sel + (int64_t)p * S;
+  const float* b = lse_all + (int64_t)p * S;
+  double acc = 0.0;
+  for (int64_t i = tid; i < S; i += kMassThreads) {
+    const float m = expf(a[i] - b[i]);
+    if (per_query) per_query[(int64_t)p * S + i] = m;
+    acc += (double)m;
+  }
+  part[tid] = acc;
+  __syncthreads();
+  for (int w = kMassThreads / 2; w > 0; w >>= 1) {
+    if (tid < w) part[tid] += part[tid + w];
+    __syncthreads();
+  }
+  if (tid == 0) mass[p] = (float)(part[0] / (double)S);
+}
+
 }  // namespace dsv
 
 using namespace dsv;
@@ -469,4 +499,13 @@ extern "C" dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const vo
   const cudaError_t e = d == 128 ? launch_fwd<128>(maps, prm, tab, geo.n_groups, st)
                                  : launch_fwd<64>(maps, prm, tab, geo.n_groups, st);
   return e == cudaSuccess ? DSV_OK : DSV_ERR_CUDA;
+}
+
+extern "C" dsv_status dsv_attn_mass(const float* LSE_sel, const float* LSE_all, int64_t S, int32_t P, float* mass,
+                                    float* per_query, void* stream) {
+  if (!LSE_sel || !LSE_all || !mass || S < 1 || P < 1 || P > kMaxProblems) return DSV_ERR_INVALID_ARG;
+  if (!aligned(LSE_sel, 4) || !aligned(LSE_all, 4) || !aligned(mass, 4) || (per_query && !aligned(per_query, 4)))
+    return DSV_ERR_INVALID_ARG;
+  k_attn_mass<<<P, kMassThreads, 0, static_cast<cudaStream_t>(stream)>>>(LSE_sel, LSE_all, S, mass, per_query);
+  return cudaGetLastError() == cudaSuccess ? DSV_OK : DSV_ERR_CUDA;
 }

@@ -58,6 +58,7 @@ SIGNATURES = [
     ("dsv_sparse_attn_fwd_workspace_size", ctypes.c_size_t, [dsv_shape, dsv_group]),
     ("dsv_sparse_attn_fwd", ctypes.c_int, [_P, _P, _P, _P, _I32P, _I64P, dsv_shape, dsv_group, ctypes.c_float, _P,
                                            _P, _P, ctypes.c_size_t, _P, _P]),
+    ("dsv_attn_mass", ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
     ("dsv_sparse_attn_bwd_workspace_size", ctypes.c_size_t, [dsv_shape, dsv_group, _I32P, _I64P]),
     ("dsv_sparse_attn_bwd_min_workspace_size", ctypes.c_size_t, [dsv_shape, dsv_group, _I32P, _I64P]),
     ("dsv_sparse_attn_bwd", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32P, _I64P, dsv_shape, dsv_group,

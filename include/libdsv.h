@@ -200,6 +200,25 @@ dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const void* V, cons
                                size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * dsv_attn_mass -- share of each query's true attention mass that its
+ * group's selected keys carry.
+ * Passage: technical summary section 2.1 (critical KV are the pairs that
+ * carry over 90% of the attention score), measured on the real scores
+ * q_i.k_j instead of the predictor's.
+ *
+ * For query i: m_i = sum_{j in I_g} exp(scale q_i.k_j) / sum_{all j} exp(scale
+ * q_i.k_j) = exp(LSE_sel,i - LSE_all,i), with LSE_sel from
+ * dsv_sparse_attn_fwd on the index sets and LSE_all from the same call with
+ * idx = NULL (dense). mass[p] = mean over the problem's S queries of m_i
+ * (fp64 sum in a fixed order: the same bits on every run).
+ * LSE_sel, LSE_all: DEVICE float [P][S]; mass: DEVICE float [P]; per_query
+ * (optional, may be NULL): DEVICE float [P][S] of m_i. No workspace.
+ * P <= 256 problems, S >= 1; DSV_ERR_INVALID_ARG otherwise.
+ * ---------------------------------------------------------------------- */
+dsv_status dsv_attn_mass(const float* LSE_sel, const float* LSE_all, int64_t S, int32_t P, float* mass,
+                         float* per_query, void* stream);
+
+/* ------------------------------------------------------------------------
  * dsv_sparse_attn_bwd -- query-grouped sparse attention, backward.
  * Passage: technical summary section 2.1 (stage 2 trains with sparse
  * attention over the critical KV, so gradients flow through the selected

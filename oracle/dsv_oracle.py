@@ -198,6 +198,24 @@ def sparse_attn_fwd(Q, K, V, idx: Optional[np.ndarray], members: np.ndarray, sca
     return O, LSE
 
 
+def true_mass(Q, K, idx: np.ndarray, members: np.ndarray, scale: float) -> np.ndarray:
+    """Share of each query's true attention mass that its group's selected keys
+    carry (section 2.1: the critical KV pairs are those carrying over 90% of
+    the attention score, here measured on the real scores q_i.k_j rather than
+    the predictor's). For query i of group g: the softmax over all S keys of
+    scale q_i.k_j, summed over j in I_g. Returns [S]."""
+    Q, K = as_f64(Q), as_f64(K)
+    S = Q.shape[0]
+    out = np.full(S, np.nan)
+    for g in range(members.shape[0]):
+        mem = members[g]
+        logits = scale * (Q[mem] @ K.T)
+        e = np.exp(logits - logits.max(axis=1, keepdims=True))
+        P = e / e.sum(axis=1, keepdims=True)
+        out[mem] = P[:, idx[g]].sum(axis=1)
+    return out
+
+
 def sparse_attn_bwd(Q, K, V, dO, idx: Optional[np.ndarray], members: np.ndarray, scale: float):
     """Gradients of sum(dO * O) for one head of sparse attention, with the
     index sets held constant. Per group g and selected key j:

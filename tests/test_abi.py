@@ -156,6 +156,14 @@ def test_coverage_topk_workspace_and_validation(lib):
                                  None, 0, ks, offs, fake, fake, 1 << 40, None, None) == 2
 
 
+def test_attn_mass_validation(lib):
+    fake = ctypes.c_void_p(256)
+    assert lib.dsv_attn_mass(None, fake, 1024, 2, fake, None, None) == 1
+    assert lib.dsv_attn_mass(fake, fake, 0, 2, fake, None, None) == 1
+    assert lib.dsv_attn_mass(fake, fake, 1024, 257, fake, None, None) == 1
+    assert lib.dsv_attn_mass(ctypes.c_void_p(258), fake, 1024, 2, fake, None, None) == 1
+
+
 def test_topk_layout_packs_rows():
     ks, offs, total = api.topk_layout(3, 16, [5, 7, 9], skip=[False, True, False])
     assert offs == [0, -1, 80] and total == 80 + 16 * 9

@@ -164,6 +164,23 @@ def test_small_backward_workspace_changes_no_bit(case):
             assert torch.equal(a, b)
 
 
+def test_true_attention_mass_matches_oracle(case):
+    """Share of each query's true softmax mass carried by its group's selected
+    keys, from the forward's sparse and dense LSE, against the oracle's direct
+    sum of the fp64 softmax over all keys."""
+    w, d = case["w"], case["dev"]
+    idx, ks, offs = _idx_tensor(case)
+    _, Ls = dsv.sparse_attn_fwd(d["Q"], d["K"], d["V"], idx, ks, offs, _grid(w), _group(w))
+    _, La = dsv.sparse_attn_fwd(d["Q"], d["K"], d["V"], None, None, None, _grid(w), _group(w))
+    mass, per_q = dsv.attn_mass(Ls, La, per_query=True)
+    for h in range(w.H):
+        ref = ora.true_mass(case["inp"]["Q"][h], case["inp"]["K"][h], case["ref"][h]["idx"], case["mem"],
+                            case["scale"])
+        got = per_q[h].cpu().numpy()
+        assert np.abs(got - ref).max() <= 3e-2, h
+        assert abs(float(mass[h]) - ref.mean()) <= 1e-2, h
+
+
 def test_dense_fwd_bwd_matches_oracle(case):
     w, d = case["w"], case["dev"]
     st = dsv.new_status()

@@ -316,3 +316,35 @@ def test_backward_dense_equals_all_keys():
     b = ora.sparse_attn_bwd(Q, K, V, dO, all_idx, mem, 0.3)
     for x, y in zip(a, b):
         np.testing.assert_allclose(x, y, atol=1e-13)
+
+
+# ------------------------------------------------------- true attention mass
+def test_true_mass_all_keys_is_one_and_uniform_scores_give_k_over_S():
+    """Selecting every key captures all of each query's mass; with Q = 0 every
+    key has the same probability 1/S, so k selected keys carry exactly k/S."""
+    rng = np.random.default_rng(7)
+    T, Y, X, d = 2, 4, 8, 16
+    S = T * Y * X
+    mem = ora.group_members(T, Y, X, 2, 2, 2)
+    K = rng.standard_normal((S, d))
+    Q = rng.standard_normal((S, d))
+    everything = np.tile(np.arange(S), (mem.shape[0], 1))
+    np.testing.assert_allclose(ora.true_mass(Q, K, everything, mem, 0.25), 1.0, rtol=0, atol=1e-12)
+    k = 11
+    some = np.stack([np.sort(rng.choice(S, k, replace=False)) for _ in range(mem.shape[0])])
+    np.testing.assert_allclose(ora.true_mass(np.zeros_like(Q), K, some, mem, 0.25), k / S, rtol=0, atol=1e-12)
+
+
+def test_true_mass_single_dominant_key():
+    """A key whose logit exceeds every other by L carries 1 / (1 + (S-1) e^-L)
+    of the mass when the others are equal."""
+    T, Y, X, d = 1, 2, 4, 8
+    S = T * Y * X
+    mem = ora.group_members(T, Y, X, 1, 2, 2)
+    K = np.zeros((S, d))
+    K[3, 0] = 5.0
+    Q = np.zeros((S, d))
+    Q[:, 0] = 1.0
+    idx = np.tile(np.array([3]), (mem.shape[0], 1))
+    want = 1.0 / (1.0 + (S - 1) * np.exp(-5.0))
+    np.testing.assert_allclose(ora.true_mass(Q, K, idx, mem, 1.0), want, rtol=1e-12)
