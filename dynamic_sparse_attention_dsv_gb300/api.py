@@ -201,6 +201,17 @@ def plan_heads(k_cov: Sequence[int], S: int, n_groups: int, lo_frac: float = 0.0
     return list(k_h), [bool(v) for v in dense], list(offs), int(total.value)
 
 
+def plan_gpus(cost: Sequence[int], n_gpus: int, equal_counts: bool = True):
+    """dsv_plan_gpus (host only): heads to GPUs by cost, longest first.
+    Returns (gpu_of list, load per GPU list)."""
+    n = len(cost)
+    gpu_of = (ctypes.c_int32 * n)()
+    load = (ctypes.c_int64 * n_gpus)()
+    code = N.load().dsv_plan_gpus(_i64(cost), n, int(n_gpus), 1 if equal_counts else 0, gpu_of, load)
+    N.check(code, "dsv_plan_gpus")
+    return list(gpu_of), list(load)
+
+
 def sparse_attn_fwd(Q, K, V, idx, k_per_head, idx_offset, grid, group, scale: Optional[float] = None, O=None,
                     LSE=None, status=None):
     """dsv_sparse_attn_fwd. idx=None runs every problem dense. Returns (O, LSE)."""

@@ -1,7 +1,9 @@
 // Host-side pieces shared by every libdsv entry point: status strings,
 // validation, the tensor-map encoder and the head dispatcher.
+#include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -102,5 +104,30 @@ extern "C" dsv_status dsv_plan_heads(const int32_t* k_cov, int32_t n, int64_t S,
     }
   }
   *idx_total = total;
+  return DSV_OK;
+}
+
+// Head-wise context-parallel re-balancing: longest processing time first.
+extern "C" dsv_status dsv_plan_gpus(const int64_t* cost, int32_t n, int32_t n_gpus, int32_t equal_counts,
+                                    int32_t* gpu_of, int64_t* load) {
+  if (!cost || !gpu_of || n < 1 || n_gpus < 1) return DSV_ERR_INVALID_ARG;
+  for (int32_t p = 0; p < n; ++p)
+    if (cost[p] < 0) return DSV_ERR_INVALID_ARG;
+  const int32_t cap = equal_counts ? (n + n_gpus - 1) / n_gpus : n;
+  std::vector<int32_t> order(n);
+  for (int32_t p = 0; p < n; ++p) order[p] = p;
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
+  std::vector<int64_t> ld(n_gpus, 0);
+  std::vector<int32_t> cnt(n_gpus, 0);
+  for (const int32_t p : order) {
+    int32_t best = -1;
+    for (int32_t g = 0; g < n_gpus; ++g)
+      if (cnt[g] < cap && (best < 0 || ld[g] < ld[best])) best = g;
+    gpu_of[p] = best;
+    ld[best] += cost[p];
+    ++cnt[best];
+  }
+  if (load)
+    for (int32_t g = 0; g < n_gpus; ++g) load[g] = ld[g];
   return DSV_OK;
 }

@@ -55,6 +55,7 @@ SIGNATURES = [
                                          ctypes.c_size_t, _P, _P]),
     ("dsv_plan_heads", ctypes.c_int, [_I32P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
                                       ctypes.c_double, ctypes.c_double, _I32P, _U8P, _I64P, _I64P]),
+    ("dsv_plan_gpus", ctypes.c_int, [_I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _I32P, _I64P]),
     ("dsv_sparse_attn_fwd_workspace_size", ctypes.c_size_t, [dsv_shape, dsv_group]),
     ("dsv_sparse_attn_fwd", ctypes.c_int, [_P, _P, _P, _P, _I32P, _I64P, dsv_shape, dsv_group, ctypes.c_float, _P,
                                            _P, _P, ctypes.c_size_t, _P, _P]),

@@ -182,6 +182,28 @@ dsv_status dsv_plan_heads(const int32_t* k_cov, int32_t n, int64_t S, int64_t n_
                           int64_t* idx_total);
 
 /* ------------------------------------------------------------------------
+ * dsv_plan_gpus -- sparse head-wise context parallelism: heads to GPUs by
+ * their cost (host only, no GPU).
+ * Passage: technical summary section 2.3 (head-wise CP re-balancing: each
+ * head's assignment to a GPU follows its sparsity so that the compute load
+ * balances across GPUs).
+ *
+ * cost[p] >= 0 is head p's work (its k_h for a sparse head, S for a dense
+ * one: attention work is proportional to S k_h d). Longest processing time
+ * first: heads in order of decreasing cost (ties: lower head first), each to
+ * the GPU with the least load so far (ties: lower GPU); with equal_counts != 0
+ * only GPUs holding fewer than ceil(n / n_gpus) heads take one (an equal split
+ * of the heads, as head-wise parallelism lays them out). gpu_of[p] receives
+ * the GPU of head p; load (optional, may be NULL) the total cost per GPU.
+ * The largest load is within 4/3 of the best possible when equal_counts = 0.
+ * All pointers are HOST memory: cost [n], gpu_of [n], load [n_gpus].
+ * DSV_ERR_INVALID_ARG for n < 1, n_gpus < 1, a NULL cost/gpu_of or a
+ * negative cost.
+ * ---------------------------------------------------------------------- */
+dsv_status dsv_plan_gpus(const int64_t* cost, int32_t n, int32_t n_gpus, int32_t equal_counts, int32_t* gpu_of,
+                         int64_t* load);
+
+/* ------------------------------------------------------------------------
  * dsv_sparse_attn_fwd -- query-grouped sparse attention, forward.
  * Passage: technical summary section 2.1 (full attention computed on the
  * critical KV pairs only) and section 2.2 (query grouping: a group of

@@ -38,6 +38,7 @@ against closed forms, brute force or library routines; none is unpinned.
 """
 from __future__ import annotations
 
+import itertools
 import math
 from typing import Optional, Sequence
 
@@ -161,6 +162,44 @@ def plan_heads(k_cov: Sequence[int], S: int, lo_frac: float = 0.01, hi_frac: flo
             ks.append(min(max(int(kc), lo), hi))
             dense.append(False)
     return ks, dense
+
+
+def plan_gpus(cost: Sequence[int], n_gpus: int, equal_counts: bool = True):
+    """Head-wise context-parallel re-balancing (section 2.3: each head's
+    assignment to a GPU follows its sparsity so that the compute balances).
+
+    Longest processing time first: heads in order of decreasing cost (ties:
+    lower head first), each to the GPU with the least load so far (ties: lower
+    GPU); with ``equal_counts`` only GPUs holding fewer than ceil(n / n_gpus)
+    heads take one. Returns (gpu_of list, load list).
+    """
+    n = len(cost)
+    cap = -(-n // n_gpus) if equal_counts else n
+    order = sorted(range(n), key=lambda p: (-int(cost[p]), p))
+    load, count, gpu_of = [0] * n_gpus, [0] * n_gpus, [0] * n
+    for p in order:
+        g = min((q for q in range(n_gpus) if count[q] < cap), key=lambda q: (load[q], q))
+        gpu_of[p] = g
+        load[g] += int(cost[p])
+        count[g] += 1
+    return gpu_of, load
+
+
+def best_makespan(cost: Sequence[int], n_gpus: int, equal_counts: bool = True) -> int:
+    """Smallest possible largest per-GPU load, by trying every assignment
+    (tiny inputs only)."""
+    n = len(cost)
+    cap = -(-n // n_gpus) if equal_counts else n
+    best = None
+    for assign in itertools.product(range(n_gpus), repeat=n):
+        if max(assign.count(g) for g in range(n_gpus)) > cap:
+            continue
+        loads = [0] * n_gpus
+        for p, g in enumerate(assign):
+            loads[g] += int(cost[p])
+        m = max(loads)
+        best = m if best is None else min(best, m)
+    return best
 
 
 # ------------------------------------------------------ sparse attention

@@ -164,6 +164,21 @@ def test_attn_mass_validation(lib):
     assert lib.dsv_attn_mass(ctypes.c_void_p(258), fake, 1024, 2, fake, None, None) == 1
 
 
+def test_plan_gpus_matches_oracle(lib):
+    rng = np.random.default_rng(5)
+    for _ in range(50):
+        n, N = int(rng.integers(1, 40)), int(rng.integers(1, 9))
+        cost = [int(c) for c in rng.integers(0, 1 << 20, n)]
+        for eq in (False, True):
+            assert api.plan_gpus(cost, N, eq) == ora.plan_gpus(cost, N, eq)
+    # ties: equal costs keep head order, lower GPUs first
+    assert api.plan_gpus([7, 7, 7], 2, False) == ora.plan_gpus([7, 7, 7], 2, False)
+    gpu_of = (ctypes.c_int32 * 2)()
+    assert lib.dsv_plan_gpus((ctypes.c_int64 * 2)(1, -1), 2, 2, 1, gpu_of, None) == 1
+    assert lib.dsv_plan_gpus((ctypes.c_int64 * 2)(1, 1), 2, 0, 1, gpu_of, None) == 1
+    assert lib.dsv_plan_gpus(None, 2, 2, 1, gpu_of, None) == 1
+
+
 def test_topk_layout_packs_rows():
     ks, offs, total = api.topk_layout(3, 16, [5, 7, 9], skip=[False, True, False])
     assert offs == [0, -1, 80] and total == 80 + 16 * 9

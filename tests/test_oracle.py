@@ -348,3 +348,39 @@ def test_true_mass_single_dominant_key():
     idx = np.tile(np.array([3]), (mem.shape[0], 1))
     want = 1.0 / (1.0 + (S - 1) * np.exp(-5.0))
     np.testing.assert_allclose(ora.true_mass(Q, K, idx, mem, 1.0), want, rtol=1e-12)
+
+
+# ------------------------------------------------- head-wise CP re-balancing
+def test_plan_gpus_hand_example():
+    """Costs 9, 8, 7, 5, 3, 1 on 3 GPUs: 9 -> 0, 8 -> 1, 7 -> 2, 5 -> 2 (7 is
+    least), 3 -> 1 (8 < 9 < 12), 1 -> 0 (9 < 11 < 12); loads 10, 11, 12."""
+    gpu_of, load = ora.plan_gpus([5, 9, 3, 7, 1, 8], 3)
+    assert gpu_of == [2, 0, 1, 2, 0, 1] and load == [10, 11, 12]
+
+
+def test_plan_gpus_within_graham_bound_of_brute_force():
+    """Longest-processing-time first is within (4/3 - 1/(3N)) of the best
+    makespan (Graham 1969); with equal head counts the result is still a valid
+    split and never better than the constrained optimum."""
+    rng = np.random.default_rng(11)
+    for _ in range(60):
+        n, N = int(rng.integers(1, 8)), int(rng.integers(1, 4))
+        cost = [int(c) for c in rng.integers(0, 50, n)]
+        for eq in (False, True):
+            gpu_of, load = ora.plan_gpus(cost, N, eq)
+            assert len(gpu_of) == n and all(0 <= g < N for g in gpu_of)
+            assert [sum(c for c, g in zip(cost, gpu_of) if g == q) for q in range(N)] == load
+            if eq:
+                assert max(gpu_of.count(q) for q in range(N)) <= -(-n // N)
+            best = ora.best_makespan(cost, N, eq)
+            assert max(load) >= best
+            if not eq:
+                assert max(load) <= (4 / 3 - 1 / (3 * N)) * best + 1e-9
+
+
+def test_plan_gpus_special_cases():
+    # equal costs spread evenly; fewer heads than GPUs: one head each
+    gpu_of, load = ora.plan_gpus([4] * 8, 4)
+    assert load == [8, 8, 8, 8] and sorted(gpu_of) == [0, 0, 1, 1, 2, 2, 3, 3]
+    gpu_of, load = ora.plan_gpus([3, 1], 4)
+    assert gpu_of == [0, 1] and load == [3, 1, 0, 0]
