@@ -10,7 +10,11 @@ forward and backward. Inputs are seeded synthetic bf16 tensors
 Prints ONE JSON line. `value` is the effective attention TFLOP/s of the whole
 step (algorithmic fwd+bwd FLOPs 14*H*S*k*d over the step time). Breakdown keys
 give each phase's time, the selection's Gscore/s (scored (group, key) pairs
-per second, coverage and top-k together) and the attention TFLOP/s.
+per second, coverage and top-k together) and the attention TFLOP/s, and two
+further workloads timed on their own: the low-rank top-k sweep at S=128K
+(H=24, r in {16,32,64} x k in {1,5,10,20}% of S, with each point's fraction
+of the HBM and tf32 rooflines) and the dispatcher-driven layer at S=256K
+(H=16: coverage, per-head plan, top-k, forward, backward).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -44,7 +48,15 @@ METRIC = "sparse attn fwd+bwd ms & TFLOP/s at S=64K; lowrank top-k Gscore/s; % r
 CFG = 2
 
 
+#: dense tf32 / bf16 tensor throughput (nominal 1.1 vs 2.25 PFLOP/s per GPU)
+TF32_OF_BF16 = 1.1 / 2.25
+
+
 def peaks():
+    """Roofline denominators. Tensor-bound phases take the burst bf16 peak:
+    the timed region is well under a second and runs at the full SM clock
+    (the sustained figure was taken over seconds under the power cap, at a
+    lower clock)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
@@ -52,6 +64,140 @@ def peaks():
         return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p.get("bf16_tflops_sustained"),
                     source="measured")
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def time_call(fn, reps: int, warmup: int = 1) -> float:
+    """Median CUDA-event time (ms) of fn() on the current stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in evs:
+        a.record(s)
+        fn()
+        b.record(s)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def topk_sweep(device, pk, reps: int = 3):
+    """The low-rank top-k sweep (H=24, 32x64x64 so S=131072, d=128, cube
+    2x8x8; r in {16, 32, 64} x k in {1, 5, 10, 20}% of S), each point timed
+    alone, and each rank's per-head coverage k. Per point: ms, Gscore/s, the
+    fraction of HBM (algorithmic bytes H (4 S d + 4 n_g k): read Q and K in
+    bf16, write the index rows) and of the tf32 tensor peak (the score
+    products of the passes actually run: three passes, three tf32 products
+    each, r padded to 32), and which of the two binds."""
+    w = syn.workload(3)
+    grid, group = (w.T, w.Y, w.X), (w.gt, w.gy, w.gx)
+    inp = syn.make_inputs_device(w, device, with_grad_out=False)
+    Q, K = inp["Q"], inp["K"]
+    tf32 = pk["bf16"] * TF32_OF_BF16
+    scores = w.H * w.n_groups * w.S
+    points, cov = [], {}
+    st = dsv.new_status(device)
+    for r in syn.TOPK_SWEEP_RANKS:
+        gen = torch.Generator(device=device)
+        gen.manual_seed(20250300 + r)
+        Wq = (torch.randn((w.H, w.d, r), device=device, generator=gen) / math.sqrt(w.d)).to(torch.bfloat16)
+        Wk = (torch.randn((w.H, w.d, r), device=device, generator=gen) / math.sqrt(w.d)).to(torch.bfloat16)
+        ws = torch.empty(max(api.lowrank_topk_workspace_size(Q, grid, group, r),
+                             api.coverage_workspace_size(Q, grid, group, r)), dtype=torch.uint8, device=device)
+        k_cov = None
+
+        def run_cov():
+            nonlocal k_cov
+            k_cov, _ = dsv.coverage(Q, K, Wq, Wk, grid, group, workspace=ws, status=st)
+
+        cov_ms = time_call(run_cov, reps)
+        cov[f"r{r}"] = {"ms": round(cov_ms, 3), "k_cov_per_head": k_cov.cpu().tolist()}
+        rp = 32 if r <= 32 else 64
+        for frac in syn.TOPK_SWEEP_FRACTIONS:
+            k = syn.k_of_fraction(frac, w.S)
+            idx = torch.empty(w.H * w.n_groups * k, dtype=torch.int32, device=device)
+            ms = time_call(lambda: dsv.lowrank_topk(Q, K, Wq, Wk, grid, group, k, idx=idx, workspace=ws,
+                                                    status=st), reps)
+            hbm_bytes = w.H * (4.0 * w.S * w.d + 4.0 * w.n_groups * k)
+            hbm_frac = hbm_bytes / (ms * 1e-3) / 1e9 / pk["hbm"]
+            tc_frac = 3 * 3 * 2.0 * rp * scores / (ms * 1e-3) / 1e12 / tf32
+            points.append({"r": r, "k": k, "k_pct": round(100 * frac), "ms": round(ms, 3),
+                           "gscore_s": round(scores / (ms * 1e-3) / 1e9, 1),
+                           "hbm_gbs": round(hbm_bytes / (ms * 1e-3) / 1e9, 1), "hbm_frac": round(hbm_frac, 4),
+                           "tf32_frac": round(tc_frac, 4), "bound": "hbm" if hbm_frac >= tc_frac else "tensor"})
+            del idx
+        del ws
+    code = dsv.read_status(st)
+    if code:
+        raise SystemExit(f"device status {dsv.native.DSV_STATUS.get(code, code)} in the top-k sweep")
+    return {"workload": "H=24, 32x64x64 (S=131072), d=128, cube 2x8x8, r in {16,32,64}, k in {1,5,10,20}% of S",
+            "inputs": "drawn on the device (same recipe, torch generator)",
+            "peaks": {"hbm_gbs": pk["hbm"], "tf32_tflops": round(tf32, 1),
+                      "tf32_source": "measured bf16 burst x 1.1/2.25 (nominal tf32/bf16)"},
+            "points": points, "coverage": cov}
+
+
+def dispatcher_layer(device, pk):
+    """The dispatcher-driven layer (H=16, 64x64x64 so S=262144, d=128, r=32,
+    cube 2x8x8, Q scale U[1, 8] per head): coverage -> per-head plan on the
+    host (k clamped to [1%, 25%] of S, dense above 50%) -> top-k of the
+    sparse heads -> forward -> backward. One warm-up, then one timed layer;
+    each phase timed with CUDA events (the plan needs k_cov on the host)."""
+    w = syn.workload(4)
+    grid, group = (w.T, w.Y, w.X), (w.gt, w.gy, w.gx)
+    inp = syn.make_inputs_device(w, device)
+    Q, K, V, dO, Wq, Wk = (inp[n] for n in ("Q", "K", "V", "dO", "Wq", "Wk"))
+    st = dsv.new_status(device)
+    cws = torch.empty(api.coverage_workspace_size(Q, grid, group, w.r), dtype=torch.uint8, device=device)
+    tws = torch.empty(api.lowrank_topk_workspace_size(Q, grid, group, w.r), dtype=torch.uint8, device=device)
+    O, LSE = torch.empty_like(Q), torch.empty(Q.shape[:-1], dtype=torch.float32, device=device)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    state = {}
+
+    def layer():
+        s = torch.cuda.current_stream()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev[0].record(s)
+        k_cov, _ = dsv.coverage(Q, K, Wq, Wk, grid, group, workspace=cws, status=st)
+        ev[1].record(s)
+        kc = k_cov.cpu().tolist()
+        k_h, dense, offs, total = dsv.plan_heads(kc, w.S, w.n_groups)
+        if state.get("plan") != (k_h, offs):
+            state["plan"] = (k_h, offs)
+            state["idx"] = torch.empty(max(total, 1), dtype=torch.int32, device=device)
+            state["bws"] = torch.empty(api.sparse_attn_bwd_workspace_size(Q, grid, group, k_h, offs),
+                                       dtype=torch.uint8, device=device)
+        idx = state["idx"]
+        ev[2].record(s)
+        if total:
+            dsv.lowrank_topk(Q, K, Wq, Wk, grid, group, k_h, idx_offset=offs, idx=idx, workspace=tws, status=st)
+        ev[3].record(s)
+        dsv.sparse_attn_fwd(Q, K, V, idx, k_h, offs, grid, group, O=O, LSE=LSE, status=st)
+        ev[4].record(s)
+        t_bwd_end = torch.cuda.Event(enable_timing=True)
+        dsv.sparse_attn_bwd(Q, K, V, O, LSE, dO, idx, k_h, offs, grid, group, dQ=dQ, dK=dK, dV=dV,
+                            workspace=state["bws"], status=st)
+        t_bwd_end.record(s)
+        torch.cuda.synchronize()
+        return dict(kc=kc, k_h=k_h, dense=dense, cov=ev[0].elapsed_time(ev[1]), topk=ev[2].elapsed_time(ev[3]),
+                    fwd=ev[3].elapsed_time(ev[4]), bwd=ev[4].elapsed_time(t_bwd_end),
+                    total=ev[0].elapsed_time(t_bwd_end))
+
+    layer()
+    r = layer()
+    code = dsv.read_status(st)
+    if code:
+        raise SystemExit(f"device status {dsv.native.DSV_STATUS.get(code, code)} in the dispatcher layer")
+    ks = [w.S if dn else kh for kh, dn in zip(r["k_h"], r["dense"])]
+    flops = 14.0 * w.S * w.d * sum(ks)
+    fb = r["fwd"] + r["bwd"]
+    return {"workload": "H=16, 64x64x64 (S=262144), d=128, r=32, cube 2x8x8, per-head k from coverage",
+            "inputs": "drawn on the device (same recipe, torch generator)",
+            "plan": [{"head": h, "k_cov": r["kc"][h], "k": ks[h], "dense": r["dense"][h]} for h in range(w.H)],
+            "coverage_ms": round(r["cov"], 3), "topk_ms": round(r["topk"], 3), "attn_fwd_ms": round(r["fwd"], 3),
+            "attn_bwd_ms": round(r["bwd"], 3), "layer_ms": round(r["total"], 3),
+            "attn_fwd_bwd_tflops": round(flops / (fb * 1e-3) / 1e12, 2),
+            "attn_fwd_bwd_frac_of_bf16_peak": round(flops / (fb * 1e-3) / 1e12 / pk["bf16"], 4)}
 
 
 def workload_dict(w):
@@ -277,6 +423,8 @@ def main():
     ap.add_argument("--impl", default="dsv", choices=["dsv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the 128K low-rank top-k sweep")
+    ap.add_argument("--no-layer", action="store_true", help="skip the 256K dispatcher-driven layer")
     ap.add_argument("--heads", type=int, default=0,
                     help="profiling aid: run the workload with only this many heads (default: all)")
     args = ap.parse_args()
@@ -355,7 +503,7 @@ def main():
     if dom in dram_per_head and (w.S, w.d, w.k, w.gt, w.gy, w.gx) == (65536, 128, 6554, 2, 8, 8):
         traffic = int(dram_per_head[dom] * w.H)
     achieved = amount / (ph[dom] * 1e-3)
-    peak = (pk["bf16_sus"] or pk["bf16"]) if bound == "tensor" else pk["hbm"]
+    peak = pk["bf16"] if bound == "tensor" else pk["hbm"]
 
     # end to end through the public API with host buffers
     e2e = None
@@ -374,18 +522,23 @@ def main():
             "attn_fwd_bwd_ms": round(fb_ms, 3),
             "attn_fwd_bwd_tflops": round(flops / (fb_ms * 1e-3) / 1e12, 2),
             "attn_fwd_tflops": round(fwd_flops / (ph["attn_fwd"] * 1e-3) / 1e12, 2),
-            "attn_fwd_bwd_frac_of_bf16_peak": round(flops / (fb_ms * 1e-3) / 1e12 / (pk["bf16_sus"] or pk["bf16"]), 4),
+            "attn_fwd_bwd_frac_of_bf16_peak": round(flops / (fb_ms * 1e-3) / 1e12 / pk["bf16"], 4),
             "select_hbm_gbs": round(sel_bytes / (ph["select"] * 1e-3) / 1e9, 1),
             "wall_s": round(wall, 3),
         },
         "roofline": {"kernel": kname, "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": pk["source"] + (" bf16 sustained" if bound == "tensor" else " HBM copy")},
+                     "peak_source": pk["source"] + (" bf16 burst (cuBLAS 8192^3, full clock)" if bound == "tensor"
+                                                    else " HBM copy")},
         "gpu_launches": launches * args.steps if launches >= 0 else None,
         "clocks": clk,
     }
     if e2e:
         line["e2e"] = e2e
+    if rank == 0 and not args.no_sweep and args.heads <= 0:
+        line["breakdown"]["cfg3_topk_sweep"] = topk_sweep(device, pk)
+    if rank == 0 and not args.no_layer and args.heads <= 0:
+        line["breakdown"]["cfg4_dispatcher_layer"] = dispatcher_layer(device, pk)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp)[0]
     if rank == 0:

@@ -10,7 +10,7 @@
 // One CTA per (query group, problem). The group's G (64 or 128) queries form
 // the M = 128 rows of every MMA (G = 64 leaves rows 64..127 zero). Per
 // 128-key tile:
-//   TMA row gather of the selected K and V rows into swizzled shared memory
+//   cp.async row gather of the selected K and V rows into swizzled shared memory
 //   S  = Q K^T        tcgen05.mma kind::f16, A = Q in TMEM (copied there once
 //                     per CTA), B = K (smem) -> TMEM
 //   P  = exp2(S*scale*log2e - m) in registers, written back to TMEM as bf16

@@ -64,7 +64,7 @@ extern "C" const char* dsv_status_string(dsv_status s) {
     case DSV_ERR_CUDA: return "DSV_ERR_CUDA: a CUDA launch or API call failed";
     case DSV_ERR_TIMEOUT: return "DSV_ERR_TIMEOUT: a bounded device wait ran out";
     case DSV_ERR_OVERFLOW: return "DSV_ERR_OVERFLOW: reserved";
-    case DSV_ERR_CANDIDATES: return "DSV_ERR_CANDIDATES: top-k boundary bin exceeded its candidate buffer";
+    case DSV_ERR_CANDIDATES: return "DSV_ERR_CANDIDATES: a top-k row failed its consistency check";
   }
   return "DSV_ERR_UNKNOWN";
 }

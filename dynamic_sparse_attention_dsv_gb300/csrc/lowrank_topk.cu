@@ -13,17 +13,26 @@
 // hi*hi + hi*lo + lo*hi of a tf32 hi/lo split: about 2^-21 relative error) into
 // TMEM and consumed in registers; they are never written to memory.
 //
-// Exact top-k per group row, ties to the lower key, in four streaming passes
-// over the same score tiles plus two small kernels:
+// Exact top-k per group row, ties to the lower key, in streaming passes over
+// the same score tiles plus small per-row kernels:
 //   MINMAX  per-row score range
-//   HIST    256 (128 for r=64) linear bins over the range; bracket kernel
-//           finds the bin b* holding the k-th largest score
-//   COLLECT scores in bin b* -> candidate list; per key-chunk counts
-//   resolve sorts the candidates (score desc, key asc): exact threshold tau,
-//           tie budget and output offset of every key chunk
-//   EMIT    marks every key with s > tau (and the budgeted s == tau keys)
-//           in a per-row bit mask; a compaction kernel writes the index row
-//           in ascending key order.
+//   HIST    256 (128 for r=64) linear bins over the range; the bracket kernel
+//           finds the bin holding the k-th largest score, i.e. an interval
+//           [lo, hi) of orderable score bits, the count of scores >= hi and
+//           the count inside the interval
+//   REFINE  (only rows whose interval holds more than kCandCap scores) the
+//           interval's scores binned again by their next 8 (7 for r=64)
+//           orderable bits; at most four (five) rounds narrow any interval to
+//           at most kCandCap scores or to a single value, so no input can
+//           overflow the candidate buffer. Rounds with nothing to refine exit
+//           at once.
+//   COLLECT marks every key scoring >= hi in a per-row bit mask and stages the
+//           interval's scores as candidates (a single-valued interval marks
+//           its keys in a tie mask instead)
+//   resolve sorts each row's candidates (score desc, key asc) and marks the
+//           ones that complete the row's k
+//   compact writes each index row in ascending key order from the masks,
+//           taking a single-valued interval's keys lowest first.
 // Coverage reuses MINMAX and a COV pass that bins exp(scale*(s - max)) by
 // log-probability (count and mass per bin); a reduce kernel searches k.
 #include <algorithm>
@@ -44,7 +53,10 @@ constexpr int kMaxChunks = 64;     // key chunks per row
 // chain costs its ramp-up and tail.
 constexpr size_t kProjBudget = 1ull << 30;
 
-enum SelMode { kMinMax = 0, kHist = 1, kCollect = 2, kEmit = 3, kCov = 4 };
+enum SelMode { kMinMax = 0, kHist = 1, kCollect = 2, kRefine = 3, kCov = 4 };
+
+// Per-row state of the boundary interval after each bracket step.
+enum RowState { kRowCollect = 0, kRowRefine = 1, kRowTied = 2 };
 
 template <int RP>
 struct SelCfg {
@@ -52,6 +64,7 @@ struct SelCfg {
   static constexpr int kTileBytes = 128 * RP * 4;      // one [128][RP] fp32 tile
   static constexpr int kStages = (RP == 32) ? 2 : 1;
   static constexpr int kHistBins = (RP == 32) ? 256 : 128;
+  static constexpr int kHistLog2 = (RP == 32) ? 8 : 7;
   static constexpr int kCovBins = (RP == 32) ? 128 : 64;
   static constexpr int kHistBytes = 128 * 1024 / (RP / 32);
   static constexpr int kOffAlo = kTileBytes;
@@ -59,35 +72,31 @@ struct SelCfg {
   static constexpr int kOffHist = kOffB + kStages * 2 * kTileBytes;
   static constexpr int kOffMisc = kOffHist + kHistBytes;
   static constexpr int kSmem = kOffMisc + 256 + 1024;  // + barriers, + alignment slack
-  // MINMAX and EMIT keep no histogram: a 2 KB exchange area, then the barriers,
+  // MINMAX keeps no histogram: a 2 KB exchange area, then the barriers,
   // so two blocks share an SM and one's start and finish overlap the other's work
   static constexpr int kOffMiscSmall = kOffHist + 2048;
   static constexpr int kSmemSmall = kOffMiscSmall + 256 + 1024;
-  __host__ __device__ static constexpr bool big(int mode) { return mode == 1 || mode == 2 || mode == 4; }   // HIST, COLLECT, COV
+  __host__ __device__ static constexpr bool big(int mode) { return mode != 0; }   // all but MINMAX
   __host__ __device__ static constexpr int smem(int mode) { return big(mode) ? kSmem : kSmemSmall; }
   __host__ __device__ static constexpr int off_misc(int mode) { return big(mode) ? kOffMisc : kOffMiscSmall; }
 };
 
 struct SelParams {
   Geometry geo;
-  int32_t g_pad, n_chunks, chunk_tiles, n_tiles;
+  int32_t g_pad, n_chunks, chunk_tiles, n_tiles, n_gt;
   float scale;
   uint32_t* mmax;        // [n][g_pad] orderable max
   uint32_t* mmin;        // [n][g_pad] orderable min
-  uint32_t* hist;        // HIST: [n][bins][g_pad]; COV: counts [n][chunks][bins][g_pad]
+  uint32_t* hist;        // HIST, REFINE: [n][bins][g_pad]; COV: counts [n][chunks][bins][g_pad]
   float* mass;           // COV: [n][chunks][bins][g_pad]
-  const int32_t* bstar;  // [n][g_pad]
-  const float* t_bin;    // COLLECT: [n][g_pad][2] least scores of bins b* and b*+1 (see k_bracket)
+  const uint32_t* blo;   // [n][g_pad] boundary interval [blo, bhi) of orderable scores
+  const uint32_t* bhi;
+  const int32_t* rstate; // [n][g_pad] RowState
+  const int32_t* tflag;  // REFINE: [n][n_gt] group tiles holding a row to refine
   uint32_t* cand_cnt;    // [n][g_pad]
   uint64_t* cand;        // [n][g_pad][kCandCap]
-  int32_t* above;        // [n][chunks][g_pad]
-  int32_t* inbin;        // [n][chunks][g_pad]
-  const float* tau;      // [n][g_pad]
-  const int32_t* out_off;    // [n][chunks][g_pad]
-  const int32_t* eq_budget;  // [n][chunks][g_pad]
-  uint32_t* sel_bits;        // EMIT: [n][g_pad][n_tiles][4] selected-key masks, 32 keys per word
-  const int32_t* tie_cut;    // [n][g_pad] last selected key among those tied at tau (-1: none)
-  int32_t* idx;
+  uint32_t* sel_bits;    // [n][g_pad][n_tiles][4] keys scoring >= bhi, 32 keys per word
+  uint32_t* eq_bits;     // same layout: keys inside a single-valued interval
   int32_t* status;
 };
 
@@ -162,6 +171,10 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   const int t0 = chunk * prm.chunk_tiles;
   const int nt = min(prm.chunk_tiles, prm.n_tiles - t0);
   const int S = prm.geo.S;
+  // REFINE: group tiles without a row to refine leave before touching TMEM
+  if constexpr (MODE == kRefine) {
+    if (prm.tflag[lp * prm.n_gt + gtile] == 0) return;
+  }
 
   if (warp == 9) {
     tmem_alloc(tslot, 256);
@@ -249,22 +262,32 @@ __global__ void __launch_bounds__(kSelThreads, 2)
 
     float lo = 0.f, inv_w = 0.f, cmax = 0.f;
     float mx = -INFINITY, mn = INFINITY;
-    int n_above = 0, n_in = 0;
-    float tau = INFINITY;
-    int tcut = -1;
+    int n_in = 0;
     // COLLECT stages up to kStage candidates per (row, half) in the unused histogram area
     constexpr int kStage = C::kHistBytes / (256 * 8);
     uint64_t* stage = reinterpret_cast<uint64_t*>(sHist) + (size_t)(half * 128 + row) * kStage;
     constexpr int NB = (MODE == kCov) ? C::kCovBins : C::kHistBins;
     const uint32_t hist_base = smem_u32(sHist);
 
-    float t_in = INFINITY, t_above = INFINITY;   // COLLECT: least scores of bins b* and b*+1
+    // COLLECT: scores >= t_above are selected, [t_in, t_above) is the boundary
+    // interval; REFINE: the interval [olo, olo + owid) of orderable scores,
+    // binned by (o - olo) >> oshift
+    float t_in = INFINITY, t_above = INFINITY;
+    uint32_t olo = 0, owid = 0, oshift = 0;
+    int state = kRowCollect;
     if constexpr (MODE == kHist) lin_range(prm.mmin[rid], prm.mmax[rid], NB, &lo, &inv_w);
-    if constexpr (MODE == kCollect) {
+    if constexpr (MODE == kCollect || MODE == kRefine) {
       if (valid) {
-        t_in = prm.t_bin[2 * (size_t)rid];
-        t_above = prm.t_bin[2 * (size_t)rid + 1];
+        olo = prm.blo[rid];
+        const uint32_t ohi = prm.bhi[rid];
+        state = prm.rstate[rid];
+        t_in = ord2f(olo);
+        t_above = ord2f(ohi);
+        owid = ohi - olo;
+        const int bits = owid > 1u ? 32 - __clz(owid - 1u) : 0;
+        oshift = (uint32_t)max(0, bits - C::kHistLog2);
       }
+      if (MODE == kRefine && state != kRowRefine) owid = 0;   // this row takes no part
     }
     float w2 = 0.f;   // COV: bin width in log2 units
     if constexpr (MODE == kCov) {
@@ -273,13 +296,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       inv_w = range > 0.f ? (float)NB / range : 0.f;
       w2 = range > 0.f ? range / (float)NB * 1.4426950408889634f : 0.f;
     }
-    if constexpr (MODE == kEmit) {
-      if (valid) {
-        tau = prm.tau[rid];
-        tcut = prm.tie_cut[rid];
-      }
-    }
-    if constexpr (MODE == kHist || MODE == kCov) {
+    if constexpr (MODE == kHist || MODE == kCov || MODE == kRefine) {
       // zero this CTA's private histograms ([bin][row] counts, then masses)
       uint32_t* h = reinterpret_cast<uint32_t*>(sHist);
       for (int i = tid; i < C::kHistBytes / 4; i += 256) h[i] = 0;
@@ -294,38 +311,15 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       }
       tc_fence_after();
       const int key0 = (t0 + i) * 128;
-      if constexpr (MODE == kEmit) {
-        // Each warp marks the selected keys of its 64 columns in a bit mask:
-        // s > tau, or s == tau for keys up to the row's tie cut (the tied keys
-        // are taken in ascending key order); k_sel_compact writes the index rows.
-        uint32_t r0[32];
-        uint32_t gm[2] = {0u, 0u}, qm[2] = {0u, 0u};
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          tmem_ld32(taddr_lane + b * 128 + half * 64 + c * 32, r0);
-          tmem_ld_wait(r0);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float sv = __uint_as_float(r0[e]) + 0.0f;
-            gm[c] |= (uint32_t)(sv > tau) << e;
-            qm[c] |= (uint32_t)(sv == tau) << e;
-          }
-        }
-        if (valid) {
-          const int lim = tcut - (key0 + half * 64);   // tied columns 0..lim are taken
-          const uint64_t keep = lim >= 63 ? ~0ull : (lim < 0 ? 0ull : (2ull << lim) - 1ull);
-          const uint64_t sel = ((uint64_t)gm[1] << 32 | gm[0]) | (((uint64_t)qm[1] << 32 | qm[0]) & keep);
-          const size_t wi = ((size_t)rid * prm.n_tiles + (t0 + i)) * 4 + half * 2;
-          *reinterpret_cast<uint2*>(prm.sel_bits + wi) = make_uint2((uint32_t)sel, (uint32_t)(sel >> 32));
-        }
-      } else {
+      {
         uint32_t r0[32], r1[32];
         tmem_ld32(taddr_lane + b * 128 + half * 64, r0);
         tmem_ld32(taddr_lane + b * 128 + half * 64 + 32, r1);
         tmem_ld_wait(r0);
         reg_fence(r1);
         const int kb = key0 + half * 64;
-        uint32_t cm_lo = 0, cm_hi = 0;   // COLLECT: columns whose score lies in bin b*
+        uint32_t gm_lo = 0, gm_hi = 0;   // COLLECT: columns scoring >= t_above
+        uint32_t cm_lo = 0, cm_hi = 0;   // COLLECT: columns inside the boundary interval
 #pragma unroll
         for (int e = 0; e < 64; ++e) {
           const float s = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]) + 0.0f;
@@ -337,12 +331,19 @@ __global__ void __launch_bounds__(kSelThreads, 2)
             red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
           } else if constexpr (MODE == kCollect) {
             // branch-free here; the rare candidates are handled after the loop.
-            // bin(s) > b* <=> s >= t_above and bin(s) == b* <=> t_in <= s < t_above
-            // (the binning is monotone and k_bracket found the exact least scores)
+            // The thresholds are exact floats of the interval's orderable
+            // bounds, so the float compares equal the orderable ones
             const bool above = s >= t_above, in = s >= t_in && !above;
-            n_above += above;
-            if (e < 32) cm_lo |= (uint32_t)in << e;
-            else cm_hi |= (uint32_t)in << (e - 32);
+            if (e < 32) {
+              gm_lo |= (uint32_t)above << e;
+              cm_lo |= (uint32_t)in << e;
+            } else {
+              gm_hi |= (uint32_t)above << (e - 32);
+              cm_hi |= (uint32_t)in << (e - 32);
+            }
+          } else if constexpr (MODE == kRefine) {
+            const uint32_t dlt = f2ord(s) - olo;   // wraps above 2^31 for scores below the interval
+            if (dlt < owid) red_smem_u32(hist_base + (uint32_t)((dlt >> oshift) * 128 + row) * 4u, 1u);
           } else if constexpr (MODE == kCov) {
             // log-probability below the row maximum, its bin b, and q = exp(b w - u)
             const float u = __fmul_rn(prm.scale, __fsub_rn(cmax, s));
@@ -358,9 +359,15 @@ __global__ void __launch_bounds__(kSelThreads, 2)
           }
         }
         if constexpr (MODE == kCollect) {
+          if (valid) {
+            const size_t wi = ((size_t)rid * prm.n_tiles + (t0 + i)) * 4 + half * 2;
+            *reinterpret_cast<uint2*>(prm.sel_bits + wi) = make_uint2(gm_lo, gm_hi);
+            // a single-valued interval: its keys are taken lowest first by the compaction
+            if (state == kRowTied) *reinterpret_cast<uint2*>(prm.eq_bits + wi) = make_uint2(cm_lo, cm_hi);
+          }
           // one short loop per candidate: pick the score out of r0/r1 with a
           // select chain (no dynamically indexed registers), stage the key
-          uint64_t cm = valid ? ((uint64_t)cm_hi << 32 | cm_lo) : 0ull;
+          uint64_t cm = (valid && state == kRowCollect) ? ((uint64_t)cm_hi << 32 | cm_lo) : 0ull;
 #pragma unroll 1
           while (cm) {
             const int e = __ffsll((long long)cm) - 1;
@@ -399,33 +406,18 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       }
       epi_barrier();
     }
-    if constexpr (MODE == kMinMax || MODE == kCollect) {
+    if constexpr (MODE == kMinMax) {
       float* ex = reinterpret_cast<float*>(sHist);   // [2][2][128], the histogram area is unused here
-      if (MODE == kMinMax) {
-        ex[(half * 2 + 0) * 128 + row] = mx;
-        ex[(half * 2 + 1) * 128 + row] = mn;
-      } else {
-        reinterpret_cast<int*>(ex)[(half * 2 + 0) * 128 + row] = n_above;
-        reinterpret_cast<int*>(ex)[(half * 2 + 1) * 128 + row] = n_in;
-      }
+      ex[(half * 2 + 0) * 128 + row] = mx;
+      ex[(half * 2 + 1) * 128 + row] = mn;
       epi_barrier();
-      if (half == 0 && valid) {
-        if (MODE == kMinMax) {
-          const float m2 = fmaxf(mx, ex[(2 + 0) * 128 + row]);
-          const float n2 = fminf(mn, ex[(2 + 1) * 128 + row]);
-          if (nt > 0) {
-            atomicMax(prm.mmax + rid, f2ord(m2));
-            atomicMin(prm.mmin + rid, f2ord(n2));
-          }
-        } else {
-          const int* exi = reinterpret_cast<int*>(ex);
-          const int ci = (lp * prm.n_chunks + chunk) * prm.g_pad + g;
-          prm.above[ci] = n_above + exi[(2 + 0) * 128 + row];
-          prm.inbin[ci] = n_in + exi[(2 + 1) * 128 + row];
-        }
+      if (half == 0 && valid && nt > 0) {
+        const float m2 = fmaxf(mx, ex[(2 + 0) * 128 + row]);
+        const float n2 = fminf(mn, ex[(2 + 1) * 128 + row]);
+        atomicMax(prm.mmax + rid, f2ord(m2));
+        atomicMin(prm.mmin + rid, f2ord(n2));
       }
-
-    } else if constexpr (MODE == kHist) {
+    } else if constexpr (MODE == kHist || MODE == kRefine) {
       epi_barrier();
       const uint32_t* h = reinterpret_cast<const uint32_t*>(sHist);
       for (int bin = half * (NB / 2); bin < (half + 1) * (NB / 2); ++bin) {
@@ -603,7 +595,7 @@ __global__ void __launch_bounds__(128) k_group_mean_proj(const __nv_bfloat16* __
 }
 
 // ---------------------------------------------------------------------------
-// Bracket: per row, the bin b* holding the k-th largest score.
+// Bracket: per row, the bin holding the k-th largest score.
 // Least score (as an orderable key in [o_lo, o_hi]) whose bin is at least
 // `target`; o_hi when no score up to the row maximum reaches it.
 __device__ uint32_t least_with_bin(int target, uint32_t o_lo, uint32_t o_hi, float lo, float inv_w, int nb) {
@@ -616,136 +608,181 @@ __device__ uint32_t least_with_bin(int target, uint32_t o_lo, uint32_t o_hi, flo
   return a;
 }
 
-__global__ void k_bracket(const uint32_t* __restrict__ hist, int nb, int g_pad, int n_groups, int32_t* bstar,
-                          int32_t* n_above_out, const uint32_t* __restrict__ mmin, const uint32_t* __restrict__ mmax,
-                          float* t_bin, const ProblemTable tab) {
-  const int lp = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
-  if (g >= n_groups) return;
-  const int k = tab.k[lp];
-  const uint32_t* h = hist + (size_t)lp * nb * g_pad + g;
-  int above = 0, b = nb - 1;
-  bool found = false;
-  for (int top = nb - 1; top >= 0 && !found; top -= 8) {
+// State of a row whose k-th score lies in [lo, hi) with `count` scores there:
+// a single value is resolved by key order, a small interval by sorting its
+// candidates, a larger one by another REFINE round.
+__device__ __forceinline__ int row_state(uint32_t lo, uint32_t hi, uint32_t count) {
+  if (hi - lo <= 1u) return kRowTied;
+  return count <= (uint32_t)kCandCap ? kRowCollect : kRowRefine;
+}
+
+// Finds the bin b of the row's histogram (nb bins, stride g_pad) where the
+// count of scores from the top first reaches k, given `above` scores above
+// bin nb-1. Returns b (or -1), with *above_out the scores above bin b.
+__device__ __forceinline__ int find_kth_bin(const uint32_t* h, int nb, int g_pad, int k, int above, int* above_out) {
+  for (int top = nb - 1; top >= 0; top -= 8) {
     uint32_t c[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) c[e] = top - e >= 0 ? __ldg(h + (size_t)(top - e) * g_pad) : 0u;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      if (!found && top - e >= 0) {
-        if (above + (int)c[e] >= k) {
-          b = top - e;
-          found = true;
-        } else {
-          above += (int)c[e];
-        }
+      if (top - e < 0) break;
+      if (above + (int)c[e] >= k) {
+        *above_out = above;
+        return top - e;
       }
+      above += (int)c[e];
     }
   }
-  if (!found) b = 0;
+  *above_out = above;
+  return -1;
+}
+
+// One thread per row. The row's boundary interval from the linear histogram:
+// [least score of bin b*, least score of bin b*+1) in orderable bits, the
+// count of scores at or above its upper end and the count inside it. A row to
+// refine has its histogram zeroed (for the first REFINE round) and flags its
+// group tile.
+__global__ void k_bracket(uint32_t* hist, int nb, int g_pad, int n_groups, int n_gt, const uint32_t* __restrict__ mmin,
+                          const uint32_t* __restrict__ mmax, uint32_t* blo, uint32_t* bhi, int32_t* nabove,
+                          uint32_t* bcount, int32_t* rstate, int32_t* tflag, int32_t* status,
+                          const ProblemTable tab) {
+  const int lp = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n_groups) return;
+  const int k = tab.k[lp];
+  uint32_t* h = hist + (size_t)lp * nb * g_pad + g;
+  int above = 0;
+  int b = find_kth_bin(h, nb, g_pad, k, 0, &above);
+  if (b < 0) {   // fewer than k scores: cannot happen for 1 <= k <= S
+    raise_status(status, DSV_ERR_CANDIDATES);
+    b = 0;
+  }
+  const uint32_t count = h[(size_t)b * g_pad];
   const int rid = lp * g_pad + g;
-  bstar[rid] = b;
-  n_above_out[rid] = above;
-  // COLLECT compares scores against the least scores of bins b and b+1: every
-  // score lies in [min, max] of its row, and past the maximum a threshold is
-  // the next float up (never reached)
+  // every score lies in [min, max] of its row; past the maximum a threshold
+  // is the next float up (never reached)
   float lo, inv_w;
   lin_range(mmin[rid], mmax[rid], nb, &lo, &inv_w);
   const uint32_t o_lo = mmin[rid], o_hi = mmax[rid] + 1u;
-  t_bin[2 * (size_t)rid] = ord2f(least_with_bin(b, o_lo, o_hi, lo, inv_w, nb));
-  t_bin[2 * (size_t)rid + 1] = ord2f(least_with_bin(b + 1, o_lo, o_hi, lo, inv_w, nb));
+  const uint32_t l = least_with_bin(b, o_lo, o_hi, lo, inv_w, nb);
+  const uint32_t u = least_with_bin(b + 1, o_lo, o_hi, lo, inv_w, nb);
+  blo[rid] = l;
+  bhi[rid] = u;
+  nabove[rid] = above;
+  bcount[rid] = count;
+  const int st = row_state(l, u, count);
+  rstate[rid] = st;
+  if (st == kRowRefine) {
+    for (int i = 0; i < nb; ++i) h[(size_t)i * g_pad] = 0u;
+    tflag[lp * n_gt + g / 128] = 1;
+  }
 }
 
-// Resolve: exact threshold, per-chunk output offsets and tie budgets.
+// After a REFINE round: the interval's sub-bin b (width 2^shift in orderable
+// bits) holding the k-th score becomes the row's interval. Each round takes
+// log2(nb) more bits, so an interval is a single value after at most
+// ceil(32 / log2(nb)) rounds.
+__global__ void k_refine_bracket(uint32_t* hist, int nb, int log2nb, int g_pad, int n_groups, int n_gt,
+                                 uint32_t* blo, uint32_t* bhi, int32_t* nabove, uint32_t* bcount, int32_t* rstate,
+                                 const int32_t* tflag, int32_t* tflag_next, int32_t* status, const ProblemTable tab) {
+  const int lp = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n_groups || tflag[lp * n_gt + g / 128] == 0) return;
+  const int rid = lp * g_pad + g;
+  if (rstate[rid] != kRowRefine) return;
+  const int k = tab.k[lp];
+  uint32_t* h = hist + (size_t)lp * nb * g_pad + g;
+  const uint32_t lo = blo[rid], hi = bhi[rid], wid = hi - lo;
+  const int bits = 32 - __clz(wid - 1u);   // wid >= 2 here
+  const int shift = max(0, bits - log2nb);
+  int above = 0;
+  const int b = find_kth_bin(h, nb, g_pad, k, nabove[rid], &above);
+  if (b < 0) {   // the sub-bins hold fewer scores than the interval did: inconsistent
+    raise_status(status, DSV_ERR_CANDIDATES);
+    rstate[rid] = kRowTied;
+    nabove[rid] = k;
+    return;
+  }
+  const uint32_t count = h[(size_t)b * g_pad];
+  const uint32_t l = lo + ((uint32_t)b << shift);
+  const uint64_t end = (uint64_t)lo + ((uint64_t)(b + 1) << shift);
+  const uint32_t u = end < (uint64_t)hi ? (uint32_t)end : hi;
+  blo[rid] = l;
+  bhi[rid] = u;
+  nabove[rid] = above;
+  bcount[rid] = count;
+  const int st = row_state(l, u, count);
+  rstate[rid] = st;
+  if (st == kRowRefine) {
+    for (int i = 0; i < nb; ++i) h[(size_t)i * g_pad] = 0u;
+    tflag_next[lp * n_gt + g / 128] = 1;
+  }
+}
+
+// Resolve: a row whose interval holds at most kCandCap candidates sorts them
+// (score desc, key asc) and marks the first k - above of them in the row's
+// selection mask. Single-valued intervals are left to the compaction.
 __global__ void __launch_bounds__(256) k_resolve(const uint64_t* __restrict__ cand, const uint32_t* cand_cnt,
-                                                 const uint32_t* mmax, const uint32_t* mmin,
-                                                 const int32_t* n_above_all, const int32_t* above,
-                                                 const int32_t* inbin, int g_pad, int n_chunks, int chunk_keys,
-                                                 float* tau_out, int32_t* out_off, int32_t* eq_budget,
-                                                 int32_t* tie_cut, int32_t* status, const ProblemTable tab) {
+                                                 const int32_t* nabove, const uint32_t* bcount,
+                                                 const int32_t* rstate, int g_pad, int n_words, uint32_t* sel_bits,
+                                                 int32_t* status, const ProblemTable tab) {
   __shared__ uint64_t keys[kCandCap];
-  __shared__ int sel_cnt[kMaxChunks], eq_cnt[kMaxChunks];
-  __shared__ float s_tau;
-  __shared__ int s_cut;
   const int g = blockIdx.x, lp = blockIdx.y, tid = threadIdx.x;
   const int rid = lp * g_pad + g;
+  const int st = rstate[rid];
+  if (st == kRowTied) return;
   const int k = tab.k[lp];
-  const int need = k - n_above_all[rid];
+  const int need = k - nabove[rid];
   const uint32_t ncand = cand_cnt[rid];
-  const bool all_equal = mmax[rid] == mmin[rid];
-  for (int c = tid; c < kMaxChunks; c += blockDim.x) sel_cnt[c] = eq_cnt[c] = 0;
-  if (tid == 0) {
-    s_tau = INFINITY;
-    s_cut = -1;
-  }
-  __syncthreads();
-  if (all_equal) {
-    if (tid == 0) {
-      int rem = need;
-      for (int c = 0; c < n_chunks; ++c) {
-        const int e = min(rem, inbin[(lp * n_chunks + c) * g_pad + g]);
-        sel_cnt[c] = e;
-        eq_cnt[c] = e;
-        rem -= e;
-      }
-      s_tau = ord2f(mmax[rid]);
-      s_cut = need - 1;   // every key ties: the first `need` keys
-    }
-  } else if (ncand > (uint32_t)kCandCap || need < 1 || (uint32_t)need > ncand) {
+  if (st != kRowCollect || ncand != bcount[rid] || ncand > (uint32_t)kCandCap || need < 1 ||
+      (uint32_t)need > ncand) {
     if (tid == 0) raise_status(status, DSV_ERR_CANDIDATES);
-  } else {
-    int n2 = 1;
-    while (n2 < (int)ncand) n2 <<= 1;
-    for (int i = tid; i < n2; i += blockDim.x) keys[i] = i < (int)ncand ? cand[(size_t)rid * kCandCap + i] : ~0ull;
-    __syncthreads();
-    for (int size = 2; size <= n2; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = tid; i < n2 / 2; i += blockDim.x) {
-          const int a = 2 * i - (i & (stride - 1));
-          const int b = a + stride;
-          const bool asc = (a & size) == 0;
-          const uint64_t x = keys[a], y = keys[b];
-          if ((x > y) == asc) {
-            keys[a] = y;
-            keys[b] = x;
-          }
-        }
-        __syncthreads();
-      }
-    }
-    const uint32_t tkey = (uint32_t)(keys[need - 1] >> 32);
-    const float tau = ord2f(~tkey);
+    return;
+  }
+  uint32_t* row_bits = sel_bits + (size_t)rid * n_words;
+  const uint64_t* c = cand + (size_t)rid * kCandCap;
+  if ((uint32_t)need == ncand) {   // the whole interval is taken
     for (int i = tid; i < need; i += blockDim.x) {
-      const uint32_t j = (uint32_t)keys[i];
-      const int c = (int)(j / (uint32_t)chunk_keys);
-      atomicAdd(&sel_cnt[c], 1);
-      if ((uint32_t)(keys[i] >> 32) == tkey) atomicAdd(&eq_cnt[c], 1);
+      const uint32_t j = (uint32_t)c[i];
+      atomicOr(row_bits + (j >> 5), 1u << (j & 31));
     }
-    if (tid == 0) {
-      s_tau = tau;
-      s_cut = (int)(uint32_t)keys[need - 1];   // sorted (score desc, key asc): the last tie taken
+    return;
+  }
+  int n2 = 1;
+  while (n2 < (int)ncand) n2 <<= 1;
+  for (int i = tid; i < n2; i += blockDim.x) keys[i] = i < (int)ncand ? c[i] : ~0ull;
+  __syncthreads();
+  for (int size = 2; size <= n2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < n2 / 2; i += blockDim.x) {
+        const int a = 2 * i - (i & (stride - 1));
+        const int b = a + stride;
+        const bool asc = (a & size) == 0;
+        const uint64_t x = keys[a], y = keys[b];
+        if ((x > y) == asc) {
+          keys[a] = y;
+          keys[b] = x;
+        }
+      }
+      __syncthreads();
     }
   }
-  __syncthreads();
-  if (tid == 0) {
-    int off = 0;
-    for (int c = 0; c < n_chunks; ++c) {
-      const int ci = (lp * n_chunks + c) * g_pad + g;
-      out_off[ci] = off;
-      eq_budget[ci] = eq_cnt[c];
-      off += above[ci] + sel_cnt[c];
-    }
-    tau_out[rid] = s_tau;
-    tie_cut[rid] = s_cut;
+  for (int i = tid; i < need; i += blockDim.x) {
+    const uint32_t j = (uint32_t)keys[i];
+    atomicOr(row_bits + (j >> 5), 1u << (j & 31));
   }
 }
 
-// Index rows from the EMIT masks: one block per group row, its 8 warps on
-// consecutive segments of the row's mask words. Each warp counts its
-// segment's selected keys, a block scan gives each segment its first output
-// position, and each warp then writes its keys 32 output positions at a time:
-// lane j finds the word of position j by binary search over the warp's prefix
-// sums and the key inside it with __fns, so every store instruction writes 32
-// consecutive indices (selected keys cluster, so per-word loops would diverge).
+// Index rows from the masks: one block per group row, its 8 warps on
+// consecutive segments of the row's mask words. A row's selection is its
+// selection mask, plus, when its boundary interval is a single value, the
+// k - above lowest keys of its tie mask (the cut is found first: each warp
+// counts its segment's ties, and the warp holding the cut walks its words).
+// Each warp counts its segment's selected keys, a block scan gives each
+// segment its first output position, and each warp then writes its keys 32
+// output positions at a time: lane j finds the word of position j by binary
+// search over the warp's prefix sums and the key inside it with __fns, so
+// every store instruction writes 32 consecutive indices (selected keys
+// cluster, so per-word loops would diverge).
 constexpr int kCompactWarps = 8;
 
 __device__ __forceinline__ int warp_incl_scan(int x, int lane) {
@@ -757,21 +794,68 @@ __device__ __forceinline__ int warp_incl_scan(int x, int lane) {
   return x;
 }
 
-__global__ void __launch_bounds__(32 * kCompactWarps) k_sel_compact(const uint32_t* __restrict__ bits, int g_pad,
-                                                                    int n_words, int32_t* idx, int32_t* status,
-                                                                    const ProblemTable tab) {
+// Tie-mask bits of word w that lie at or below key `cut`.
+__device__ __forceinline__ uint32_t keep_upto(int w, int cut) {
+  const int d = cut - w * 32;
+  return d >= 31 ? ~0u : (d < 0 ? 0u : (2u << d) - 1u);
+}
+
+__global__ void __launch_bounds__(32 * kCompactWarps) k_sel_compact(const uint32_t* __restrict__ bits,
+                                                                    const uint32_t* __restrict__ eq_bits,
+                                                                    const int32_t* rstate, const int32_t* nabove,
+                                                                    int g_pad, int n_words, int32_t* idx,
+                                                                    int32_t* status, const ProblemTable tab) {
   __shared__ int seg_total[kCompactWarps];
+  __shared__ int s_cut;
   const int g = blockIdx.x, lp = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int k = tab.k[lp];
+  const int rid = lp * g_pad + g;
   int32_t* out = idx + tab.off[lp] + (int64_t)g * k;
-  const uint32_t* row = bits + ((size_t)lp * g_pad + g) * n_words;
+  const uint32_t* row = bits + (size_t)rid * n_words;
+  const uint32_t* eq = eq_bits + (size_t)rid * n_words;
   const int seg = ((n_words + kCompactWarps * 32 - 1) / (kCompactWarps * 32)) * 32;   // words per warp
   const int w_begin = min(n_words, warp * seg), w_end = min(n_words, w_begin + seg);
+  const bool tied = rstate[rid] == kRowTied;
+  if (threadIdx.x == 0) s_cut = -1;
+  if (tied) {
+    const int budget = k - nabove[rid];
+    int ce = 0;
+    for (int w = w_begin + lane; w < w_end; w += 32) ce += __popc(__ldg(eq + w));
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) ce += __shfl_xor_sync(0xffffffffu, ce, d);
+    if (lane == 0) seg_total[warp] = ce;
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += seg_total[i];
+    if (before < budget && budget <= before + ce) {
+      int rem = budget - before;   // >= 1: the rem-th tie of this segment is the last one taken
+      for (int w0 = w_begin; w0 < w_end; w0 += 32) {
+        const uint32_t m = w0 + lane < w_end ? __ldg(eq + w0 + lane) : 0u;
+        const int c = __popc(m);
+        const int incl = warp_incl_scan(c, lane);
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (rem <= total) {
+          const uint32_t hit = __ballot_sync(0xffffffffu, incl >= rem);
+          const int L = __ffs(hit) - 1;
+          if (lane == L) s_cut = (w0 + L) * 32 + (int)__fns(m, 0, rem - (incl - c));
+          break;
+        }
+        rem -= total;
+      }
+    }
+  }
+  __syncthreads();
+  const int cut = s_cut;
+  auto word = [&](int w) -> uint32_t {
+    const uint32_t m = __ldg(row + w);
+    return tied ? (m | (__ldg(eq + w) & keep_upto(w, cut))) : m;
+  };
   int cnt = 0;
 #pragma unroll 8
-  for (int w = w_begin + lane; w < w_end; w += 32) cnt += __popc(__ldg(row + w));
+  for (int w = w_begin + lane; w < w_end; w += 32) cnt += __popc(word(w));
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, d);
+  __syncthreads();   // every warp has read seg_total (tie counts) before it is reused
   if (lane == 0) seg_total[warp] = cnt;
   __syncthreads();
   int base = 0, row_total = 0;
@@ -780,7 +864,7 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_sel_compact(const uint32
     row_total += seg_total[i];
   }
   for (int w0 = w_begin; w0 < w_end; w0 += 32) {
-    const uint32_t m = w0 + lane < w_end ? __ldg(row + w0 + lane) : 0u;
+    const uint32_t m = w0 + lane < w_end ? word(w0 + lane) : 0u;
     const int c = __popc(m);
     const int incl = warp_incl_scan(c, lane);
     const int total = __shfl_sync(0xffffffffu, incl, 31);
@@ -1058,18 +1142,23 @@ struct TopkWs {
   uint32_t *mmax, *mmin, *hist, *cand_cnt;
   uint32_t* cov_hist;
   float* mass;
-  int32_t *bstar, *nabove, *above, *inbin, *out_off, *eqb;
-  float* tbin;
-  uint32_t* selb;
-  int32_t* tcut;
+  uint32_t *blo, *bhi, *bcount;
+  int32_t *nabove, *rstate, *tflag;
+  uint32_t *selb, *eqb;
   uint64_t* cand;
-  float* tau;
   int32_t* cum_cnt;
   double* cum_mass;
   float* width;
   double* cov_partial;
   int32_t* cov_range;
 };
+
+// REFINE rounds: each narrows an interval by log2(bins) bits of the 32, so
+// this many leave a single value.
+static int refine_rounds(const TopkPlan& pl) {
+  const int lg = pl.RP == 32 ? SelCfg<32>::kHistLog2 : SelCfg<64>::kHistLog2;
+  return (32 + lg - 1) / lg;
+}
 
 // Carves the workspace (base == nullptr: sizing only): the projections and
 // row ranges, then the top-k buffers, the coverage buffers, or both.
@@ -1085,18 +1174,16 @@ static size_t carve(void* base, const TopkPlan& pl, int mode, TopkWs* w) {
   w->mmin = c.take<uint32_t>(pc * gp);
   if (mode & kCarveTopk) {
     w->hist = c.take<uint32_t>(pc * pl.hist_bins * gp);
-    w->bstar = c.take<int32_t>(pc * gp);
-    w->tbin = c.take<float>(pc * gp * 2);
+    w->blo = c.take<uint32_t>(pc * gp);
+    w->bhi = c.take<uint32_t>(pc * gp);
+    w->bcount = c.take<uint32_t>(pc * gp);
     w->nabove = c.take<int32_t>(pc * gp);
+    w->rstate = c.take<int32_t>(pc * gp);
+    w->tflag = c.take<int32_t>((size_t)(refine_rounds(pl) + 1) * pc * pl.n_gt);
     w->cand_cnt = c.take<uint32_t>(pc * gp);
     w->cand = c.take<uint64_t>(pc * gp * kCandCap);
-    w->above = c.take<int32_t>(pc * pl.max_chunks * gp);
-    w->inbin = c.take<int32_t>(pc * pl.max_chunks * gp);
-    w->out_off = c.take<int32_t>(pc * pl.max_chunks * gp);
     w->selb = c.take<uint32_t>(pc * gp * pl.n_tiles * 4);
-    w->tcut = c.take<int32_t>(pc * gp);
-    w->eqb = c.take<int32_t>(pc * pl.max_chunks * gp);
-    w->tau = c.take<float>(pc * gp);
+    w->eqb = c.take<uint32_t>(pc * gp * pl.n_tiles * 4);
   }
   if (mode & kCarveCov) {
     w->cov_hist = c.take<uint32_t>(pc * pl.max_chunks * pl.cov_bins * gp);
@@ -1202,43 +1289,51 @@ static cudaError_t topk_passes(const TopkPlan& pl, const TopkWs& w, const Proble
   prm.n_chunks = n_chunks;
   prm.chunk_tiles = chunk_tiles;
   prm.n_tiles = pl.n_tiles;
+  prm.n_gt = pl.n_gt;
   prm.mmax = w.mmax;
   prm.mmin = w.mmin;
   prm.hist = w.hist;
-  prm.bstar = w.bstar;
-  prm.t_bin = w.tbin;
+  prm.blo = w.blo;
+  prm.bhi = w.bhi;
+  prm.rstate = w.rstate;
   prm.cand_cnt = w.cand_cnt;
   prm.cand = w.cand;
-  prm.above = w.above;
-  prm.inbin = w.inbin;
-  prm.tau = w.tau;
-  prm.out_off = w.out_off;
-  prm.eq_budget = w.eqb;
   prm.sel_bits = w.selb;
-  prm.tie_cut = w.tcut;
-  prm.idx = idx;
+  prm.eq_bits = w.eqb;
   prm.status = status;
   const dim3 grid(pl.n_gt, n_chunks, n);
   const size_t rows = (size_t)n * pl.g_pad;
+  const int rounds = refine_rounds(pl);
+  const int lg = pl.RP == 32 ? SelCfg<32>::kHistLog2 : SelCfg<64>::kHistLog2;
+  const size_t nflag = (size_t)n * pl.n_gt;
+  const dim3 rgrid(pl.n_gt, n);
   if (minmax) {
     if (cudaMemsetAsync(w.mmax, 0, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
     if (cudaMemsetAsync(w.mmin, 0xFF, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
     if (select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
   }
   if (cudaMemsetAsync(w.hist, 0, rows * pl.hist_bins * 4, st) != cudaSuccess) return cudaErrorUnknown;
+  if (cudaMemsetAsync(w.tflag, 0, (rounds + 1) * nflag * 4, st) != cudaSuccess) return cudaErrorUnknown;
   if (select_pass<kHist>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
-  k_bracket<<<dim3(pl.n_gt, n), 128, 0, st>>>(w.hist, pl.hist_bins, pl.g_pad, pl.geo.n_groups, w.bstar,
-                                               w.nabove, w.mmin, w.mmax, w.tbin, tab);
+  k_bracket<<<rgrid, 128, 0, st>>>(w.hist, pl.hist_bins, pl.g_pad, pl.geo.n_groups, pl.n_gt, w.mmin, w.mmax, w.blo,
+                                   w.bhi, w.nabove, w.bcount, w.rstate, w.tflag, status, tab);
   if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
+  // REFINE rounds: group tiles with no row to refine leave at once
+  for (int r = 0; r < rounds; ++r) {
+    prm.tflag = w.tflag + r * nflag;
+    if (select_pass<kRefine>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+    k_refine_bracket<<<rgrid, 128, 0, st>>>(w.hist, pl.hist_bins, lg, pl.g_pad, pl.geo.n_groups, pl.n_gt, w.blo,
+                                            w.bhi, w.nabove, w.bcount, w.rstate, w.tflag + r * nflag,
+                                            w.tflag + (r + 1) * nflag, status, tab);
+    if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
+  }
   if (cudaMemsetAsync(w.cand_cnt, 0, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
   if (select_pass<kCollect>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
-  k_resolve<<<dim3(pl.geo.n_groups, n), 256, 0, st>>>(w.cand, w.cand_cnt, w.mmax, w.mmin, w.nabove, w.above,
-                                                        w.inbin, pl.g_pad, n_chunks, chunk_tiles * 128, w.tau,
-                                                        w.out_off, w.eqb, w.tcut, status, tab);
+  k_resolve<<<dim3(pl.geo.n_groups, n), 256, 0, st>>>(w.cand, w.cand_cnt, w.nabove, w.bcount, w.rstate, pl.g_pad,
+                                                        pl.n_tiles * 4, w.selb, status, tab);
   if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
-  if (select_pass<kEmit>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
-  k_sel_compact<<<dim3(pl.geo.n_groups, n), 32 * kCompactWarps, 0, st>>>(w.selb, pl.g_pad, pl.n_tiles * 4, idx,
-                                                                          status, tab);
+  k_sel_compact<<<dim3(pl.geo.n_groups, n), 32 * kCompactWarps, 0, st>>>(w.selb, w.eqb, w.rstate, w.nabove, pl.g_pad,
+                                                                          pl.n_tiles * 4, idx, status, tab);
   return cudaGetLastError();
 }
 
@@ -1468,22 +1563,52 @@ namespace dsv {
 constexpr size_t kStaticScratchBytes = 64ull << 20;   // 64 MiB
 static __device__ __align__(256) uint8_t g_topk_scratch[kStaticScratchBytes];
 
+// Unique id of the calling thread's current CUDA context, 0 when there is
+// none yet or the driver cannot report it. A device reset or a context torn
+// down and made again gives a new id.
+static unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 // Device address of g_topk_scratch for the current device. The host-side name
-// is only a stand-in, so the address is looked up (once per device, with that
-// device current) through the runtime; the first lookup also loads this
-// module on that device.
+// is only a stand-in, so the address is looked up through the runtime, with
+// the device current: once per device and context (the first lookup also
+// loads this module there). The cached address is keyed by the context's id,
+// so after a device reset the next call looks it up again instead of using an
+// address of the old context; when no id can be read, every call looks it up.
 static void* static_scratch_address(cudaError_t* err) {
   static std::mutex mu;
   static void* addr[128] = {};
+  static unsigned long long ctx_of[128] = {};
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  const unsigned long long id = current_context_id();
+  if (!addr[dev] || id == 0 || ctx_of[dev] != id) {
     void* p = nullptr;
     *err = cudaGetSymbolAddress(&p, g_topk_scratch);
     if (*err != cudaSuccess) return nullptr;
     addr[dev] = p;
+    ctx_of[dev] = current_context_id();   // the lookup made the device's primary context current
   }
   return addr[dev];
 }

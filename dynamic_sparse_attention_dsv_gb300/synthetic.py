@@ -150,3 +150,78 @@ def make_inputs(w: Workload, seed: Optional[int] = None, with_grad_out: Optional
         for h in range(H):
             dO[h] = to_bf16(rng.standard_normal((S, d)))
     return dict(Q=Q, K=K, V=V, Wq=Wq, Wk=Wk, dO=dO, qscale=qs)
+
+
+def make_clustered_inputs(T: int, Y: int, X: int, d: int, r: int, H: int, mode: str = "spread",
+                          seed: int = 7) -> dict:
+    """Adversarial predictor inputs for the top-k boundary: one key far above
+    and one far below the others, and every other key in a narrow cluster.
+
+    W_lr^Q = W_lr^K = [I_r; 0], so the predictor's q_lr, k_lr are the first r
+    channels of Q and K. Every query of head h is e_0 + c_h e_1 with c_h a
+    power of two, and key j carries a_j in channel 0 and b_j in channel 1:
+    a = 1 except a_0 = 100 and a_1 = -100; b is a seeded bf16 multiple of
+    2^-12 in [-1, 1] ("spread": many distinct values, some repeated) or one of
+    {-1, -1/2, 0, 1/2, 1} ("ties": large groups of exactly equal keys).
+    Channels past 1 hold small seeded noise. Every a_j + c_h b_j is exact in
+    fp32 (at most 21 significant bits), so any correct fp32 computation of
+    the predictor scores gives them exactly.
+    Returns Q, K, V, Wq, Wk as CPU bf16 tensors ([H,S,d] and [H,d,r]) and
+    the per-head c (float64 [H]).
+    """
+    S = T * Y * X
+    rng = np.random.default_rng(seed)
+    eye = np.zeros((d, r))
+    eye[np.arange(r), np.arange(r)] = 1.0
+    Wq = to_bf16(np.broadcast_to(eye, (H, d, r)))
+    Wk = Wq.clone()
+    c = np.array([2.0 ** -(3 + 2 * (h % 3)) * (-1) ** h for h in range(H)])
+    Q = np.zeros((H, S, d))
+    Q[:, :, 0] = 1.0
+    Q[:, :, 1] = c[:, None]
+    K = 0.01 * rng.standard_normal((H, S, d))
+    K[:, :, 0] = 1.0
+    K[:, 0, 0], K[:, 1, 0] = 100.0, -100.0
+    if mode == "spread":
+        K[:, :, 1] = np.round(rng.uniform(-1.0, 1.0, (H, S)) * 4096.0) / 4096.0
+    elif mode == "ties":
+        K[:, :, 1] = rng.choice(np.array([-1.0, -0.5, 0.0, 0.5, 1.0]), (H, S))
+    else:
+        raise ValueError(mode)
+    V = rng.standard_normal((H, S, d))
+    return dict(Q=to_bf16(Q), K=to_bf16(K), V=to_bf16(V), Wq=Wq, Wk=Wk, c=c)
+
+
+def make_inputs_device(w: Workload, device, heads: Optional[int] = None, seed: Optional[int] = None,
+                       with_grad_out: Optional[bool] = None, r: Optional[int] = None) -> dict:
+    """The recipe of ``make_inputs`` drawn on ``device`` with torch's seeded
+    generator: the same distributions and structure, not the same bits. For
+    timing runs at sizes where drawing on the host takes minutes (the 128K
+    sweep, the 256K layer); parity tests use ``make_inputs``. ``r``
+    overrides the workload's predictor rank."""
+    H = w.H if heads is None else heads
+    S, d = w.S, w.d
+    r = w.r if r is None else r
+    gen = torch.Generator(device=device)
+    gen.manual_seed(20250000 + w.cfg if seed is None else seed)
+    host = np.random.default_rng(20250000 + w.cfg if seed is None else seed)
+    P = torch.from_numpy(sinusoid_3d(w.T, w.Y, w.X, d)).to(device=device, dtype=torch.float32)
+    kw = dict(device=device, dtype=torch.float32, generator=gen)
+    Q = torch.empty((H, S, d), dtype=torch.bfloat16, device=device)
+    K = torch.empty_like(Q)
+    V = torch.empty_like(Q)
+    Wq = torch.empty((H, d, r), dtype=torch.bfloat16, device=device)
+    Wk = torch.empty_like(Wq)
+    qs = np.empty(H)
+    for h in range(H):
+        Gh = torch.randn((d, d), **kw) / math.sqrt(d)
+        Wq[h] = (torch.randn((d, r), **kw) / math.sqrt(d)).to(torch.bfloat16)
+        Wk[h] = (torch.randn((d, r), **kw) / math.sqrt(d)).to(torch.bfloat16)
+        qs[h] = w.qscale[1] if w.qscale[0] == "const" else host.uniform(w.qscale[1], w.qscale[2])
+        base = P @ Gh
+        Q[h] = (qs[h] * (base + 0.5 * torch.randn((S, d), **kw))).to(torch.bfloat16)
+        K[h] = (base + 0.5 * torch.randn((S, d), **kw)).to(torch.bfloat16)
+        V[h] = (base + 0.5 * torch.randn((S, d), **kw)).to(torch.bfloat16)
+    want = w.backward if with_grad_out is None else with_grad_out
+    dO = torch.randn((H, S, d), **kw).to(torch.bfloat16) if want else None
+    return dict(Q=Q, K=K, V=V, Wq=Wq, Wk=Wk, dO=dO, qscale=qs)

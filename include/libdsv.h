@@ -26,7 +26,7 @@
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*).
  *    Argument errors are returned synchronously before anything is launched.
  *    Launch failures return DSV_ERR_CUDA. Conditions found on the device
- *    (a wait that ran out, a candidate buffer overflow) are written to the caller's device word `dev_status`
+ *    (a wait that ran out) are written to the caller's device word `dev_status`
  *    (int32, zero it before the call; libdsv only ever raises it), which the
  *    caller reads after synchronising (dsv_read_status does both).
  *  - Supported sizes: d in {64, 128}; r in {16, 32, 64}; G = gt*gy*gx in
@@ -50,7 +50,8 @@ typedef enum {
   DSV_ERR_CUDA = 4,          /* a CUDA launch or API call failed */
   DSV_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out */
   DSV_ERR_OVERFLOW = 6,      /* reserved (no current call raises it) */
-  DSV_ERR_CANDIDATES = 7     /* device: a top-k boundary bin exceeded its candidate buffer */
+  DSV_ERR_CANDIDATES = 7     /* device: a top-k row failed its internal consistency check (it did not come
+                                out with exactly k keys); no valid input raises it */
 } dsv_status;
 
 /* Problem shape: B batches x H heads, latent grid T x Y x X, head dim d. */
@@ -84,10 +85,14 @@ dsv_status dsv_read_status(const int32_t* dev_status, int32_t* host_out, void* s
  *   idx row (p, g) = the k_p keys j with the largest s_gj, ties to the lower
  *   j, written in ascending order.
  * Problems with idx_offset[p] < 0 are skipped (dense heads).
+ * The selection is exact for every input with finite scores, however the
+ * scores cluster: the k-th score's histogram bin is narrowed by radix
+ * rounds over the score's bits until it holds at most 4096 keys (sorted) or
+ * a single value (taken lowest key first).
  * k_per_head, idx_offset: HOST arrays of B*H entries (read during the call).
- * Device errors: DSV_ERR_CANDIDATES if a row's boundary bin held more
- * candidates than the workspace provides for (the row is then left
- * incomplete); DSV_ERR_TIMEOUT on a stalled pipeline.
+ * Device errors: DSV_ERR_TIMEOUT on a stalled pipeline (the rows are then
+ * incomplete); DSV_ERR_CANDIDATES only if an internal consistency check
+ * fails.
  * ---------------------------------------------------------------------- */
 size_t dsv_lowrank_topk_workspace_size(dsv_shape shape, int32_t r, dsv_group group);
 dsv_status dsv_lowrank_topk(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr, dsv_shape shape,
@@ -112,6 +117,9 @@ dsv_status dsv_lowrank_topk(const void* Q, const void* K, const void* Wq_lr, con
  *    rejected with DSV_ERR_WORKSPACE before anything is launched.
  *  - The first call on a device looks up the array's device address (and
  *    loads the module there); make that first call before any stream capture.
+ *    The address is kept per device and CUDA context: after a device reset
+ *    (a new context) the next call looks it up again, so it too should come
+ *    before any capture.
  *  - Every call uses the same array. The call clears what must start at zero
  *    itself, but calls whose work overlaps on the GPU (different streams, or
  *    several host threads) race on it: serialise them.

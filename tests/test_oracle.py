@@ -358,6 +358,21 @@ def test_plan_gpus_hand_example():
     assert gpu_of == [2, 0, 1, 2, 0, 1] and load == [10, 11, 12]
 
 
+def test_best_makespan_hand_examples():
+    """Optima worked out by hand. [3, 3, 2, 2, 2] on 2 GPUs: the total is 12,
+    so 6 is a lower bound, reached by {3, 3} | {2, 2, 2} (longest processing
+    time first only reaches 7). [5, 4, 3, 3, 3]: {5, 4} | {3, 3, 3} = 9 = 18/2.
+    [10, 1, 1, 1]: alone, 10 is the largest cost and {10} | {1, 1, 1} reaches
+    it; with at most two heads per GPU the best is {10, 1} | {1, 1} = 11."""
+    assert ora.best_makespan([3, 3, 2, 2, 2], 2, False) == 6
+    assert ora.best_makespan([3, 3, 2, 2, 2], 2, True) == 6
+    assert max(ora.plan_gpus([3, 3, 2, 2, 2], 2, False)[1]) == 7
+    assert ora.best_makespan([5, 4, 3, 3, 3], 2, True) == 9
+    assert ora.best_makespan([10, 1, 1, 1], 2, False) == 10
+    assert ora.best_makespan([10, 1, 1, 1], 2, True) == 11
+    assert ora.best_makespan([7], 3, True) == 7
+
+
 def test_plan_gpus_within_graham_bound_of_brute_force():
     """Longest-processing-time first is within (4/3 - 1/(3N)) of the best
     makespan (Graham 1969); with equal head counts the result is still a valid
