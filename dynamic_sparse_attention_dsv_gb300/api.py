@@ -152,6 +152,10 @@ def coverage(Q, K, Wq, Wk, grid, group, scale: Optional[float] = None, mass: flo
     return k_cov, curve
 
 
+def coverage_workspace_size(x, grid, group, r) -> int:
+    return int(N.load().dsv_coverage_workspace_size(make_shape(x, grid), int(r), make_group(group)))
+
+
 def coverage_topk_workspace_size(x, grid, group, r) -> int:
     return int(N.load().dsv_coverage_topk_workspace_size(make_shape(x, grid), int(r), make_group(group)))
 

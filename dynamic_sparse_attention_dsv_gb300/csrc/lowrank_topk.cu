@@ -53,7 +53,7 @@ constexpr int kMaxChunks = 64;     // key chunks per row
 // chain costs its ramp-up and tail.
 constexpr size_t kProjBudget = 1ull << 30;
 
-enum SelMode { kMinMax = 0, kHist = 1, kCollect = 2, kRefine = 3, kCov = 4 };
+enum SelMode { kMinMax = 0, kHist = 1, kCollect = 2, kRefine = 3, kCov = 4, kCovFine = 5 };
 
 // Per-row state of the boundary interval after each bracket step.
 enum RowState { kRowCollect = 0, kRowRefine = 1, kRowTied = 2 };
@@ -97,6 +97,7 @@ struct SelParams {
   uint64_t* cand;        // [n][g_pad][kCandCap]
   uint32_t* sel_bits;    // [n][g_pad][n_tiles][4] keys scoring >= bhi, 32 keys per word
   uint32_t* eq_bits;     // same layout: keys inside a single-valued interval
+  const int32_t* cwin;   // COV_FINE: [n][g_pad][2] window of coarse bins [wa, wb]
   int32_t* status;
 };
 
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     // COLLECT stages up to kStage candidates per (row, half) in the unused histogram area
     constexpr int kStage = C::kHistBytes / (256 * 8);
     uint64_t* stage = reinterpret_cast<uint64_t*>(sHist) + (size_t)(half * 128 + row) * kStage;
-    constexpr int NB = (MODE == kCov) ? C::kCovBins : C::kHistBins;
+    constexpr int NB = (MODE == kCov || MODE == kCovFine) ? C::kCovBins : C::kHistBins;
     const uint32_t hist_base = smem_u32(sHist);
 
     // COLLECT: scores >= t_above are selected, [t_in, t_above) is the boundary
@@ -290,13 +291,26 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       if (MODE == kRefine && state != kRowRefine) owid = 0;   // this row takes no part
     }
     float w2 = 0.f;   // COV: bin width in log2 units
-    if constexpr (MODE == kCov) {
+    // COV_FINE: the row's window of coarse bins, NB fine bins over it (fine
+    // coordinate (x - wa) * fscale, fine width fw2 in log2 units)
+    int wa = NB, wb = -1;
+    float fscale = 0.f, fw2 = 0.f;
+    if constexpr (MODE == kCov || MODE == kCovFine) {
       cmax = ord2f(prm.mmax[rid]);
       const float range = prm.scale * (cmax - ord2f(prm.mmin[rid]));
       inv_w = range > 0.f ? (float)NB / range : 0.f;
       w2 = range > 0.f ? range / (float)NB * 1.4426950408889634f : 0.f;
     }
-    if constexpr (MODE == kHist || MODE == kCov || MODE == kRefine) {
+    if constexpr (MODE == kCovFine) {
+      if (valid) {
+        wa = prm.cwin[2 * (size_t)rid];
+        wb = prm.cwin[2 * (size_t)rid + 1];
+      }
+      const int nw = wb - wa + 1;
+      fscale = nw > 0 ? (float)NB / (float)nw : 0.f;
+      fw2 = nw > 0 ? w2 * (float)nw / (float)NB : 0.f;
+    }
+    if constexpr (MODE == kHist || MODE == kCov || MODE == kRefine || MODE == kCovFine) {
       // zero this CTA's private histograms ([bin][row] counts, then masses)
       uint32_t* h = reinterpret_cast<uint32_t*>(sHist);
       for (int i = tid; i < C::kHistBytes / 4; i += 256) h[i] = 0;
@@ -356,6 +370,20 @@ __global__ void __launch_bounds__(kSelThreads, 2)
             const uint32_t qf = __float_as_uint(fmaf(q, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
             red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
             red_smem_u32(hist_base + (uint32_t)(NB * 128 + bin * 128 + row) * 4u, qf);
+          } else if constexpr (MODE == kCovFine) {
+            // the COV pass's arithmetic bit for bit, so window membership
+            // agrees with the coarse bins
+            const float u = __fmul_rn(prm.scale, __fsub_rn(cmax, s));
+            const float x = __fmul_rn(u, inv_w);
+            const int bin = bin_of(bin_round(x), NB);
+            if (bin >= wa && bin <= wb) {
+              const float y = (x - (float)wa) * fscale;
+              const int fb = min(NB - 1, max(0, (int)y));
+              const float q = ex2_fast(((float)fb - y) * fw2);   // exp(fb fw - u'), in (exp(-fw), 1]
+              const uint32_t qf = __float_as_uint(fmaf(q, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
+              red_smem_u32(hist_base + (uint32_t)(fb * 128 + row) * 4u, 1u);
+              red_smem_u32(hist_base + (uint32_t)(NB * 128 + fb * 128 + row) * 4u, qf);
+            }
           }
         }
         if constexpr (MODE == kCollect) {
@@ -424,14 +452,17 @@ __global__ void __launch_bounds__(kSelThreads, 2)
         const uint32_t v = h[bin * 128 + row];
         if (v) atomicAdd(prm.hist + ((size_t)lp * NB + bin) * prm.g_pad + g, v);
       }
-    } else if constexpr (MODE == kCov) {
+    } else if constexpr (MODE == kCov || MODE == kCovFine) {
       epi_barrier();
       const uint32_t* h = reinterpret_cast<const uint32_t*>(sHist);
       const uint32_t* m = h + NB * 128;
+      // a bin's probabilities were summed relative to its upper edge
+      const float edge0 = MODE == kCovFine ? (float)wa * w2 : 0.f;
+      const float step = MODE == kCovFine ? fw2 : w2;
       for (int bin = half * (NB / 2); bin < (half + 1) * (NB / 2); ++bin) {
         const size_t o = (((size_t)lp * prm.n_chunks + chunk) * NB + bin) * prm.g_pad + g;
         prm.hist[o] = h[bin * 128 + row];
-        prm.mass[o] = (float)m[bin * 128 + row] * (1.f / 65536.f) * ex2_fast(-(float)bin * w2);
+        prm.mass[o] = (float)m[bin * 128 + row] * (1.f / 65536.f) * ex2_fast(-(edge0 + (float)bin * step));
       }
     }
   }
@@ -895,10 +926,30 @@ __global__ void k_fill_all(int32_t* idx, int64_t off, int S, int64_t total) {
 }
 
 // ---------------------------------------------------------------------------
-// Coverage reduce, in three steps:
+// Coverage reduce. The COV pass gives every group row a coarse table: per
+// bin of log-probability below the row maximum (width w), the count of keys
+// and their exact total probability. Then:
 //   k_cov_merge   (group, bin) totals over key chunks, one thread per pair
-//   k_cov_scan    per group: cumulative counts and normalised masses over bins
-//   k_cov_eval/k_cov_pick  two wide rounds locating the smallest k with C(k) >= mass
+//   k_cov_scan    per group: cumulative counts and normalised masses, the
+//                 bin width and 1 / (total probability)
+//   bounds search the smallest k whose upper bound on C reaches the target
+//                 (k_lo) and the smallest whose lower bound does (k_hi):
+//                 within a bin the keys' probabilities lie between the bin's
+//                 edge values, which bounds any j of them; k_cov is in
+//                 [k_lo, k_hi]
+//   k_cov_window  per group, the coarse bins holding its ranks k_lo..k_hi
+//   COV_FINE      the window's keys again, in as many fine bins as coarse
+//                 ones (count and exact probability), then merged and scanned
+//   final search  k_cov in [k_lo, k_hi] on the combined table (coarse bins
+//                 outside the window, fine bins inside), interpolating inside
+//                 a bin as if its log-probabilities were evenly spread; the
+//                 fine bins bring that error down by their count.
+// Every search is a sequence of wide rounds (k_cov_eval / k_cov_pick): each
+// evaluates C at up to kCovPoints values of k spread evenly over the current
+// interval and keeps the sub-interval where C first reaches the target; once
+// the interval holds at most kCovPoints values all are evaluated. Evaluation
+// blocks take kCovGroupsPerBlock groups each and their partial sums are
+// added in block order, so the result does not depend on scheduling.
 __global__ void k_cov_merge(const uint32_t* __restrict__ cnt, const float* __restrict__ mass, int nb, int n_chunks,
                             int g_pad, int n_groups, int32_t* cum_cnt, double* cum_mass) {
   const int lp = blockIdx.z, b = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
@@ -915,9 +966,13 @@ __global__ void k_cov_merge(const uint32_t* __restrict__ cnt, const float* __res
   cum_mass[rid * nb + b] = m;
 }
 
-// One warp per group: lane l owns bins [4l, 4l+4) of the (at most 128) bins.
+// One warp per group: lane l owns bins [l*per, l*per + per) of the (at most
+// 128) bins. Cumulative counts; masses cumulated and divided by `norm_total`
+// (the group's total when null), scaled by `norm_scale` (a per-group factor,
+// 1 when null). `width`/`zinv` (optional): the bin width in natural-log units
+// and 1 / total probability.
 __global__ void k_cov_scan(const uint32_t* mmax, const uint32_t* mmin, int nb, int g_pad, int n_groups, float scale,
-                           int32_t* cum_cnt, double* cum_mass, float* width) {
+                           int32_t* cum_cnt, double* cum_mass, float* width, float* zinv, const double* norm_scale) {
   const int lp = blockIdx.y, lane = threadIdx.x & 31;
   const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (g >= n_groups) return;
@@ -946,7 +1001,8 @@ __global__ void k_cov_scan(const uint32_t* mmax, const uint32_t* mmin, int nb, i
     }
   }
   const double total = __shfl_sync(0xffffffffu, mi, 31);
-  const double inv = total > 0.0 ? 1.0 / total : 0.0;
+  const double f = norm_scale ? norm_scale[rid] : 1.0;
+  const double inv = total > 0.0 ? f / total : 0.0;
   int crun = ci - csum;
   double mrun = mi - msum;
   for (int e = 0; e < per; ++e) {
@@ -955,36 +1011,70 @@ __global__ void k_cov_scan(const uint32_t* mmax, const uint32_t* mmin, int nb, i
     cc[lane * per + e] = crun;
     cm[lane * per + e] = mrun * inv;
   }
-  if (lane == 0) width[rid] = scale * (ord2f(mmax[rid]) - ord2f(mmin[rid])) / (float)nb;
+  if (lane == 0 && width) width[rid] = scale * (ord2f(mmax[rid]) - ord2f(mmin[rid])) / (float)nb;
+  if (lane == 0 && zinv) zinv[rid] = total > 0.0 ? (float)(1.0 / total) : 0.f;
 }
 
-// Smallest k with C(k) >= target, in wide rounds. Each round evaluates C at
-// up to kCovPoints values of k spread evenly over the current interval
-// [lo, hi] (initially [1, S]) and keeps the sub-interval where C first
-// reaches the target; once the interval holds at most kCovPoints values,
-// every one of them is evaluated and the smallest qualifying k is the answer.
-// Each evaluation block takes kCovGroupsPerBlock groups and all points;
-// per-block partial sums are added in block order, so the result does not
-// depend on scheduling.
 constexpr int kCovPoints = 1024;
 constexpr int kCovGroupsPerBlock = 16;
 
-// C's per-group term: mass of the group's k most probable keys, interpolated
-// inside the boundary bin assuming evenly spread log-probabilities. cc / cm
-// are the group's cumulative counts and masses over its nb bins.
-__device__ __forceinline__ float cov_group_mass(const int32_t* cc, const float* cm, int nb, float dw, int k) {
-  int lo = 0, hi = nb - 1;  // first bin with cumulative count >= k
+enum CovEval { kCovBoundLo = 0, kCovBoundHi = 1, kCovCombined = 2 };
+
+// First index of a cumulative table (n entries) whose count reaches k.
+__device__ __forceinline__ int first_reaching(const int32_t* cc, int n, int k) {
+  int lo = 0, hi = n - 1;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (cc[mid] >= k) hi = mid; else lo = mid + 1;
+    if (cc[mid] >= k) hi = mid;
+    else lo = mid + 1;
   }
-  const int pc = lo > 0 ? cc[lo - 1] : 0;
-  const float pm = lo > 0 ? cm[lo - 1] : 0.f;
-  const int n = cc[lo] - pc;
-  const float mb = cm[lo] - pm;
-  const float f = n > 0 ? (float)(k - pc) / (float)n : 1.f;
-  const float part = dw > 1e-6f ? mb * (1.f - __expf(-f * dw)) / (1.f - __expf(-dw)) : mb * f;
-  return pm + part;
+  return lo;
+}
+
+// Mass of j of a bin's n keys (bin mass mb, log-probabilities spread evenly
+// over a width dw).
+__device__ __forceinline__ float spread_part(float mb, int j, int n, float dw) {
+  const float f = n > 0 ? (float)j / (float)n : 1.f;
+  return dw > 1e-6f ? mb * (1.f - __expf(-f * dw)) / (1.f - __expf(-dw)) : mb * f;
+}
+
+// A group's tables as staged by k_cov_eval: coarse cumulative counts/masses
+// over nb bins of width w; the window [wa, wb] of coarse bins and its fine
+// cumulative counts/masses over nb bins (masses as shares of the group's
+// total, like the coarse ones).
+struct CovTables {
+  const int32_t* cc;
+  const float* cm;
+  const int32_t* fc;
+  const float* fm;
+  int nb, wa, wb;
+  float w, zinv;
+};
+
+// C's per-group term at k: the mass of the group's k most probable keys, as
+// a lower or upper bound from the coarse bins, or interpolated on the
+// combined table.
+__device__ float cov_group_mass(const CovTables& t, int k, int mode) {
+  const int b = first_reaching(t.cc, t.nb, k);
+  const int pc = b > 0 ? t.cc[b - 1] : 0;
+  const float pm = b > 0 ? t.cm[b - 1] : 0.f;
+  const int n = t.cc[b] - pc, j = k - pc;
+  const float mb = t.cm[b] - pm;
+  if (mode != kCovCombined) {
+    // every key of bin b has a probability between its edges' values
+    const float pmax = __expf(-(float)b * t.w) * t.zinv, pmin = __expf(-(float)(b + 1) * t.w) * t.zinv;
+    if (mode == kCovBoundLo) return pm + fmaxf((float)j * pmin, mb - (float)(n - j) * pmax);
+    return pm + fminf((float)j * pmax, mb - (float)(n - j) * pmin);
+  }
+  if (b < t.wa || b > t.wb) return pm + spread_part(mb, j, n, t.w);
+  const int base_c = t.wa > 0 ? t.cc[t.wa - 1] : 0;
+  const float base_m = t.wa > 0 ? t.cm[t.wa - 1] : 0.f;
+  const int kk = k - base_c;
+  const int f = first_reaching(t.fc, t.nb, kk);
+  const int fpc = f > 0 ? t.fc[f - 1] : 0;
+  const float fpm = f > 0 ? t.fm[f - 1] : 0.f;
+  const float fw = t.w * (float)(t.wb - t.wa + 1) / (float)t.nb;
+  return base_m + fpm + spread_part(t.fm[f] - fpm, kk - fpc, t.fc[f] - fpc, fw);
 }
 
 // The k of point p for interval [lo, hi] (search), or the curve's point p
@@ -996,55 +1086,68 @@ __device__ __forceinline__ int cov_point(bool curve, int lo, int hi, int p, int 
   return (int)(lo - 1 + ((int64_t)(p + 1) * span + kCovPoints - 1) / kCovPoints);
 }
 
-// range[2*lp .. 2*lp+1] holds the current interval; round 0 ignores it and
-// starts from [1, S].
-__device__ __forceinline__ void cov_interval(int round, const int32_t* range, int lp, int S, int& lo, int& hi) {
-  lo = round == 0 ? 1 : range[2 * lp];
-  hi = round == 0 ? S : range[2 * lp + 1];
+// range[2*lp .. 2*lp+1]: [lo, hi] of a search, or of the fine window when
+// fine tables are read.
+__global__ void k_cov_range_init(int32_t* range, const int32_t* from_lo, const int32_t* from_hi, int S, int n) {
+  const int lp = blockIdx.x * blockDim.x + threadIdx.x;
+  if (lp >= n) return;
+  range[2 * lp] = from_lo ? from_lo[lp] : 1;
+  range[2 * lp + 1] = from_hi ? from_hi[lp] : S;
 }
 
 // One thread per point; the block's kCovGroupsPerBlock group tables are
-// staged in shared memory first.
-__global__ void __launch_bounds__(kCovPoints) k_cov_eval(int round, bool curve, int nb, int g_pad, int n_groups,
+// staged in shared memory first. fine_cnt == nullptr: coarse tables only.
+__global__ void __launch_bounds__(kCovPoints) k_cov_eval(int mode, bool curve, int nb, int g_pad, int n_groups,
                                                          int S, const int32_t* cum_cnt, const double* cum_mass,
-                                                         const float* width, const int32_t* range, int n_curve,
-                                                         double* partial) {
+                                                         const float* width, const float* zinv, const int32_t* win,
+                                                         const int32_t* fine_cnt, const double* fine_mass,
+                                                         const int32_t* range, int n_curve, double* partial) {
   static_assert(SelCfg<32>::kCovBins <= 128 && SelCfg<64>::kCovBins <= 128, "coverage tables hold 128 bins");
   static_assert(SelCfg<32>::kCovBins * 128 * 8 <= SelCfg<32>::kHistBytes &&
                     SelCfg<64>::kCovBins * 128 * 8 <= SelCfg<64>::kHistBytes,
                 "COV counts and sums fit the histogram area");
-  __shared__ int32_t s_cc[kCovGroupsPerBlock * 128];
-  __shared__ float s_cm[kCovGroupsPerBlock * 128];
-  __shared__ float s_w[kCovGroupsPerBlock];
+  __shared__ int32_t s_cc[kCovGroupsPerBlock * 128], s_fc[kCovGroupsPerBlock * 128];
+  __shared__ float s_cm[kCovGroupsPerBlock * 128], s_fm[kCovGroupsPerBlock * 128];
+  __shared__ float s_w[kCovGroupsPerBlock], s_z[kCovGroupsPerBlock];
+  __shared__ int s_wa[kCovGroupsPerBlock], s_wb[kCovGroupsPerBlock];
   const int lp = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x, p = threadIdx.x;
   const int g0 = blk * kCovGroupsPerBlock, ng = min(n_groups - g0, kCovGroupsPerBlock);
   const size_t base = (size_t)lp * g_pad + g0;
   for (int i = p; i < ng * nb; i += blockDim.x) {
     s_cc[i] = cum_cnt[base * nb + i];
     s_cm[i] = (float)cum_mass[base * nb + i];
+    s_fc[i] = fine_cnt ? fine_cnt[base * nb + i] : 0;
+    s_fm[i] = fine_cnt ? (float)fine_mass[base * nb + i] : 0.f;
   }
-  if (p < ng) s_w[p] = width[base + p];
+  if (p < ng) {
+    s_w[p] = width[base + p];
+    s_z[p] = zinv[base + p];
+    s_wa[p] = fine_cnt ? win[2 * (base + p)] : nb;   // no window: every bin is coarse
+    s_wb[p] = fine_cnt ? win[2 * (base + p) + 1] : -1;
+  }
   __syncthreads();
-  int lo, hi;
-  cov_interval(round, range, lp, S, lo, hi);
-  const int k = cov_point(curve, lo, hi, p, S, n_curve);
+  const int k = cov_point(curve, range[2 * lp], range[2 * lp + 1], p, S, n_curve);
   double acc = 0.0;
   if (k >= 1)
-    for (int g = 0; g < ng; ++g) acc += (double)cov_group_mass(s_cc + g * nb, s_cm + g * nb, nb, s_w[g], k);
+    for (int g = 0; g < ng; ++g) {
+      const CovTables t{s_cc + g * nb, s_cm + g * nb, s_fc + g * nb, s_fm + g * nb, nb, s_wa[g], s_wb[g], s_w[g],
+                        s_z[g]};
+      acc += (double)cov_group_mass(t, k, mode);
+    }
   partial[((size_t)lp * nblk + blk) * kCovPoints + p] = acc;
 }
 
 // Sums the partials of each point in block order. Search: narrow range[lp]
 // to the sub-interval where C first reaches the target, or, when every k of
-// the interval was evaluated, write k_cov. Curve: write the curve.
-__global__ void __launch_bounds__(1024) k_cov_pick(int round, bool curve, int nblk, int n_groups, int S,
-                                                   float target, const double* partial, int32_t* range,
-                                                   int32_t* k_cov, float* curve_out, int n_curve,
+// the interval was evaluated, write the answer to out[out_idx]. Curve: write
+// the curve.
+__global__ void __launch_bounds__(1024) k_cov_pick(bool curve, int nblk, int n_groups, int S, float target,
+                                                   const double* partial, int32_t* range, int32_t* out,
+                                                   bool out_by_problem, float* curve_out, int n_curve,
                                                    const ProblemTable tab) {
   __shared__ int first;
   const int lp = blockIdx.x, p = threadIdx.x;
-  int lo, hi;
-  cov_interval(round, range, lp, S, lo, hi);
+  const int lo = range[2 * lp], hi = range[2 * lp + 1];
   if (p == 0) first = kCovPoints;
   __syncthreads();  // every thread has read range before thread 0 rewrites it
   const int k = cov_point(curve, lo, hi, p, S, n_curve);
@@ -1061,12 +1164,29 @@ __global__ void __launch_bounds__(1024) k_cov_pick(int round, bool curve, int nb
   const int64_t span = (int64_t)hi - lo + 1;
   if (span <= kCovPoints) {
     // C(S) = 1 >= target up to rounding; with no qualifying point keep hi
-    k_cov[tab.p[lp]] = first < kCovPoints ? lo + first : hi;
+    out[out_by_problem ? tab.p[lp] : lp] = first < kCovPoints ? lo + first : hi;
     return;
   }
   const int f = first < kCovPoints ? first : kCovPoints - 1;  // answer in (k_{f-1}, k_f]
   range[2 * lp] = f > 0 ? cov_point(false, lo, hi, f - 1, S, 0) + 1 : lo;
   range[2 * lp + 1] = cov_point(false, lo, hi, f, S, 0);
+}
+
+// Per group: the coarse bins [wa, wb] holding its ranks k_lo .. k_hi, and
+// the factor that makes the fine masses (shares of the window's own total)
+// shares of the group's total.
+__global__ void k_cov_window(int nb, int g_pad, int n_groups, const int32_t* cum_cnt, const double* cum_mass,
+                             const int32_t* k_lo, const int32_t* k_hi, int32_t* win, double* fine_scale) {
+  const int lp = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n_groups) return;
+  const size_t rid = (size_t)lp * g_pad + g;
+  const int32_t* cc = cum_cnt + rid * nb;
+  const double* cm = cum_mass + rid * nb;
+  const int wa = first_reaching(cc, nb, k_lo[lp]);
+  const int wb = first_reaching(cc, nb, k_hi[lp]);
+  win[2 * rid] = wa;
+  win[2 * rid + 1] = wb;
+  fine_scale[rid] = cm[wb] - (wa > 0 ? cm[wa - 1] : 0.0);
 }
 
 // ---------------------------------------------------------------------------
@@ -1148,7 +1268,9 @@ struct TopkWs {
   uint64_t* cand;
   int32_t* cum_cnt;
   double* cum_mass;
-  float* width;
+  float *width, *zinv;
+  int32_t *fine_cnt, *cov_win, *kwin_lo, *kwin_hi;
+  double *fine_mass, *fine_scale;
   double* cov_partial;
   int32_t* cov_range;
 };
@@ -1191,6 +1313,13 @@ static size_t carve(void* base, const TopkPlan& pl, int mode, TopkWs* w) {
     w->cum_cnt = c.take<int32_t>(pc * gp * pl.cov_bins);
     w->cum_mass = c.take<double>(pc * gp * pl.cov_bins);
     w->width = c.take<float>(pc * gp);
+    w->zinv = c.take<float>(pc * gp);
+    w->fine_cnt = c.take<int32_t>(pc * gp * pl.cov_bins);
+    w->fine_mass = c.take<double>(pc * gp * pl.cov_bins);
+    w->fine_scale = c.take<double>(pc * gp);
+    w->cov_win = c.take<int32_t>(pc * gp * 2);
+    w->kwin_lo = c.take<int32_t>(pc);
+    w->kwin_hi = c.take<int32_t>(pc);
     w->cov_partial = c.take<double>(pc * ((gp + kCovGroupsPerBlock - 1) / kCovGroupsPerBlock) * kCovPoints);
     w->cov_range = c.take<int32_t>(pc * 2);
   }
@@ -1352,41 +1481,62 @@ static cudaError_t cov_passes(const TopkPlan& pl, const TopkWs& w, const Problem
   prm.n_chunks = n_chunks;
   prm.chunk_tiles = chunk_tiles;
   prm.n_tiles = pl.n_tiles;
+  prm.n_gt = pl.n_gt;
   prm.scale = scale;
   prm.mmax = w.mmax;
   prm.mmin = w.mmin;
   prm.hist = w.cov_hist;
   prm.mass = w.mass;
+  prm.cwin = w.cov_win;
   prm.status = status;
   const dim3 grid(pl.n_gt, n_chunks, n);
   const size_t rows = (size_t)n * pl.g_pad;
+  const int nb = pl.cov_bins, ng = pl.geo.n_groups, S = pl.geo.S;
   if (minmax) {
     if (cudaMemsetAsync(w.mmax, 0, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
     if (cudaMemsetAsync(w.mmin, 0xFF, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
     if (select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
   }
+  // coarse tables
   if (select_pass<kCov>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
-  const int gb = (pl.geo.n_groups + 127) / 128;
-  k_cov_merge<<<dim3(gb, pl.cov_bins, n), 128, 0, st>>>(w.cov_hist, w.mass, pl.cov_bins, n_chunks, pl.g_pad,
-                                                         pl.geo.n_groups, w.cum_cnt, w.cum_mass);
-  k_cov_scan<<<dim3((pl.geo.n_groups + 7) / 8, n), 256, 0, st>>>(w.mmax, w.mmin, pl.cov_bins, pl.g_pad,
-                                                                  pl.geo.n_groups, scale, w.cum_cnt, w.cum_mass,
-                                                                  w.width);
-  const int nblk = (pl.geo.n_groups + kCovGroupsPerBlock - 1) / kCovGroupsPerBlock;
+  const dim3 mgrid((ng + 127) / 128, nb, n), sgrid((ng + 7) / 8, n), wgrid((ng + 127) / 128, n);
+  k_cov_merge<<<mgrid, 128, 0, st>>>(w.cov_hist, w.mass, nb, n_chunks, pl.g_pad, ng, w.cum_cnt, w.cum_mass);
+  k_cov_scan<<<sgrid, 256, 0, st>>>(w.mmax, w.mmin, nb, pl.g_pad, ng, scale, w.cum_cnt, w.cum_mass, w.width, w.zinv,
+                                    nullptr);
+  const int nblk = (ng + kCovGroupsPerBlock - 1) / kCovGroupsPerBlock;
   // rounds: the interval shrinks from S values to at most ceil(span / kCovPoints) per round
   int rounds = 1;
-  for (int64_t span = pl.geo.S; span > kCovPoints; span = (span + kCovPoints - 1) / kCovPoints) ++rounds;
-  for (int round = 0; round < rounds; ++round) {
-    k_cov_eval<<<dim3(nblk, n), kCovPoints, 0, st>>>(round, false, pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.geo.S,
-                                               w.cum_cnt, w.cum_mass, w.width, w.cov_range, 0, w.cov_partial);
-    k_cov_pick<<<n, kCovPoints, 0, st>>>(round, false, nblk, pl.geo.n_groups, pl.geo.S, mass, w.cov_partial,
-                                          w.cov_range, k_cov, nullptr, 0, tab);
-  }
+  for (int64_t span = S; span > kCovPoints; span = (span + kCovPoints - 1) / kCovPoints) ++rounds;
+  auto search = [&](int mode, const int32_t* fc, const double* fm, int32_t* out, bool by_problem) {
+    for (int r = 0; r < rounds; ++r) {
+      k_cov_eval<<<dim3(nblk, n), kCovPoints, 0, st>>>(mode, false, nb, pl.g_pad, ng, S, w.cum_cnt, w.cum_mass,
+                                                       w.width, w.zinv, w.cov_win, fc, fm, w.cov_range, 0,
+                                                       w.cov_partial);
+      k_cov_pick<<<n, kCovPoints, 0, st>>>(false, nblk, ng, S, mass, w.cov_partial, w.cov_range, out, by_problem,
+                                            nullptr, 0, tab);
+    }
+  };
+  // certified interval [k_lo, k_hi] from the bin-edge bounds
+  k_cov_range_init<<<1, 256, 0, st>>>(w.cov_range, nullptr, nullptr, S, n);
+  search(kCovBoundHi, nullptr, nullptr, w.kwin_lo, false);
+  k_cov_range_init<<<1, 256, 0, st>>>(w.cov_range, nullptr, nullptr, S, n);
+  search(kCovBoundLo, nullptr, nullptr, w.kwin_hi, false);
+  // fine tables over each group's window of coarse bins
+  k_cov_window<<<wgrid, 128, 0, st>>>(nb, pl.g_pad, ng, w.cum_cnt, w.cum_mass, w.kwin_lo, w.kwin_hi, w.cov_win,
+                                      w.fine_scale);
+  if (select_pass<kCovFine>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  k_cov_merge<<<mgrid, 128, 0, st>>>(w.cov_hist, w.mass, nb, n_chunks, pl.g_pad, ng, w.fine_cnt, w.fine_mass);
+  k_cov_scan<<<sgrid, 256, 0, st>>>(w.mmax, w.mmin, nb, pl.g_pad, ng, scale, w.fine_cnt, w.fine_mass, nullptr,
+                                    nullptr, w.fine_scale);
+  // k_cov within [k_lo, k_hi] on the combined tables
+  k_cov_range_init<<<1, 256, 0, st>>>(w.cov_range, w.kwin_lo, w.kwin_hi, S, n);
+  search(kCovCombined, w.fine_cnt, w.fine_mass, k_cov, true);
   if (curve) {
-    k_cov_eval<<<dim3(nblk, n), kCovPoints, 0, st>>>(0, true, pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.geo.S,
-                                               w.cum_cnt, w.cum_mass, w.width, w.cov_range, n_curve, w.cov_partial);
-    k_cov_pick<<<n, kCovPoints, 0, st>>>(0, true, nblk, pl.geo.n_groups, pl.geo.S, mass, w.cov_partial,
-                                          w.cov_range, k_cov, curve, n_curve, tab);
+    k_cov_eval<<<dim3(nblk, n), kCovPoints, 0, st>>>(kCovCombined, true, nb, pl.g_pad, ng, S, w.cum_cnt,
+                                                     w.cum_mass, w.width, w.zinv, w.cov_win, w.fine_cnt,
+                                                     w.fine_mass, w.cov_range, n_curve, w.cov_partial);
+    k_cov_pick<<<n, kCovPoints, 0, st>>>(true, nblk, ng, S, mass, w.cov_partial, w.cov_range, k_cov, true, curve,
+                                          n_curve, tab);
   }
   return cudaGetLastError();
 }

@@ -166,6 +166,11 @@ def make_clustered_inputs(T: int, Y: int, X: int, d: int, r: int, H: int, mode: 
     Channels past 1 hold small seeded noise. Every a_j + c_h b_j is exact in
     fp32 (at most 21 significant bits), so any correct fp32 computation of
     the predictor scores gives them exactly.
+
+    Two peaked shapes for the coverage search set b = 0: "two_level" puts
+    every 32nd key at a = 32 and the rest at a = 0, besides a_1 = -64 (so the
+    lower level sits inside the score range, not at its edge); "dominant"
+    puts key 0 at a = 256 and every other key at a = 0.
     Returns Q, K, V, Wq, Wk as CPU bf16 tensors ([H,S,d] and [H,d,r]) and
     the per-head c (float64 [H]).
     """
@@ -186,6 +191,15 @@ def make_clustered_inputs(T: int, Y: int, X: int, d: int, r: int, H: int, mode: 
         K[:, :, 1] = np.round(rng.uniform(-1.0, 1.0, (H, S)) * 4096.0) / 4096.0
     elif mode == "ties":
         K[:, :, 1] = rng.choice(np.array([-1.0, -0.5, 0.0, 0.5, 1.0]), (H, S))
+    elif mode == "two_level":
+        K[:, :, 0] = 0.0
+        K[:, ::32, 0] = 32.0
+        K[:, 1, 0] = -64.0
+        K[:, :, 1] = 0.0
+    elif mode == "dominant":
+        K[:, :, 0] = 0.0
+        K[:, 0, 0] = 256.0
+        K[:, :, 1] = 0.0
     else:
         raise ValueError(mode)
     V = rng.standard_normal((H, S, d))
