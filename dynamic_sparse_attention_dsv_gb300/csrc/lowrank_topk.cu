@@ -67,6 +67,10 @@ struct SelCfg {
   static constexpr int kHistLog2 = (RP == 32) ? 8 : 7;
   static constexpr int kCovBins = (RP == 32) ? 128 : 64;
   static constexpr int kHistBytes = 128 * 1024 / (RP / 32);
+  // Coverage bins (coarse or fine) in the histogram area: 32-bit counts
+  // ([bin][row]) at 0, then 32-bit fixed-point masses ([bin][row]).
+  static constexpr int kCovMassOff = kCovBins * 128 * 4;
+  static_assert(2 * kCovMassOff <= kHistBytes, "coverage counts and masses fit the histogram area");
   static constexpr int kOffAlo = kTileBytes;
   static constexpr int kOffB = 2 * kTileBytes;
   static constexpr int kOffHist = kOffB + kStages * 2 * kTileBytes;
@@ -87,8 +91,9 @@ struct SelParams {
   float scale;
   uint32_t* mmax;        // [n][g_pad] orderable max
   uint32_t* mmin;        // [n][g_pad] orderable min
-  uint32_t* hist;        // HIST, REFINE: [n][bins][g_pad]; COV: counts [n][chunks][bins][g_pad]
-  float* mass;           // COV: [n][chunks][bins][g_pad]
+  uint32_t* hist;        // HIST, REFINE, COVHIST: [n][bins][g_pad] top-k histogram
+  uint32_t* cov_cnt;     // COV, COV_FINE (and fused): [n][chunks][bins][g_pad] coverage counts
+  float* mass;           // COV, COV_FINE (and fused): [n][chunks][bins][g_pad] coverage masses
   const uint32_t* blo;   // [n][g_pad] boundary interval [blo, bhi) of orderable scores
   const uint32_t* bhi;
   const int32_t* rstate; // [n][g_pad] RowState
@@ -254,6 +259,13 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     }
   } else {
     // ------------------------------------------------------- score consumers
+    constexpr bool kCovPart = MODE == kCov;        // coverage coarse bins
+    constexpr bool kFinePart = MODE == kCovFine;   // coverage fine bins
+    constexpr bool kHistPart = MODE == kHist;      // top-k linear histogram
+    constexpr bool kCollectPart = MODE == kCollect;
+    constexpr bool kCovLike = kCovPart || kFinePart;
+    constexpr int NBc = C::kCovBins;
+    constexpr int NBh = C::kHistBins;
     const int q = warp & 3, half = warp >> 2;
     const int row = q * 32 + lane;
     const int g = gtile * 128 + row;
@@ -261,14 +273,15 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     const int rid = lp * prm.g_pad + g;
     const uint32_t taddr_lane = tbase + ((uint32_t)(q * 32) << 16);
 
-    float lo = 0.f, inv_w = 0.f, cmax = 0.f;
+    float h_lo = 0.f, h_inv = 0.f, inv_w = 0.f, cmax = 0.f;
     float mx = -INFINITY, mn = INFINITY;
-    int n_in = 0;
-    // COLLECT stages up to kStage candidates per (row, half) in the unused histogram area
+    // COLLECT stages candidates per (row, half) in the histogram area,
+    // flushing kStage at a time
     constexpr int kStage = C::kHistBytes / (256 * 8);
     uint64_t* stage = reinterpret_cast<uint64_t*>(sHist) + (size_t)(half * 128 + row) * kStage;
-    constexpr int NB = (MODE == kCov || MODE == kCovFine) ? C::kCovBins : C::kHistBins;
+    int n_st = 0;
     const uint32_t hist_base = smem_u32(sHist);
+    const uint32_t cmass_base = hist_base + C::kCovMassOff;
 
     // COLLECT: scores >= t_above are selected, [t_in, t_above) is the boundary
     // interval; REFINE: the interval [olo, olo + owid) of orderable scores,
@@ -276,8 +289,8 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     float t_in = INFINITY, t_above = INFINITY;
     uint32_t olo = 0, owid = 0, oshift = 0;
     int state = kRowCollect;
-    if constexpr (MODE == kHist) lin_range(prm.mmin[rid], prm.mmax[rid], NB, &lo, &inv_w);
-    if constexpr (MODE == kCollect || MODE == kRefine) {
+    if constexpr (kHistPart) lin_range(prm.mmin[rid], prm.mmax[rid], NBh, &h_lo, &h_inv);
+    if constexpr (kCollectPart || MODE == kRefine) {
       if (valid) {
         olo = prm.blo[rid];
         const uint32_t ohi = prm.bhi[rid];
@@ -290,32 +303,38 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       }
       if (MODE == kRefine && state != kRowRefine) owid = 0;   // this row takes no part
     }
-    float w2 = 0.f;   // COV: bin width in log2 units
-    // COV_FINE: the row's window of coarse bins, NB fine bins over it (fine
-    // coordinate (x - wa) * fscale, fine width fw2 in log2 units)
-    int wa = NB, wb = -1;
+    float w2 = 0.f;   // coverage: coarse bin width in log2 units
+    // fine bins: the row's window of coarse bins [wa, wb], NBc fine bins over
+    // it (fine coordinate (x - wa) * fscale, fine width fw2 in log2 units)
+    int wa = NBc, wb = -1;
     float fscale = 0.f, fw2 = 0.f;
-    if constexpr (MODE == kCov || MODE == kCovFine) {
+    if constexpr (kCovLike) {
       cmax = ord2f(prm.mmax[rid]);
       const float range = prm.scale * (cmax - ord2f(prm.mmin[rid]));
-      inv_w = range > 0.f ? (float)NB / range : 0.f;
-      w2 = range > 0.f ? range / (float)NB * 1.4426950408889634f : 0.f;
+      inv_w = range > 0.f ? (float)NBc / range : 0.f;
+      w2 = range > 0.f ? range / (float)NBc * 1.4426950408889634f : 0.f;
     }
-    if constexpr (MODE == kCovFine) {
+    if constexpr (kFinePart) {
       if (valid) {
         wa = prm.cwin[2 * (size_t)rid];
         wb = prm.cwin[2 * (size_t)rid + 1];
       }
       const int nw = wb - wa + 1;
-      fscale = nw > 0 ? (float)NB / (float)nw : 0.f;
-      fw2 = nw > 0 ? w2 * (float)nw / (float)NB : 0.f;
+      fscale = nw > 0 ? (float)NBc / (float)nw : 0.f;
+      fw2 = nw > 0 ? w2 * (float)nw / (float)NBc : 0.f;
     }
-    if constexpr (MODE == kHist || MODE == kCov || MODE == kRefine || MODE == kCovFine) {
-      // zero this CTA's private histograms ([bin][row] counts, then masses)
+    if constexpr (MODE != kMinMax && MODE != kCollect) {
+      // zero this CTA's private histograms
       uint32_t* h = reinterpret_cast<uint32_t*>(sHist);
       for (int i = tid; i < C::kHistBytes / 4; i += 256) h[i] = 0;
       epi_barrier();
     }
+    // writes the staged candidates of this (row, half) with one slot reservation
+    auto flush = [&](int n) {
+      const uint32_t slot0 = atomicAdd(prm.cand_cnt + rid, (uint32_t)n);
+      for (int i = 0; i < n; ++i)
+        if (slot0 + i < (uint32_t)kCandCap) prm.cand[(size_t)rid * kCandCap + slot0 + i] = stage[i];
+    };
 
     for (int i = 0; i < nt; ++i) {
       const int b = i & 1;
@@ -340,10 +359,38 @@ __global__ void __launch_bounds__(kSelThreads, 2)
           if constexpr (MODE == kMinMax) {
             mx = fmaxf(mx, s);
             mn = fminf(mn, s);
-          } else if constexpr (MODE == kHist) {
-            const int bin = lin_bin(s, lo, inv_w, NB);
+          }
+          if constexpr (kCovLike) {
+            // log-probability below the row maximum u, its coarse coordinate
+            // x and bin; the fine bins reuse this arithmetic bit for bit, so
+            // window membership agrees with the coarse bins
+            const float u = __fmul_rn(prm.scale, __fsub_rn(cmax, s));
+            const float x = __fmul_rn(u, inv_w);
+            const float t = bin_round(x);
+            const int bin = bin_of(t, NBc);
+            if constexpr (kCovPart) {
+              // q = exp(b w - u) in (exp(-w), 1], as 16.16 fixed point through the float bits
+              const float frac = x - fminf(t - kRoundMagic, (float)(NBc - 1));   // in [0, 1], more when clamped
+              const float qv = ex2_fast(-frac * w2);
+              const uint32_t qf = __float_as_uint(fmaf(qv, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
+              red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
+              red_smem_u32(cmass_base + (uint32_t)(bin * 128 + row) * 4u, qf);
+            } else {
+              if (bin >= wa && bin <= wb) {
+                const float y = (x - (float)wa) * fscale;
+                const int fb = min(NBc - 1, max(0, (int)y));
+                const float qv = ex2_fast(((float)fb - y) * fw2);   // exp(fb fw - u'), in (exp(-fw), 1]
+                const uint32_t qf = __float_as_uint(fmaf(qv, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
+                red_smem_u32(hist_base + (uint32_t)(fb * 128 + row) * 4u, 1u);
+                red_smem_u32(cmass_base + (uint32_t)(fb * 128 + row) * 4u, qf);
+              }
+            }
+          }
+          if constexpr (kHistPart) {
+            const int bin = lin_bin(s, h_lo, h_inv, NBh);
             red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
-          } else if constexpr (MODE == kCollect) {
+          }
+          if constexpr (kCollectPart) {
             // branch-free here; the rare candidates are handled after the loop.
             // The thresholds are exact floats of the interval's orderable
             // bounds, so the float compares equal the orderable ones
@@ -355,38 +402,13 @@ __global__ void __launch_bounds__(kSelThreads, 2)
               gm_hi |= (uint32_t)above << (e - 32);
               cm_hi |= (uint32_t)in << (e - 32);
             }
-          } else if constexpr (MODE == kRefine) {
+          }
+          if constexpr (MODE == kRefine) {
             const uint32_t dlt = f2ord(s) - olo;   // wraps above 2^31 for scores below the interval
             if (dlt < owid) red_smem_u32(hist_base + (uint32_t)((dlt >> oshift) * 128 + row) * 4u, 1u);
-          } else if constexpr (MODE == kCov) {
-            // log-probability below the row maximum, its bin b, and q = exp(b w - u)
-            const float u = __fmul_rn(prm.scale, __fsub_rn(cmax, s));
-            const float x = __fmul_rn(u, inv_w);
-            const float t = bin_round(x);
-            const int bin = bin_of(t, NB);
-            const float frac = x - fminf(t - kRoundMagic, (float)(NB - 1));   // in [0, 1], more when clamped
-            const float q = ex2_fast(-frac * w2);
-            // 16.16 fixed point through the same float-bits route
-            const uint32_t qf = __float_as_uint(fmaf(q, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
-            red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
-            red_smem_u32(hist_base + (uint32_t)(NB * 128 + bin * 128 + row) * 4u, qf);
-          } else if constexpr (MODE == kCovFine) {
-            // the COV pass's arithmetic bit for bit, so window membership
-            // agrees with the coarse bins
-            const float u = __fmul_rn(prm.scale, __fsub_rn(cmax, s));
-            const float x = __fmul_rn(u, inv_w);
-            const int bin = bin_of(bin_round(x), NB);
-            if (bin >= wa && bin <= wb) {
-              const float y = (x - (float)wa) * fscale;
-              const int fb = min(NB - 1, max(0, (int)y));
-              const float q = ex2_fast(((float)fb - y) * fw2);   // exp(fb fw - u'), in (exp(-fw), 1]
-              const uint32_t qf = __float_as_uint(fmaf(q, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
-              red_smem_u32(hist_base + (uint32_t)(fb * 128 + row) * 4u, 1u);
-              red_smem_u32(hist_base + (uint32_t)(NB * 128 + fb * 128 + row) * 4u, qf);
-            }
           }
         }
-        if constexpr (MODE == kCollect) {
+        if constexpr (kCollectPart) {
           if (valid) {
             const size_t wi = ((size_t)rid * prm.n_tiles + (t0 + i)) * 4 + half * 2;
             *reinterpret_cast<uint2*>(prm.sel_bits + wi) = make_uint2(gm_lo, gm_hi);
@@ -406,14 +428,11 @@ __global__ void __launch_bounds__(kSelThreads, 2)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v = (u == i) ? (hi ? r1[i] : r0[i]) : v;
             const float sv = __uint_as_float(v) + 0.0f;
-            const uint64_t key = ((uint64_t)(~f2ord(sv)) << 32) | (uint32_t)(kb + e);
-            if (n_in < kStage) {
-              stage[n_in] = key;
-            } else {   // staging full: reserve a slot directly
-              const uint32_t slot = atomicAdd(prm.cand_cnt + rid, 1u);
-              if (slot < (uint32_t)kCandCap) prm.cand[(size_t)rid * kCandCap + slot] = key;
+            if (n_st == kStage) {
+              flush(kStage);
+              n_st = 0;
             }
-            ++n_in;
+            stage[n_st++] = ((uint64_t)(~f2ord(sv)) << 32) | (uint32_t)(kb + e);
           }
         }
       }
@@ -423,16 +442,8 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     }
 
     // ----------------------------------------------------- per-row results
-    if constexpr (MODE == kCollect) {
-      // flush this (row, half)'s staged candidates with one slot reservation,
-      // before the exchange below reuses the start of the staging area
-      const int ns = min(n_in, kStage);
-      if (valid && ns > 0) {
-        const uint32_t slot0 = atomicAdd(prm.cand_cnt + rid, (uint32_t)ns);
-        for (int i = 0; i < ns; ++i)
-          if (slot0 + i < (uint32_t)kCandCap) prm.cand[(size_t)rid * kCandCap + slot0 + i] = stage[i];
-      }
-      epi_barrier();
+    if constexpr (kCollectPart) {
+      if (valid && n_st > 0) flush(n_st);
     }
     if constexpr (MODE == kMinMax) {
       float* ex = reinterpret_cast<float*>(sHist);   // [2][2][128], the histogram area is unused here
@@ -445,24 +456,25 @@ __global__ void __launch_bounds__(kSelThreads, 2)
         atomicMax(prm.mmax + rid, f2ord(m2));
         atomicMin(prm.mmin + rid, f2ord(n2));
       }
-    } else if constexpr (MODE == kHist || MODE == kRefine) {
-      epi_barrier();
+    }
+    if constexpr (MODE != kMinMax && MODE != kCollect) epi_barrier();
+    if constexpr (kCovLike) {
       const uint32_t* h = reinterpret_cast<const uint32_t*>(sHist);
-      for (int bin = half * (NB / 2); bin < (half + 1) * (NB / 2); ++bin) {
-        const uint32_t v = h[bin * 128 + row];
-        if (v) atomicAdd(prm.hist + ((size_t)lp * NB + bin) * prm.g_pad + g, v);
-      }
-    } else if constexpr (MODE == kCov || MODE == kCovFine) {
-      epi_barrier();
-      const uint32_t* h = reinterpret_cast<const uint32_t*>(sHist);
-      const uint32_t* m = h + NB * 128;
+      const uint32_t* m = reinterpret_cast<const uint32_t*>(sHist + C::kCovMassOff);
       // a bin's probabilities were summed relative to its upper edge
-      const float edge0 = MODE == kCovFine ? (float)wa * w2 : 0.f;
-      const float step = MODE == kCovFine ? fw2 : w2;
-      for (int bin = half * (NB / 2); bin < (half + 1) * (NB / 2); ++bin) {
-        const size_t o = (((size_t)lp * prm.n_chunks + chunk) * NB + bin) * prm.g_pad + g;
-        prm.hist[o] = h[bin * 128 + row];
+      const float edge0 = kFinePart ? (float)wa * w2 : 0.f;
+      const float step = kFinePart ? fw2 : w2;
+      for (int bin = half * (NBc / 2); bin < (half + 1) * (NBc / 2); ++bin) {
+        const size_t o = (((size_t)lp * prm.n_chunks + chunk) * NBc + bin) * prm.g_pad + g;
+        prm.cov_cnt[o] = h[bin * 128 + row];
         prm.mass[o] = (float)m[bin * 128 + row] * (1.f / 65536.f) * ex2_fast(-(edge0 + (float)bin * step));
+      }
+    }
+    if constexpr (kHistPart || MODE == kRefine) {
+      const uint32_t* h = reinterpret_cast<const uint32_t*>(sHist);
+      for (int bin = half * (NBh / 2); bin < (half + 1) * (NBh / 2); ++bin) {
+        const uint32_t v = h[bin * 128 + row];
+        if (v) atomicAdd(prm.hist + ((size_t)lp * NBh + bin) * prm.g_pad + g, v);
       }
     }
   }
@@ -1404,76 +1416,9 @@ static dsv_status validate_lowrank(const void* Q, const void* K, const void* Wq,
   return DSV_OK;
 }
 
-// The top-k passes of one launch of problems whose projections are in the
-// workspace; `minmax` = false when the row ranges are already there.
-static cudaError_t topk_passes(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, const CUtensorMap* maps,
-                               bool minmax, int32_t* idx, int32_t* status, cudaStream_t st) {
-  const int n = tab.n;
-  int n_chunks, chunk_tiles;
-  chunking(pl, n, &n_chunks, &chunk_tiles);
-  SelParams prm;
-  memset(&prm, 0, sizeof(prm));
-  prm.geo = pl.geo;
-  prm.g_pad = pl.g_pad;
-  prm.n_chunks = n_chunks;
-  prm.chunk_tiles = chunk_tiles;
-  prm.n_tiles = pl.n_tiles;
-  prm.n_gt = pl.n_gt;
-  prm.mmax = w.mmax;
-  prm.mmin = w.mmin;
-  prm.hist = w.hist;
-  prm.blo = w.blo;
-  prm.bhi = w.bhi;
-  prm.rstate = w.rstate;
-  prm.cand_cnt = w.cand_cnt;
-  prm.cand = w.cand;
-  prm.sel_bits = w.selb;
-  prm.eq_bits = w.eqb;
-  prm.status = status;
-  const dim3 grid(pl.n_gt, n_chunks, n);
-  const size_t rows = (size_t)n * pl.g_pad;
-  const int rounds = refine_rounds(pl);
-  const int lg = pl.RP == 32 ? SelCfg<32>::kHistLog2 : SelCfg<64>::kHistLog2;
-  const size_t nflag = (size_t)n * pl.n_gt;
-  const dim3 rgrid(pl.n_gt, n);
-  if (minmax) {
-    if (cudaMemsetAsync(w.mmax, 0, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
-    if (cudaMemsetAsync(w.mmin, 0xFF, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
-    if (select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
-  }
-  if (cudaMemsetAsync(w.hist, 0, rows * pl.hist_bins * 4, st) != cudaSuccess) return cudaErrorUnknown;
-  if (cudaMemsetAsync(w.tflag, 0, (rounds + 1) * nflag * 4, st) != cudaSuccess) return cudaErrorUnknown;
-  if (select_pass<kHist>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
-  k_bracket<<<rgrid, 128, 0, st>>>(w.hist, pl.hist_bins, pl.g_pad, pl.geo.n_groups, pl.n_gt, w.mmin, w.mmax, w.blo,
-                                   w.bhi, w.nabove, w.bcount, w.rstate, w.tflag, status, tab);
-  if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
-  // REFINE rounds: group tiles with no row to refine leave at once
-  for (int r = 0; r < rounds; ++r) {
-    prm.tflag = w.tflag + r * nflag;
-    if (select_pass<kRefine>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
-    k_refine_bracket<<<rgrid, 128, 0, st>>>(w.hist, pl.hist_bins, lg, pl.g_pad, pl.geo.n_groups, pl.n_gt, w.blo,
-                                            w.bhi, w.nabove, w.bcount, w.rstate, w.tflag + r * nflag,
-                                            w.tflag + (r + 1) * nflag, status, tab);
-    if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
-  }
-  if (cudaMemsetAsync(w.cand_cnt, 0, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
-  if (select_pass<kCollect>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
-  k_resolve<<<dim3(pl.geo.n_groups, n), 256, 0, st>>>(w.cand, w.cand_cnt, w.nabove, w.bcount, w.rstate, pl.g_pad,
-                                                        pl.n_tiles * 4, w.selb, status, tab);
-  if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
-  k_sel_compact<<<dim3(pl.geo.n_groups, n), 32 * kCompactWarps, 0, st>>>(w.selb, w.eqb, w.rstate, w.nabove, pl.g_pad,
-                                                                          pl.n_tiles * 4, idx, status, tab);
-  return cudaGetLastError();
-}
-
-// The coverage passes of one launch of problems whose projections are in the
-// workspace; `minmax` = false when the row ranges are already there.
-static cudaError_t cov_passes(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, const CUtensorMap* maps,
-                              bool minmax, float scale, float mass, int32_t* k_cov, float* curve, int n_curve,
-                              int32_t* status, cudaStream_t st) {
-  const int n = tab.n;
-  int n_chunks, chunk_tiles;
-  chunking(pl, n, &n_chunks, &chunk_tiles, kCovMaxTiles);
+// Parameters of the score passes of one launch of problems.
+static SelParams sel_params(const TopkPlan& pl, const TopkWs& w, int n_chunks, int chunk_tiles, float scale,
+                            int32_t* status) {
   SelParams prm;
   memset(&prm, 0, sizeof(prm));
   prm.geo = pl.geo;
@@ -1485,60 +1430,172 @@ static cudaError_t cov_passes(const TopkPlan& pl, const TopkWs& w, const Problem
   prm.scale = scale;
   prm.mmax = w.mmax;
   prm.mmin = w.mmin;
-  prm.hist = w.cov_hist;
+  prm.hist = w.hist;
+  prm.cov_cnt = w.cov_hist;
   prm.mass = w.mass;
+  prm.blo = w.blo;
+  prm.bhi = w.bhi;
+  prm.rstate = w.rstate;
+  prm.cand_cnt = w.cand_cnt;
+  prm.cand = w.cand;
+  prm.sel_bits = w.selb;
+  prm.eq_bits = w.eqb;
   prm.cwin = w.cov_win;
   prm.status = status;
-  const dim3 grid(pl.n_gt, n_chunks, n);
-  const size_t rows = (size_t)n * pl.g_pad;
-  const int nb = pl.cov_bins, ng = pl.geo.n_groups, S = pl.geo.S;
-  if (minmax) {
-    if (cudaMemsetAsync(w.mmax, 0, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
-    if (cudaMemsetAsync(w.mmin, 0xFF, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
-    if (select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  return prm;
+}
+
+static cudaError_t minmax_pass(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, const CUtensorMap* maps,
+                               dim3 grid, const SelParams& prm, cudaStream_t st) {
+  const size_t rows = (size_t)tab.n * pl.g_pad;
+  if (cudaMemsetAsync(w.mmax, 0, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
+  if (cudaMemsetAsync(w.mmin, 0xFF, rows * 4, st) != cudaSuccess) return cudaErrorUnknown;
+  return select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab);
+}
+
+// Top-k, once the linear histogram (nb bins) is in w.hist: the bracket and
+// the REFINE rounds (group tiles with no row to refine leave at once).
+static cudaError_t topk_bracket_refine(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab,
+                                       const CUtensorMap* maps, dim3 grid, SelParams prm, int nb, int32_t* status,
+                                       cudaStream_t st) {
+  const int n = tab.n;
+  const int rounds = refine_rounds(pl);
+  const int lg = pl.RP == 32 ? SelCfg<32>::kHistLog2 : SelCfg<64>::kHistLog2;
+  const size_t nflag = (size_t)n * pl.n_gt;
+  const dim3 rgrid(pl.n_gt, n);
+  k_bracket<<<rgrid, 128, 0, st>>>(w.hist, nb, pl.g_pad, pl.geo.n_groups, pl.n_gt, w.mmin, w.mmax, w.blo, w.bhi,
+                                   w.nabove, w.bcount, w.rstate, w.tflag, status, tab);
+  if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
+  for (int r = 0; r < rounds; ++r) {
+    prm.tflag = w.tflag + r * nflag;
+    if (select_pass<kRefine>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+    k_refine_bracket<<<rgrid, 128, 0, st>>>(w.hist, pl.hist_bins, lg, pl.g_pad, pl.geo.n_groups, pl.n_gt, w.blo,
+                                            w.bhi, w.nabove, w.bcount, w.rstate, w.tflag + r * nflag,
+                                            w.tflag + (r + 1) * nflag, status, tab);
+    if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
   }
-  // coarse tables
-  if (select_pass<kCov>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  return cudaSuccess;
+}
+
+// Top-k, once COLLECT has run: resolve the candidates, write the index rows.
+static cudaError_t topk_finish(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, int32_t* idx,
+                               int32_t* status, cudaStream_t st) {
+  const int n = tab.n;
+  k_resolve<<<dim3(pl.geo.n_groups, n), 256, 0, st>>>(w.cand, w.cand_cnt, w.nabove, w.bcount, w.rstate, pl.g_pad,
+                                                        pl.n_tiles * 4, w.selb, status, tab);
+  if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
+  k_sel_compact<<<dim3(pl.geo.n_groups, n), 32 * kCompactWarps, 0, st>>>(w.selb, w.eqb, w.rstate, w.nabove, pl.g_pad,
+                                                                          pl.n_tiles * 4, idx, status, tab);
+  return cudaGetLastError();
+}
+
+// Memsets before the top-k histogram of one launch.
+static cudaError_t topk_clear(const TopkPlan& pl, const TopkWs& w, int n, cudaStream_t st) {
+  const size_t rows = (size_t)n * pl.g_pad;
+  if (cudaMemsetAsync(w.hist, 0, rows * pl.hist_bins * 4, st) != cudaSuccess) return cudaErrorUnknown;
+  if (cudaMemsetAsync(w.tflag, 0, (size_t)(refine_rounds(pl) + 1) * n * pl.n_gt * 4, st) != cudaSuccess)
+    return cudaErrorUnknown;
+  return cudaMemsetAsync(w.cand_cnt, 0, rows * 4, st);
+}
+
+// The top-k passes of one launch of problems whose projections are in the
+// workspace; `minmax` = false when the row ranges are already there.
+static cudaError_t topk_passes(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, const CUtensorMap* maps,
+                               bool minmax, int32_t* idx, int32_t* status, cudaStream_t st) {
+  int n_chunks, chunk_tiles;
+  chunking(pl, tab.n, &n_chunks, &chunk_tiles);
+  const SelParams prm = sel_params(pl, w, n_chunks, chunk_tiles, 0.f, status);
+  const dim3 grid(pl.n_gt, n_chunks, tab.n);
+  if (minmax && minmax_pass(pl, w, tab, maps, grid, prm, st) != cudaSuccess) return cudaErrorUnknown;
+  if (topk_clear(pl, w, tab.n, st) != cudaSuccess) return cudaErrorUnknown;
+  if (select_pass<kHist>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  if (topk_bracket_refine(pl, w, tab, maps, grid, prm, pl.hist_bins, status, st) != cudaSuccess)
+    return cudaErrorUnknown;
+  if (select_pass<kCollect>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  return topk_finish(pl, w, tab, idx, status, st);
+}
+
+struct CovSearch {
+  int nblk, rounds;
+};
+
+static CovSearch cov_search_shape(const TopkPlan& pl) {
+  CovSearch c;
+  c.nblk = (pl.geo.n_groups + kCovGroupsPerBlock - 1) / kCovGroupsPerBlock;
+  // rounds: the interval shrinks from S values to at most ceil(span / kCovPoints) per round
+  c.rounds = 1;
+  for (int64_t span = pl.geo.S; span > kCovPoints; span = (span + kCovPoints - 1) / kCovPoints) ++c.rounds;
+  return c;
+}
+
+static void cov_search(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, int mode, bool fine,
+                       float mass, int32_t* out, bool by_problem, cudaStream_t st) {
+  const CovSearch cs = cov_search_shape(pl);
+  const int n = tab.n, ng = pl.geo.n_groups, S = pl.geo.S, nb = pl.cov_bins;
+  for (int r = 0; r < cs.rounds; ++r) {
+    k_cov_eval<<<dim3(cs.nblk, n), kCovPoints, 0, st>>>(mode, false, nb, pl.g_pad, ng, S, w.cum_cnt, w.cum_mass,
+                                                        w.width, w.zinv, w.cov_win, fine ? w.fine_cnt : nullptr,
+                                                        w.fine_mass, w.cov_range, 0, w.cov_partial);
+    k_cov_pick<<<n, kCovPoints, 0, st>>>(false, cs.nblk, ng, S, mass, w.cov_partial, w.cov_range, out, by_problem,
+                                          nullptr, 0, tab);
+  }
+}
+
+// Coverage, once the coarse pass has run: merged tables, the certified
+// interval [k_lo, k_hi] from the bin-edge bounds, each group's window.
+static cudaError_t cov_after_coarse(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, int n_chunks,
+                                    float scale, float mass, cudaStream_t st) {
+  const int n = tab.n, nb = pl.cov_bins, ng = pl.geo.n_groups, S = pl.geo.S;
   const dim3 mgrid((ng + 127) / 128, nb, n), sgrid((ng + 7) / 8, n), wgrid((ng + 127) / 128, n);
   k_cov_merge<<<mgrid, 128, 0, st>>>(w.cov_hist, w.mass, nb, n_chunks, pl.g_pad, ng, w.cum_cnt, w.cum_mass);
   k_cov_scan<<<sgrid, 256, 0, st>>>(w.mmax, w.mmin, nb, pl.g_pad, ng, scale, w.cum_cnt, w.cum_mass, w.width, w.zinv,
                                     nullptr);
-  const int nblk = (ng + kCovGroupsPerBlock - 1) / kCovGroupsPerBlock;
-  // rounds: the interval shrinks from S values to at most ceil(span / kCovPoints) per round
-  int rounds = 1;
-  for (int64_t span = S; span > kCovPoints; span = (span + kCovPoints - 1) / kCovPoints) ++rounds;
-  auto search = [&](int mode, const int32_t* fc, const double* fm, int32_t* out, bool by_problem) {
-    for (int r = 0; r < rounds; ++r) {
-      k_cov_eval<<<dim3(nblk, n), kCovPoints, 0, st>>>(mode, false, nb, pl.g_pad, ng, S, w.cum_cnt, w.cum_mass,
-                                                       w.width, w.zinv, w.cov_win, fc, fm, w.cov_range, 0,
-                                                       w.cov_partial);
-      k_cov_pick<<<n, kCovPoints, 0, st>>>(false, nblk, ng, S, mass, w.cov_partial, w.cov_range, out, by_problem,
-                                            nullptr, 0, tab);
-    }
-  };
-  // certified interval [k_lo, k_hi] from the bin-edge bounds
   k_cov_range_init<<<1, 256, 0, st>>>(w.cov_range, nullptr, nullptr, S, n);
-  search(kCovBoundHi, nullptr, nullptr, w.kwin_lo, false);
+  cov_search(pl, w, tab, kCovBoundHi, false, mass, w.kwin_lo, false, st);
   k_cov_range_init<<<1, 256, 0, st>>>(w.cov_range, nullptr, nullptr, S, n);
-  search(kCovBoundLo, nullptr, nullptr, w.kwin_hi, false);
-  // fine tables over each group's window of coarse bins
+  cov_search(pl, w, tab, kCovBoundLo, false, mass, w.kwin_hi, false, st);
   k_cov_window<<<wgrid, 128, 0, st>>>(nb, pl.g_pad, ng, w.cum_cnt, w.cum_mass, w.kwin_lo, w.kwin_hi, w.cov_win,
                                       w.fine_scale);
-  if (select_pass<kCovFine>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  return cudaGetLastError();
+}
+
+// Coverage, once the fine pass has run: k_cov within [k_lo, k_hi] on the
+// combined tables, and the curve.
+static cudaError_t cov_after_fine(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, int n_chunks,
+                                  float scale, float mass, int32_t* k_cov, float* curve, int n_curve,
+                                  cudaStream_t st) {
+  const int n = tab.n, nb = pl.cov_bins, ng = pl.geo.n_groups, S = pl.geo.S;
+  const dim3 mgrid((ng + 127) / 128, nb, n), sgrid((ng + 7) / 8, n);
   k_cov_merge<<<mgrid, 128, 0, st>>>(w.cov_hist, w.mass, nb, n_chunks, pl.g_pad, ng, w.fine_cnt, w.fine_mass);
   k_cov_scan<<<sgrid, 256, 0, st>>>(w.mmax, w.mmin, nb, pl.g_pad, ng, scale, w.fine_cnt, w.fine_mass, nullptr,
                                     nullptr, w.fine_scale);
-  // k_cov within [k_lo, k_hi] on the combined tables
   k_cov_range_init<<<1, 256, 0, st>>>(w.cov_range, w.kwin_lo, w.kwin_hi, S, n);
-  search(kCovCombined, w.fine_cnt, w.fine_mass, k_cov, true);
+  cov_search(pl, w, tab, kCovCombined, true, mass, k_cov, true, st);
   if (curve) {
-    k_cov_eval<<<dim3(nblk, n), kCovPoints, 0, st>>>(kCovCombined, true, nb, pl.g_pad, ng, S, w.cum_cnt,
-                                                     w.cum_mass, w.width, w.zinv, w.cov_win, w.fine_cnt,
-                                                     w.fine_mass, w.cov_range, n_curve, w.cov_partial);
-    k_cov_pick<<<n, kCovPoints, 0, st>>>(true, nblk, ng, S, mass, w.cov_partial, w.cov_range, k_cov, true, curve,
+    const CovSearch cs = cov_search_shape(pl);
+    k_cov_eval<<<dim3(cs.nblk, n), kCovPoints, 0, st>>>(kCovCombined, true, nb, pl.g_pad, ng, S, w.cum_cnt,
+                                                        w.cum_mass, w.width, w.zinv, w.cov_win, w.fine_cnt,
+                                                        w.fine_mass, w.cov_range, n_curve, w.cov_partial);
+    k_cov_pick<<<n, kCovPoints, 0, st>>>(true, cs.nblk, ng, S, mass, w.cov_partial, w.cov_range, k_cov, true, curve,
                                           n_curve, tab);
   }
   return cudaGetLastError();
+}
+
+// The coverage passes of one launch of problems whose projections are in the
+// workspace; `minmax` = false when the row ranges are already there.
+static cudaError_t cov_passes(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, const CUtensorMap* maps,
+                              bool minmax, float scale, float mass, int32_t* k_cov, float* curve, int n_curve,
+                              int32_t* status, cudaStream_t st) {
+  int n_chunks, chunk_tiles;
+  chunking(pl, tab.n, &n_chunks, &chunk_tiles, kCovMaxTiles);
+  const SelParams prm = sel_params(pl, w, n_chunks, chunk_tiles, scale, status);
+  const dim3 grid(pl.n_gt, n_chunks, tab.n);
+  if (minmax && minmax_pass(pl, w, tab, maps, grid, prm, st) != cudaSuccess) return cudaErrorUnknown;
+  if (select_pass<kCov>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  if (cov_after_coarse(pl, w, tab, n_chunks, scale, mass, st) != cudaSuccess) return cudaErrorUnknown;
+  if (select_pass<kCovFine>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  return cov_after_fine(pl, w, tab, n_chunks, scale, mass, k_cov, curve, n_curve, st);
 }
 
 }  // namespace dsv
