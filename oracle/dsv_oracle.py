@@ -255,6 +255,26 @@ def true_mass(Q, K, idx: np.ndarray, members: np.ndarray, scale: float) -> np.nd
     return out
 
 
+def predicted_mass(Q, K, Wq, Wk, idx: np.ndarray, members: np.ndarray, scale: float) -> np.ndarray:
+    """Share of each query's own predicted softmax mass that its group's
+    selected keys carry (section 2.1: critical KV carry over 90% of the
+    attention score; the per-query reading of the coverage criterion, on the
+    low-rank predictor's logits). For query i of group g, with the
+    predictor's logits scale * q_lr,i . k_lr,j over all S keys (q_lr = Q
+    W_lr^Q, k_lr = K W_lr^K): the softmax of those logits summed over j in
+    I_g. Returns [S]."""
+    q_lr, k_lr = lowrank_project(Q, Wq), lowrank_project(K, Wk)
+    S = q_lr.shape[0]
+    out = np.full(S, np.nan)
+    for g in range(members.shape[0]):
+        mem = members[g]
+        logits = scale * (q_lr[mem] @ k_lr.T)
+        e = np.exp(logits - logits.max(axis=1, keepdims=True))
+        P = e / e.sum(axis=1, keepdims=True)
+        out[mem] = P[:, idx[g]].sum(axis=1)
+    return out
+
+
 def sparse_attn_bwd(Q, K, V, dO, idx: Optional[np.ndarray], members: np.ndarray, scale: float):
     """Gradients of sum(dO * O) for one head of sparse attention, with the
     index sets held constant. Per group g and selected key j:

@@ -350,6 +350,47 @@ def test_true_mass_single_dominant_key():
     np.testing.assert_allclose(ora.true_mass(Q, K, idx, mem, 1.0), want, rtol=1e-12)
 
 
+def test_predicted_mass_equals_true_mass_with_identity_predictor():
+    """With r = d and W_lr^Q = W_lr^K = I the predictor's logits are the true
+    ones, so the per-query predicted mass is the true mass (a separate
+    function that works on Q K^T directly)."""
+    rng = np.random.default_rng(5)
+    T, Y, X, d = 2, 4, 4, 8
+    S = T * Y * X
+    mem = ora.group_members(T, Y, X, 1, 2, 2)
+    Q, K = rng.standard_normal((S, d)), rng.standard_normal((S, d))
+    idx = np.stack([np.sort(rng.choice(S, 5, replace=False)) for _ in range(mem.shape[0])])
+    eye = np.eye(d)
+    np.testing.assert_allclose(ora.predicted_mass(Q, K, eye, eye, idx, mem, 0.3), ora.true_mass(Q, K, idx, mem, 0.3),
+                               rtol=0, atol=1e-13)
+
+
+def test_predicted_mass_closed_forms():
+    """All keys selected gives 1; W_lr^Q = 0 makes every logit 0, so each key
+    carries 1/S and k selected keys carry k/S; one key whose predicted logit
+    is L above all others (which are equal) carries 1/(1 + (S-1) e^-L)."""
+    rng = np.random.default_rng(6)
+    T, Y, X, d, r = 1, 4, 8, 8, 4
+    S = T * Y * X
+    mem = ora.group_members(T, Y, X, 1, 2, 2)
+    Q, K = rng.standard_normal((S, d)), rng.standard_normal((S, d))
+    Wq, Wk = rng.standard_normal((d, r)), rng.standard_normal((d, r))
+    everything = np.tile(np.arange(S), (mem.shape[0], 1))
+    np.testing.assert_allclose(ora.predicted_mass(Q, K, Wq, Wk, everything, mem, 0.5), 1.0, rtol=0, atol=1e-12)
+    k = 7
+    some = np.stack([np.sort(rng.choice(S, k, replace=False)) for _ in range(mem.shape[0])])
+    np.testing.assert_allclose(ora.predicted_mass(Q, K, np.zeros((d, r)), Wk, some, mem, 0.5), k / S, rtol=0,
+                               atol=1e-12)
+    # q_lr = e_0 for every query, k_lr,j = 0 except k_lr,3 = L e_0 (scale 1)
+    L = 4.0
+    Q1 = np.zeros((S, d)); Q1[:, 0] = 1.0
+    K1 = np.zeros((S, d)); K1[3, 0] = L
+    W = np.zeros((d, r)); W[0, 0] = 1.0
+    idx = np.tile(np.array([3]), (mem.shape[0], 1))
+    np.testing.assert_allclose(ora.predicted_mass(Q1, K1, W, W, idx, mem, 1.0), 1.0 / (1.0 + (S - 1) * np.exp(-L)),
+                               rtol=1e-12)
+
+
 # ------------------------------------------------- head-wise CP re-balancing
 def test_plan_gpus_hand_example():
     """Costs 9, 8, 7, 5, 3, 1 on 3 GPUs: 9 -> 0, 8 -> 1, 7 -> 2, 5 -> 2 (7 is
