@@ -61,6 +61,12 @@ def _i64(vals):
     return (ctypes.c_int64 * len(vals))(*[int(v) for v in vals])
 
 
+def set_wait_limit_ns(ns: int) -> int:
+    """dsv_set_wait_limit_ns: the limit (ns) of every pipeline wait inside the
+    kernels launched from now on, for this process; returns the previous one."""
+    return int(N.load().dsv_set_wait_limit_ns(int(ns)))
+
+
 def new_status(device=None) -> torch.Tensor:
     """A zeroed device status word (int32) for one or more calls."""
     return torch.zeros(1, dtype=torch.int32, device=device or "cuda")

@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
   uint64_t* sdp_free = bars + 15;    // S, dP of the current tile read out of TMEM
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
   uint64_t* pv_free = bars + 17;     // P of the previous tile read by its dV MMAs (dS may still be in use)
+  uint64_t* mma_drain = bars + 18;   // every MMA issued has completed (unwind)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int u = blockIdx.y;
@@ -183,6 +184,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     mbar_init(part_free, 4);
     mbar_init(dq_done, 1);
     mbar_init(sdp_free, 4);
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -206,6 +208,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     const int prow0 = p * geo.S;
     int rows[Gather<D>::kIters], nxt[Gather<D>::kIters];
     if (idx_row) gather_rows<D>(nxt, idx_row, k, 0, prow0, pw, lane);
+    int k_issued = 0, v_issued = 0;   // tiles whose K (V) copies this warp started
     for (int t = 0; t < nt; ++t) {
       const int ks = t % C::kKStages, vs = t % C::kVStages;
       if (idx_row) {
@@ -213,7 +216,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         for (int i = 0; i < Gather<D>::kIters; ++i) rows[i] = nxt[i];
         if (t + 1 < nt) gather_rows<D>(nxt, idx_row, k, t + 1, prow0, pw, lane);
       }
-      if (t >= C::kKStages && !mbar_wait_warp(k_empty + ks, ((t / C::kKStages) - 1) & 1, kWaitLimitNs)) {
+      if (t >= C::kKStages && !mbar_wait_warp(k_empty + ks, ((t / C::kKStages) - 1) & 1, prm.wait_ns)) {
         if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
         break;
       }
@@ -224,7 +227,8 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         mbar_arrive_expect_tx(k_full + ks, C::kTile);
         load_dense_tile<D>(sK + ks * C::kTile, &maps.k_tile, k_full + ks, t, prow0);
       }
-      if (t >= C::kVStages && !mbar_wait_warp(v_empty + vs, ((t / C::kVStages) - 1) & 1, kWaitLimitNs)) {
+      k_issued = t + 1;
+      if (t >= C::kVStages && !mbar_wait_warp(v_empty + vs, ((t / C::kVStages) - 1) & 1, prm.wait_ns)) {
         if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
         break;
       }
@@ -235,7 +239,19 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         mbar_arrive_expect_tx(v_full + vs, C::kTile);
         load_dense_tile<D>(sV + vs * C::kTile, &maps.v_tile, v_full + vs, t, prow0);
       }
+      v_issued = t + 1;
     }
+    // the warp leaves only once the copies it started have landed (a
+    // timed-out pipeline may not have consumed them)
+    if (idx_row) {
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (pw == 0 && lane == 0) {
+      for (int t = max(0, k_issued - C::kKStages); t < k_issued; ++t)
+        mbar_wait(k_full + t % C::kKStages, (t / C::kKStages) & 1, kDrainLimitNs);
+      for (int t = max(0, v_issued - C::kVStages); t < v_issued; ++t)
+        mbar_wait(v_full + t % C::kVStages, (t / C::kVStages) & 1, kDrainLimitNs);
+    }
+    if (pw == 0 && lane == 0) mbar_wait(q_full, 0, kDrainLimitNs);
    } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
@@ -247,11 +263,11 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       constexpr uint64_t kMn = (uint64_t)((16384 >> 4) - (16 >> 4)) << 16;
       const uint64_t dq_k = smem_desc(smem_u32(sQ), 16, 1024), ddo_k = smem_desc(smem_u32(sDO), 16, 1024);
       const uint64_t dp_k = smem_desc(smem_u32(sP), 16, 1024), dds_k = smem_desc(smem_u32(sDS), 16, 1024);
-      bool ok = mbar_wait(q_full, 0, kWaitLimitNs);
+      bool ok = mbar_wait(q_full, 0, prm.wait_ns);
       auto issue_sdp = [&](int t) -> bool {
         const int ks = t % C::kKStages, vs = t % C::kVStages;
-        if (!mbar_wait(k_full + ks, (t / C::kKStages) & 1, kWaitLimitNs) ||
-            !mbar_wait(v_full + vs, (t / C::kVStages) & 1, kWaitLimitNs))
+        if (!mbar_wait(k_full + ks, (t / C::kKStages) & 1, prm.wait_ns) ||
+            !mbar_wait(v_full + vs, (t / C::kVStages) & 1, prm.wait_ns))
           return false;
         fence_proxy_async_smem();   // rows written by cp.async (generic proxy) -> tensor core reads
         tc_fence_after();
@@ -274,7 +290,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       };
       int job = 0;   // dV/dK jobs issued so far
       auto issue_job = [&](int jb) -> bool {
-        if (job >= 1 && !mbar_wait(part_free, (job - 1) & 1, kWaitLimitNs)) return false;
+        if (job >= 1 && !mbar_wait(part_free, (job - 1) & 1, prm.wait_ns)) return false;
         tc_fence_after();
         if (D == 64 || jb == 0) {
           const uint64_t a = opaque(dp_k + kMn), b = opaque(ddo_k + kMn);
@@ -297,8 +313,8 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       for (int t = 0; ok && t < nt; ++t) {
         const int ks = t % C::kKStages;
         // the next tile's S and dP may overwrite TMEM once tile t's are read out
-        if (t + 1 < nt && (!mbar_wait(sdp_free, t & 1, kWaitLimitNs) || !issue_sdp(t + 1))) { ok = false; break; }
-        if (!mbar_wait(ps_full, t & 1, kWaitLimitNs)) { ok = false; break; }
+        if (t + 1 < nt && (!mbar_wait(sdp_free, t & 1, prm.wait_ns) || !issue_sdp(t + 1))) { ok = false; break; }
+        if (!mbar_wait(ps_full, t & 1, prm.wait_ns)) { ok = false; break; }
         tc_fence_after();
         const uint64_t dk_m = smem_desc(smem_u32(sK + ks * C::kTile), 16, 1024) + kMn;
         const uint64_t dds = opaque(dds_k);
@@ -322,6 +338,9 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       }
       if (ok) mma_commit(dq_done);
       else raise_status(prm.status, DSV_ERR_TIMEOUT);
+      // every MMA issued completes before TMEM is released
+      mma_commit(mma_drain);
+      mbar_wait(mma_drain, 0, kDrainLimitNs);
     }
    }
   } else if (warp < 4) {
@@ -356,7 +375,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     const float dsc = prm.scale, ndd = -delta * prm.scale;
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
-      ok = ok && mbar_wait_warp(sdp_full, t & 1, kWaitLimitNs);
+      ok = ok && mbar_wait_warp(sdp_full, t & 1, prm.wait_ns);
       tc_fence_after();
       const int nvalid = min(128, k - t * 128);
       // TMEM loads complete long after they issue, so they go out in two
@@ -415,11 +434,11 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         }
       // P of the previous tile is free once its dV MMAs completed, dS once its
       // dK MMAs did: P goes out while the tensor cores may still read dS
-      if (t >= 1) ok = ok && mbar_wait_warp(pv_free, (t - 1) & 1, kWaitLimitNs);
+      if (t >= 1) ok = ok && mbar_wait_warp(pv_free, (t - 1) & 1, prm.wait_ns);
 #pragma unroll
       for (int q = 0; q < 16; ++q)
         st_sw128_chunk(sP, row, q, make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]));
-      if (t >= 1) ok = ok && mbar_wait_warp(p_free, (t - 1) & 1, kWaitLimitNs);
+      if (t >= 1) ok = ok && mbar_wait_warp(p_free, (t - 1) & 1, prm.wait_ns);
 #pragma unroll
       for (int q = 0; q < 16; ++q)
         st_sw128_chunk(sDS, row, q, make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]));
@@ -454,7 +473,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       const int nslot = (t + 1) * 128 + row;
       j_next = (t + 1 < nt && nslot < k) ? __ldg(idx_row + nslot) : -1;   // next tile's key, loaded early
       for (int jb = 0; jb < C::kJobs; ++jb, ++job) {
-        ok = ok && mbar_wait_warp(part_full, job & 1, kWaitLimitNs);
+        ok = ok && mbar_wait_warp(part_full, job & 1, prm.wait_ns);
         tc_fence_after();
 #pragma unroll 1
         for (int c2 = 0; c2 < 4; c2 += 2) {
@@ -485,7 +504,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       }
     }
     // ----------------------------------------------------------- dQ out
-    ok = ok && mbar_wait_warp(dq_done, 0, kWaitLimitNs);
+    ok = ok && mbar_wait_warp(dq_done, 0, prm.wait_ns);
     if (!ok) {
       if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
     } else {
@@ -553,6 +572,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* sdp_full = bars + 3;
   uint64_t* ps_full = bars + 4;
   uint64_t* mma_done = bars + 5;
+  uint64_t* mma_drain = bars + 6;   // every MMA issued has completed (unwind)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -572,6 +592,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(sdp_full, 1);
     mbar_init(ps_full, 4);
     mbar_init(mma_done, 1);
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -587,8 +608,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_2d(sK + a * 16384, &maps.k_tile, kv_full, a * 64, prow0 + kt * 128);
         tma_load_2d(sV + a * 16384, &maps.v_tile, kv_full, a * 64, prow0 + kt * 128);
       }
+      int issued = 0;
       for (int u = 0; u < nq; ++u) {
-        if (u >= 1 && !mbar_wait(q_empty, (u - 1) & 1, kWaitLimitNs)) {
+        if (u >= 1 && !mbar_wait(q_empty, (u - 1) & 1, prm.wait_ns)) {
           raise_status(prm.status, DSV_ERR_TIMEOUT);
           break;
         }
@@ -597,7 +619,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_2d(sQ + a * 16384, &q_tile, q_full, a * 64, prow0 + u * 128);
           tma_load_2d(sDO + a * 16384, &do_tile, q_full, a * 64, prow0 + u * 128);
         }
+        issued = u + 1;
       }
+      // the block leaves only once every copy it started has landed
+      mbar_wait(kv_full, 0, kDrainLimitNs);
+      if (issued > 0) mbar_wait(q_full, (issued - 1) & 1, kDrainLimitNs);
     }
   } else if (warp == 5) {
     if (lane == 0) {
@@ -605,9 +631,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t id_acc = instr_desc(128, D, 1, 0, 1);     // P^T dO, dS^T Q (B MN-major)
       const uint32_t ak = smem_u32(sK), av = smem_u32(sV), aq = smem_u32(sQ), ado = smem_u32(sDO);
       const uint32_t ap = smem_u32(sP), ads = smem_u32(sDS);
-      bool ok = mbar_wait(kv_full, 0, kWaitLimitNs);
+      bool ok = mbar_wait(kv_full, 0, prm.wait_ns);
       for (int u = 0; ok && u < nq; ++u) {
-        if (!mbar_wait(q_full, u & 1, kWaitLimitNs)) { ok = false; break; }
+        if (!mbar_wait(q_full, u & 1, prm.wait_ns)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -620,7 +646,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_f16_ss(tbase + kColDP, smem_desc(av + off, 16, 1024), smem_desc(ado + off, 16, 1024), id_sdp, kk > 0);
         }
         mma_commit(sdp_full);
-        if (!mbar_wait(ps_full, u & 1, kWaitLimitNs)) { ok = false; break; }
+        if (!mbar_wait(ps_full, u & 1, prm.wait_ns)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -638,6 +664,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit(mma_done);
       }
       if (!ok) raise_status(prm.status, DSV_ERR_TIMEOUT);
+      // every MMA issued completes before TMEM is released
+      mma_commit(mma_drain);
+      mbar_wait(mma_drain, 0, kDrainLimitNs);
     }
   } else {
     const int row = warp * 32 + lane;   // key slot of the tile
@@ -647,11 +676,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     for (int u = 0; u < nq; ++u) {
       // P^T/dS^T smem and the S/dP TMEM columns are free once tile u-1's MMAs are done
-      if (u >= 1) ok = ok && mbar_wait_warp(mma_done, (u - 1) & 1, kWaitLimitNs);
+      if (u >= 1) ok = ok && mbar_wait_warp(mma_done, (u - 1) & 1, prm.wait_ns);
       sLse[row] = prm.LSE[(int64_t)prow0 + u * 128 + row] * 1.4426950408889634f;
       sDelta[row] = delta_all[(int64_t)prow0 + u * 128 + row];
       compute_barrier();
-      ok = ok && mbar_wait_warp(sdp_full, u & 1, kWaitLimitNs);
+      ok = ok && mbar_wait_warp(sdp_full, u & 1, prm.wait_ns);
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -682,7 +711,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       compute_barrier();   // sLse/sDelta reads done before the next tile overwrites them
       if (lane == 0) mbar_arrive(ps_full);
     }
-    if (ok && !mbar_wait_warp(mma_done, (nq - 1) & 1, kWaitLimitNs)) ok = false;
+    if (ok && !mbar_wait_warp(mma_done, (nq - 1) & 1, prm.wait_ns)) ok = false;
     if (!ok) {
       if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
     } else {
@@ -1167,6 +1196,7 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
   prm.LSE = LSE;
   prm.out = static_cast<__nv_bfloat16*>(dQ);
   prm.status = dev_status;
+  prm.wait_ns = wait_limit_ns();
   CscParams csc;
   memset(&csc, 0, sizeof(csc));
   csc.bits = w.bits;

@@ -29,6 +29,7 @@ struct AttnParams {
   __nv_bfloat16* out;        // fwd: O; bwd: dQ
   float* lse_out;            // fwd
   int32_t* status;
+  uint64_t wait_ns;          // limit of each pipeline wait
 };
 
 // 4D map over a [P*T][Y][X][d] view of a [P][S][d] tensor.

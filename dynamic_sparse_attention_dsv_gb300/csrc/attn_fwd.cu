@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   uint64_t* o_ready = bars + 17;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 18);
   uint64_t* q_tm = bars + 19;                   // Q copied into TMEM by the eight softmax warps
+  uint64_t* mma_done = bars + 20;               // every MMA issued has completed (unwind)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x, lp = blockIdx.y;
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
     mbar_init(o_ready, 1);
     mbar_init(q_tm, 8);
+    mbar_init(mma_done, 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -122,6 +124,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   const uint32_t tbase = *tslot;
 
   // ------------------------------------------------------------- producers
+  // Producers leave only once their own copies have landed (a timed-out
+  // pipeline may not have consumed them): cp.async by waiting for all of this
+  // thread's copies, TMA by waiting for the last phase of each barrier armed.
   auto produce = [&](const int pw) {
     const int ct = g / (geo.ncy * geo.ncx), cy = (g / geo.ncx) % geo.ncy, cx = g % geo.ncx;
     if (pw == 0 && lane == 0) {
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < Gather<D, W>::kIters; ++i) rows[i] = nxt[i];
         if (t + 1 < nt) gather_rows<D, W>(nxt, idx_row, k, t + 1, prow0, pw, lane);
-        if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, kWaitLimitNs)) {
+        if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, prm.wait_ns)) {
           if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
           break;
         }
@@ -148,10 +153,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         gather_tile<D, W>(sV + s * C::kTile, prm.V, rows, pw, lane);
         cp_async_arrive_noinc(v_full + s);
       }
+      asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (pw == 0) {
+      int issued = 0;
       for (int t = 0; t < nt; ++t) {
         const int s = t % C::kStages;
-        if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, kWaitLimitNs)) {
+        if (t >= C::kStages && !mbar_wait_warp(kv_empty + s, ((t / C::kStages) - 1) & 1, prm.wait_ns)) {
           if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
           break;
         }
@@ -161,8 +168,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           mbar_arrive_expect_tx(v_full + s, C::kTile);
           load_dense_tile<D>(sV + s * C::kTile, &maps.v_tile, v_full + s, t, prow0);
         }
+        issued = t + 1;
       }
+      if (lane == 0)
+        for (int t = max(0, issued - C::kStages); t < issued; ++t) {
+          mbar_wait(k_full + t % C::kStages, (t / C::kStages) & 1, kDrainLimitNs);
+          mbar_wait(v_full + t % C::kStages, (t / C::kStages) & 1, kDrainLimitNs);
+        }
     }
+    if (pw == 0 && lane == 0) mbar_wait(q_full, 0, kDrainLimitNs);
   };
   if (warp >= kProdWarp && warp < kMmaWarp) {
     setmaxnreg_dec<C::kRegsLoad>();
@@ -177,12 +191,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       constexpr uint32_t idesc_qk = instr_desc(128, 128, 1, 0, 0);
       constexpr uint32_t idesc_pv = instr_desc(128, D, 1, 0, 1);
       // Q is read from TMEM: the shared-memory operand traffic of S = Q K^T halves
-      bool ok = mbar_wait(q_tm, 0, kWaitLimitNs);
+      bool ok = mbar_wait(q_tm, 0, prm.wait_ns);
       tc_fence_after();
       auto issue_pv = [&](int t) -> bool {
         const int s = t % C::kStages, b = t & 1;
-        if (!mbar_wait(p_full + b, (t >> 1) & 1, kWaitLimitNs)) return false;
-        if (!mbar_wait(v_full + s, (t / C::kStages) & 1, kWaitLimitNs)) return false;
+        if (!mbar_wait(p_full + b, (t >> 1) & 1, prm.wait_ns)) return false;
+        if (!mbar_wait(v_full + s, (t / C::kStages) & 1, prm.wait_ns)) return false;
         fence_proxy_async_smem();   // rows written by cp.async (generic proxy) -> tensor core reads
         tc_fence_after();
         const uint64_t dv0 = smem_desc(smem_u32(sV + s * C::kTile), 16384, 1024);
@@ -196,7 +210,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       };
       for (int t = 0; ok && t < nt; ++t) {
         const int s = t % C::kStages, b = t & 1;
-        if (!mbar_wait(k_full + s, (t / C::kStages) & 1, kWaitLimitNs)) { ok = false; break; }
+        if (!mbar_wait(k_full + s, (t / C::kStages) & 1, prm.wait_ns)) { ok = false; break; }
         fence_proxy_async_smem();
         tc_fence_after();
         const uint64_t dk0 = smem_desc(smem_u32(sK + s * C::kTile), 16, 1024);
@@ -211,6 +225,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       }
       if (ok && nt > 0) ok = issue_pv(nt - 1);
       if (!ok) raise_status(prm.status, DSV_ERR_TIMEOUT);
+      // every MMA issued completes before TMEM is released
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0, kDrainLimitNs);
     }
   } else {
     // ----------------------------------------------------- softmax (warps 0-7)
@@ -236,7 +253,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     constexpr int kOChunks = D / 64;   // 32-column chunks of O per warp
     const float sc = prm.scale_log2;
     float m = -INFINITY, l = 0.f;
-    bool ok = mbar_wait_warp(q_full, 0, kWaitLimitNs);
+    bool ok = mbar_wait_warp(q_full, 0, prm.wait_ns);
     {
       // this warp's 32 rows of Q, half of the columns, from the swizzled tile into TMEM
       constexpr int kQc = D / 16;   // 16-byte chunks
@@ -261,7 +278,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
     for (int t = 0; t < nt; ++t) {
       const int b = t & 1;
-      ok = ok && mbar_wait_warp(s_full + b, (t >> 1) & 1, kWaitLimitNs);
+      ok = ok && mbar_wait_warp(s_full + b, (t >> 1) & 1, prm.wait_ns);
       tc_fence_after();
       uint32_t r[2][32];
       tmem_ld32(lane_addr + b * 128 + half * 64, r[0]);
@@ -296,7 +313,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       } else if (__any_sync(0xffffffffu, want)) {
         // O must be quiescent: wait for PV(t-1), then rescale the rows whose
         // max grew (warp-collective TMEM access; other rows use factor 1)
-        ok = ok && mbar_wait_warp(o_ready, (t - 1) & 1, kWaitLimitNs);
+        ok = ok && mbar_wait_warp(o_ready, (t - 1) & 1, prm.wait_ns);
         waited = true;
         const float f = want ? ex2_fast(m - mt) : 1.f;
         if (ok) {
@@ -350,13 +367,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       // P of keys 64*half .. +63, packed two per column, in place of S
       tmem_st32(lane_addr + b * 128 + half * 32, pk);
       tmem_st_wait();
-      if (t >= 1 && !waited) ok = ok && mbar_wait_warp(o_ready, (t - 1) & 1, kWaitLimitNs);
+      if (t >= 1 && !waited) ok = ok && mbar_wait_warp(o_ready, (t - 1) & 1, prm.wait_ns);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full + b);
     }
     // ---------------------------------------------------------- epilogue
-    if (nt > 0) ok = ok && mbar_wait_warp(o_ready, (nt - 1) & 1, kWaitLimitNs);
+    if (nt > 0) ok = ok && mbar_wait_warp(o_ready, (nt - 1) & 1, prm.wait_ns);
     l += exchange(l, ok);
     if (!ok) {
       if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
@@ -495,6 +512,7 @@ extern "C" dsv_status dsv_sparse_attn_fwd(const void* Q, const void* K, const vo
   prm.out = static_cast<__nv_bfloat16*>(O);
   prm.lse_out = LSE;
   prm.status = dev_status;
+  prm.wait_ns = wait_limit_ns();
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const cudaError_t e = d == 128 ? launch_fwd<128>(maps, prm, tab, geo.n_groups, st)
                                  : launch_fwd<64>(maps, prm, tab, geo.n_groups, st);

@@ -13,7 +13,11 @@
 namespace dsv {
 
 constexpr int kMaxProblems = 256;                     // B*H per call
-constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s per bounded wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;      // default limit of a bounded wait (2 s)
+// Limit of the waits that drain copies and MMAs a block has already issued,
+// after one of its pipeline waits ran out: those complete whatever the
+// pipeline's state, so this one does not follow the settable limit.
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 // Per-problem table passed by value as a kernel parameter (3 KB).
 struct ProblemTable {
@@ -51,6 +55,12 @@ __host__ __device__ inline int32_t token_of(const Geometry& q, int32_t g, int32_
 __device__ __forceinline__ void raise_status(int32_t* st, int32_t code) {
   if (st) atomicMax(st, code);
 }
+// Raises a consistency-check failure only when nothing was raised before:
+// after a wait ran out, the later kernels of the call see incomplete data,
+// and the status word keeps reporting the cause.
+__device__ __forceinline__ void raise_status_if_clear(int32_t* st, int32_t code) {
+  if (st && atomicAdd(st, 0) == 0) atomicMax(st, code);
+}
 
 // Float -> uint32 with the same ordering (-0 and +0 must be unified first).
 __host__ __device__ __forceinline__ uint32_t f2ord(float f) {
@@ -86,6 +96,10 @@ struct Carver {
 
 // Checks shape/group/pointers common to every call. Returns DSV_OK or the error.
 dsv_status validate_common(const dsv_shape& s, const dsv_group& g, bool need_d_supported);
+
+// The pipeline wait limit passed to every kernel launched from now on
+// (kWaitLimitNs unless dsv_set_wait_limit_ns changed it).
+uint64_t wait_limit_ns();
 
 // Returns the driver's tensor-map encoder (resolved once).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();

@@ -1,6 +1,7 @@
 // Host-side pieces shared by every libdsv entry point: status strings,
 // validation, the tensor-map encoder and the head dispatcher.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <vector>
@@ -22,6 +23,10 @@ dsv_status validate_common(const dsv_shape& s, const dsv_group& g, bool need_d_s
   if (need_d_supported && s.d != 64 && s.d != 128) return DSV_ERR_UNSUPPORTED;
   return DSV_OK;
 }
+
+static std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -68,6 +73,8 @@ extern "C" const char* dsv_status_string(dsv_status s) {
   }
   return "DSV_ERR_UNKNOWN";
 }
+
+extern "C" uint64_t dsv_set_wait_limit_ns(uint64_t ns) { return g_wait_limit_ns.exchange(ns); }
 
 extern "C" dsv_status dsv_read_status(const int32_t* dev_status, int32_t* host_out, void* stream) {
   if (!dev_status || !host_out) return DSV_ERR_INVALID_ARG;

@@ -104,6 +104,7 @@ struct SelParams {
   uint32_t* eq_bits;     // same layout: keys inside a single-valued interval
   const int32_t* cwin;   // COV_FINE: [n][g_pad][2] window of coarse bins [wa, wb]
   int32_t* status;
+  uint64_t wait_ns;      // limit of each pipeline wait
 };
 
 __device__ __forceinline__ float tf32_rna(float x) {
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   uint64_t* s_full = bars + 5;            // [2]
   uint64_t* s_empty = bars + 7;           // [2]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* mma_done = bars + 11;         // every MMA issued has completed (unwind)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gtile = blockIdx.x, chunk = blockIdx.y, lp = blockIdx.z;
@@ -196,6 +198,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       mbar_init(s_full + i, 1);
       mbar_init(s_empty + i, 8);
     }
+    mbar_init(mma_done, 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -214,9 +217,10 @@ __global__ void __launch_bounds__(kSelThreads, 2)
         tma_load_2d(sAhi + a * 16384, &map_qhi, a_full, a * 32, ya);
         tma_load_2d(sAlo + a * 16384, &map_qlo, a_full, a * 32, ya);
       }
+      int issued = 0;
       for (int i = 0; i < nt; ++i) {
         const int s = i % C::kStages;
-        if (i >= C::kStages && !mbar_wait(b_empty + s, ((i / C::kStages) - 1) & 1, kWaitLimitNs)) {
+        if (i >= C::kStages && !mbar_wait(b_empty + s, ((i / C::kStages) - 1) & 1, prm.wait_ns)) {
           raise_status(prm.status, DSV_ERR_TIMEOUT);
           break;
         }
@@ -228,18 +232,23 @@ __global__ void __launch_bounds__(kSelThreads, 2)
           tma_load_2d(bh + a * 16384, &map_khi, b_full + s, a * 32, yb);
           tma_load_2d(bl + a * 16384, &map_klo, b_full + s, a * 32, yb);
         }
+        issued = i + 1;
       }
+      // the block leaves only once every copy it started has landed
+      mbar_wait(a_full, 0, kDrainLimitNs);
+      for (int i = max(0, issued - C::kStages); i < issued; ++i)
+        mbar_wait(b_full + i % C::kStages, (i / C::kStages) & 1, kDrainLimitNs);
     }
   } else if (warp == 9) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idesc = instr_desc(128, 128, 2, 0, 0);
       const uint64_t dah0 = smem_desc(smem_u32(sAhi), 16, 1024), dal0 = smem_desc(smem_u32(sAlo), 16, 1024);
-      bool ok = mbar_wait(a_full, 0, kWaitLimitNs);
+      bool ok = mbar_wait(a_full, 0, prm.wait_ns);
       for (int i = 0; ok && i < nt; ++i) {
         const int s = i % C::kStages, b = i & 1;
-        if (!mbar_wait(b_full + s, (i / C::kStages) & 1, kWaitLimitNs)) { ok = false; break; }
-        if (i >= 2 && !mbar_wait(s_empty + b, ((i >> 1) - 1) & 1, kWaitLimitNs)) { ok = false; break; }
+        if (!mbar_wait(b_full + s, (i / C::kStages) & 1, prm.wait_ns)) { ok = false; break; }
+        if (i >= 2 && !mbar_wait(s_empty + b, ((i >> 1) - 1) & 1, prm.wait_ns)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tbase + b * 128;
         const uint64_t ah = opaque(dah0), al = opaque(dal0);
@@ -256,6 +265,9 @@ __global__ void __launch_bounds__(kSelThreads, 2)
         mma_commit(s_full + b);
       }
       if (!ok) raise_status(prm.status, DSV_ERR_TIMEOUT);
+      // every MMA issued completes before TMEM is released
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0, kDrainLimitNs);
     }
   } else {
     // ------------------------------------------------------- score consumers
@@ -338,7 +350,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
 
     for (int i = 0; i < nt; ++i) {
       const int b = i & 1;
-      if (!mbar_wait_warp(s_full + b, (i >> 1) & 1, kWaitLimitNs)) {
+      if (!mbar_wait_warp(s_full + b, (i >> 1) & 1, prm.wait_ns)) {
         if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
         break;
       }
@@ -504,7 +516,7 @@ template <int RP>
 __global__ void __launch_bounds__(128) k_key_proj(const __grid_constant__ CUtensorMap kmap,
                                                   const __nv_bfloat16* __restrict__ Wk, int R, int64_t H, int d,
                                                   int S, float* __restrict__ khi, float* __restrict__ klo,
-                                                  int32_t* status, const ProblemTable tab) {
+                                                  int32_t* status, uint64_t wait_ns, const ProblemTable tab) {
   using C = ProjCfg<RP>;
   extern __shared__ uint8_t proj_smem[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(proj_smem) + 1023) & ~uintptr_t(1023));
@@ -541,10 +553,11 @@ __global__ void __launch_bounds__(128) k_key_proj(const __grid_constant__ CUtens
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  bool ok = true;
+  bool ok = true, issued = false;
   if (tid == 0) {
-    ok = mbar_wait(a_full, 0, kWaitLimitNs);
+    ok = mbar_wait(a_full, 0, wait_ns);
     if (ok) {
+      issued = true;
       constexpr uint32_t idesc = instr_desc(128, RP, 1, 0, 0);
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
       for (int kk = 0; kk < d / 16; ++kk) {
@@ -558,7 +571,7 @@ __global__ void __launch_bounds__(128) k_key_proj(const __grid_constant__ CUtens
     }
   }
   // every thread waits for the accumulator (the issuing thread's failure shows as a timeout here too)
-  ok = mbar_wait_warp(d_full, 0, kWaitLimitNs);
+  ok = mbar_wait_warp(d_full, 0, wait_ns);
   if (ok) {
     tc_fence_after();
     const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
@@ -584,6 +597,10 @@ __global__ void __launch_bounds__(128) k_key_proj(const __grid_constant__ CUtens
     }
   } else if ((tid & 31) == 0) {
     raise_status(status, DSV_ERR_TIMEOUT);
+  }
+  if (tid == 0) {   // the tile's copy and MMAs complete before the block leaves
+    mbar_wait(a_full, 0, kDrainLimitNs);
+    if (issued) mbar_wait(d_full, 0, kDrainLimitNs);
   }
   tc_fence_before();
   __syncthreads();
@@ -697,7 +714,7 @@ __global__ void k_bracket(uint32_t* hist, int nb, int g_pad, int n_groups, int n
   int above = 0;
   int b = find_kth_bin(h, nb, g_pad, k, 0, &above);
   if (b < 0) {   // fewer than k scores: cannot happen for 1 <= k <= S
-    raise_status(status, DSV_ERR_CANDIDATES);
+    raise_status_if_clear(status, DSV_ERR_CANDIDATES);
     b = 0;
   }
   const uint32_t count = h[(size_t)b * g_pad];
@@ -740,7 +757,7 @@ __global__ void k_refine_bracket(uint32_t* hist, int nb, int log2nb, int g_pad, 
   int above = 0;
   const int b = find_kth_bin(h, nb, g_pad, k, nabove[rid], &above);
   if (b < 0) {   // the sub-bins hold fewer scores than the interval did: inconsistent
-    raise_status(status, DSV_ERR_CANDIDATES);
+    raise_status_if_clear(status, DSV_ERR_CANDIDATES);
     rstate[rid] = kRowTied;
     nabove[rid] = k;
     return;
@@ -778,7 +795,7 @@ __global__ void __launch_bounds__(256) k_resolve(const uint64_t* __restrict__ ca
   const uint32_t ncand = cand_cnt[rid];
   if (st != kRowCollect || ncand != bcount[rid] || ncand > (uint32_t)kCandCap || need < 1 ||
       (uint32_t)need > ncand) {
-    if (tid == 0) raise_status(status, DSV_ERR_CANDIDATES);
+    if (tid == 0) raise_status_if_clear(status, DSV_ERR_CANDIDATES);
     return;
   }
   uint32_t* row_bits = sel_bits + (size_t)rid * n_words;
@@ -928,7 +945,7 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_sel_compact(const uint32
     }
     base += total;
   }
-  if (threadIdx.x == 0 && row_total != k) raise_status(status, DSV_ERR_CANDIDATES);
+  if (threadIdx.x == 0 && row_total != k) raise_status_if_clear(status, DSV_ERR_CANDIDATES);
 }
 
 // Rows with k == S select every key.
@@ -1383,15 +1400,15 @@ static cudaError_t launch_proj(int r, const void* Q, const void* K, const void* 
     return cudaErrorInvalidValue;
   switch (r) {
     case 16:
-      k_key_proj<32><<<gk, 128, ProjCfg<32>::kSmem, st>>>(kmap, Wkp, 16, s.H, d, pl.geo.S, w.khi, w.klo, status, tab);
+      k_key_proj<32><<<gk, 128, ProjCfg<32>::kSmem, st>>>(kmap, Wkp, 16, s.H, d, pl.geo.S, w.khi, w.klo, status, wait_limit_ns(), tab);
       k_group_mean_proj<16><<<gq, 128, 0, st>>>(Qp, Wqp, s.H, d, pl.geo, pl.g_pad, w.qhi, w.qlo, tab);
       break;
     case 32:
-      k_key_proj<32><<<gk, 128, ProjCfg<32>::kSmem, st>>>(kmap, Wkp, 32, s.H, d, pl.geo.S, w.khi, w.klo, status, tab);
+      k_key_proj<32><<<gk, 128, ProjCfg<32>::kSmem, st>>>(kmap, Wkp, 32, s.H, d, pl.geo.S, w.khi, w.klo, status, wait_limit_ns(), tab);
       k_group_mean_proj<32><<<gq, 128, 0, st>>>(Qp, Wqp, s.H, d, pl.geo, pl.g_pad, w.qhi, w.qlo, tab);
       break;
     default:
-      k_key_proj<64><<<gk, 128, ProjCfg<64>::kSmem, st>>>(kmap, Wkp, 64, s.H, d, pl.geo.S, w.khi, w.klo, status, tab);
+      k_key_proj<64><<<gk, 128, ProjCfg<64>::kSmem, st>>>(kmap, Wkp, 64, s.H, d, pl.geo.S, w.khi, w.klo, status, wait_limit_ns(), tab);
       k_group_mean_proj<64><<<gq, 128, 0, st>>>(Qp, Wqp, s.H, d, pl.geo, pl.g_pad, w.qhi, w.qlo, tab);
       break;
   }
@@ -1442,6 +1459,7 @@ static SelParams sel_params(const TopkPlan& pl, const TopkWs& w, int n_chunks, i
   prm.eq_bits = w.eqb;
   prm.cwin = w.cov_win;
   prm.status = status;
+  prm.wait_ns = wait_limit_ns();
   return prm;
 }
 

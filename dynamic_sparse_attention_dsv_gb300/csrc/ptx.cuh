@@ -48,8 +48,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Waits for the phase with the given parity to complete. Returns false if it
 // has not completed after `limit_ns` nanoseconds of wall-clock time.
+// A limit of 0 gives up at once if the phase has not completed.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (limit_ns == 0) return false;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;

@@ -41,6 +41,7 @@ _U8P = ctypes.POINTER(ctypes.c_uint8)
 SIGNATURES = [
     ("dsv_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("dsv_read_status", ctypes.c_int, [_P, _I32P, _P]),
+    ("dsv_set_wait_limit_ns", ctypes.c_uint64, [ctypes.c_uint64]),
     ("dsv_lowrank_topk_workspace_size", ctypes.c_size_t, [dsv_shape, ctypes.c_int32, dsv_group]),
     ("dsv_lowrank_topk", ctypes.c_int, [_P, _P, _P, _P, dsv_shape, ctypes.c_int32, dsv_group, _I32P, _I64P, _P, _P,
                                         ctypes.c_size_t, _P, _P]),

@@ -28,7 +28,9 @@
  *    Launch failures return DSV_ERR_CUDA. Conditions found on the device
  *    (a wait that ran out) are written to the caller's device word `dev_status`
  *    (int32, zero it before the call; libdsv only ever raises it), which the
- *    caller reads after synchronising (dsv_read_status does both).
+ *    caller reads after synchronising (dsv_read_status does both). After a
+ *    wait ran out, the call's later kernels see incomplete data; their
+ *    consistency checks then leave the word at DSV_ERR_TIMEOUT.
  *  - Supported sizes: d in {64, 128}; r in {16, 32, 64}; G = gt*gy*gx in
  *    {64, 128}; S a multiple of 128 and < 2^31; 1 <= k <= S; B*H <= 256.
  */
@@ -70,6 +72,22 @@ const char* dsv_status_string(dsv_status s);
 /* Synchronises `stream`, then copies the device status word to *host_out.
  * Returns DSV_ERR_CUDA if either step fails. */
 dsv_status dsv_read_status(const int32_t* dev_status, int32_t* host_out, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsv_set_wait_limit_ns -- how long a kernel's pipeline waits before giving up.
+ * Not part of the DSV method (the pages have no counterpart): it sets the
+ * failure path that guards every wait inside the libdsv kernels. A wait that
+ * runs out raises DSV_ERR_TIMEOUT in the call's dev_status word and the block
+ * unwinds: it waits for the copies and MMAs it has already issued (those
+ * complete by themselves, under a fixed 2 s limit), releases its tensor
+ * memory and exits, so the call's outputs are incomplete but the context
+ * stays usable. The default is 2,000,000,000 ns (2 s). The value applies to
+ * every call launched after this returns, from any host thread of the
+ * process; the previous value is returned. 0 makes every wait that has not
+ * already completed give up at once, which is how the tests run the failure
+ * path; production code has no reason to lower it.
+ * ---------------------------------------------------------------------- */
+uint64_t dsv_set_wait_limit_ns(uint64_t ns);
 
 /* ------------------------------------------------------------------------
  * dsv_lowrank_topk -- fused low-rank MatMul + per-group Top-K.

@@ -182,3 +182,14 @@ def test_plan_gpus_matches_oracle(lib):
 def test_topk_layout_packs_rows():
     ks, offs, total = api.topk_layout(3, 16, [5, 7, 9], skip=[False, True, False])
     assert offs == [0, -1, 80] and total == 80 + 16 * 9
+
+
+def test_wait_limit_setter_is_host_only(lib):
+    """dsv_set_wait_limit_ns only swaps a host value (no CUDA call): it works
+    without a GPU and returns the previous limit (2 s by default)."""
+    prev = lib.dsv_set_wait_limit_ns(7)
+    try:
+        assert prev == 2_000_000_000
+        assert lib.dsv_set_wait_limit_ns(11) == 7
+    finally:
+        lib.dsv_set_wait_limit_ns(prev)
