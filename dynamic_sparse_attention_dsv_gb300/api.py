@@ -264,6 +264,30 @@ def attn_mass(LSE_sel, LSE_all, per_query: bool = False):
     return mass, pq
 
 
+def predicted_mass(Q, K, Wq, Wk, grid, group, idx=None, k_per_head=None, idx_offset=None,
+                   scale: Optional[float] = None, per_query: bool = False, workspace=None, status=None):
+    """dsv_predicted_mass: the share of each query's own predicted softmax
+    mass that its group's selected keys carry. idx=None: every key.
+    Returns (mean per problem float32 [P], per-query shares [P, S] or None)."""
+    _check_bf16(Q, K, Wq, Wk)
+    lib = N.load()
+    shape, grp = make_shape(Q, grid), make_group(group)
+    P, S = shape.B * shape.H, shape.T * shape.Y * shape.X
+    scale = 1.0 / math.sqrt(shape.d) if scale is None else float(scale)
+    r = Wq.shape[-1]
+    mass = torch.empty(P, dtype=torch.float32, device=Q.device)
+    pq = torch.empty((P, S), dtype=torch.float32, device=Q.device) if per_query else None
+    ws = _workspace(int(lib.dsv_predicted_mass_workspace_size(shape, r, grp)), Q.device, workspace)
+    st = status if status is not None else new_status(Q.device)
+    kp = _i32(k_per_head) if idx is not None else None
+    op = _i64(idx_offset) if idx is not None else None
+    code = lib.dsv_predicted_mass(_ptr(Q), _ptr(K), _ptr(Wq), _ptr(Wk), shape, r, grp, _ptr(idx), kp, op,
+                                  ctypes.c_float(scale), _ptr(mass), _ptr(pq), _ptr(ws), ws.numel(), _ptr(st),
+                                  _stream())
+    N.check(code, "dsv_predicted_mass")
+    return mass, pq
+
+
 def sparse_attn_bwd_min_workspace_size(x, grid, group, k_per_head=None, idx_offset=None) -> int:
     kp = _i32(k_per_head) if k_per_head is not None else None
     op = _i64(idx_offset) if idx_offset is not None else None

@@ -40,7 +40,7 @@
 #include <mutex>
 #include <vector>
 
-#include "common.cuh"
+#include "attn_common.cuh"
 
 namespace dsv {
 
@@ -53,7 +53,7 @@ constexpr int kMaxChunks = 64;     // key chunks per row
 // chain costs its ramp-up and tail.
 constexpr size_t kProjBudget = 1ull << 30;
 
-enum SelMode { kMinMax = 0, kHist = 1, kCollect = 2, kRefine = 3, kCov = 4, kCovFine = 5 };
+enum SelMode { kMinMax = 0, kHist = 1, kCollect = 2, kRefine = 3, kCov = 4, kCovFine = 5, kMass = 6 };
 
 // Per-row state of the boundary interval after each bracket step.
 enum RowState { kRowCollect = 0, kRowRefine = 1, kRowTied = 2 };
@@ -76,11 +76,12 @@ struct SelCfg {
   static constexpr int kOffHist = kOffB + kStages * 2 * kTileBytes;
   static constexpr int kOffMisc = kOffHist + kHistBytes;
   static constexpr int kSmem = kOffMisc + 256 + 1024;  // + barriers, + alignment slack
-  // MINMAX keeps no histogram: a 2 KB exchange area, then the barriers,
+  // MINMAX and MASS keep no histogram: a 2 KB exchange area, then the barriers,
   // so two blocks share an SM and one's start and finish overlap the other's work
   static constexpr int kOffMiscSmall = kOffHist + 2048;
   static constexpr int kSmemSmall = kOffMiscSmall + 256 + 1024;
-  __host__ __device__ static constexpr bool big(int mode) { return mode != 0; }   // all but MINMAX
+  // all but MINMAX and MASS keep a histogram area
+  __host__ __device__ static constexpr bool big(int mode) { return mode != kMinMax && mode != kMass; }
   __host__ __device__ static constexpr int smem(int mode) { return big(mode) ? kSmem : kSmemSmall; }
   __host__ __device__ static constexpr int off_misc(int mode) { return big(mode) ? kOffMisc : kOffMiscSmall; }
 };
@@ -103,6 +104,10 @@ struct SelParams {
   uint32_t* sel_bits;    // [n][g_pad][n_tiles][4] keys scoring >= bhi, 32 keys per word
   uint32_t* eq_bits;     // same layout: keys inside a single-valued interval
   const int32_t* cwin;   // COV_FINE: [n][g_pad][2] window of coarse bins [wa, wb]
+  // MASS (rows are single queries in group-major order):
+  const uint32_t* qsel;  // [n][qn_groups][S/32] selection bitmap of each query group
+  float* msum;           // [n][chunks][g_pad][2] per-row sums of exp(scale (s - max)): all keys, selected keys
+  int32_t q_group, qn_groups;   // queries per group, groups per problem
   int32_t* status;
   uint64_t wait_ns;      // limit of each pipeline wait
 };
@@ -315,6 +320,16 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       }
       if (MODE == kRefine && state != kRowRefine) owid = 0;   // this row takes no part
     }
+    // MASS: this row's maximum score, the scale in log2 units, its group's
+    // selection words and the running sums
+    float m_sc = 0.f, m_all = 0.f, m_sel = 0.f;
+    const uint32_t* m_bits = nullptr;
+    if constexpr (MODE == kMass) {
+      cmax = ord2f(prm.mmax[rid]);
+      m_sc = prm.scale * 1.4426950408889634f;
+      const int gq = min(g, prm.geo.S - 1) / prm.q_group;
+      m_bits = prm.qsel + ((size_t)lp * prm.qn_groups + gq) * (size_t)(prm.geo.S / 32);
+    }
     float w2 = 0.f;   // coverage: coarse bin width in log2 units
     // fine bins: the row's window of coarse bins [wa, wb], NBc fine bins over
     // it (fine coordinate (x - wa) * fscale, fine width fw2 in log2 units)
@@ -335,7 +350,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       fscale = nw > 0 ? (float)NBc / (float)nw : 0.f;
       fw2 = nw > 0 ? w2 * (float)nw / (float)NBc : 0.f;
     }
-    if constexpr (MODE != kMinMax && MODE != kCollect) {
+    if constexpr (C::big(MODE) && MODE != kCollect) {
       // zero this CTA's private histograms
       uint32_t* h = reinterpret_cast<uint32_t*>(sHist);
       for (int i = tid; i < C::kHistBytes / 4; i += 256) h[i] = 0;
@@ -363,6 +378,8 @@ __global__ void __launch_bounds__(kSelThreads, 2)
         tmem_ld_wait(r0);
         reg_fence(r1);
         const int kb = key0 + half * 64;
+        uint64_t selm = 0;   // MASS: selected columns of this half-tile
+        if constexpr (MODE == kMass) selm = *reinterpret_cast<const uint64_t*>(m_bits + kb / 32);
         uint32_t gm_lo = 0, gm_hi = 0;   // COLLECT: columns scoring >= t_above
         uint32_t cm_lo = 0, cm_hi = 0;   // COLLECT: columns inside the boundary interval
 #pragma unroll
@@ -371,6 +388,11 @@ __global__ void __launch_bounds__(kSelThreads, 2)
           if constexpr (MODE == kMinMax) {
             mx = fmaxf(mx, s);
             mn = fminf(mn, s);
+          }
+          if constexpr (MODE == kMass) {
+            const float ev = ex2_fast(__fmul_rn(__fsub_rn(s, cmax), m_sc));   // exp(scale (s - max)) in (0, 1]
+            m_all += ev;
+            m_sel += ((selm >> e) & 1ull) ? ev : 0.f;
           }
           if constexpr (kCovLike) {
             // log-probability below the row maximum u, its coarse coordinate
@@ -457,6 +479,17 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     if constexpr (kCollectPart) {
       if (valid && n_st > 0) flush(n_st);
     }
+    if constexpr (MODE == kMass) {
+      float* ex = reinterpret_cast<float*>(sHist);   // [2][2][128] exchange of the two halves' sums
+      ex[(half * 2 + 0) * 128 + row] = m_all;
+      ex[(half * 2 + 1) * 128 + row] = m_sel;
+      epi_barrier();
+      if (half == 0 && valid) {
+        const size_t o = (((size_t)lp * prm.n_chunks + chunk) * prm.g_pad + g) * 2;
+        prm.msum[o] = m_all + ex[(2 + 0) * 128 + row];
+        prm.msum[o + 1] = m_sel + ex[(2 + 1) * 128 + row];
+      }
+    }
     if constexpr (MODE == kMinMax) {
       float* ex = reinterpret_cast<float*>(sHist);   // [2][2][128], the histogram area is unused here
       ex[(half * 2 + 0) * 128 + row] = mx;
@@ -469,7 +502,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
         atomicMin(prm.mmin + rid, f2ord(n2));
       }
     }
-    if constexpr (MODE != kMinMax && MODE != kCollect) epi_barrier();
+    if constexpr (C::big(MODE) && MODE != kCollect) epi_barrier();
     if constexpr (kCovLike) {
       const uint32_t* h = reinterpret_cast<const uint32_t*>(sHist);
       const uint32_t* m = reinterpret_cast<const uint32_t*>(sHist + C::kCovMassOff);
@@ -652,6 +685,179 @@ __global__ void __launch_bounds__(128) k_group_mean_proj(const __nv_bfloat16* __
     qhi[((size_t)lp * g_pad + g) * RP + tid] = hi;
     qlo[((size_t)lp * g_pad + g) * RP + tid] = tf32_rna(v - hi);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Per-query predicted mass (the share of each query's own predicted softmax
+// mass that its group's selected keys carry).
+//
+// q_lr of every query, rows in group-major order (row g*G + member), split
+// into tf32 hi/lo parts like k_lr: one 128-row tile (one group of 128, or
+// two groups of 64, each brought in as one TMA box over the latent cube) per
+// block, the d/16 MMAs (128 x RP x 16, bf16 in, fp32 in TMEM), then hi/lo.
+template <int RP>
+__global__ void __launch_bounds__(128) k_query_proj(const __grid_constant__ CUtensorMap qcube,
+                                                    const __nv_bfloat16* __restrict__ Wq, int R, int64_t H, int d,
+                                                    Geometry geo, float* __restrict__ qhi, float* __restrict__ qlo,
+                                                    int32_t* status, uint64_t wait_ns, const ProblemTable tab) {
+  using C = ProjCfg<RP>;
+  extern __shared__ uint8_t qproj_smem[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qproj_smem) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = sm;
+  uint8_t* sB = sm + C::kOffB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  uint64_t* a_full = bars;
+  uint64_t* d_full = bars + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+  const int lp = blockIdx.y, p = tab.p[lp], h = p % H;
+  const int tid = threadIdx.x, warp = tid >> 5, r0 = blockIdx.x * 128;
+  const int S = geo.S;
+  if (warp == 0) {
+    tmem_alloc(tslot, RP);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(a_full, 1);
+    mbar_init(d_full, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(a_full, 128 * d * 2);
+    for (int gi = 0; gi < 128 / geo.G; ++gi) {
+      const int g = r0 / geo.G + gi;
+      const int ct = g / (geo.ncy * geo.ncx), cy = (g / geo.ncx) % geo.ncy, cx = g % geo.ncx;
+      for (int a = 0; a < d / 64; ++a)
+        tma_load_4d(sA + a * 16384 + gi * geo.G * 128, &qcube, a_full, a * 64, cx * geo.gx, cy * geo.gy,
+                    p * geo.T + ct * geo.gt);
+    }
+  }
+  const __nv_bfloat16* W = Wq + (size_t)h * d * R;
+  for (int i = tid; i < RP * d; i += 128) {
+    const int c = i / RP, n = i % RP;
+    const __nv_bfloat16 v = n < R ? W[c * R + n] : __float2bfloat16(0.f);
+    const int cc = c & 63;
+    *reinterpret_cast<__nv_bfloat16*>(sB + (c >> 6) * (RP * 128) + n * 128 + ((((cc >> 3) ^ (n & 7))) << 4) +
+                                      (cc & 7) * 2) = v;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  bool ok = true, issued = false;
+  if (tid == 0) {
+    ok = mbar_wait(a_full, 0, wait_ns);
+    if (ok) {
+      issued = true;
+      constexpr uint32_t idesc = instr_desc(128, RP, 1, 0, 0);
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      for (int kk = 0; kk < d / 16; ++kk) {
+        const uint32_t offa = (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t offb = (kk >> 2) * (RP * 128) + (kk & 3) * 32;
+        mma_f16_ss(tbase, smem_desc(a0 + offa, 16, 1024), smem_desc(b0 + offb, 16, 1024), idesc, kk > 0);
+      }
+      mma_commit(d_full);
+    } else {
+      raise_status(status, DSV_ERR_TIMEOUT);
+    }
+  }
+  ok = mbar_wait_warp(d_full, 0, wait_ns);
+  if (ok) {
+    tc_fence_after();
+    const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+    const size_t o = ((size_t)lp * S + r0 + tid) * RP;
+#pragma unroll
+    for (int c32 = 0; c32 < RP / 32; ++c32) {
+      uint32_t v[32];
+      tmem_ld32(lane_addr + c32 * 32, v);
+      tmem_ld_wait(v);
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        uint32_t hv[8], lv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float x = __uint_as_float(v[c8 * 8 + e]);
+          const float hi = tf32_rna(x);
+          hv[e] = __float_as_uint(hi);
+          lv[e] = __float_as_uint(tf32_rna(x - hi));
+        }
+        st_global_v8(qhi + o + c32 * 32 + c8 * 8, hv);
+        st_global_v8(qlo + o + c32 * 32 + c8 * 8, lv);
+      }
+    }
+  } else if ((tid & 31) == 0) {
+    raise_status(status, DSV_ERR_TIMEOUT);
+  }
+  if (tid == 0) {   // the tile's copies and MMAs complete before the block leaves
+    mbar_wait(a_full, 0, kDrainLimitNs);
+    if (issued) mbar_wait(d_full, 0, kDrainLimitNs);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, RP);
+}
+
+// Selection bitmap of each query group (bit j of row (p, g): key j is in the
+// group's index set); a dense problem (offset -1) selects every key. One
+// block per (group, problem), built in shared memory (S/32 words). Keys
+// outside [0, S) are ignored.
+__global__ void __launch_bounds__(256) k_idx_bitmap(const int32_t* __restrict__ idx, int S, int n_groups,
+                                                    uint32_t* bits, const ProblemTable tab) {
+  extern __shared__ uint32_t sbits[];
+  const int g = blockIdx.x, lp = blockIdx.y, tid = threadIdx.x;
+  const int nw = S / 32;
+  const bool dense = tab.off[lp] < 0;
+  for (int i = tid; i < nw; i += blockDim.x) sbits[i] = dense ? ~0u : 0u;
+  __syncthreads();
+  if (!dense) {
+    const int k = tab.k[lp];
+    const int32_t* row = idx + tab.off[lp] + (int64_t)g * k;
+    for (int i = tid; i < k; i += blockDim.x) {
+      const int j = __ldg(row + i);
+      if (j >= 0 && j < S) atomicOr(sbits + (j >> 5), 1u << (j & 31));
+    }
+  }
+  __syncthreads();
+  uint32_t* out = bits + ((size_t)lp * n_groups + g) * nw;
+  for (int i = tid; i < nw; i += blockDim.x) out[i] = sbits[i];
+}
+
+// Per query: the share m = (sum over selected keys) / (sum over all keys) of
+// exp(scale (s - max)), the chunks' partial sums added in chunk order in
+// fp64; written at the query's token position (optional) and summed per
+// block of 256 queries in a fixed tree for the per-problem mean.
+constexpr int kMassThreadsR = 256;
+__global__ void __launch_bounds__(kMassThreadsR) k_mass_reduce(const float* __restrict__ msum, int n_chunks,
+                                                               Geometry geo, float* per_query, double* block_sums,
+                                                               const ProblemTable tab) {
+  __shared__ double part[kMassThreadsR];
+  const int lp = blockIdx.y, tid = threadIdx.x;
+  const int r = blockIdx.x * kMassThreadsR + tid;   // row in group-major order
+  double m = 0.0;
+  if (r < geo.S) {
+    double a = 0.0, sel = 0.0;
+    for (int c = 0; c < n_chunks; ++c) {
+      const size_t o = (((size_t)lp * n_chunks + c) * geo.S + r) * 2;
+      a += (double)msum[o];
+      sel += (double)msum[o + 1];
+    }
+    m = a > 0.0 ? sel / a : 0.0;
+    if (per_query) per_query[(int64_t)tab.p[lp] * geo.S + token_of(geo, r / geo.G, r % geo.G)] = (float)m;
+  }
+  part[tid] = m;
+  __syncthreads();
+  for (int w = kMassThreadsR / 2; w > 0; w >>= 1) {
+    if (tid < w) part[tid] += part[tid + w];
+    __syncthreads();
+  }
+  if (tid == 0) block_sums[(size_t)lp * gridDim.x + blockIdx.x] = part[0];
+}
+
+// Per problem: the mean over its S queries, block sums added in block order.
+__global__ void k_mass_mean(const double* block_sums, int nblk, int S, float* mass, const ProblemTable tab) {
+  const int lp = blockIdx.x;
+  if (threadIdx.x != 0) return;
+  double acc = 0.0;
+  for (int b = 0; b < nblk; ++b) acc += block_sums[(size_t)lp * nblk + b];
+  mass[tab.p[lp]] = (float)(acc / (double)S);
 }
 
 // ---------------------------------------------------------------------------
@@ -1770,6 +1976,168 @@ extern "C" dsv_status dsv_coverage_topk(const void* Q, const void* K, const void
     if (cov_passes(pl, w, tab, maps, true, scale, mass, k_cov, curve, n_curve, dev_status, st) != cudaSuccess)
       return DSV_ERR_CUDA;
     if (topk_passes(pl, w, tab, maps, false, idx, dev_status, st) != cudaSuccess) return DSV_ERR_CUDA;
+  }
+  return DSV_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Per-query predicted mass: workspace and launches.
+namespace dsv {
+
+struct MassWs {
+  float *khi, *klo, *qhi, *qlo;
+  uint32_t *mmax, *mmin, *bits;
+  float* msum;
+  double* bsum;
+};
+
+// The score passes of the per-query rows: one 128-query tile per row tile.
+static TopkPlan query_plan(const TopkPlan& pl) {
+  TopkPlan q = pl;
+  q.n_gt = pl.geo.S / 128;
+  q.g_pad = pl.geo.S;
+  return q;
+}
+
+// Problems per launch: the key and query projections within the budget.
+static int mass_problems_per_launch(const TopkPlan& pl, int P) {
+  const size_t per = (size_t)pl.geo.S * pl.RP * 16;
+  return (int)std::max<size_t>(1, std::min<size_t>((size_t)P, kProjBudget / per));
+}
+
+static size_t carve_mass(void* base, const TopkPlan& pl, int P, MassWs* w) {
+  const TopkPlan qp = query_plan(pl);
+  const int pc = mass_problems_per_launch(pl, P);
+  int max_chunks = 1, nc, ct;
+  for (int n_local : {pc, P % pc}) {
+    if (n_local <= 0) continue;
+    chunking(qp, n_local, &nc, &ct);
+    max_chunks = std::max(max_chunks, nc);
+  }
+  Carver c(base);
+  const size_t S = pl.geo.S, RP = pl.RP, n = pc;
+  w->khi = c.take<float>(n * S * RP);
+  w->klo = c.take<float>(n * S * RP);
+  w->qhi = c.take<float>(n * S * RP);
+  w->qlo = c.take<float>(n * S * RP);
+  w->mmax = c.take<uint32_t>(n * S);
+  w->mmin = c.take<uint32_t>(n * S);
+  w->bits = c.take<uint32_t>(n * pl.geo.n_groups * (S / 32));
+  w->msum = c.take<float>(n * max_chunks * S * 2);
+  w->bsum = c.take<double>(n * ((S + kMassThreadsR - 1) / kMassThreadsR));
+  return c.used + 256;
+}
+
+}  // namespace dsv
+
+extern "C" size_t dsv_predicted_mass_workspace_size(dsv_shape shape, int32_t r, dsv_group group) {
+  if (validate_common(shape, group, true) != DSV_OK || (r != 16 && r != 32 && r != 64)) return 0;
+  const TopkPlan pl = make_plan(shape, r, group);
+  MassWs w;
+  return carve_mass(nullptr, pl, (int)(shape.B * shape.H), &w);
+}
+
+extern "C" dsv_status dsv_predicted_mass(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr,
+                                         dsv_shape shape, int32_t r, dsv_group group, const int32_t* idx,
+                                         const int32_t* k_per_head, const int64_t* idx_offset, float scale,
+                                         float* mass, float* per_query, void* workspace, size_t workspace_bytes,
+                                         int32_t* dev_status, void* stream) {
+  dsv_status v = validate_lowrank(Q, K, Wq_lr, Wk_lr, shape, r, group);
+  if (v != DSV_OK) return v;
+  if (!mass || !(scale > 0.f) || !aligned(mass, 4) || (per_query && !aligned(per_query, 4)))
+    return DSV_ERR_INVALID_ARG;
+  if (idx && (!k_per_head || !idx_offset || !aligned(idx, 4))) return DSV_ERR_INVALID_ARG;
+  const TopkPlan pl = make_plan(shape, r, group);
+  const Geometry& geo = pl.geo;
+  const int P = (int)(shape.B * shape.H), S = geo.S, d = (int)shape.d;
+  if (S > 262144) return DSV_ERR_UNSUPPORTED;   // a group's bitmap is built in 32 KB of shared memory
+  if (idx)
+    for (int p = 0; p < P; ++p)
+      if (idx_offset[p] >= 0 && (k_per_head[p] < 1 || k_per_head[p] > S)) return DSV_ERR_INVALID_ARG;
+  MassWs w;
+  const size_t need = carve_mass(nullptr, pl, P, &w);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DSV_ERR_WORKSPACE;
+  carve_mass(workspace, pl, P, &w);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const TopkPlan qp = query_plan(pl);
+  const int pc = mass_problems_per_launch(pl, P);
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(k_key_proj<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, ProjCfg<32>::kSmem);
+    cudaFuncSetAttribute(k_key_proj<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, ProjCfg<64>::kSmem);
+    cudaFuncSetAttribute(k_query_proj<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, ProjCfg<32>::kSmem);
+    cudaFuncSetAttribute(k_query_proj<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, ProjCfg<64>::kSmem);
+    configured = true;
+  }
+  CUtensorMap kmap, qcube;
+  if (!make_map_2d(&kmap, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d, (uint64_t)P * S, 64, 128) ||
+      !make_cube_map(&qcube, Q, geo, d, P))
+    return DSV_ERR_CUDA;
+  auto Wk = static_cast<const __nv_bfloat16*>(Wk_lr);
+  auto Wq = static_cast<const __nv_bfloat16*>(Wq_lr);
+  const uint64_t lim = wait_limit_ns();
+  for (int c0 = 0; c0 < P; c0 += pc) {
+    ProblemTable tab;
+    memset(&tab, 0, sizeof(tab));
+    tab.n = std::min(pc, P - c0);
+    for (int i = 0; i < tab.n; ++i) {
+      const int p = c0 + i;
+      const bool dense = !idx || idx_offset[p] < 0;
+      tab.p[i] = p;
+      tab.k[i] = dense ? S : k_per_head[p];
+      tab.off[i] = dense ? -1 : idx_offset[p];
+    }
+    const int n = tab.n;
+    const dim3 pgrid(S / 128, n);
+    if (pl.RP == 32) {
+      k_key_proj<32><<<pgrid, 128, ProjCfg<32>::kSmem, st>>>(kmap, Wk, r, shape.H, d, S, w.khi, w.klo, dev_status,
+                                                              lim, tab);
+      k_query_proj<32><<<pgrid, 128, ProjCfg<32>::kSmem, st>>>(qcube, Wq, r, shape.H, d, geo, w.qhi, w.qlo,
+                                                                dev_status, lim, tab);
+    } else {
+      k_key_proj<64><<<pgrid, 128, ProjCfg<64>::kSmem, st>>>(kmap, Wk, r, shape.H, d, S, w.khi, w.klo, dev_status,
+                                                              lim, tab);
+      k_query_proj<64><<<pgrid, 128, ProjCfg<64>::kSmem, st>>>(qcube, Wq, r, shape.H, d, geo, w.qhi, w.qlo,
+                                                                dev_status, lim, tab);
+    }
+    k_idx_bitmap<<<dim3(geo.n_groups, n), 256, (size_t)(S / 32) * 4, st>>>(idx, S, geo.n_groups, w.bits, tab);
+    if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
+    const uint64_t RP = pl.RP;
+    CUtensorMap maps[4];
+    if (!make_map_2d(&maps[0], w.qhi, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, RP, (uint64_t)n * S, 32, 128) ||
+        !make_map_2d(&maps[1], w.qlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, RP, (uint64_t)n * S, 32, 128) ||
+        !make_map_2d(&maps[2], w.khi, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, RP, (uint64_t)n * S, 32, 128) ||
+        !make_map_2d(&maps[3], w.klo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, RP, (uint64_t)n * S, 32, 128))
+      return DSV_ERR_CUDA;
+    int n_chunks, chunk_tiles;
+    chunking(qp, n, &n_chunks, &chunk_tiles);
+    SelParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.geo = geo;
+    prm.geo.n_groups = S;   // rows of the score tiles are single queries
+    prm.g_pad = S;
+    prm.n_chunks = n_chunks;
+    prm.chunk_tiles = chunk_tiles;
+    prm.n_tiles = pl.n_tiles;
+    prm.n_gt = qp.n_gt;
+    prm.scale = scale;
+    prm.mmax = w.mmax;
+    prm.mmin = w.mmin;
+    prm.qsel = w.bits;
+    prm.msum = w.msum;
+    prm.q_group = geo.G;
+    prm.qn_groups = geo.n_groups;
+    prm.status = dev_status;
+    prm.wait_ns = lim;
+    const dim3 grid(qp.n_gt, n_chunks, n);
+    if (cudaMemsetAsync(w.mmax, 0, (size_t)n * S * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
+    if (cudaMemsetAsync(w.mmin, 0xFF, (size_t)n * S * 4, st) != cudaSuccess) return DSV_ERR_CUDA;
+    if (select_pass<kMinMax>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
+    if (select_pass<kMass>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return DSV_ERR_CUDA;
+    const int nblk = (S + kMassThreadsR - 1) / kMassThreadsR;
+    k_mass_reduce<<<dim3(nblk, n), kMassThreadsR, 0, st>>>(w.msum, n_chunks, geo, per_query, w.bsum, tab);
+    k_mass_mean<<<n, 32, 0, st>>>(w.bsum, nblk, S, mass, tab);
+    if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
   }
   return DSV_OK;
 }

@@ -48,6 +48,9 @@ SIGNATURES = [
     ("dsv_lowrank_topk_noalloc", ctypes.c_int, [_P, _P, _P, _P, dsv_shape, ctypes.c_int32, dsv_group, _I32P, _I64P,
                                                 _P, _P, _P]),
     ("dsv_coverage_workspace_size", ctypes.c_size_t, [dsv_shape, ctypes.c_int32, dsv_group]),
+    ("dsv_predicted_mass_workspace_size", ctypes.c_size_t, [dsv_shape, ctypes.c_int32, dsv_group]),
+    ("dsv_predicted_mass", ctypes.c_int, [_P, _P, _P, _P, dsv_shape, ctypes.c_int32, dsv_group, _P, _I32P, _I64P,
+                                          ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     ("dsv_coverage", ctypes.c_int, [_P, _P, _P, _P, dsv_shape, ctypes.c_int32, dsv_group, ctypes.c_float,
                                     ctypes.c_float, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P, _P]),
     ("dsv_coverage_topk_workspace_size", ctypes.c_size_t, [dsv_shape, ctypes.c_int32, dsv_group]),

@@ -267,6 +267,32 @@ dsv_status dsv_attn_mass(const float* LSE_sel, const float* LSE_all, int64_t S, 
                          float* per_query, void* stream);
 
 /* ------------------------------------------------------------------------
+ * dsv_predicted_mass -- share of each query's own predicted softmax mass
+ * that its group's selected keys carry.
+ * Passage: technical summary section 2.1 (critical KV are the pairs that
+ * carry over 90% of the attention score), read per query on the low-rank
+ * predictor's logits; dsv_coverage is the pooled, group-level reading.
+ *
+ * For query i of group g of problem p, with the predictor's logits
+ * l_ij = scale q_lr,i . k_lr,j over all S keys (q_lr = Q W_lr^Q,
+ * k_lr = K W_lr^K as in dsv_lowrank_topk, the score to about 2^-21
+ * relative): m_i = sum_{j in I_g} softmax_j(l_ij). idx, k_per_head and
+ * idx_offset are as for dsv_sparse_attn_fwd (idx == NULL or
+ * idx_offset[p] < 0: every key is selected and m_i = 1).
+ * mass: DEVICE float [B*H], the mean of m_i over the problem's S queries
+ * (fp64 sums in a fixed order: the same bits on every run). per_query
+ * (optional, may be NULL): DEVICE float [B*H][S] of m_i in token order.
+ * It scores every (query, key) pair, 3 tf32 products of rank r each: a
+ * diagnostic, not part of a training step. S <= 262144
+ * (DSV_ERR_UNSUPPORTED otherwise).
+ * ---------------------------------------------------------------------- */
+size_t dsv_predicted_mass_workspace_size(dsv_shape shape, int32_t r, dsv_group group);
+dsv_status dsv_predicted_mass(const void* Q, const void* K, const void* Wq_lr, const void* Wk_lr, dsv_shape shape,
+                              int32_t r, dsv_group group, const int32_t* idx, const int32_t* k_per_head,
+                              const int64_t* idx_offset, float scale, float* mass, float* per_query, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * dsv_sparse_attn_bwd -- query-grouped sparse attention, backward.
  * Passage: technical summary section 2.1 (stage 2 trains with sparse
  * attention over the critical KV, so gradients flow through the selected
