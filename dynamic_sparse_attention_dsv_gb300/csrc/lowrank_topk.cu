@@ -410,11 +410,15 @@ __global__ void __launch_bounds__(kSelThreads, 2)
               red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
               red_smem_u32(cmass_base + (uint32_t)(bin * 128 + row) * 4u, qf);
             } else {
+              // computed for every key without branching; only the two adds
+              // are predicated on the key lying in the row's window
+              const float y = fmaxf(__fmul_rn(__fsub_rn(x, (float)wa), fscale), 0.f);
+              const float ty = bin_round(y);
+              const int fb = bin_of(ty, NBc);
+              const float fy = y - fminf(ty - kRoundMagic, (float)(NBc - 1));   // in [0, 1], more when clamped
+              const float qv = ex2_fast(-fy * fw2);   // exp(fb fw - u'), in (exp(-fw), 1]
+              const uint32_t qf = __float_as_uint(fmaf(qv, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
               if (bin >= wa && bin <= wb) {
-                const float y = (x - (float)wa) * fscale;
-                const int fb = min(NBc - 1, max(0, (int)y));
-                const float qv = ex2_fast(((float)fb - y) * fw2);   // exp(fb fw - u'), in (exp(-fw), 1]
-                const uint32_t qf = __float_as_uint(fmaf(qv, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
                 red_smem_u32(hist_base + (uint32_t)(fb * 128 + row) * 4u, 1u);
                 red_smem_u32(cmass_base + (uint32_t)(fb * 128 + row) * 4u, qf);
               }
