@@ -103,7 +103,8 @@ struct SelParams {
   uint64_t* cand;        // [n][g_pad][kCandCap]
   uint32_t* sel_bits;    // [n][g_pad][n_tiles][4] keys scoring >= bhi, 32 keys per word
   uint32_t* eq_bits;     // same layout: keys inside a single-valued interval
-  const int32_t* cwin;   // COV_FINE: [n][g_pad][2] window of coarse bins [wa, wb]
+  const int32_t* cwin;   // COV_FINE: [n][g_pad][4] window of coarse bins [wa, wb] and its score interval
+                         // [lo, hi] as orderable bits
   // MASS (rows are single queries in group-major order):
   const uint32_t* qsel;  // [n][qn_groups][S/32] selection bitmap of each query group
   float* msum;           // [n][chunks][g_pad][2] per-row sums of exp(scale (s - max)): all keys, selected keys
@@ -155,11 +156,28 @@ __device__ __forceinline__ void lin_range(uint32_t mmin_ord, uint32_t mmax_ord, 
   *inv_w = hi > *lo ? (float)nb / __fsub_rn(hi, *lo) : 0.f;
 }
 
+// Coverage's coarse bin of score s: log-probability below the row maximum
+// u = scale (cmax - s), coordinate x = u inv_w, bin round(x - 1/2) clamped.
+// One definition for the COV and COV_FINE passes and the window search, so
+// they agree bit for bit; non-increasing in s.
+__device__ __forceinline__ float cov_coord(float s, float cmax, float scale, float inv_w) {
+  return __fmul_rn(__fmul_rn(scale, __fsub_rn(cmax, s)), inv_w);
+}
+__device__ __forceinline__ void cov_row_scale(uint32_t mmax_ord, uint32_t mmin_ord, float scale, int nb, float* cmax,
+                                              float* inv_w, float* w2) {
+  *cmax = ord2f(mmax_ord);
+  const float range = __fmul_rn(scale, __fsub_rn(*cmax, ord2f(mmin_ord)));
+  *inv_w = range > 0.f ? __fdiv_rn((float)nb, range) : 0.f;
+  *w2 = range > 0.f ? __fmul_rn(__fdiv_rn(range, (float)nb), 1.4426950408889634f) : 0.f;
+}
+
 // ---------------------------------------------------------------------------
 // Score-tile pipeline with a per-mode consumer.
 // grid = (group tiles, key chunks, problems); block = 320 threads.
+// Two blocks per SM, except COV_FINE: its histogram area leaves room for one
+// block, so its registers are not capped for two.
 template <int RP, int MODE>
-__global__ void __launch_bounds__(kSelThreads, 2)
+__global__ void __launch_bounds__(kSelThreads, MODE == kCovFine ? 1 : 2)
     k_select(const __grid_constant__ CUtensorMap map_qhi, const __grid_constant__ CUtensorMap map_qlo,
              const __grid_constant__ CUtensorMap map_khi, const __grid_constant__ CUtensorMap map_klo,
              const SelParams prm, const ProblemTable tab) {
@@ -335,16 +353,15 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     // it (fine coordinate (x - wa) * fscale, fine width fw2 in log2 units)
     int wa = NBc, wb = -1;
     float fscale = 0.f, fw2 = 0.f;
-    if constexpr (kCovLike) {
-      cmax = ord2f(prm.mmax[rid]);
-      const float range = prm.scale * (cmax - ord2f(prm.mmin[rid]));
-      inv_w = range > 0.f ? (float)NBc / range : 0.f;
-      w2 = range > 0.f ? range / (float)NBc * 1.4426950408889634f : 0.f;
-    }
+    float f_lo = INFINITY, f_hi = -INFINITY;   // the window's scores: [f_lo, f_hi]
+    if constexpr (kCovLike) cov_row_scale(prm.mmax[rid], prm.mmin[rid], prm.scale, NBc, &cmax, &inv_w, &w2);
     if constexpr (kFinePart) {
       if (valid) {
-        wa = prm.cwin[2 * (size_t)rid];
-        wb = prm.cwin[2 * (size_t)rid + 1];
+        const int4 wv = *reinterpret_cast<const int4*>(prm.cwin + 4 * (size_t)rid);
+        wa = wv.x;
+        wb = wv.y;
+        f_lo = ord2f((uint32_t)wv.z);
+        f_hi = ord2f((uint32_t)wv.w);
       }
       const int nw = wb - wa + 1;
       fscale = nw > 0 ? (float)NBc / (float)nw : 0.f;
@@ -394,35 +411,25 @@ __global__ void __launch_bounds__(kSelThreads, 2)
             m_all += ev;
             m_sel += ((selm >> e) & 1ull) ? ev : 0.f;
           }
-          if constexpr (kCovLike) {
-            // log-probability below the row maximum u, its coarse coordinate
-            // x and bin; the fine bins reuse this arithmetic bit for bit, so
-            // window membership agrees with the coarse bins
-            const float u = __fmul_rn(prm.scale, __fsub_rn(cmax, s));
-            const float x = __fmul_rn(u, inv_w);
+          if constexpr (kCovPart) {
+            // coarse coordinate x and bin of the key's log-probability below
+            // the row maximum; q = exp(b w - u) in (exp(-w), 1], as 16.16
+            // fixed point through the float bits
+            const float x = cov_coord(s, cmax, prm.scale, inv_w);
             const float t = bin_round(x);
             const int bin = bin_of(t, NBc);
-            if constexpr (kCovPart) {
-              // q = exp(b w - u) in (exp(-w), 1], as 16.16 fixed point through the float bits
-              const float frac = x - fminf(t - kRoundMagic, (float)(NBc - 1));   // in [0, 1], more when clamped
-              const float qv = ex2_fast(-frac * w2);
-              const uint32_t qf = __float_as_uint(fmaf(qv, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
-              red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
-              red_smem_u32(cmass_base + (uint32_t)(bin * 128 + row) * 4u, qf);
-            } else {
-              // computed for every key without branching; only the two adds
-              // are predicated on the key lying in the row's window
-              const float y = fmaxf(__fmul_rn(__fsub_rn(x, (float)wa), fscale), 0.f);
-              const float ty = bin_round(y);
-              const int fb = bin_of(ty, NBc);
-              const float fy = y - fminf(ty - kRoundMagic, (float)(NBc - 1));   // in [0, 1], more when clamped
-              const float qv = ex2_fast(-fy * fw2);   // exp(fb fw - u'), in (exp(-fw), 1]
-              const uint32_t qf = __float_as_uint(fmaf(qv, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
-              if (bin >= wa && bin <= wb) {
-                red_smem_u32(hist_base + (uint32_t)(fb * 128 + row) * 4u, 1u);
-                red_smem_u32(cmass_base + (uint32_t)(fb * 128 + row) * 4u, qf);
-              }
-            }
+            const float frac = x - fminf(t - kRoundMagic, (float)(NBc - 1));   // in [0, 1], more when clamped
+            const float qv = ex2_fast(-frac * w2);
+            const uint32_t qf = __float_as_uint(fmaf(qv, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
+            red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
+            red_smem_u32(cmass_base + (uint32_t)(bin * 128 + row) * 4u, qf);
+          }
+          if constexpr (kFinePart) {
+            // the window's keys, by two compares against its exact score
+            // interval (the coarse binning is monotone); binned after the tile
+            const bool in = s >= f_lo && s <= f_hi;
+            if (e < 32) cm_lo |= (uint32_t)in << e;
+            else cm_hi |= (uint32_t)in << (e - 32);
           }
           if constexpr (kHistPart) {
             const int bin = lin_bin(s, h_lo, h_inv, NBh);
@@ -444,6 +451,31 @@ __global__ void __launch_bounds__(kSelThreads, 2)
           if constexpr (MODE == kRefine) {
             const uint32_t dlt = f2ord(s) - olo;   // wraps above 2^31 for scores below the interval
             if (dlt < owid) red_smem_u32(hist_base + (uint32_t)((dlt >> oshift) * 128 + row) * 4u, 1u);
+          }
+        }
+        if constexpr (kFinePart) {
+          // one short loop per window key: its score picked out of r0/r1 by a
+          // select chain, its fine bin (NBc bins over the window's width) and
+          // q = exp(fb fw - u') in (exp(-fw), 1] added in shared memory
+          uint64_t fm = valid ? ((uint64_t)cm_hi << 32 | cm_lo) : 0ull;
+#pragma unroll 1
+          while (fm) {
+            const int e = __ffsll((long long)fm) - 1;
+            fm &= fm - 1;
+            const int u = e & 31;
+            const bool hi = e >= 32;
+            uint32_t v = 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v = (u == i) ? (hi ? r1[i] : r0[i]) : v;
+            const float x = cov_coord(__uint_as_float(v) + 0.0f, cmax, prm.scale, inv_w);
+            const float y = fmaxf(__fmul_rn(__fsub_rn(x, (float)wa), fscale), 0.f);
+            const float ty = bin_round(y);
+            const int fb = bin_of(ty, NBc);
+            const float fy = y - fminf(ty - kRoundMagic, (float)(NBc - 1));   // in [0, 1], more when clamped
+            const float qv = ex2_fast(-fy * fw2);
+            const uint32_t qf = __float_as_uint(fmaf(qv, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
+            red_smem_u32(hist_base + (uint32_t)(fb * 128 + row) * 4u, 1u);
+            red_smem_u32(cmass_base + (uint32_t)(fb * 128 + row) * 4u, qf);
           }
         }
         if constexpr (kCollectPart) {
@@ -1350,6 +1382,14 @@ __global__ void __launch_bounds__(kCovPoints) k_cov_eval(int mode, bool curve, i
   __shared__ float s_w[kCovGroupsPerBlock], s_z[kCovGroupsPerBlock];
   __shared__ int s_wa[kCovGroupsPerBlock], s_wb[kCovGroupsPerBlock];
   const int lp = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x, p = threadIdx.x;
+  // blockIdx.z > 0: the second of two searches launched together (the two
+  // bound searches), with its own range and partials
+  if (gridDim.z > 1) {
+    mode = blockIdx.z == 0 ? kCovBoundHi : kCovBoundLo;
+    range += (size_t)blockIdx.z * 2 * gridDim.y;
+    partial += (size_t)blockIdx.z * gridDim.y * nblk * kCovPoints;
+  }
+  if (!curve && range[2 * lp] < 0) return;   // this search already has its answer
   const int g0 = blk * kCovGroupsPerBlock, ng = min(n_groups - g0, kCovGroupsPerBlock);
   const size_t base = (size_t)lp * g_pad + g0;
   for (int i = p; i < ng * nb; i += blockDim.x) {
@@ -1361,8 +1401,8 @@ __global__ void __launch_bounds__(kCovPoints) k_cov_eval(int mode, bool curve, i
   if (p < ng) {
     s_w[p] = width[base + p];
     s_z[p] = zinv[base + p];
-    s_wa[p] = fine_cnt ? win[2 * (base + p)] : nb;   // no window: every bin is coarse
-    s_wb[p] = fine_cnt ? win[2 * (base + p) + 1] : -1;
+    s_wa[p] = fine_cnt ? win[4 * (base + p)] : nb;   // no window: every bin is coarse
+    s_wb[p] = fine_cnt ? win[4 * (base + p) + 1] : -1;
   }
   __syncthreads();
   const int k = cov_point(curve, range[2 * lp], range[2 * lp + 1], p, S, n_curve);
@@ -1382,11 +1422,18 @@ __global__ void __launch_bounds__(kCovPoints) k_cov_eval(int mode, bool curve, i
 // the curve.
 __global__ void __launch_bounds__(1024) k_cov_pick(bool curve, int nblk, int n_groups, int S, float target,
                                                    const double* partial, int32_t* range, int32_t* out,
-                                                   bool out_by_problem, float* curve_out, int n_curve,
+                                                   int32_t* out2, bool out_by_problem, float* curve_out, int n_curve,
                                                    const ProblemTable tab) {
   __shared__ int first;
   const int lp = blockIdx.x, p = threadIdx.x;
+  // blockIdx.y > 0: the second of two searches launched together (answer in out2)
+  if (blockIdx.y > 0) {
+    range += (size_t)blockIdx.y * 2 * gridDim.x;
+    partial += (size_t)blockIdx.y * gridDim.x * nblk * kCovPoints;
+    out = out2;
+  }
   const int lo = range[2 * lp], hi = range[2 * lp + 1];
+  if (!curve && lo < 0) return;   // this search already has its answer
   if (p == 0) first = kCovPoints;
   __syncthreads();  // every thread has read range before thread 0 rewrites it
   const int k = cov_point(curve, lo, hi, p, S, n_curve);
@@ -1404,6 +1451,7 @@ __global__ void __launch_bounds__(1024) k_cov_pick(bool curve, int nblk, int n_g
   if (span <= kCovPoints) {
     // C(S) = 1 >= target up to rounding; with no qualifying point keep hi
     out[out_by_problem ? tab.p[lp] : lp] = first < kCovPoints ? lo + first : hi;
+    range[2 * lp] = -1;   // later rounds of this search leave at once
     return;
   }
   const int f = first < kCovPoints ? first : kCovPoints - 1;  // answer in (k_{f-1}, k_f]
@@ -1414,8 +1462,24 @@ __global__ void __launch_bounds__(1024) k_cov_pick(bool curve, int nblk, int n_g
 // Per group: the coarse bins [wa, wb] holding its ranks k_lo .. k_hi, and
 // the factor that makes the fine masses (shares of the window's own total)
 // shares of the group's total.
-__global__ void k_cov_window(int nb, int g_pad, int n_groups, const int32_t* cum_cnt, const double* cum_mass,
-                             const int32_t* k_lo, const int32_t* k_hi, int32_t* win, double* fine_scale) {
+// The window's scores: coarse bins are non-increasing in the score, so the
+// scores whose bin lies in [wa, wb] form the interval [lo, hi] of orderable
+// bits, found by binary search with the passes' own binning arithmetic
+// (empty when lo > hi).
+__device__ uint32_t least_with_cbin_at_most(int target, uint32_t o_lo, uint32_t o_hi, float cmax, float scale,
+                                            float inv_w, int nb) {
+  uint32_t a = o_lo, b = o_hi;   // answer in [a, b]; o_hi when no score reaches it
+  while (a < b) {
+    const uint32_t m = a + (b - a) / 2;
+    if (bin_of(bin_round(cov_coord(ord2f(m) + 0.0f, cmax, scale, inv_w)), nb) <= target) b = m;
+    else a = m + 1;
+  }
+  return a;
+}
+
+__global__ void k_cov_window(int nb, int g_pad, int n_groups, float scale, const uint32_t* mmax, const uint32_t* mmin,
+                             const int32_t* cum_cnt, const double* cum_mass, const int32_t* k_lo, const int32_t* k_hi,
+                             int32_t* win, double* fine_scale) {
   const int lp = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= n_groups) return;
   const size_t rid = (size_t)lp * g_pad + g;
@@ -1423,8 +1487,17 @@ __global__ void k_cov_window(int nb, int g_pad, int n_groups, const int32_t* cum
   const double* cm = cum_mass + rid * nb;
   const int wa = first_reaching(cc, nb, k_lo[lp]);
   const int wb = first_reaching(cc, nb, k_hi[lp]);
-  win[2 * rid] = wa;
-  win[2 * rid + 1] = wb;
+  float cmax, inv_w, w2;
+  cov_row_scale(mmax[rid], mmin[rid], scale, nb, &cmax, &inv_w, &w2);
+  const uint32_t o_lo = mmin[rid], o_hi = mmax[rid] + 1u;
+  const uint32_t lo = least_with_cbin_at_most(wb, o_lo, o_hi, cmax, scale, inv_w, nb);       // bin <= wb
+  const uint32_t hi = least_with_cbin_at_most(wa - 1, o_lo, o_hi, cmax, scale, inv_w, nb);   // bin < wa
+  int4 out;
+  out.x = wa;
+  out.y = wb;
+  out.z = (int)lo;
+  out.w = (int)(hi - 1u);   // the last score with bin >= wa
+  *reinterpret_cast<int4*>(win + 4 * rid) = out;
   fine_scale[rid] = cm[wb] - (wa > 0 ? cm[wa - 1] : 0.0);
 }
 
@@ -1556,11 +1629,12 @@ static size_t carve(void* base, const TopkPlan& pl, int mode, TopkWs* w) {
     w->fine_cnt = c.take<int32_t>(pc * gp * pl.cov_bins);
     w->fine_mass = c.take<double>(pc * gp * pl.cov_bins);
     w->fine_scale = c.take<double>(pc * gp);
-    w->cov_win = c.take<int32_t>(pc * gp * 2);
+    w->cov_win = c.take<int32_t>(pc * gp * 4);
     w->kwin_lo = c.take<int32_t>(pc);
     w->kwin_hi = c.take<int32_t>(pc);
-    w->cov_partial = c.take<double>(pc * ((gp + kCovGroupsPerBlock - 1) / kCovGroupsPerBlock) * kCovPoints);
-    w->cov_range = c.take<int32_t>(pc * 2);
+    // two searches can run together (the two bounds): partials and ranges for both
+    w->cov_partial = c.take<double>(2 * pc * ((gp + kCovGroupsPerBlock - 1) / kCovGroupsPerBlock) * kCovPoints);
+    w->cov_range = c.take<int32_t>(2 * pc * 2);
   }
   return c.used + 256;
 }
@@ -1756,16 +1830,20 @@ static CovSearch cov_search_shape(const TopkPlan& pl) {
   return c;
 }
 
+// One search (mode, answer in out) or, with `out2`, the two bound searches
+// together (grid z / y selects the search; answers in out and out2).
 static void cov_search(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, int mode, bool fine,
-                       float mass, int32_t* out, bool by_problem, cudaStream_t st) {
+                       float mass, int32_t* out, int32_t* out2, bool by_problem, cudaStream_t st) {
   const CovSearch cs = cov_search_shape(pl);
   const int n = tab.n, ng = pl.geo.n_groups, S = pl.geo.S, nb = pl.cov_bins;
+  const int ns = out2 ? 2 : 1;
   for (int r = 0; r < cs.rounds; ++r) {
-    k_cov_eval<<<dim3(cs.nblk, n), kCovPoints, 0, st>>>(mode, false, nb, pl.g_pad, ng, S, w.cum_cnt, w.cum_mass,
-                                                        w.width, w.zinv, w.cov_win, fine ? w.fine_cnt : nullptr,
-                                                        w.fine_mass, w.cov_range, 0, w.cov_partial);
-    k_cov_pick<<<n, kCovPoints, 0, st>>>(false, cs.nblk, ng, S, mass, w.cov_partial, w.cov_range, out, by_problem,
-                                          nullptr, 0, tab);
+    k_cov_eval<<<dim3(cs.nblk, n, ns), kCovPoints, 0, st>>>(mode, false, nb, pl.g_pad, ng, S, w.cum_cnt,
+                                                            w.cum_mass, w.width, w.zinv, w.cov_win,
+                                                            fine ? w.fine_cnt : nullptr, w.fine_mass, w.cov_range, 0,
+                                                            w.cov_partial);
+    k_cov_pick<<<dim3(n, ns), kCovPoints, 0, st>>>(false, cs.nblk, ng, S, mass, w.cov_partial, w.cov_range, out,
+                                                   out2, by_problem, nullptr, 0, tab);
   }
 }
 
@@ -1778,12 +1856,11 @@ static cudaError_t cov_after_coarse(const TopkPlan& pl, const TopkWs& w, const P
   k_cov_merge<<<mgrid, 128, 0, st>>>(w.cov_hist, w.mass, nb, n_chunks, pl.g_pad, ng, w.cum_cnt, w.cum_mass);
   k_cov_scan<<<sgrid, 256, 0, st>>>(w.mmax, w.mmin, nb, pl.g_pad, ng, scale, w.cum_cnt, w.cum_mass, w.width, w.zinv,
                                     nullptr);
-  k_cov_range_init<<<1, 256, 0, st>>>(w.cov_range, nullptr, nullptr, S, n);
-  cov_search(pl, w, tab, kCovBoundHi, false, mass, w.kwin_lo, false, st);
-  k_cov_range_init<<<1, 256, 0, st>>>(w.cov_range, nullptr, nullptr, S, n);
-  cov_search(pl, w, tab, kCovBoundLo, false, mass, w.kwin_hi, false, st);
-  k_cov_window<<<wgrid, 128, 0, st>>>(nb, pl.g_pad, ng, w.cum_cnt, w.cum_mass, w.kwin_lo, w.kwin_hi, w.cov_win,
-                                      w.fine_scale);
+  // both bounds at once: k_lo from the upper bound, k_hi from the lower bound
+  k_cov_range_init<<<2, 256, 0, st>>>(w.cov_range, nullptr, nullptr, S, 2 * n);
+  cov_search(pl, w, tab, kCovBoundHi, false, mass, w.kwin_lo, w.kwin_hi, false, st);
+  k_cov_window<<<wgrid, 128, 0, st>>>(nb, pl.g_pad, ng, scale, w.mmax, w.mmin, w.cum_cnt, w.cum_mass, w.kwin_lo,
+                                      w.kwin_hi, w.cov_win, w.fine_scale);
   return cudaGetLastError();
 }
 
@@ -1798,14 +1875,14 @@ static cudaError_t cov_after_fine(const TopkPlan& pl, const TopkWs& w, const Pro
   k_cov_scan<<<sgrid, 256, 0, st>>>(w.mmax, w.mmin, nb, pl.g_pad, ng, scale, w.fine_cnt, w.fine_mass, nullptr,
                                     nullptr, w.fine_scale);
   k_cov_range_init<<<1, 256, 0, st>>>(w.cov_range, w.kwin_lo, w.kwin_hi, S, n);
-  cov_search(pl, w, tab, kCovCombined, true, mass, k_cov, true, st);
+  cov_search(pl, w, tab, kCovCombined, true, mass, k_cov, nullptr, true, st);
   if (curve) {
     const CovSearch cs = cov_search_shape(pl);
     k_cov_eval<<<dim3(cs.nblk, n), kCovPoints, 0, st>>>(kCovCombined, true, nb, pl.g_pad, ng, S, w.cum_cnt,
                                                         w.cum_mass, w.width, w.zinv, w.cov_win, w.fine_cnt,
                                                         w.fine_mass, w.cov_range, n_curve, w.cov_partial);
-    k_cov_pick<<<n, kCovPoints, 0, st>>>(true, cs.nblk, ng, S, mass, w.cov_partial, w.cov_range, k_cov, true, curve,
-                                          n_curve, tab);
+    k_cov_pick<<<n, kCovPoints, 0, st>>>(true, cs.nblk, ng, S, mass, w.cov_partial, w.cov_range, k_cov, nullptr,
+                                          true, curve, n_curve, tab);
   }
   return cudaGetLastError();
 }
