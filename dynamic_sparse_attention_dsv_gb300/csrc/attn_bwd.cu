@@ -468,26 +468,32 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     int j_next = (partials && row < k) ? __ldg(idx_row + row) : -1;
     int64_t pos_next = j_next >= 0 ? slot_of(j_next) : 0;
     for (int t = 0; partials && t < nt; ++t) {
-      const bool kvalid = t * 128 + row < k;
+      // The drain reads 16 rows per TMEM load, each row's 64 columns split
+      // over two threads (lane l and l + 16), so one store instruction covers
+      // 16 rows x 64 bytes instead of 32 rows x 32: half the cache lines per
+      // instruction. Thread `lane` stores row 16h + (lane & 15) of the warp's 32.
       const int64_t pos = pos_next;
+      const int64_t hpos0 = __shfl_sync(0xffffffffu, pos, lane & 15);
+      const int64_t hpos1 = __shfl_sync(0xffffffffu, pos, 16 + (lane & 15));
+      const int hrow0 = t * 128 + q * 32 + (lane & 15);   // row of the first half within the problem's keys
       const int nslot = (t + 1) * 128 + row;
       j_next = (t + 1 < nt && nslot < k) ? __ldg(idx_row + nslot) : -1;   // next tile's key, loaded early
       for (int jb = 0; jb < C::kJobs; ++jb, ++job) {
         ok = ok && mbar_wait_warp(part_full, job & 1, prm.wait_ns);
         tc_fence_after();
 #pragma unroll 1
-        for (int c2 = 0; c2 < 4; c2 += 2) {
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int c = c2; c < c2 + 2; ++c) {
-            // 32-column chunk c of the job region: d = 128: columns c*32.. of dV (job 0) or dK (job 1);
-            // d = 64: dV columns for c < 2, dK columns for c >= 2
-            const int tensor = D == 128 ? jb : (c >> 1);
-            const int dcol = D == 128 ? c * 32 : (c & 1) * 32;
+          for (int cb = 0; cb < 2; ++cb) {
+            // 64-column block cb of the job region: d = 128: columns cb*64.. of dV (job 0) or dK (job 1);
+            // d = 64: dV for cb = 0, dK for cb = 1
+            const int tensor = D == 128 ? jb : cb;
+            const int dcol = (D == 128 ? cb * 64 : 0) + (lane >= 16 ? 32 : 0);
             uint32_t v[32];
-            tmem_ld32(lane_addr + C::kColJob + c * 32, v);
+            tmem_ld16x2<32>(lane_addr + ((uint32_t)(16 * h) << 16) + C::kColJob + cb * 64, v);
             tmem_ld_wait(v);
-            if (kvalid) {
-              __nv_bfloat16* dst = (tensor == 0 ? csc.part_v : csc.part_k) + pos * D + dcol;
+            if (hrow0 + 16 * h < k) {
+              __nv_bfloat16* dst = (tensor == 0 ? csc.part_v : csc.part_k) + (h ? hpos1 : hpos0) * D + dcol;
               uint32_t pk[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e)

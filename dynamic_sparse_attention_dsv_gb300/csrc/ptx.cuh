@@ -167,6 +167,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : DSV_R8(0), DSV_R8(8)
       : "r"(taddr));
 }
+// Two 16-lane halves of a warp's 32 lanes per call: threads 0-15 read lanes
+// base..base+15 at columns col..col+31, threads 16-31 the same lanes at
+// columns col+kOff..col+kOff+31 (register j = column j of the thread's block).
+template <int kOff>
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], %33;"
+      : DSV_R8(0), DSV_R8(8), DSV_R8(16), DSV_R8(24)
+      : "r"(taddr), "n"(kOff));
+}
 // Waits for outstanding TMEM loads. The registers are passed through so the
 // compiler cannot hoist their uses above the wait.
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
