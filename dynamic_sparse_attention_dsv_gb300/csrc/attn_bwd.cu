@@ -40,7 +40,8 @@ constexpr int kBwdQThreads = 384;
 constexpr int kBwdQLaunchRegs = 168;
 constexpr int kRegsSoftmax = 232, kRegsDrain = 136, kRegsLoad = 136;
 static_assert(kRegsSoftmax + kRegsDrain + kRegsLoad == 3 * kBwdQLaunchRegs, "register split must equal the launch");
-static_assert(kGatherWarps == 2, "warps 8-9 gather, warp 10 issues MMAs, warp 11 idles");
+// Warps 8-10 gather the selected K/V rows, warp 11 issues the MMAs.
+constexpr int kBwdGatherWarps = 3;
 constexpr int kMaxUnits = 48;                       // work units per group-major launch
 constexpr size_t kPartialBudget = 48ull << 30;      // bytes of bf16 dK/dV partials in flight
 constexpr int kMaxBlocks = 1024;                    // 256-key blocks per problem (S <= 2^18)
@@ -78,9 +79,6 @@ struct BwdCfg {
   static constexpr int kTile = 128 * D * 2;      // one [128][D] bf16 tile
   static constexpr int kKStages = 2;
   static constexpr int kVStages = D == 128 ? 1 : 2;
-  // dV/dK jobs share one 128-column TMEM region: with d = 128 a job is dV,
-  // then dK, over the full width; with d = 64 one job holds both.
-  static constexpr int kJobs = D == 128 ? 2 : 1;
   static constexpr int kOffDO = kTile;           // Q at 0
   static constexpr int kOffK = 2 * kTile;
   static constexpr int kOffV = kOffK + kKStages * kTile;
@@ -89,11 +87,14 @@ struct BwdCfg {
   static constexpr int kOffBar = kOffDS + 32768;
   static constexpr int kSmemUsed = kOffBar + 1024 + 1024;
   static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
-  // TMEM columns: S, dP, dQ accumulator, then the dV/dK job region
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColJob = 256 + D;
+  // TMEM columns: S and dP of a tile share one 128-column region (dP(t) is
+  // computed once S(t) is in registers, S(t+1) once dP(t) is), which leaves
+  // room for the dQ accumulator and separate dV and dK regions: each job
+  // drains while the tensor cores compute the other.
+  static constexpr uint32_t kColSDP = 0, kColDQ = 128, kColDV = 128 + D, kColDK = 128 + 2 * D;
 };
 static_assert(BwdCfg<128>::kSmemUsed <= 232448, "group-major backward exceeds shared memory");
-static_assert(BwdCfg<128>::kColJob + 128 <= 512 && BwdCfg<64>::kColJob + 128 <= 512, "TMEM budget");
+static_assert(BwdCfg<128>::kColDK + 128 <= 512 && BwdCfg<64>::kColDK + 64 <= 512, "TMEM budget");
 
 __device__ __forceinline__ void compute_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -104,14 +105,34 @@ __device__ __forceinline__ void st_sw128_chunk(uint8_t* tile, int row, int chunk
   *reinterpret_cast<uint4*>(tile + atom * 16384 + row * 128 + ((c ^ (row & 7)) << 4)) = v;
 }
 
+// Columns 32c..32c+31 of one dS row: dS = P (scale dP - scale Delta) from
+// the row's fp32 P and dP, packed to bf16 and written to the K-major tile.
+__device__ __forceinline__ void ds_chunk(uint8_t* sDS, int row, int c, const uint32_t (&p)[32],
+                                         const uint32_t (&dp)[32], float dsc, float ndd) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = q * 8 + e * 2;
+      w[e] = pack_bf16x2(__uint_as_float(p[i]) * fmaf(__uint_as_float(dp[i]), dsc, ndd),
+                         __uint_as_float(p[i + 1]) * fmaf(__uint_as_float(dp[i + 1]), dsc, ndd));
+    }
+    st_sw128_chunk(sDS, row, c * 4 + q, make_uint4(w[0], w[1], w[2], w[3]));
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Group-major backward. Warps 0-3 turn S, dP into P, dS (shared memory);
-// warps 4-7 drain the dV/dK partial halves to their slots and write dQ at
-// the end; warps 8-9 load (cp.async row gather or TMA boxes); warp 10 issues
-// the MMAs. Per 128-key tile t:
-//   S, dP (TMEM) -> P, dS (smem) -> dQ += dS K; then dV = P^T dO and
-//   dK = dS^T Q, one after the other, in a shared 128-column TMEM region,
-//   each drained while the tensor cores move on.
+// warps 4-7 drain the dV/dK partial rows to their slots and write dQ at the
+// end; warps 8-10 load (cp.async row gather or TMA boxes); warp 11 issues
+// the MMAs. Per 128-key tile t, in the order the MMAs are issued:
+//   dP(t) = dO V^T     once S(t) is in registers (same TMEM columns)
+//   dV(t) = P(t)^T dO  once P(t) is in shared memory and dV(t-1) drained
+//   S(t+1) = Q K^T     once dP(t) is in registers
+//   dQ += dS(t) K; dK(t) = dS(t)^T Q  once dS(t) is in shared memory
+// so the softmax warps compute P(t) while dP(t) runs and dS(t) while S(t+1)
+// runs, and the drain of one job overlaps the other job's MMAs.
 template <int D>
 __global__ void __launch_bounds__(kBwdQThreads, 1)
     k_attn_bwd_q(const __grid_constant__ AttnMaps maps, const __grid_constant__ CUtensorMap do_cube,
@@ -131,16 +152,21 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
   uint64_t* k_empty = bars + 3;      // [2]
   uint64_t* v_full = bars + 5;       // [2]
   uint64_t* v_empty = bars + 7;      // [2]
-  uint64_t* sdp_full = bars + 9;
-  uint64_t* ps_full = bars + 10;
-  uint64_t* p_free = bars + 11;
-  uint64_t* part_full = bars + 12;
-  uint64_t* part_free = bars + 13;
-  uint64_t* dq_done = bars + 14;
-  uint64_t* sdp_free = bars + 15;    // S, dP of the current tile read out of TMEM
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
-  uint64_t* pv_free = bars + 17;     // P of the previous tile read by its dV MMAs (dS may still be in use)
-  uint64_t* mma_drain = bars + 18;   // every MMA issued has completed (unwind)
+  uint64_t* s_full = bars + 9;       // S(t) in TMEM
+  uint64_t* s_free = bars + 10;      // S(t) in registers: dP(t) may overwrite its columns
+  uint64_t* dp_full = bars + 11;     // dP(t) in TMEM
+  uint64_t* dp_free = bars + 12;     // dP(t) in registers: S(t+1) may overwrite its columns
+  uint64_t* p_full = bars + 13;      // P(t) in shared memory
+  uint64_t* p_free = bars + 14;      // P(t) read by the dV MMAs
+  uint64_t* ds_full = bars + 15;     // dS(t) in shared memory
+  uint64_t* ds_free = bars + 16;     // dS(t) read by the dQ and dK MMAs
+  uint64_t* dv_full = bars + 17;     // dV partials of tile t in TMEM
+  uint64_t* dv_free = bars + 18;     // ... drained to their slots
+  uint64_t* dk_full = bars + 19;
+  uint64_t* dk_free = bars + 20;
+  uint64_t* dq_done = bars + 21;
+  uint64_t* mma_drain = bars + 22;   // every MMA issued has completed (unwind)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 23);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int u = blockIdx.y;
@@ -153,7 +179,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
   const int nt = (k + 127) / 128;
   const int32_t* idx_row = dense ? nullptr : prm.idx + tab.off[u] + (int64_t)g * k;
   const int G = geo.G;
-  constexpr int kProdWarp = 8, kMmaWarp = 8 + kGatherWarps;
+  constexpr int kProdWarp = 8, kMmaWarp = 8 + kBwdGatherWarps;
 
   if (G < 128) {
     for (int i = tid; i < (128 - G) * (D / 64) * 8; i += blockDim.x) {
@@ -169,21 +195,26 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
   }
   if (tid == 0) {
     mbar_init(q_full, 1);
-    const uint32_t fills = dense ? 1u : 32u * kGatherWarps;   // TMA tx arrival, or one per gathering lane
+    const uint32_t fills = dense ? 1u : 32u * kBwdGatherWarps;   // TMA tx arrival, or one per gathering lane
     for (int i = 0; i < 2; ++i) {
       mbar_init(k_full + i, fills);
       mbar_init(v_full + i, fills);
       mbar_init(k_empty + i, 1);
       mbar_init(v_empty + i, 1);
     }
-    mbar_init(sdp_full, 1);
-    mbar_init(ps_full, 4);
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 4);
+    mbar_init(dp_full, 1);
+    mbar_init(dp_free, 4);
+    mbar_init(p_full, 4);
     mbar_init(p_free, 1);
-    mbar_init(pv_free, 1);
-    mbar_init(part_full, 1);
-    mbar_init(part_free, 4);
+    mbar_init(ds_full, 4);
+    mbar_init(ds_free, 1);
+    mbar_init(dv_full, 1);
+    mbar_init(dv_free, 4);
+    mbar_init(dk_full, 1);
+    mbar_init(dk_free, 4);
     mbar_init(dq_done, 1);
-    mbar_init(sdp_free, 4);
     mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
@@ -206,22 +237,22 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       }
     }
     const int prow0 = p * geo.S;
-    int rows[Gather<D>::kIters], nxt[Gather<D>::kIters];
-    if (idx_row) gather_rows<D>(nxt, idx_row, k, 0, prow0, pw, lane);
+    int rows[Gather<D, kBwdGatherWarps>::kIters], nxt[Gather<D, kBwdGatherWarps>::kIters];
+    if (idx_row) gather_rows<D, kBwdGatherWarps>(nxt, idx_row, k, 0, prow0, pw, lane);
     int k_issued = 0, v_issued = 0;   // tiles whose K (V) copies this warp started
     for (int t = 0; t < nt; ++t) {
       const int ks = t % C::kKStages, vs = t % C::kVStages;
       if (idx_row) {
 #pragma unroll
-        for (int i = 0; i < Gather<D>::kIters; ++i) rows[i] = nxt[i];
-        if (t + 1 < nt) gather_rows<D>(nxt, idx_row, k, t + 1, prow0, pw, lane);
+        for (int i = 0; i < Gather<D, kBwdGatherWarps>::kIters; ++i) rows[i] = nxt[i];
+        if (t + 1 < nt) gather_rows<D, kBwdGatherWarps>(nxt, idx_row, k, t + 1, prow0, pw, lane);
       }
       if (t >= C::kKStages && !mbar_wait_warp(k_empty + ks, ((t / C::kKStages) - 1) & 1, prm.wait_ns)) {
         if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
         break;
       }
       if (idx_row) {
-        gather_tile<D>(sK + ks * C::kTile, prm.K, rows, pw, lane);
+        gather_tile<D, kBwdGatherWarps>(sK + ks * C::kTile, prm.K, rows, pw, lane);
         cp_async_arrive_noinc(k_full + ks);
       } else if (pw == 0 && lane == 0) {
         mbar_arrive_expect_tx(k_full + ks, C::kTile);
@@ -233,7 +264,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         break;
       }
       if (idx_row) {
-        gather_tile<D>(sV + vs * C::kTile, prm.V, rows, pw, lane);
+        gather_tile<D, kBwdGatherWarps>(sV + vs * C::kTile, prm.V, rows, pw, lane);
         cp_async_arrive_noinc(v_full + vs);
       } else if (pw == 0 && lane == 0) {
         mbar_arrive_expect_tx(v_full + vs, C::kTile);
@@ -257,84 +288,85 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_sdp = instr_desc(128, 128, 1, 0, 0);   // Q K^T, dO V^T
       constexpr uint32_t id_dq = instr_desc(128, D, 1, 0, 1);      // dS K (B = K, MN-major)
-      constexpr uint32_t id_kv = instr_desc(128, D == 128 ? 128 : 64, 1, 1, 1);   // P^T dO, dS^T Q (MN-major)
+      constexpr uint32_t id_kv = instr_desc(128, D, 1, 1, 1);      // P^T dO, dS^T Q (MN-major)
       // base descriptors (K-major), built once; an operand is a fixed offset from one of
       // them, and the MN-major form differs only by a constant in the stride field
       constexpr uint64_t kMn = (uint64_t)((16384 >> 4) - (16 >> 4)) << 16;
       const uint64_t dq_k = smem_desc(smem_u32(sQ), 16, 1024), ddo_k = smem_desc(smem_u32(sDO), 16, 1024);
       const uint64_t dp_k = smem_desc(smem_u32(sP), 16, 1024), dds_k = smem_desc(smem_u32(sDS), 16, 1024);
       bool ok = mbar_wait(q_full, 0, prm.wait_ns);
-      auto issue_sdp = [&](int t) -> bool {
-        const int ks = t % C::kKStages, vs = t % C::kVStages;
-        if (!mbar_wait(k_full + ks, (t / C::kKStages) & 1, prm.wait_ns) ||
-            !mbar_wait(v_full + vs, (t / C::kVStages) & 1, prm.wait_ns))
-          return false;
+      auto issue_s = [&](int t) -> bool {   // S(t) = Q K(t)^T
+        const int ks = t % C::kKStages;
+        if (!mbar_wait(k_full + ks, (t / C::kKStages) & 1, prm.wait_ns)) return false;
         fence_proxy_async_smem();   // rows written by cp.async (generic proxy) -> tensor core reads
         tc_fence_after();
         const uint64_t dk = smem_desc(smem_u32(sK + ks * C::kTile), 16, 1024);
-        const uint64_t dv = smem_desc(smem_u32(sV + vs * C::kTile), 16, 1024);
-        const uint64_t dq = opaque(dq_k), ddo = opaque(ddo_k);
+        const uint64_t dq = opaque(dq_k);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tbase + C::kColS, desc_at(dq, off), desc_at(dk, off), id_sdp, kk > 0);
+          mma_f16_ss(tbase + C::kColSDP, desc_at(dq, off), desc_at(dk, off), id_sdp, kk > 0);
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tbase + C::kColDP, desc_at(ddo, off), desc_at(dv, off), id_sdp, kk > 0);
-        }
-        mma_commit(sdp_full);
-        mma_commit(v_empty + vs);
+        mma_commit(s_full);
         return true;
       };
-      int job = 0;   // dV/dK jobs issued so far
-      auto issue_job = [&](int jb) -> bool {
-        if (job >= 1 && !mbar_wait(part_free, (job - 1) & 1, prm.wait_ns)) return false;
+      if (ok && nt > 0) ok = issue_s(0);
+      for (int t = 0; ok && t < nt; ++t) {
+        const int ks = t % C::kKStages, vs = t % C::kVStages;
+        // dP(t) = dO V(t)^T into the columns S(t) has left
+        if (!mbar_wait(s_free, t & 1, prm.wait_ns) ||
+            !mbar_wait(v_full + vs, (t / C::kVStages) & 1, prm.wait_ns)) { ok = false; break; }
+        fence_proxy_async_smem();
         tc_fence_after();
-        if (D == 64 || jb == 0) {
+        {
+          const uint64_t dv = smem_desc(smem_u32(sV + vs * C::kTile), 16, 1024);
+          const uint64_t ddo = opaque(ddo_k);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_f16_ss(tbase + C::kColSDP, desc_at(ddo, off), desc_at(dv, off), id_sdp, kk > 0);
+          }
+        }
+        mma_commit(dp_full);
+        mma_commit(v_empty + vs);
+        // dV(t) = P(t)^T dO (sparse problems only: dense ones take dK/dV key-major)
+        if (partials) {
+          if (!mbar_wait(p_full, t & 1, prm.wait_ns) ||
+              (t >= 1 && !mbar_wait(dv_free, (t - 1) & 1, prm.wait_ns))) { ok = false; break; }
+          tc_fence_after();
           const uint64_t a = opaque(dp_k + kMn), b = opaque(ddo_k + kMn);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ss(tbase + C::kColJob, desc_at(a, kk * 2048), desc_at(b, kk * 2048), id_kv, kk > 0);
+            mma_f16_ss(tbase + C::kColDV, desc_at(a, kk * 2048), desc_at(b, kk * 2048), id_kv, kk > 0);
+          mma_commit(dv_full);
+          mma_commit(p_free);
         }
-        if (D == 64 || jb == 1) {
-          const uint64_t a = opaque(dds_k + kMn), b = opaque(dq_k + kMn);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ss(tbase + C::kColJob + (D == 64 ? 64 : 0), desc_at(a, kk * 2048), desc_at(b, kk * 2048), id_kv,
-                       kk > 0);
-        }
-        mma_commit(part_full);
-        ++job;
-        return true;
-      };
-      if (ok && nt > 0) ok = issue_sdp(0);
-      for (int t = 0; ok && t < nt; ++t) {
-        const int ks = t % C::kKStages;
-        // the next tile's S and dP may overwrite TMEM once tile t's are read out
-        if (t + 1 < nt && (!mbar_wait(sdp_free, t & 1, prm.wait_ns) || !issue_sdp(t + 1))) { ok = false; break; }
-        if (!mbar_wait(ps_full, t & 1, prm.wait_ns)) { ok = false; break; }
+        // S(t+1) into the columns dP(t) has left
+        if (t + 1 < nt && (!mbar_wait(dp_free, t & 1, prm.wait_ns) || !issue_s(t + 1))) { ok = false; break; }
+        // dQ += dS(t) K(t), then dK(t) = dS(t)^T Q
+        if (!mbar_wait(ds_full, t & 1, prm.wait_ns)) { ok = false; break; }
         tc_fence_after();
-        const uint64_t dk_m = smem_desc(smem_u32(sK + ks * C::kTile), 16, 1024) + kMn;
-        const uint64_t dds = opaque(dds_k);
+        {
+          const uint64_t dk_m = smem_desc(smem_u32(sK + ks * C::kTile), 16, 1024) + kMn;
+          const uint64_t dds = opaque(dds_k);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t offa = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tbase + C::kColDQ, desc_at(dds, offa), desc_at(dk_m, kk * 2048), id_dq,
-                     (t > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t offa = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_f16_ss(tbase + C::kColDQ, desc_at(dds, offa), desc_at(dk_m, kk * 2048), id_dq,
+                       (t > 0 || kk > 0) ? 1u : 0u);
+          }
         }
         mma_commit(k_empty + ks);
         if (partials) {
-          for (int jb = 0; jb < C::kJobs; ++jb) {
-            if (!issue_job(jb)) { ok = false; break; }
-            if (jb == 0) mma_commit(pv_free);   // P(t) read: the dV MMAs are the first job
-          }
-          if (!ok) break;
-        } else {
-          mma_commit(pv_free);
+          if (t >= 1 && !mbar_wait(dk_free, (t - 1) & 1, prm.wait_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t a = opaque(dds_k + kMn), b = opaque(dq_k + kMn);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ss(tbase + C::kColDK, desc_at(a, kk * 2048), desc_at(b, kk * 2048), id_kv, kk > 0);
+          mma_commit(dk_full);
         }
-        mma_commit(p_free);
+        mma_commit(ds_free);
       }
       if (ok) mma_commit(dq_done);
       else raise_status(prm.status, DSV_ERR_TIMEOUT);
@@ -375,76 +407,75 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     const float dsc = prm.scale, ndd = -delta * prm.scale;
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
-      ok = ok && mbar_wait_warp(sdp_full, t & 1, prm.wait_ns);
-      tc_fence_after();
       const int nvalid = min(128, k - t * 128);
-      // TMEM loads complete long after they issue, so they go out in two
-      // batches: S (all 128 columns) with dP columns 0-63, then dP 64-127,
-      // whose latency hides behind the first half's arithmetic.
-      uint32_t sr[4][32], da[2][32];
+      ok = ok && mbar_wait_warp(s_full, t & 1, prm.wait_ns);
+      tc_fence_after();
+      uint32_t sr[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + C::kColS + c * 32, sr[c]);
-      tmem_ld32(lane_addr + C::kColDP, da[0]);
-      tmem_ld32(lane_addr + C::kColDP + 32, da[1]);
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + C::kColSDP + c * 32, sr[c]);
       tmem_ld_wait(sr[0]);
       reg_fence(sr[1]);
       reg_fence(sr[2]);
       reg_fence(sr[3]);
-      reg_fence(da[0]);
-      reg_fence(da[1]);
-      uint32_t pw[64], dw[64];
-      // columns 0-63: P and dS
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int j = c * 32 + e;
-          const float p0 = j < nvalid ? ex2_fast(__uint_as_float(sr[c][e]) * sc - lse2) : 0.f;
-          const float p1 = j + 1 < nvalid ? ex2_fast(__uint_as_float(sr[c][e + 1]) * sc - lse2) : 0.f;
-          pw[j >> 1] = pack_bf16x2(p0, p1);
-          dw[j >> 1] = pack_bf16x2(p0 * fmaf(__uint_as_float(da[c][e]), dsc, ndd),
-                                   p1 * fmaf(__uint_as_float(da[c][e + 1]), dsc, ndd));
-        }
-      // dP columns 64-127 into the registers just freed
-#pragma unroll
-      for (int c = 0; c < 2; ++c) tmem_ld32(lane_addr + C::kColDP + 64 + c * 32, da[c]);
-      // columns 64-127: P (fp32, in place of S) while the dP loads are in flight
-#pragma unroll
-      for (int c = 2; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = c * 32 + e;
-          const float pv = j < nvalid ? ex2_fast(__uint_as_float(sr[c][e]) * sc - lse2) : 0.f;
-          sr[c][e] = __float_as_uint(pv);
-        }
-      tmem_ld_wait(da[0]);
-      reg_fence(da[1]);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sdp_free);   // S and dP of tile t are in registers
+      if (lane == 0) mbar_arrive(s_free);   // S(t) in registers: dP(t) may take its columns
+      // P (fp32, in place of S), while dP(t) is computed. The exponential is
+      // taken for every column (the padding columns hold finite scores of a
+      // repeated key) and the padding zeroed afterwards: a choice around the
+      // exponential itself costs far more than the exponential.
 #pragma unroll
-      for (int c = 2; c < 4; ++c)
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int j = c * 32 + e;
-          const float p0 = __uint_as_float(sr[c][e]), p1 = __uint_as_float(sr[c][e + 1]);
-          pw[j >> 1] = pack_bf16x2(p0, p1);
-          dw[j >> 1] = pack_bf16x2(p0 * fmaf(__uint_as_float(da[c - 2][e]), dsc, ndd),
-                                   p1 * fmaf(__uint_as_float(da[c - 2][e + 1]), dsc, ndd));
+        for (int e = 0; e < 32; ++e) sr[c][e] = __float_as_uint(ex2_fast(fmaf(__uint_as_float(sr[c][e]), sc, -lse2)));
+      if (nvalid < 128) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e >= nvalid) sr[c][e] = 0u;
+      }
+      if (partials) {
+        // P(t-1) is free once its dV MMAs completed
+        if (t >= 1) ok = ok && mbar_wait_warp(p_free, (t - 1) & 1, prm.wait_ns);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const uint32_t* x = &sr[q >> 2][(q & 3) * 8];
+          st_sw128_chunk(sP, row, q,
+                         make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                                    pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                                    pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                                    pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7]))));
         }
-      // P of the previous tile is free once its dV MMAs completed, dS once its
-      // dK MMAs did: P goes out while the tensor cores may still read dS
-      if (t >= 1) ok = ok && mbar_wait_warp(pv_free, (t - 1) & 1, prm.wait_ns);
-#pragma unroll
-      for (int q = 0; q < 16; ++q)
-        st_sw128_chunk(sP, row, q, make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]));
-      if (t >= 1) ok = ok && mbar_wait_warp(p_free, (t - 1) & 1, prm.wait_ns);
-#pragma unroll
-      for (int q = 0; q < 16; ++q)
-        st_sw128_chunk(sDS, row, q, make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      // dS = P (scale dP - scale Delta), 32 columns at a time with the next
+      // chunk's TMEM load in flight
+      ok = ok && mbar_wait_warp(dp_full, t & 1, prm.wait_ns);
+      tc_fence_after();
+      uint32_t da[2][32];
+      tmem_ld32(lane_addr + C::kColSDP, da[0]);
+      tmem_ld32(lane_addr + C::kColSDP + 32, da[1]);
+      tmem_ld_wait(da[0]);
+      reg_fence(da[1]);
+      // dS(t-1) is free once its dQ and dK MMAs completed
+      if (t >= 1) ok = ok && mbar_wait_warp(ds_free, (t - 1) & 1, prm.wait_ns);
+      ds_chunk(sDS, row, 0, sr[0], da[0], dsc, ndd);
+      tmem_ld32(lane_addr + C::kColSDP + 64, da[0]);
+      ds_chunk(sDS, row, 1, sr[1], da[1], dsc, ndd);
+      tmem_ld_wait(da[0]);
+      tmem_ld32(lane_addr + C::kColSDP + 96, da[1]);
+      ds_chunk(sDS, row, 2, sr[2], da[0], dsc, ndd);
+      tmem_ld_wait(da[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dp_free);   // dP(t) in registers: S(t+1) may take its columns
+      ds_chunk(sDS, row, 3, sr[3], da[1], dsc, ndd);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ps_full);
+      if (lane == 0) mbar_arrive(ds_full);
     }
     if (!ok && lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
   } else if (warp >= 4 && warp < 8) {
@@ -454,7 +485,6 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     const int row = q * 32 + lane;   // key slot of the tile for the partials; query row for dQ
     const uint32_t lane_addr = tbase + ((uint32_t)(q * 32) << 16);
     bool ok = true;
-    int job = 0;
     // Slot of this key row for tile t: off[key] + groups below ours that chose it.
     const int gl = g - tab.g0[u];
     const uint64_t* bits_u = partials ? csc.bits + tab.bits_base[u] : nullptr;
@@ -478,22 +508,21 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
       const int hrow0 = t * 128 + q * 32 + (lane & 15);   // row of the first half within the problem's keys
       const int nslot = (t + 1) * 128 + row;
       j_next = (t + 1 < nt && nslot < k) ? __ldg(idx_row + nslot) : -1;   // next tile's key, loaded early
-      for (int jb = 0; jb < C::kJobs; ++jb, ++job) {
-        ok = ok && mbar_wait_warp(part_full, job & 1, prm.wait_ns);
+      for (int jb = 0; jb < 2; ++jb) {   // dV, then dK
+        ok = ok && mbar_wait_warp(jb == 0 ? dv_full : dk_full, t & 1, prm.wait_ns);
         tc_fence_after();
+        const uint32_t col = jb == 0 ? C::kColDV : C::kColDK;
+        __nv_bfloat16* part = jb == 0 ? csc.part_v : csc.part_k;
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb) {
-            // 64-column block cb of the job region: d = 128: columns cb*64.. of dV (job 0) or dK (job 1);
-            // d = 64: dV for cb = 0, dK for cb = 1
-            const int tensor = D == 128 ? jb : cb;
-            const int dcol = (D == 128 ? cb * 64 : 0) + (lane >= 16 ? 32 : 0);
+          for (int cb = 0; cb < D / 64; ++cb) {
+            const int dcol = cb * 64 + (lane >= 16 ? 32 : 0);
             uint32_t v[32];
-            tmem_ld16x2<32>(lane_addr + ((uint32_t)(16 * h) << 16) + C::kColJob + cb * 64, v);
+            tmem_ld16x2<32>(lane_addr + ((uint32_t)(16 * h) << 16) + col + cb * 64, v);
             tmem_ld_wait(v);
             if (hrow0 + 16 * h < k) {
-              __nv_bfloat16* dst = (tensor == 0 ? csc.part_v : csc.part_k) + (h ? hpos1 : hpos0) * D + dcol;
+              __nv_bfloat16* dst = part + (h ? hpos1 : hpos0) * D + dcol;
               uint32_t pk[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e)
@@ -505,7 +534,7 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(part_free);
+        if (lane == 0) mbar_arrive(jb == 0 ? dv_free : dk_free);
         if (jb == 0) pos_next = j_next >= 0 ? slot_of(j_next) : 0;   // overlaps the next job's MMAs
       }
     }
