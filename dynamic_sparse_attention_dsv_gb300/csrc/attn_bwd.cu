@@ -777,18 +777,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 5) tmem_dealloc(tbase, 512);
 }
 
-// Delta_i = sum_c dO_ic O_ic for every row of the listed problems.
-__global__ void k_bwd_delta(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO, int S, int d,
-                            float* __restrict__ delta, const ProblemTable tab) {
+// Delta_i = sum_c dO_ic O_ic for every row of the listed problems. Each
+// thread takes one 16-byte chunk of a row (d / 8 threads per row, a divisor
+// of the warp), so the loads are coalesced; the row's threads then reduce in
+// a fixed order by shuffles.
+__global__ void __launch_bounds__(256) k_bwd_delta(const __nv_bfloat16* __restrict__ O,
+                                                   const __nv_bfloat16* __restrict__ dO, int S, int d,
+                                                   float* __restrict__ delta, const ProblemTable tab) {
   const int lp = blockIdx.y, p = tab.p[lp];
-  const int s = blockIdx.x * blockDim.x + threadIdx.x;
-  if (s >= S) return;
-  const int64_t o = ((int64_t)p * S + s) * d;
-  const uint4* a = reinterpret_cast<const uint4*>(O + o);
-  const uint4* b = reinterpret_cast<const uint4*>(dO + o);
+  const int cpr = d / 8;
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t s = gid / cpr;
+  const int c = (int)(gid % cpr);
   float acc = 0.f;
-  for (int c = 0; c < d / 8; ++c) {
-    const uint4 x = a[c], y = b[c];
+  if (s < S) {
+    const int64_t o = ((int64_t)p * S + s) * d + c * 8;
+    const uint4 x = *reinterpret_cast<const uint4*>(O + o), y = *reinterpret_cast<const uint4*>(dO + o);
     const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&x);
     const __nv_bfloat162* y2 = reinterpret_cast<const __nv_bfloat162*>(&y);
 #pragma unroll
@@ -798,7 +802,8 @@ __global__ void k_bwd_delta(const __nv_bfloat16* __restrict__ O, const __nv_bflo
       acc = fmaf(u.y, v.y, acc);
     }
   }
-  delta[(int64_t)p * S + s] = acc;
+  for (int m = cpr / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (s < S && c == 0) delta[(int64_t)p * S + s] = acc;
 }
 
 // ---------------------------------------------------------------------------
@@ -1287,7 +1292,8 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
                                : launch_bwd_q<64>(maps, do_cube, prm, none, dt, geo.n_groups, st);
       if (e != cudaSuccess) return DSV_ERR_CUDA;
     }
-    k_bwd_delta<<<dim3((geo.S + 255) / 256, ptab.n), 256, 0, st>>>(prm.O, prm.dO, geo.S, d, w.delta, ptab);
+    k_bwd_delta<<<dim3((unsigned)(((int64_t)geo.S * (d / 8) + 255) / 256), ptab.n), 256, 0, st>>>(
+        prm.O, prm.dO, geo.S, d, w.delta, ptab);
     if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
     const cudaError_t e =
         d == 128 ? launch_bwd_kv<128>(maps, q_tile, do_tile, prm, w.delta, csc.dK, csc.dV, ptab, geo.S, st)

@@ -189,12 +189,14 @@ def test_fullsize_256k_dispatcher_layer():
     _check_kcov(w, inp, kc, [int(np.argmin(kc))])
     sparse_heads = [h for h in range(w.H) if not dense[h]]
     dense_heads = [h for h in range(w.H) if dense[h]]
-    if sparse_heads:
-        h = sparse_heads[0]
-        _check_topk_rows(w, inp, idx, k_h, offs, [h], [0, w.n_groups - 1])
+    # every head: 16 sampled groups of each sparse head (index rows, O, LSE, dQ)
+    # and one key's dK/dV; 2 sampled groups of each dense head (O, LSE, dQ)
+    for n, h in enumerate(sparse_heads):
+        groups = sorted({int(g) for g in (np.linspace(0, w.n_groups - 1, 16) + 37 * n) % w.n_groups})
+        _check_topk_rows(w, inp, idx, k_h, offs, [h], groups)
         rows = _rows(idx, offs[h], k_h[h], w.n_groups)
-        _check_attention(w, inp, rows, O, L, dQ, h, [5])
+        _check_attention(w, inp, rows, O, L, dQ, h, groups)
         _check_keys(w, inp, rows, dK, dV, h, n_keys=1, max_hits=8)
-    if dense_heads:
-        _check_attention(w, inp, None, O, L, dQ, dense_heads[0], [7])
+    for n, h in enumerate(dense_heads):
+        _check_attention(w, inp, None, O, L, dQ, h, [(7 + 211 * n) % w.n_groups, (w.n_groups - 1 - 97 * n) % w.n_groups])
     _check_grad_identities(dK, dV, d["dO"], range(w.H))
