@@ -1020,14 +1020,46 @@ __global__ void k_refine_bracket(uint32_t* hist, int nb, int log2nb, int g_pad, 
   }
 }
 
-// Resolve: a row whose interval holds at most kCandCap candidates sorts them
-// (score desc, key asc) and marks the first k - above of them in the row's
-// selection mask. Single-valued intervals are left to the compaction.
-__global__ void __launch_bounds__(256) k_resolve(const uint64_t* __restrict__ cand, const uint32_t* cand_cnt,
-                                                 const int32_t* nabove, const uint32_t* bcount,
-                                                 const int32_t* rstate, int g_pad, int n_words, uint32_t* sel_bits,
-                                                 int32_t* status, const ProblemTable tab) {
-  __shared__ uint64_t keys[kCandCap];
+// Resolve: a row whose interval holds at most kCandCap candidates marks the
+// first k - above of them in (score desc, key asc) order in the row's
+// selection mask. The candidates are (~score << 32 | key) words; with r the
+// rank of the score below the interval's top, x = r << kb | key orders them
+// the same way and is unique per candidate. A most-significant-digit radix
+// select over x (11-bit digits, a shared-memory histogram per digit) finds
+// the boundary: the candidates below the chosen digit are taken, those above
+// dropped, and the next digit splits the rest, until the chosen digit's
+// candidates are exactly the ones still needed. Single-valued intervals are
+// left to the compaction.
+constexpr int kResolveThreads = 512;
+constexpr int kResolvePer = kCandCap / kResolveThreads;   // candidates per thread
+constexpr int kDigitBits = 11;
+
+// Block-wide exclusive prefix sum of one value per thread (kResolveThreads).
+__device__ __forceinline__ uint32_t block_exclusive_sum(uint32_t v, uint32_t* warp_tot) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_tot[wid] = inc;
+  __syncthreads();
+  uint32_t base = 0;
+  for (int w = 0; w < wid; ++w) base += warp_tot[w];
+  return base + inc - v;
+}
+
+__global__ void __launch_bounds__(kResolveThreads, 2) k_resolve(const uint64_t* __restrict__ cand,
+                                                           const uint32_t* cand_cnt, const uint32_t* bhi,
+                                                           const int32_t* nabove, const uint32_t* bcount,
+                                                           const int32_t* rstate, int g_pad, int n_words, int S,
+                                                           uint32_t* sel_bits, int32_t* status,
+                                                           const ProblemTable tab) {
+  constexpr int kBuckets = 1 << kDigitBits;
+  __shared__ uint32_t hist[kBuckets];
+  __shared__ uint32_t warp_tot[kResolveThreads / 32];
+  __shared__ uint32_t s_digit, s_before;
   const int g = blockIdx.x, lp = blockIdx.y, tid = threadIdx.x;
   const int rid = lp * g_pad + g;
   const int st = rstate[rid];
@@ -1042,36 +1074,92 @@ __global__ void __launch_bounds__(256) k_resolve(const uint64_t* __restrict__ ca
   }
   uint32_t* row_bits = sel_bits + (size_t)rid * n_words;
   const uint64_t* c = cand + (size_t)rid * kCandCap;
+  const int kb = 32 - __clz((uint32_t)(S - 1) | 1u);   // key bits
+  const uint32_t kmask = (1u << kb) - 1u;
   if ((uint32_t)need == ncand) {   // the whole interval is taken
-    for (int i = tid; i < need; i += blockDim.x) {
+    for (int i = tid; i < need; i += kResolveThreads) {
       const uint32_t j = (uint32_t)c[i];
       atomicOr(row_bits + (j >> 5), 1u << (j & 31));
     }
     return;
   }
-  int n2 = 1;
-  while (n2 < (int)ncand) n2 <<= 1;
-  for (int i = tid; i < n2; i += blockDim.x) keys[i] = i < (int)ncand ? c[i] : ~0ull;
-  __syncthreads();
-  for (int size = 2; size <= n2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < n2 / 2; i += blockDim.x) {
-        const int a = 2 * i - (i & (stride - 1));
-        const int b = a + stride;
-        const bool asc = (a & size) == 0;
-        const uint64_t x = keys[a], y = keys[b];
-        if ((x > y) == asc) {
-          keys[a] = y;
-          keys[b] = x;
-        }
-      }
-      __syncthreads();
+  // r = (~score of the interval's top) - (~score): 0 for the highest score
+  const uint32_t top = ~(bhi[rid] - 1u);
+  uint64_t x[kResolvePer];
+  uint32_t live = 0;
+  uint32_t rmax = 0;
+#pragma unroll
+  for (int e = 0; e < kResolvePer; ++e) {
+    const int i = tid + e * kResolveThreads;
+    x[e] = 0;
+    if (i < (int)ncand) {
+      const uint64_t w = c[i];
+      const uint32_t r = (uint32_t)(w >> 32) - top;
+      rmax = max(rmax, r);
+      x[e] = ((uint64_t)r << kb) | ((uint32_t)w & kmask);
+      live |= 1u << e;
     }
   }
-  for (int i = tid; i < need; i += blockDim.x) {
-    const uint32_t j = (uint32_t)keys[i];
-    atomicOr(row_bits + (j >> 5), 1u << (j & 31));
+  // the interval's width bounds r, so the select starts at the top bit of x
+  const int rbits = 32 - __clz(__reduce_max_sync(0xffffffffu, rmax) | 0u);
+  if ((tid & 31) == 0) warp_tot[tid >> 5] = (uint32_t)rbits;
+  __syncthreads();
+  int L = kb;
+  for (int w = 0; w < kResolveThreads / 32; ++w) L = max(L, kb + (int)warp_tot[w]);
+  __syncthreads();
+  uint32_t remaining = (uint32_t)need;
+  uint64_t prefix = 0;
+  for (int hb = L; hb > 0; hb -= kDigitBits) {
+    const int shift = hb > kDigitBits ? hb - kDigitBits : 0, bits = hb - shift;
+    const uint32_t dmask = (1u << bits) - 1u;
+    for (int i = tid; i < kBuckets; i += kResolveThreads) hist[i] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < kResolvePer; ++e)
+      if (((live >> e) & 1u) && (x[e] >> hb) == prefix) atomicAdd(&hist[(uint32_t)(x[e] >> shift) & dmask], 1u);
+    __syncthreads();
+    // the digit whose bucket holds the remaining-th live candidate
+    constexpr int kPerThread = kBuckets / kResolveThreads;
+    uint32_t v = 0;
+#pragma unroll
+    for (int q = 0; q < kPerThread; ++q) {
+      const int bkt = tid * kPerThread + q;
+      v += bkt < (1 << bits) ? hist[bkt] : 0u;
+    }
+    const uint32_t before = block_exclusive_sum(v, warp_tot);
+    if (before < remaining && remaining <= before + v) {
+      uint32_t acc = before;
+      for (int q = 0; q < kPerThread; ++q) {
+        const uint32_t h = hist[tid * kPerThread + q];
+        if (acc + h >= remaining) {
+          s_digit = (uint32_t)(tid * kPerThread + q);
+          s_before = acc;
+          break;
+        }
+        acc += h;
+      }
+    }
+    __syncthreads();
+    const uint32_t d = s_digit, below = s_before, at = hist[d];
+    // take the live candidates below the digit; keep those at it only if
+    // they are not all needed
+    const bool take_at = remaining - below == at;
+#pragma unroll
+    for (int e = 0; e < kResolvePer; ++e) {
+      if (!((live >> e) & 1u) || (x[e] >> hb) != prefix) continue;
+      const uint32_t dg = (uint32_t)(x[e] >> shift) & dmask;
+      if (dg < d || (dg == d && take_at)) {
+        const uint32_t j = (uint32_t)x[e] & kmask;
+        atomicOr(row_bits + (j >> 5), 1u << (j & 31));
+      }
+      if (dg != d || take_at) live &= ~(1u << e);
+    }
+    if (take_at) return;
+    remaining -= below;
+    prefix = (prefix << bits) | d;
+    __syncthreads();   // hist and the shared digit are rewritten next round
   }
+  if (tid == 0) raise_status_if_clear(status, DSV_ERR_CANDIDATES);   // x is unique: cannot be reached
 }
 
 // Index rows from the masks: one block per group row, its 8 warps on
@@ -1501,6 +1589,44 @@ __global__ void k_cov_window(int nb, int g_pad, int n_groups, float scale, const
   fine_scale[rid] = cm[wb] - (wa > 0 ? cm[wa - 1] : 0.0);
 }
 
+// Top-k bracket from the coverage pass's coarse table (counts cumulated from
+// the top bin). Its bins are linear in the score over the row's [min, max],
+// like the top-k histogram's, so once coverage has run the bin holding the
+// k-th largest score, the scores above it and the scores inside it are read
+// from that table and the histogram pass is not needed. Same outputs as
+// k_bracket: the interval [least score of bin b*, least score of bin b*-1)
+// in orderable bits, found with the coverage passes' own binning arithmetic.
+__global__ void k_bracket_cov(int nb, int g_pad, int n_groups, int n_gt, float scale, const uint32_t* mmax,
+                              const uint32_t* mmin, const int32_t* cum_cnt, uint32_t* hist, int hist_nb,
+                              uint32_t* blo, uint32_t* bhi, int32_t* nabove, uint32_t* bcount, int32_t* rstate,
+                              int32_t* tflag, int32_t* status, const ProblemTable tab) {
+  const int lp = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n_groups) return;
+  const int k = tab.k[lp];
+  const size_t rid = (size_t)lp * g_pad + g;
+  const int32_t* cc = cum_cnt + rid * nb;
+  const int b = first_reaching(cc, nb, k);
+  if (cc[b] < k) raise_status_if_clear(status, DSV_ERR_CANDIDATES);   // fewer than k scores: inconsistent
+  const int above = b > 0 ? cc[b - 1] : 0;
+  const uint32_t count = (uint32_t)(cc[b] - above);
+  float cmax, inv_w, w2;
+  cov_row_scale(mmax[rid], mmin[rid], scale, nb, &cmax, &inv_w, &w2);
+  const uint32_t o_lo = mmin[rid], o_hi = mmax[rid] + 1u;
+  const uint32_t l = least_with_cbin_at_most(b, o_lo, o_hi, cmax, scale, inv_w, nb);
+  const uint32_t u = least_with_cbin_at_most(b - 1, o_lo, o_hi, cmax, scale, inv_w, nb);   // o_hi for b = 0
+  blo[rid] = l;
+  bhi[rid] = u;
+  nabove[rid] = above;
+  bcount[rid] = count;
+  const int st = row_state(l, u, count);
+  rstate[rid] = st;
+  if (st == kRowRefine) {
+    uint32_t* h = hist + (size_t)lp * hist_nb * g_pad + g;
+    for (int i = 0; i < hist_nb; ++i) h[(size_t)i * g_pad] = 0u;
+    tflag[lp * n_gt + g / 128] = 1;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host orchestration.
 struct TopkPlan {
@@ -1757,16 +1883,23 @@ static cudaError_t minmax_pass(const TopkPlan& pl, const TopkWs& w, const Proble
 
 // Top-k, once the linear histogram (nb bins) is in w.hist: the bracket and
 // the REFINE rounds (group tiles with no row to refine leave at once).
+// With `cov_scale` > 0 the bracket comes from the coverage pass's coarse table
+// (coverage ran on these rows with that scale) instead of the histogram.
 static cudaError_t topk_bracket_refine(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab,
                                        const CUtensorMap* maps, dim3 grid, SelParams prm, int nb, int32_t* status,
-                                       cudaStream_t st) {
+                                       cudaStream_t st, float cov_scale = 0.f) {
   const int n = tab.n;
   const int rounds = refine_rounds(pl);
   const int lg = pl.RP == 32 ? SelCfg<32>::kHistLog2 : SelCfg<64>::kHistLog2;
   const size_t nflag = (size_t)n * pl.n_gt;
   const dim3 rgrid(pl.n_gt, n);
-  k_bracket<<<rgrid, 128, 0, st>>>(w.hist, nb, pl.g_pad, pl.geo.n_groups, pl.n_gt, w.mmin, w.mmax, w.blo, w.bhi,
-                                   w.nabove, w.bcount, w.rstate, w.tflag, status, tab);
+  if (cov_scale > 0.f)
+    k_bracket_cov<<<rgrid, 128, 0, st>>>(pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.n_gt, cov_scale, w.mmax, w.mmin,
+                                         w.cum_cnt, w.hist, pl.hist_bins, w.blo, w.bhi, w.nabove, w.bcount, w.rstate,
+                                         w.tflag, status, tab);
+  else
+    k_bracket<<<rgrid, 128, 0, st>>>(w.hist, nb, pl.g_pad, pl.geo.n_groups, pl.n_gt, w.mmin, w.mmax, w.blo, w.bhi,
+                                     w.nabove, w.bcount, w.rstate, w.tflag, status, tab);
   if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
   for (int r = 0; r < rounds; ++r) {
     prm.tflag = w.tflag + r * nflag;
@@ -1783,8 +1916,9 @@ static cudaError_t topk_bracket_refine(const TopkPlan& pl, const TopkWs& w, cons
 static cudaError_t topk_finish(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, int32_t* idx,
                                int32_t* status, cudaStream_t st) {
   const int n = tab.n;
-  k_resolve<<<dim3(pl.geo.n_groups, n), 256, 0, st>>>(w.cand, w.cand_cnt, w.nabove, w.bcount, w.rstate, pl.g_pad,
-                                                        pl.n_tiles * 4, w.selb, status, tab);
+  k_resolve<<<dim3(pl.geo.n_groups, n), kResolveThreads, 0, st>>>(w.cand, w.cand_cnt, w.bhi, w.nabove, w.bcount,
+                                                                    w.rstate, pl.g_pad, pl.n_tiles * 4, pl.geo.S,
+                                                                    w.selb, status, tab);
   if (cudaGetLastError() != cudaSuccess) return cudaErrorUnknown;
   k_sel_compact<<<dim3(pl.geo.n_groups, n), 32 * kCompactWarps, 0, st>>>(w.selb, w.eqb, w.rstate, w.nabove, pl.g_pad,
                                                                           pl.n_tiles * 4, idx, status, tab);
@@ -1802,16 +1936,18 @@ static cudaError_t topk_clear(const TopkPlan& pl, const TopkWs& w, int n, cudaSt
 
 // The top-k passes of one launch of problems whose projections are in the
 // workspace; `minmax` = false when the row ranges are already there.
+// `cov_scale` > 0: coverage has just run on the same rows with that scale,
+// and its coarse table gives the bracket in place of the histogram pass.
 static cudaError_t topk_passes(const TopkPlan& pl, const TopkWs& w, const ProblemTable& tab, const CUtensorMap* maps,
-                               bool minmax, int32_t* idx, int32_t* status, cudaStream_t st) {
+                               bool minmax, int32_t* idx, int32_t* status, cudaStream_t st, float cov_scale = 0.f) {
   int n_chunks, chunk_tiles;
   chunking(pl, tab.n, &n_chunks, &chunk_tiles);
   const SelParams prm = sel_params(pl, w, n_chunks, chunk_tiles, 0.f, status);
   const dim3 grid(pl.n_gt, n_chunks, tab.n);
   if (minmax && minmax_pass(pl, w, tab, maps, grid, prm, st) != cudaSuccess) return cudaErrorUnknown;
   if (topk_clear(pl, w, tab.n, st) != cudaSuccess) return cudaErrorUnknown;
-  if (select_pass<kHist>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
-  if (topk_bracket_refine(pl, w, tab, maps, grid, prm, pl.hist_bins, status, st) != cudaSuccess)
+  if (cov_scale <= 0.f && select_pass<kHist>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
+  if (topk_bracket_refine(pl, w, tab, maps, grid, prm, pl.hist_bins, status, st, cov_scale) != cudaSuccess)
     return cudaErrorUnknown;
   if (select_pass<kCollect>(pl.RP, grid, st, maps, prm, tab) != cudaSuccess) return cudaErrorUnknown;
   return topk_finish(pl, w, tab, idx, status, st);
@@ -2056,7 +2192,8 @@ extern "C" dsv_status dsv_coverage_topk(const void* Q, const void* K, const void
     if (!make_score_maps(maps, pl, w, tab.n)) return DSV_ERR_CUDA;
     if (cov_passes(pl, w, tab, maps, true, scale, mass, k_cov, curve, n_curve, dev_status, st) != cudaSuccess)
       return DSV_ERR_CUDA;
-    if (topk_passes(pl, w, tab, maps, false, idx, dev_status, st) != cudaSuccess) return DSV_ERR_CUDA;
+    // the coverage pass's coarse table brackets the k-th score: no histogram pass
+    if (topk_passes(pl, w, tab, maps, false, idx, dev_status, st, scale) != cudaSuccess) return DSV_ERR_CUDA;
   }
   return DSV_OK;
 }
