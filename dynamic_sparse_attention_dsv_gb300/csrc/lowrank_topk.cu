@@ -1168,11 +1168,11 @@ __global__ void __launch_bounds__(kResolveThreads, 2) k_resolve(const uint64_t* 
 // k - above lowest keys of its tie mask (the cut is found first: each warp
 // counts its segment's ties, and the warp holding the cut walks its words).
 // Each warp counts its segment's selected keys, a block scan gives each
-// segment its first output position, and each warp then writes its keys 32
-// output positions at a time: lane j finds the word of position j by binary
-// search over the warp's prefix sums and the key inside it with __fns, so
-// every store instruction writes 32 consecutive indices (selected keys
-// cluster, so per-word loops would diverge).
+// segment its first output position, and each warp then takes its words 32
+// at a time: every lane writes its word's keys into the warp's shared staging
+// area at the word's prefix position (a short loop over the set bits; the
+// keys cluster, so the counts differ, but only shared stores diverge), and
+// the warp copies the staged keys out with stores of 32 consecutive indices.
 constexpr int kCompactWarps = 8;
 
 __device__ __forceinline__ int warp_incl_scan(int x, int lane) {
@@ -1197,6 +1197,7 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_sel_compact(const uint32
                                                                     int32_t* status, const ProblemTable tab) {
   __shared__ int seg_total[kCompactWarps];
   __shared__ int s_cut;
+  __shared__ int32_t stage[kCompactWarps][32 * 32];
   const int g = blockIdx.x, lp = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int k = tab.k[lp];
   const int rid = lp * g_pad + g;
@@ -1253,26 +1254,24 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_sel_compact(const uint32
     base += i < warp ? seg_total[i] : 0;
     row_total += seg_total[i];
   }
+  // 32 words (1024 keys) per step: each lane writes its word's selected keys
+  // into the warp's staging area at its exclusive prefix, then the warp
+  // copies them out in order with coalesced stores
+  int32_t* st = stage[warp];
   for (int w0 = w_begin; w0 < w_end; w0 += 32) {
     const uint32_t m = w0 + lane < w_end ? word(w0 + lane) : 0u;
     const int c = __popc(m);
     const int incl = warp_incl_scan(c, lane);
     const int total = __shfl_sync(0xffffffffu, incl, 31);
-    for (int q0 = 0; q0 < total; q0 += 32) {
-      const int q = q0 + lane;   // this lane's position among the step's selected keys
-      int lo = 0;                // first lane (word) whose inclusive count exceeds q
-#pragma unroll
-      for (int step = 16; step > 0; step >>= 1) {
-        const int v = __shfl_sync(0xffffffffu, incl, lo + step - 1);
-        if (v <= q) lo += step;
-      }
-      const uint32_t wm = __shfl_sync(0xffffffffu, m, lo);
-      const int excl = __shfl_sync(0xffffffffu, incl - c, lo);
-      if (q < total) {
-        const int p = base + q;
-        if (p < k) out[p] = (w0 + lo) * 32 + (int)__fns(wm, 0, q - excl + 1);
-      }
+    int pos = incl - c;
+    const int kbase = (w0 + lane) * 32;
+    for (uint32_t mm = m; mm; mm &= mm - 1u) st[pos++] = kbase + __ffs(mm) - 1;
+    __syncwarp();
+    for (int q = lane; q < total; q += 32) {
+      const int p = base + q;
+      if (p < k) out[p] = st[q];
     }
+    __syncwarp();
     base += total;
   }
   if (threadIdx.x == 0 && row_total != k) raise_status_if_clear(status, DSV_ERR_CANDIDATES);
