@@ -127,8 +127,11 @@ __device__ __forceinline__ void red_smem_u32(uint32_t addr, uint32_t v) {
 // maximum, so each key adds q = exp(b w - u) in (exp(-w), 1] as 16.16 fixed
 // point (relative precision 2^-17 whatever the probability's size); the bin's
 // sum is scaled back by exp(-b w) afterwards. Integer sums are exact and
-// order-independent. A chunk holds at most kCovMaxTiles * 128 (< 65536) keys of a row, so
-// neither the count nor the fixed-point sum overflows 32 bits.
+// order-independent. The counts are kept per half bin, two 16-bit counts to a
+// word (low half: the bin's upper half in score, high half: its lower half),
+// which gives the top-k bracket twice the coarse resolution at no extra
+// shared memory. A chunk holds at most kCovMaxTiles * 128 (< 65536) keys of a
+// row, so neither a half count nor the fixed-point sum overflows.
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Bin of x >= 0 (x < 2^22): x - 1/2 rounded to the nearest integer by adding
@@ -162,6 +165,14 @@ __device__ __forceinline__ void lin_range(uint32_t mmin_ord, uint32_t mmax_ord, 
 // they agree bit for bit; non-increasing in s.
 __device__ __forceinline__ float cov_coord(float s, float cmax, float scale, float inv_w) {
   return __fmul_rn(__fmul_rn(scale, __fsub_rn(cmax, s)), inv_w);
+}
+// Coarse bin of coordinate x and its offset inside the bin (in [0, 1], more
+// when clamped to the last bin); the half bin is 2 bin + (offset >= 1/2).
+// Monotone in x, and the same arithmetic everywhere.
+__device__ __forceinline__ int cov_bin(float x, int nb, float* frac) {
+  const float t = bin_round(x);
+  *frac = x - fminf(t - kRoundMagic, (float)(nb - 1));
+  return bin_of(t, nb);
 }
 __device__ __forceinline__ void cov_row_scale(uint32_t mmax_ord, uint32_t mmin_ord, float scale, int nb, float* cmax,
                                               float* inv_w, float* w2) {
@@ -416,12 +427,12 @@ __global__ void __launch_bounds__(kSelThreads, MODE == kCovFine ? 1 : 2)
             // the row maximum; q = exp(b w - u) in (exp(-w), 1], as 16.16
             // fixed point through the float bits
             const float x = cov_coord(s, cmax, prm.scale, inv_w);
-            const float t = bin_round(x);
-            const int bin = bin_of(t, NBc);
-            const float frac = x - fminf(t - kRoundMagic, (float)(NBc - 1));   // in [0, 1], more when clamped
+            float frac;
+            const int bin = cov_bin(x, NBc, &frac);
             const float qv = ex2_fast(-frac * w2);
             const uint32_t qf = __float_as_uint(fmaf(qv, 65536.f, 8388608.f)) - __float_as_uint(8388608.f);
-            red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, 1u);
+            // the count goes to the half bin: low half word below the middle, high half above
+            red_smem_u32(hist_base + (uint32_t)(bin * 128 + row) * 4u, frac >= 0.5f ? 65536u : 1u);
             red_smem_u32(cmass_base + (uint32_t)(bin * 128 + row) * 4u, qf);
           }
           if constexpr (kFinePart) {
@@ -1308,20 +1319,33 @@ __global__ void k_fill_all(int32_t* idx, int64_t off, int S, int64_t total) {
 // the interval holds at most kCovPoints values all are evaluated. Evaluation
 // blocks take kCovGroupsPerBlock groups each and their partial sums are
 // added in block order, so the result does not depend on scheduling.
+// `half_cnt` non-null: the count words hold two half-bin counts (the coarse
+// pass); their sums go to cum_cnt and the half counts to half_cnt
+// ([problem][2 nb][g_pad]).
 __global__ void k_cov_merge(const uint32_t* __restrict__ cnt, const float* __restrict__ mass, int nb, int n_chunks,
-                            int g_pad, int n_groups, int32_t* cum_cnt, double* cum_mass) {
+                            int g_pad, int n_groups, int32_t* cum_cnt, double* cum_mass, int32_t* half_cnt) {
   const int lp = blockIdx.z, b = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= n_groups) return;
-  int c = 0;
+  int c0 = 0, c1 = 0;
   double m = 0.0;
   for (int ch = 0; ch < n_chunks; ++ch) {
     const size_t o = (((size_t)lp * n_chunks + ch) * nb + b) * g_pad + g;
-    c += (int)cnt[o];
+    const uint32_t v = cnt[o];
+    if (half_cnt) {
+      c0 += (int)(v & 0xffffu);
+      c1 += (int)(v >> 16);
+    } else {
+      c0 += (int)v;
+    }
     m += (double)mass[o];
   }
   const size_t rid = (size_t)lp * g_pad + g;
-  cum_cnt[rid * nb + b] = c;
+  cum_cnt[rid * nb + b] = c0 + c1;
   cum_mass[rid * nb + b] = m;
+  if (half_cnt) {
+    half_cnt[((size_t)lp * 2 * nb + 2 * b) * g_pad + g] = c0;
+    half_cnt[((size_t)lp * 2 * nb + 2 * b + 1) * g_pad + g] = c1;
+  }
 }
 
 // One warp per group: lane l owns bins [l*per, l*per + per) of the (at most
@@ -1553,12 +1577,15 @@ __global__ void __launch_bounds__(1024) k_cov_pick(bool curve, int nblk, int n_g
 // scores whose bin lies in [wa, wb] form the interval [lo, hi] of orderable
 // bits, found by binary search with the passes' own binning arithmetic
 // (empty when lo > hi).
+// `half` = true: the same for half bins (2 nb of them).
 __device__ uint32_t least_with_cbin_at_most(int target, uint32_t o_lo, uint32_t o_hi, float cmax, float scale,
-                                            float inv_w, int nb) {
+                                            float inv_w, int nb, bool half = false) {
   uint32_t a = o_lo, b = o_hi;   // answer in [a, b]; o_hi when no score reaches it
   while (a < b) {
     const uint32_t m = a + (b - a) / 2;
-    if (bin_of(bin_round(cov_coord(ord2f(m) + 0.0f, cmax, scale, inv_w)), nb) <= target) b = m;
+    float frac;
+    const int bin = cov_bin(cov_coord(ord2f(m) + 0.0f, cmax, scale, inv_w), nb, &frac);
+    if ((half ? 2 * bin + (frac >= 0.5f ? 1 : 0) : bin) <= target) b = m;
     else a = m + 1;
   }
   return a;
@@ -1588,31 +1615,41 @@ __global__ void k_cov_window(int nb, int g_pad, int n_groups, float scale, const
   fine_scale[rid] = cm[wb] - (wa > 0 ? cm[wa - 1] : 0.0);
 }
 
-// Top-k bracket from the coverage pass's coarse table (counts cumulated from
-// the top bin). Its bins are linear in the score over the row's [min, max],
-// like the top-k histogram's, so once coverage has run the bin holding the
-// k-th largest score, the scores above it and the scores inside it are read
-// from that table and the histogram pass is not needed. Same outputs as
-// k_bracket: the interval [least score of bin b*, least score of bin b*-1)
-// in orderable bits, found with the coverage passes' own binning arithmetic.
+// Top-k bracket from the coverage pass's half-bin counts. Its bins are
+// linear in the score over the row's [min, max], like the top-k histogram's,
+// so once coverage has run, the half bin holding the k-th largest score, the
+// scores above it and the scores inside it are read from that table and the
+// histogram pass is not needed. Same outputs as k_bracket: the interval
+// [least score of half bin h*, least score of half bin h*-1) in orderable
+// bits, found with the coverage passes' own binning arithmetic.
 __global__ void k_bracket_cov(int nb, int g_pad, int n_groups, int n_gt, float scale, const uint32_t* mmax,
-                              const uint32_t* mmin, const int32_t* cum_cnt, uint32_t* hist, int hist_nb,
+                              const uint32_t* mmin, const int32_t* cum_cnt, const int32_t* half_cnt, uint32_t* hist,
+                              int hist_nb,
                               uint32_t* blo, uint32_t* bhi, int32_t* nabove, uint32_t* bcount, int32_t* rstate,
                               int32_t* tflag, int32_t* status, const ProblemTable tab) {
   const int lp = blockIdx.y, g = blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= n_groups) return;
   const int k = tab.k[lp];
   const size_t rid = (size_t)lp * g_pad + g;
+  // the coarse bin from the cumulative coarse counts, then one of its halves
   const int32_t* cc = cum_cnt + rid * nb;
   const int b = first_reaching(cc, nb, k);
   if (cc[b] < k) raise_status_if_clear(status, DSV_ERR_CANDIDATES);   // fewer than k scores: inconsistent
-  const int above = b > 0 ? cc[b - 1] : 0;
-  const uint32_t count = (uint32_t)(cc[b] - above);
+  int above = b > 0 ? cc[b - 1] : 0;
+  const int32_t* hc = half_cnt + (size_t)lp * 2 * nb * g_pad + g;
+  const int h0 = __ldg(hc + (size_t)(2 * b) * g_pad), h1 = __ldg(hc + (size_t)(2 * b + 1) * g_pad);
+  int hb = 2 * b;
+  uint32_t count = (uint32_t)h0;
+  if (above + h0 < k) {
+    hb = 2 * b + 1;
+    above += h0;
+    count = (uint32_t)h1;
+  }
   float cmax, inv_w, w2;
   cov_row_scale(mmax[rid], mmin[rid], scale, nb, &cmax, &inv_w, &w2);
   const uint32_t o_lo = mmin[rid], o_hi = mmax[rid] + 1u;
-  const uint32_t l = least_with_cbin_at_most(b, o_lo, o_hi, cmax, scale, inv_w, nb);
-  const uint32_t u = least_with_cbin_at_most(b - 1, o_lo, o_hi, cmax, scale, inv_w, nb);   // o_hi for b = 0
+  const uint32_t l = least_with_cbin_at_most(hb, o_lo, o_hi, cmax, scale, inv_w, nb, true);
+  const uint32_t u = least_with_cbin_at_most(hb - 1, o_lo, o_hi, cmax, scale, inv_w, nb, true);   // o_hi for hb = 0
   blo[rid] = l;
   bhi[rid] = u;
   nabove[rid] = above;
@@ -1704,6 +1741,7 @@ struct TopkWs {
   uint32_t *selb, *eqb;
   uint64_t* cand;
   int32_t* cum_cnt;
+  int32_t* half_cnt;   // [n][2 * cov_bins][g_pad] half-bin counts of the coarse pass
   double* cum_mass;
   float *width, *zinv;
   int32_t *fine_cnt, *cov_win, *kwin_lo, *kwin_hi;
@@ -1748,6 +1786,7 @@ static size_t carve(void* base, const TopkPlan& pl, int mode, TopkWs* w) {
     w->cov_hist = c.take<uint32_t>(pc * pl.max_chunks * pl.cov_bins * gp);
     w->mass = c.take<float>(pc * pl.max_chunks * pl.cov_bins * gp);
     w->cum_cnt = c.take<int32_t>(pc * gp * pl.cov_bins);
+    w->half_cnt = c.take<int32_t>(pc * gp * 2 * pl.cov_bins);
     w->cum_mass = c.take<double>(pc * gp * pl.cov_bins);
     w->width = c.take<float>(pc * gp);
     w->zinv = c.take<float>(pc * gp);
@@ -1894,7 +1933,8 @@ static cudaError_t topk_bracket_refine(const TopkPlan& pl, const TopkWs& w, cons
   const dim3 rgrid(pl.n_gt, n);
   if (cov_scale > 0.f)
     k_bracket_cov<<<rgrid, 128, 0, st>>>(pl.cov_bins, pl.g_pad, pl.geo.n_groups, pl.n_gt, cov_scale, w.mmax, w.mmin,
-                                         w.cum_cnt, w.hist, pl.hist_bins, w.blo, w.bhi, w.nabove, w.bcount, w.rstate,
+                                         w.cum_cnt, w.half_cnt, w.hist, pl.hist_bins, w.blo, w.bhi, w.nabove, w.bcount,
+                                         w.rstate,
                                          w.tflag, status, tab);
   else
     k_bracket<<<rgrid, 128, 0, st>>>(w.hist, nb, pl.g_pad, pl.geo.n_groups, pl.n_gt, w.mmin, w.mmax, w.blo, w.bhi,
@@ -1988,7 +2028,8 @@ static cudaError_t cov_after_coarse(const TopkPlan& pl, const TopkWs& w, const P
                                     float scale, float mass, cudaStream_t st) {
   const int n = tab.n, nb = pl.cov_bins, ng = pl.geo.n_groups, S = pl.geo.S;
   const dim3 mgrid((ng + 127) / 128, nb, n), sgrid((ng + 7) / 8, n), wgrid((ng + 127) / 128, n);
-  k_cov_merge<<<mgrid, 128, 0, st>>>(w.cov_hist, w.mass, nb, n_chunks, pl.g_pad, ng, w.cum_cnt, w.cum_mass);
+  k_cov_merge<<<mgrid, 128, 0, st>>>(w.cov_hist, w.mass, nb, n_chunks, pl.g_pad, ng, w.cum_cnt, w.cum_mass,
+                                     w.half_cnt);
   k_cov_scan<<<sgrid, 256, 0, st>>>(w.mmax, w.mmin, nb, pl.g_pad, ng, scale, w.cum_cnt, w.cum_mass, w.width, w.zinv,
                                     nullptr);
   // both bounds at once: k_lo from the upper bound, k_hi from the lower bound
@@ -2006,7 +2047,8 @@ static cudaError_t cov_after_fine(const TopkPlan& pl, const TopkWs& w, const Pro
                                   cudaStream_t st) {
   const int n = tab.n, nb = pl.cov_bins, ng = pl.geo.n_groups, S = pl.geo.S;
   const dim3 mgrid((ng + 127) / 128, nb, n), sgrid((ng + 7) / 8, n);
-  k_cov_merge<<<mgrid, 128, 0, st>>>(w.cov_hist, w.mass, nb, n_chunks, pl.g_pad, ng, w.fine_cnt, w.fine_mass);
+  k_cov_merge<<<mgrid, 128, 0, st>>>(w.cov_hist, w.mass, nb, n_chunks, pl.g_pad, ng, w.fine_cnt, w.fine_mass,
+                                     nullptr);
   k_cov_scan<<<sgrid, 256, 0, st>>>(w.mmax, w.mmin, nb, pl.g_pad, ng, scale, w.fine_cnt, w.fine_mass, nullptr,
                                     nullptr, w.fine_scale);
   k_cov_range_init<<<1, 256, 0, st>>>(w.cov_range, w.kwin_lo, w.kwin_hi, S, n);
