@@ -63,20 +63,24 @@ def test_topk_exact_on_clustered_scores(name):
             _check_all_rows(idx, ks, offs, n_groups, h, ref)
 
 
-def test_coverage_topk_exact_on_clustered_scores():
-    """The combined call (shared projections and row ranges) writes the same
-    exact rows on the same inputs."""
-    grid, d, r, H, mode, _ = CASES["spread_r32"]
+@pytest.mark.parametrize("name", list(CASES))
+def test_coverage_topk_exact_on_clustered_scores(name):
+    """The combined call writes the same exact rows on the same inputs. Its
+    bracket for the k-th score comes from the coverage pass's half-bin counts
+    (no histogram pass), so these inputs also drive the REFINE rounds, the
+    tied rows and the resolve from that bracket."""
+    grid, d, r, H, mode, kvals = CASES[name]
     inp = syn.make_clustered_inputs(*grid, d, r, H, mode)
     dev = {n: inp[n].cuda() for n in ("Q", "K", "Wq", "Wk")}
     S = grid[0] * grid[1] * grid[2]
-    n_groups = S // 128
-    st = dsv.new_status()
-    _, _, idx, ks, offs = dsv.coverage_topk(dev["Q"], dev["K"], dev["Wq"], dev["Wk"], grid, GROUP, 7000, status=st)
-    dsv.check_status(st, "coverage_topk clustered")
-    for h in range(H):
-        ref, _ = _oracle_row(inp, h, grid, 7000)
-        _check_all_rows(idx, ks, offs, n_groups, h, ref)
+    n_groups = S // (GROUP[0] * GROUP[1] * GROUP[2])
+    for k in tuple(kvals) + (7000,):
+        st = dsv.new_status()
+        _, _, idx, ks, offs = dsv.coverage_topk(dev["Q"], dev["K"], dev["Wq"], dev["Wk"], grid, GROUP, k, status=st)
+        dsv.check_status(st, f"coverage_topk {name} k={k}")
+        for h in range(H):
+            ref, _ = _oracle_row(inp, h, grid, k)
+            _check_all_rows(idx, ks, offs, n_groups, h, ref)
 
 
 @pytest.mark.parametrize("k", [65536, 2621])
