@@ -180,8 +180,10 @@ dsv_status dsv_coverage(const void* Q, const void* K, const void* Wq_lr, const v
  * idx_offset, idx); k_cov, curve and idx hold exactly the values the two
  * separate calls write. When every problem takes a top-k with 1 <= k < S
  * (no dense entry, no k = S), the key projection, the group-mean
- * projection and the per-row score range are computed once and serve both;
- * otherwise the two calls run one after the other. The workspace is at least
+ * projection and the per-row score range are computed once and serve both,
+ * and the coverage pass's per-row bin counts locate each row's k-th score,
+ * so the top-k runs no histogram pass of its own; otherwise the two calls
+ * run one after the other. The workspace is at least
  * dsv_coverage_topk_workspace_size() bytes (the two calls' buffers side by
  * side); S <= 4186112 as for dsv_coverage.
  * ---------------------------------------------------------------------- */
