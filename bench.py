@@ -201,7 +201,7 @@ def dispatcher_layer(device, pk):
 
 
 def workload_dict(w):
-    return {"workload": f"cfg{w.cfg}: " + w.name, "B": 1, "H": w.H, "grid": [w.T, w.Y, w.X], "S": w.S, "d": w.d,
+    return {"workload": w.name, "B": 1, "H": w.H, "grid": [w.T, w.Y, w.X], "S": w.S, "d": w.d,
             "r": w.r, "group": [w.gt, w.gy, w.gx], "k": w.k,
             "l2": f"inputs larger than L2 ({4 * w.H * w.S * w.d * 2 / 1e9:.2f} GB of Q/K/V/dO)"}
 
@@ -536,9 +536,9 @@ def main():
     if e2e:
         line["e2e"] = e2e
     if rank == 0 and not args.no_sweep and args.heads <= 0:
-        line["breakdown"]["cfg3_topk_sweep"] = topk_sweep(device, pk)
+        line["breakdown"]["topk_sweep_s128k"] = topk_sweep(device, pk)
     if rank == 0 and not args.no_layer and args.heads <= 0:
-        line["breakdown"]["cfg4_dispatcher_layer"] = dispatcher_layer(device, pk)
+        line["breakdown"]["dispatcher_layer_s256k"] = dispatcher_layer(device, pk)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp)[0]
     if rank == 0:

@@ -11,9 +11,10 @@ here; these seeded tensors stand in for video-latent Q/K/V):
 * P is a per-token 3D sinusoidal embedding of width d: d/4 channels for the
   time axis and 3d/8 each for the two spatial axes; each axis uses the
   textbook 1D sinusoid [sin(p*w_m), cos(p*w_m)], w_m = 10000^(-2m/n).
-* Per head h, in this draw order from numpy ``default_rng(20250000 + cfg)``:
+* Per head h, in this draw order from numpy ``default_rng(20250000 + index)``
+  (index: the workload's position in ``WORKLOADS``):
   G_h (d x d, N(0,1)/sqrt(d)), Wq_h and Wk_h (d x r, N(0, 1/d)), the head's
-  Q scale (constant or uniform, per config), then noise N_Q, N_K, N_V
+  Q scale (constant or uniform, per workload), then noise N_Q, N_K, N_V
   (S x d, N(0,1)).  Q = qscale_h*(P G_h + 0.5 N_Q), K = P G_h + 0.5 N_K,
   V = P G_h + 0.5 N_V.  After all heads, dO ~ N(0,1) of shape [H, S, d].
 * Every tensor is rounded fp64 -> fp32 -> bf16 (round to nearest even) on the
@@ -35,7 +36,7 @@ class Workload:
     query-group cube gt x gy x gx and k selected keys per group."""
 
     name: str
-    cfg: int
+    index: int                  # position in WORKLOADS; offsets the default seed
     H: int
     T: int
     Y: int
@@ -85,8 +86,8 @@ TOPK_SWEEP_FRACTIONS = (0.01, 0.05, 0.10, 0.20)
 TOPK_SWEEP_RANKS = (16, 32, 64)
 
 
-def workload(cfg: int, **overrides) -> Workload:
-    return dataclasses.replace(WORKLOADS[cfg], **overrides) if overrides else WORKLOADS[cfg]
+def workload(n: int, **overrides) -> Workload:
+    return dataclasses.replace(WORKLOADS[n], **overrides) if overrides else WORKLOADS[n]
 
 
 def sinusoid_3d(T: int, Y: int, X: int, d: int) -> np.ndarray:
@@ -123,7 +124,7 @@ def make_inputs(w: Workload, seed: Optional[int] = None, with_grad_out: Optional
     """
     H = w.H if heads is None else heads
     S, d, r = w.S, w.d, w.r
-    rng = np.random.default_rng(20250000 + w.cfg if seed is None else seed)
+    rng = np.random.default_rng(20250000 + w.index if seed is None else seed)
     P = sinusoid_3d(w.T, w.Y, w.X, d)
     Q = torch.empty((H, S, d), dtype=torch.bfloat16)
     K = torch.empty_like(Q)
@@ -217,8 +218,8 @@ def make_inputs_device(w: Workload, device, heads: Optional[int] = None, seed: O
     S, d = w.S, w.d
     r = w.r if r is None else r
     gen = torch.Generator(device=device)
-    gen.manual_seed(20250000 + w.cfg if seed is None else seed)
-    host = np.random.default_rng(20250000 + w.cfg if seed is None else seed)
+    gen.manual_seed(20250000 + w.index if seed is None else seed)
+    host = np.random.default_rng(20250000 + w.index if seed is None else seed)
     P = torch.from_numpy(sinusoid_3d(w.T, w.Y, w.X, d)).to(device=device, dtype=torch.float32)
     kw = dict(device=device, dtype=torch.float32, generator=gen)
     Q = torch.empty((H, S, d), dtype=torch.bfloat16, device=device)

@@ -95,7 +95,7 @@ def _check_keys(w, inp, idx_rows, dK, dV, h, n_keys=2, max_hits=80):
         assert rel_l2(dV[h, key].float().cpu().numpy(), dv) <= GRAD_REL_L2, (h, key)
 
 
-# ------------------------------------------------------------------ cfg 1
+# --------------------------------------------- S=16K forward+backward
 def test_fullsize_16k_forward_backward():
     """H=8, 8x32x64 (S=16384), d=64, r=32, cube 4x4x4, k=1638: every output of
     one head against the full oracle, sampled rows of the others."""
@@ -125,7 +125,7 @@ def test_fullsize_16k_forward_backward():
     _check_grad_identities(dK, dV, d["dO"], range(w.H))
 
 
-# ------------------------------------------------------------------ cfg 2
+# --------------------------------------------- S=64K video-DiT layer
 def test_fullsize_64k_bench_step():
     """The bench step itself (H=24, 16x64x64, d=128, r=32, cube 2x8x8, k=6554):
     coverage, top-k, forward and backward with the bench's buffers."""
@@ -145,7 +145,7 @@ def test_fullsize_64k_bench_step():
     _check_grad_identities(step.dK, step.dV, step.dO, range(w.H))
 
 
-# ------------------------------------------------------------------ cfg 3
+# --------------------------------------------- S=128K top-k sweep
 @pytest.mark.parametrize("r", syn.TOPK_SWEEP_RANKS)
 def test_fullsize_128k_topk_sweep(r):
     """32x64x64 (S=131072), d=128, cube 2x8x8, k in {1, 5, 10, 20}% of S, for
@@ -166,7 +166,7 @@ def test_fullsize_128k_topk_sweep(r):
     _check_kcov(w, inp, k_cov.cpu().numpy(), [1])
 
 
-# ------------------------------------------------------------------ cfg 4
+# --------------------------------------------- S=256K dispatcher-driven layer
 def test_fullsize_256k_dispatcher_layer():
     """H=16, 64x64x64 (S=262144), d=128, r=32, cube 2x8x8: coverage -> per-head
     plan (clamp to [1%, 25%] S, dense above 50%) -> top-k for sparse heads ->

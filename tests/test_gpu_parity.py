@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 CASES = {
     # the oracle-scale workload exactly: H=1, 4x16x16, d=64, r=16, cube 4x4x4, k=128
-    "cfg0": syn.workload(0, backward=True),
+    "oracle_scale": syn.workload(0, backward=True),
     # d=128, G=128, two full key tiles and a 44-key tail
     "ragged_d128": syn.Workload("ragged", 101, 2, 4, 16, 32, 128, 32, 2, 8, 8, 300, ("uniform", 2.0, 8.0), True),
     # d=64, G=64, r=64 (two 128-byte atoms per predictor row)

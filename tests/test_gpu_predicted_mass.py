@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 PQ_ABS, MEAN_ABS = 1e-4, 1e-5
 
 CASES = {
-    "cfg0": syn.workload(0),
+    "oracle_scale": syn.workload(0),
     "ragged_d128_g128": syn.Workload("ragged", 101, 2, 4, 16, 32, 128, 32, 2, 8, 8, 300, ("uniform", 2.0, 8.0), False),
     "d64_r64": syn.Workload("d64r64", 102, 2, 4, 8, 16, 64, 64, 4, 4, 4, 200, ("const", 4.0), False),
     "r16_h3": syn.Workload("r16", 103, 3, 8, 16, 16, 64, 16, 4, 4, 4, 129, ("uniform", 1.0, 8.0), False),
