@@ -29,12 +29,16 @@
 //   COLLECT marks every key scoring >= hi in a per-row bit mask and stages the
 //           interval's scores as candidates (a single-valued interval marks
 //           its keys in a tie mask instead)
-//   resolve sorts each row's candidates (score desc, key asc) and marks the
-//           ones that complete the row's k
+//   resolve selects the candidates that complete each row's k (score desc,
+//           key asc) by a radix select and marks them
 //   compact writes each index row in ascending key order from the masks,
 //           taking a single-valued interval's keys lowest first.
-// Coverage reuses MINMAX and a COV pass that bins exp(scale*(s - max)) by
-// log-probability (count and mass per bin); a reduce kernel searches k.
+// Coverage reuses MINMAX: a COV pass bins every key by log-probability below
+// the row maximum (count per half bin and mass per bin), bound searches over
+// those tables give an interval for k_cov, a COV_FINE pass re-bins each
+// group's window of coarse bins, and a final search on the combined tables
+// gives k_cov. When coverage and top-k run in one call, the COV pass's half-bin
+// counts give the bracket in place of the HIST pass.
 #include <algorithm>
 #include <cmath>
 #include <mutex>
