@@ -594,6 +594,21 @@ def end_to_end(w, inp, device, args, step0=None, windows=9, nsets=3):
     for i in range(max(1, args.warmup)):
         once(i)
     torch.cuda.synchronize()
+    # the copies of one step alone (no compute running): what the pipeline has to hide
+    copy_ms = {}
+    for name, stream, jobs in (("h2d", s_in, [(dst, host_in[n]) for n, dst in (("Q", steps[0].Q), ("K", steps[0].K),
+                                                                              ("V", steps[0].V), ("dO", steps[0].dO),
+                                                                              ("Wq", steps[0].Wq), ("Wk", steps[0].Wk))]),
+                               ("d2h", s_out, [(outs[0][n], src) for n, src in (("O", steps[0].O), ("dQ", steps[0].dQ),
+                                                                               ("dK", steps[0].dK), ("dV", steps[0].dV))])):
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for dst, src in jobs:
+                dst.copy_(src, non_blocking=True)
+            e.record(stream)
+        torch.cuda.synchronize()
+        copy_ms[name] = round(a.elapsed_time(e), 3)
     K = args.steps
     # Steady state, as a training loop runs: windows * K steps back to back with
     # no synchronisation; a window is K steps between two compute-done events,
@@ -629,7 +644,7 @@ def end_to_end(w, inp, device, args, step0=None, windows=9, nsets=3):
     ms = statistics.median(per_window)
     return {"value": round(attn_flops(w, steps[0].ks) / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "pipelined": True, "buffer_sets": nsets, "windows_ms_per_step": [round(x, 3) for x in per_window],
+            "pipelined": True, "buffer_sets": nsets, "copy_ms_alone": copy_ms, "windows_ms_per_step": [round(x, 3) for x in per_window],
             "reported": f"median of {windows} back-to-back windows of {K} steps (steady state)",
             "cold_window_ms_per_step": round(cold, 3)}
 
