@@ -105,8 +105,9 @@ uint64_t dsv_set_wait_limit_ns(uint64_t ns);
  * Problems with idx_offset[p] < 0 are skipped (dense heads).
  * The selection is exact for every input with finite scores, however the
  * scores cluster: the k-th score's histogram bin is narrowed by radix
- * rounds over the score's bits until it holds at most 4096 keys (sorted) or
- * a single value (taken lowest key first).
+ * rounds over the score's bits until it holds at most 4096 keys (the ones
+ * completing the row found by a radix select over score and key) or a
+ * single value (taken lowest key first).
  * k_per_head, idx_offset: HOST arrays of B*H entries (read during the call).
  * Device errors: DSV_ERR_TIMEOUT on a stalled pipeline (the rows are then
  * incomplete); DSV_ERR_CANDIDATES only if an internal consistency check
