@@ -926,7 +926,7 @@ __device__ uint32_t least_with_bin(int target, uint32_t o_lo, uint32_t o_hi, flo
 }
 
 // State of a row whose k-th score lies in [lo, hi) with `count` scores there:
-// a single value is resolved by key order, a small interval by sorting its
+// a single value is resolved by key order, a small interval by selecting among its
 // candidates, a larger one by another REFINE round.
 __device__ __forceinline__ int row_state(uint32_t lo, uint32_t hi, uint32_t count) {
   if (hi - lo <= 1u) return kRowTied;
