@@ -569,26 +569,34 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Key-major dK/dV for dense problems. grid = (S/128, problems).
+// Key-major dK/dV for dense problems. grid = (S/128, problems). One CTA owns
+// a 128-key tile and loops over every 128-query tile u:
+//   S^T = K Q^T, dP^T = V dO^T       tcgen05 (smem x smem) -> TMEM
+//   P^T, dS^T (registers, key per thread), written back to TMEM as bf16 in
+//   place of S^T and dP^T
+//   dV += P^T dO, dK += dS^T Q       tcgen05 with A in TMEM (no shared-memory
+//                                    copy of P or dS) -> TMEM accumulators
+// Q, dO and the tile's LSE*log2(e) and Delta rows are double-buffered, so the
+// next tile's copies overlap this tile's work. Warps 0-3 compute P and dS,
+// warp 4 loads, warp 5 issues the MMAs.
 template <int D>
 struct KvCfg {
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kOffV = kTile;            // K at 0
-  static constexpr int kOffQ = 2 * kTile;
-  static constexpr int kOffDO = 3 * kTile;
-  static constexpr int kOffP = 4 * kTile;        // P^T [128 keys][128 q] bf16
-  static constexpr int kOffDS = kOffP + 32768;
-  static constexpr int kOffStat = kOffDS + 32768;   // LSE2[128], Delta[128]
-  static constexpr int kOffBar = kOffStat + 1024;
-  static constexpr int kSmemUsed = kOffBar + 1024 + 1024;
+  static constexpr int kOffQ = 2 * kTile;        // [2 stages]
+  static constexpr int kOffDO = 4 * kTile;       // [2 stages]
+  static constexpr int kOffStat = 6 * kTile;     // [2 stages][LSE2[128], Delta[128]]
+  static constexpr int kOffBar = kOffStat + 2 * 1024;
+  static constexpr int kSmemUsed = kOffBar + 256 + 1024;
   static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
 };
+static_assert(KvCfg<128>::kSmemUsed <= 232448, "key-major backward exceeds shared memory");
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     k_attn_bwd_kv(const __grid_constant__ AttnMaps maps, const __grid_constant__ CUtensorMap q_tile,
                   const __grid_constant__ CUtensorMap do_tile, const AttnParams prm, const float* delta_all,
-                  __nv_bfloat16* dK, __nv_bfloat16* dV, const ProblemTable tab) {
+                  const float* lse2_all, __nv_bfloat16* dK, __nv_bfloat16* dV, const ProblemTable tab) {
   using C = KvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -596,18 +604,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sV = sm + C::kOffV;
   uint8_t* sQ = sm + C::kOffQ;
   uint8_t* sDO = sm + C::kOffDO;
-  uint8_t* sP = sm + C::kOffP;
-  uint8_t* sDS = sm + C::kOffDS;
-  float* sLse = reinterpret_cast<float*>(sm + C::kOffStat);
-  float* sDelta = sLse + 128;
+  float* sStat = reinterpret_cast<float*>(sm + C::kOffStat);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   uint64_t* kv_full = bars + 0;
-  uint64_t* q_full = bars + 1;
-  uint64_t* q_empty = bars + 2;
-  uint64_t* sdp_full = bars + 3;
-  uint64_t* ps_full = bars + 4;
-  uint64_t* mma_done = bars + 5;
-  uint64_t* mma_drain = bars + 6;   // every MMA issued has completed (unwind)
+  uint64_t* q_full = bars + 1;      // [2] Q, dO, LSE2 and Delta of the stage's query tile
+  uint64_t* q_empty = bars + 3;     // [2] the stage's MMAs (and so its P/dS pass) are done
+  uint64_t* sdp_full = bars + 5;    // S^T, dP^T of tile u in TMEM
+  uint64_t* ps_full = bars + 6;     // P^T, dS^T of tile u in TMEM
+  uint64_t* mma_drain = bars + 7;   // every MMA issued has completed (end, or unwind)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -622,11 +626,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   if (tid == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(q_full + i, 1);
+      mbar_init(q_empty + i, 1);
+    }
     mbar_init(sdp_full, 1);
     mbar_init(ps_full, 4);
-    mbar_init(mma_done, 1);
     mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
@@ -645,30 +650,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       int issued = 0;
       for (int u = 0; u < nq; ++u) {
-        if (u >= 1 && !mbar_wait(q_empty, (u - 1) & 1, prm.wait_ns)) {
+        const int st = u & 1;
+        if (u >= 2 && !mbar_wait(q_empty + st, ((u >> 1) - 1) & 1, prm.wait_ns)) {
           raise_status(prm.status, DSV_ERR_TIMEOUT);
           break;
         }
-        mbar_arrive_expect_tx(q_full, 2 * C::kTile);
+        mbar_arrive_expect_tx(q_full + st, 2 * C::kTile + 1024);
         for (int a = 0; a < D / 64; ++a) {
-          tma_load_2d(sQ + a * 16384, &q_tile, q_full, a * 64, prow0 + u * 128);
-          tma_load_2d(sDO + a * 16384, &do_tile, q_full, a * 64, prow0 + u * 128);
+          tma_load_2d(sQ + st * C::kTile + a * 16384, &q_tile, q_full + st, a * 64, prow0 + u * 128);
+          tma_load_2d(sDO + st * C::kTile + a * 16384, &do_tile, q_full + st, a * 64, prow0 + u * 128);
         }
+        bulk_load(sStat + st * 256, lse2_all + (int64_t)prow0 + u * 128, 512, q_full + st);
+        bulk_load(sStat + st * 256 + 128, delta_all + (int64_t)prow0 + u * 128, 512, q_full + st);
         issued = u + 1;
       }
       // the block leaves only once every copy it started has landed
       mbar_wait(kv_full, 0, kDrainLimitNs);
-      if (issued > 0) mbar_wait(q_full, (issued - 1) & 1, kDrainLimitNs);
+      for (int u = max(0, issued - 2); u < issued; ++u) mbar_wait(q_full + (u & 1), (u >> 1) & 1, kDrainLimitNs);
     }
   } else if (warp == 5) {
     if (lane == 0) {
       constexpr uint32_t id_sdp = instr_desc(128, 128, 1, 0, 0);   // K Q^T, V dO^T
-      constexpr uint32_t id_acc = instr_desc(128, D, 1, 0, 1);     // P^T dO, dS^T Q (B MN-major)
-      const uint32_t ak = smem_u32(sK), av = smem_u32(sV), aq = smem_u32(sQ), ado = smem_u32(sDO);
-      const uint32_t ap = smem_u32(sP), ads = smem_u32(sDS);
+      constexpr uint32_t id_acc = instr_desc(128, D, 1, 0, 1);     // P^T dO, dS^T Q (A in TMEM, B MN-major)
+      const uint32_t ak = smem_u32(sK), av = smem_u32(sV);
       bool ok = mbar_wait(kv_full, 0, prm.wait_ns);
       for (int u = 0; ok && u < nq; ++u) {
-        if (!mbar_wait(q_full, u & 1, prm.wait_ns)) { ok = false; break; }
+        const int st = u & 1;
+        const uint32_t aq = smem_u32(sQ + st * C::kTile), ado = smem_u32(sDO + st * C::kTile);
+        if (!mbar_wait(q_full + st, (u >> 1) & 1, prm.wait_ns)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -683,23 +692,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit(sdp_full);
         if (!mbar_wait(ps_full, u & 1, prm.wait_ns)) { ok = false; break; }
         tc_fence_after();
+        // P^T and dS^T: bf16 pairs in the first 64 columns of the S^T and dP^T regions
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t offa = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tbase + kColDV, smem_desc(ap + offa, 16, 1024), smem_desc(ado + kk * 2048, 16384, 1024), id_acc,
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ts(tbase + kColDV, tbase + kColS + kk * 8, smem_desc(ado + kk * 2048, 16384, 1024), id_acc,
                      (u > 0 || kk > 0) ? 1u : 0u);
-        }
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t offa = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tbase + kColDK, smem_desc(ads + offa, 16, 1024), smem_desc(aq + kk * 2048, 16384, 1024), id_acc,
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ts(tbase + kColDK, tbase + kColDP + kk * 8, smem_desc(aq + kk * 2048, 16384, 1024), id_acc,
                      (u > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(q_empty);
-        mma_commit(mma_done);
+        mma_commit(q_empty + st);
       }
       if (!ok) raise_status(prm.status, DSV_ERR_TIMEOUT);
-      // every MMA issued completes before TMEM is released
+      // every MMA issued completes before the results are read and TMEM is released
       mma_commit(mma_drain);
       mbar_wait(mma_drain, 0, kDrainLimitNs);
     }
@@ -707,46 +712,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int row = warp * 32 + lane;   // key slot of the tile
     const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
     const float sc = prm.scale_log2;
-    // as in the group-major kernel: no early exit from a loop with named barriers
     bool ok = true;
-    for (int u = 0; u < nq; ++u) {
-      // P^T/dS^T smem and the S/dP TMEM columns are free once tile u-1's MMAs are done
-      if (u >= 1) ok = ok && mbar_wait_warp(mma_done, (u - 1) & 1, prm.wait_ns);
-      sLse[row] = prm.LSE[(int64_t)prow0 + u * 128 + row] * 1.4426950408889634f;
-      sDelta[row] = delta_all[(int64_t)prow0 + u * 128 + row];
-      compute_barrier();
+    for (int u = 0; ok && u < nq; ++u) {
+      const int st = u & 1;
+      // the stage's LSE2 and Delta rows arrived with its Q and dO
+      ok = ok && mbar_wait_warp(q_full + st, (u >> 1) & 1, prm.wait_ns);
       ok = ok && mbar_wait_warp(sdp_full, u & 1, prm.wait_ns);
+      if (!ok) break;
       tc_fence_after();
-#pragma unroll 1
+      const float* lse2 = sStat + st * 256;
+      const float* dl = lse2 + 128;
+      // 32 queries at a time; P^T and dS^T of chunk c go to columns 16c .. 16c+15,
+      // which hold S^T / dP^T values already read (chunks <= c)
+      uint32_t sr[2][32], dr[2][32];
+      tmem_ld32(lane_addr + kColS, sr[0]);
+      tmem_ld32(lane_addr + kColDP, dr[0]);
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(lane_addr + kColS + c * 32, sr);
-        tmem_ld32(lane_addr + kColDP + c * 32, dr);
-        tmem_ld_wait(sr);
-        reg_fence(dr);
+        const int b = c & 1;
+        tmem_ld_wait(sr[b]);
+        reg_fence(dr[b]);
+        if (c + 1 < 4) {
+          tmem_ld32(lane_addr + kColS + (c + 1) * 32, sr[b ^ 1]);
+          tmem_ld32(lane_addr + kColDP + (c + 1) * 32, dr[b ^ 1]);
+        }
         uint32_t pw[16], dw[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int q = c * 32 + e;
-          const float p0 = ex2_fast(__uint_as_float(sr[e]) * sc - sLse[q]);
-          const float p1 = ex2_fast(__uint_as_float(sr[e + 1]) * sc - sLse[q + 1]);
-          const float d0 = p0 * (__uint_as_float(dr[e]) - sDelta[q]);
-          const float d1 = p1 * (__uint_as_float(dr[e + 1]) - sDelta[q + 1]);
+          const float p0 = ex2_fast(fmaf(__uint_as_float(sr[b][e]), sc, -lse2[q]));
+          const float p1 = ex2_fast(fmaf(__uint_as_float(sr[b][e + 1]), sc, -lse2[q + 1]));
           pw[e >> 1] = pack_bf16x2(p0, p1);
-          dw[e >> 1] = pack_bf16x2(d0, d1);
+          dw[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dr[b][e]) - dl[q]),
+                                   p1 * (__uint_as_float(dr[b][e + 1]) - dl[q + 1]));
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          st_sw128_chunk(sP, row, c * 4 + q, make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]));
-          st_sw128_chunk(sDS, row, c * 4 + q, make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]));
-        }
+        tmem_st16(lane_addr + kColS + c * 16, pw);
+        tmem_st16(lane_addr + kColDP + c * 16, dw);
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
-      compute_barrier();   // sLse/sDelta reads done before the next tile overwrites them
+      __syncwarp();
       if (lane == 0) mbar_arrive(ps_full);
     }
-    if (ok && !mbar_wait_warp(mma_done, (nq - 1) & 1, prm.wait_ns)) ok = false;
+    ok = ok && mbar_wait_warp(mma_drain, 0, prm.wait_ns);
     if (!ok) {
       if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
     } else {
@@ -781,9 +789,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // thread takes one 16-byte chunk of a row (d / 8 threads per row, a divisor
 // of the warp), so the loads are coalesced; the row's threads then reduce in
 // a fixed order by shuffles.
+// With `lse2` non-null it also writes LSE_i * log2(e) (the exponent offset of
+// the key-major kernel, which stages it per query tile).
 __global__ void __launch_bounds__(256) k_bwd_delta(const __nv_bfloat16* __restrict__ O,
                                                    const __nv_bfloat16* __restrict__ dO, int S, int d,
-                                                   float* __restrict__ delta, const ProblemTable tab) {
+                                                   float* __restrict__ delta, const float* __restrict__ LSE,
+                                                   float* __restrict__ lse2, const ProblemTable tab) {
   const int lp = blockIdx.y, p = tab.p[lp];
   const int cpr = d / 8;
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -803,7 +814,10 @@ __global__ void __launch_bounds__(256) k_bwd_delta(const __nv_bfloat16* __restri
     }
   }
   for (int m = cpr / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if (s < S && c == 0) delta[(int64_t)p * S + s] = acc;
+  if (s < S && c == 0) {
+    delta[(int64_t)p * S + s] = acc;
+    if (lse2) lse2[(int64_t)p * S + s] = LSE[(int64_t)p * S + s] * 1.4426950408889634f;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -999,10 +1013,10 @@ static cudaError_t launch_bwd_q(const AttnMaps& maps, const CUtensorMap& do_cube
 
 template <int D>
 static cudaError_t launch_bwd_kv(const AttnMaps& maps, const CUtensorMap& q_tile, const CUtensorMap& do_tile,
-                                 const AttnParams& prm, const float* delta, __nv_bfloat16* dK, __nv_bfloat16* dV,
-                                 const ProblemTable& tab, int S, cudaStream_t st) {
+                                 const AttnParams& prm, const float* delta, const float* lse2, __nv_bfloat16* dK,
+                                 __nv_bfloat16* dV, const ProblemTable& tab, int S, cudaStream_t st) {
   k_attn_bwd_kv<D><<<dim3(S / 128, tab.n), kBwdThreads, KvCfg<D>::kSmem, st>>>(maps, q_tile, do_tile, prm, delta,
-                                                                                dK, dV, tab);
+                                                                                lse2, dK, dV, tab);
   return cudaGetLastError();
 }
 
@@ -1115,6 +1129,7 @@ struct BwdWs {
   float* acc_v;
   float* acc_k;
   float* delta;
+  float* lse2;
 };
 
 static size_t carve_bwd(void* base, const dsv_shape& s, const BwdPlan& pl, BwdWs* w) {
@@ -1128,6 +1143,7 @@ static size_t carve_bwd(void* base, const dsv_shape& s, const BwdPlan& pl, BwdWs
   w->acc_v = c.take<float>(pl.split ? S * s.d : 0);
   w->acc_k = c.take<float>(pl.split ? S * s.d : 0);
   w->delta = c.take<float>(pl.dense.n ? P * S : 0);
+  w->lse2 = c.take<float>(pl.dense.n ? P * S : 0);
   return c.used + 256;
 }
 
@@ -1293,11 +1309,11 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
       if (e != cudaSuccess) return DSV_ERR_CUDA;
     }
     k_bwd_delta<<<dim3((unsigned)(((int64_t)geo.S * (d / 8) + 255) / 256), ptab.n), 256, 0, st>>>(
-        prm.O, prm.dO, geo.S, d, w.delta, ptab);
+        prm.O, prm.dO, geo.S, d, w.delta, prm.LSE, w.lse2, ptab);
     if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
     const cudaError_t e =
-        d == 128 ? launch_bwd_kv<128>(maps, q_tile, do_tile, prm, w.delta, csc.dK, csc.dV, ptab, geo.S, st)
-                 : launch_bwd_kv<64>(maps, q_tile, do_tile, prm, w.delta, csc.dK, csc.dV, ptab, geo.S, st);
+        d == 128 ? launch_bwd_kv<128>(maps, q_tile, do_tile, prm, w.delta, w.lse2, csc.dK, csc.dV, ptab, geo.S, st)
+                 : launch_bwd_kv<64>(maps, q_tile, do_tile, prm, w.delta, w.lse2, csc.dK, csc.dV, ptab, geo.S, st);
     if (e != cudaSuccess) return DSV_ERR_CUDA;
   }
   return DSV_OK;
