@@ -610,9 +610,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* q_full = bars + 1;      // [2] Q, dO, LSE2 and Delta of the stage's query tile
   uint64_t* q_empty = bars + 3;     // [2] the stage's MMAs (and so its P/dS pass) are done
   uint64_t* sdp_full = bars + 5;    // S^T, dP^T of tile u in TMEM
-  uint64_t* ps_full = bars + 6;     // P^T, dS^T of tile u in TMEM
-  uint64_t* mma_drain = bars + 7;   // every MMA issued has completed (end, or unwind)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
+  uint64_t* ps_half = bars + 6;     // [2] P^T, dS^T of queries 0-63 / 64-127 of tile u in TMEM
+  uint64_t* mma_drain = bars + 8;   // every MMA issued has completed (end, or unwind)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 9);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kt = blockIdx.x, lp = blockIdx.y, p = tab.p[lp];
@@ -631,7 +631,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(q_empty + i, 1);
     }
     mbar_init(sdp_full, 1);
-    mbar_init(ps_full, 4);
+    mbar_init(ps_half, 4);
+    mbar_init(ps_half + 1, 4);
     mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
@@ -690,17 +691,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_f16_ss(tbase + kColDP, smem_desc(av + off, 16, 1024), smem_desc(ado + off, 16, 1024), id_sdp, kk > 0);
         }
         mma_commit(sdp_full);
-        if (!mbar_wait(ps_full, u & 1, prm.wait_ns)) { ok = false; break; }
-        tc_fence_after();
-        // P^T and dS^T: bf16 pairs in the first 64 columns of the S^T and dP^T regions
+        // P^T and dS^T: bf16 pairs in the first 64 columns of the S^T and dP^T regions; the
+        // MMAs of the first 64 queries run while the second 64 are computed
+        for (int h = 0; h < 2; ++h) {
+          if (!mbar_wait(ps_half + h, u & 1, prm.wait_ns)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f16_ts(tbase + kColDV, tbase + kColS + kk * 8, smem_desc(ado + kk * 2048, 16384, 1024), id_acc,
-                     (u > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+            mma_f16_ts(tbase + kColDV, tbase + kColS + kk * 8, smem_desc(ado + kk * 2048, 16384, 1024), id_acc,
+                       (u > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f16_ts(tbase + kColDK, tbase + kColDP + kk * 8, smem_desc(aq + kk * 2048, 16384, 1024), id_acc,
-                     (u > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+            mma_f16_ts(tbase + kColDK, tbase + kColDP + kk * 8, smem_desc(aq + kk * 2048, 16384, 1024), id_acc,
+                       (u > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
         mma_commit(q_empty + st);
       }
       if (!ok) raise_status(prm.status, DSV_ERR_TIMEOUT);
@@ -748,11 +753,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         tmem_st16(lane_addr + kColS + c * 16, pw);
         tmem_st16(lane_addr + kColDP + c * 16, dw);
+        if (c & 1) {   // queries 0-63 (c = 1) or 64-127 (c = 3) complete
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ps_half + (c >> 1));
+        }
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ps_full);
     }
     ok = ok && mbar_wait_warp(mma_drain, 0, prm.wait_ns);
     if (!ok) {
