@@ -792,6 +792,276 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 5) tmem_dealloc(tbase, 512);
 }
 
+// ---------------------------------------------------------------------------
+// dQ of a dense problem, group-major: one CTA per (query group, problem)
+// over all S keys in 128-key tiles. With no dK/dV partials to produce, the
+// group-major kernel's shared-memory copies of P and dS are not needed: dS
+// goes back to TMEM as bf16 in place of dP, and dQ += dS K takes its A
+// operand from there. Two TMEM regions alternate between tiles (S, then dP,
+// then dS of tile t in region t % 2), so tile t+1's S is computed while tile
+// t's P and dS are. Warps 0-3: P, dS and the final dQ rows (one query per
+// thread); warp 4 loads (TMA); warp 5 issues the MMAs.
+template <int D>
+struct DqCfg {
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kKStages = 3, kVStages = 2;
+  static constexpr int kOffDO = kTile;       // Q at 0
+  static constexpr int kOffK = 2 * kTile;
+  static constexpr int kOffV = kOffK + kKStages * kTile;
+  static constexpr int kOffBar = kOffV + kVStages * kTile;
+  static constexpr int kSmemUsed = kOffBar + 256 + 1024;
+  static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
+  static constexpr uint32_t kColR0 = 0, kColDQ = 128, kColR1 = 256;
+};
+static_assert(DqCfg<128>::kSmemUsed <= 232448, "dense dQ kernel exceeds shared memory");
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    k_attn_bwd_dq(const __grid_constant__ AttnMaps maps, const __grid_constant__ CUtensorMap do_cube,
+                  const AttnParams prm, const float* delta_all, const UnitTable tab) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm;
+  uint8_t* sDO = sm + C::kOffDO;
+  uint8_t* sK = sm + C::kOffK;
+  uint8_t* sV = sm + C::kOffV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;       // [3]
+  uint64_t* k_empty = bars + 4;      // [3]
+  uint64_t* v_full = bars + 7;       // [2]
+  uint64_t* v_empty = bars + 9;      // [2]
+  uint64_t* s_full = bars + 11;      // [2] S of the region's tile in TMEM
+  uint64_t* s_free = bars + 13;      // S(t) in registers: dP(t) may overwrite it
+  uint64_t* dp_full = bars + 14;     // dP(t) in TMEM
+  uint64_t* ds_full = bars + 15;     // dS(t) in TMEM
+  uint64_t* dq_done = bars + 16;
+  uint64_t* mma_drain = bars + 17;   // every MMA issued has completed (unwind)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 18);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int u = blockIdx.y;
+  if ((int)blockIdx.x >= tab.ng[u]) return;
+  const int g = tab.g0[u] + blockIdx.x, p = tab.p[u];
+  const Geometry& geo = prm.geo;
+  const int G = geo.G, nt = geo.S / 128, prow0 = p * geo.S;
+
+  if (G < 128) {   // padding query rows stay zero: the Q/dO boxes write only the group's G rows
+    for (int i = tid; i < (128 - G) * (D / 64) * 8; i += blockDim.x) {
+      const int a = i / ((128 - G) * 8), rem = i % ((128 - G) * 8);
+      reinterpret_cast<uint4*>(sQ + a * 16384 + G * 128)[rem] = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4*>(sDO + a * 16384 + G * 128)[rem] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == 5) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < C::kKStages; ++i) {
+      mbar_init(k_full + i, 1);
+      mbar_init(k_empty + i, 1);
+    }
+    for (int i = 0; i < C::kVStages; ++i) {
+      mbar_init(v_full + i, 1);
+      mbar_init(v_empty + i, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_full + 1, 1);
+    mbar_init(s_free, 4);
+    mbar_init(dp_full, 1);
+    mbar_init(ds_full, 4);
+    mbar_init(dq_done, 1);
+    mbar_init(mma_drain, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      const int ct = g / (geo.ncy * geo.ncx), cy = (g / geo.ncx) % geo.ncy, cx = g % geo.ncx;
+      mbar_arrive_expect_tx(q_full, 2 * G * D * 2);
+      for (int a = 0; a < D / 64; ++a) {
+        tma_load_4d(sQ + a * 16384, &maps.q_cube, q_full, a * 64, cx * geo.gx, cy * geo.gy, p * geo.T + ct * geo.gt);
+        tma_load_4d(sDO + a * 16384, &do_cube, q_full, a * 64, cx * geo.gx, cy * geo.gy, p * geo.T + ct * geo.gt);
+      }
+      int k_issued = 0, v_issued = 0;
+      for (int t = 0; t < nt; ++t) {
+        const int ks = t % C::kKStages, vs = t % C::kVStages;
+        if (t >= C::kKStages && !mbar_wait(k_empty + ks, ((t / C::kKStages) - 1) & 1, prm.wait_ns)) {
+          raise_status(prm.status, DSV_ERR_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(k_full + ks, C::kTile);
+        load_dense_tile<D>(sK + ks * C::kTile, &maps.k_tile, k_full + ks, t, prow0);
+        k_issued = t + 1;
+        if (t >= C::kVStages && !mbar_wait(v_empty + vs, ((t / C::kVStages) - 1) & 1, prm.wait_ns)) {
+          raise_status(prm.status, DSV_ERR_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(v_full + vs, C::kTile);
+        load_dense_tile<D>(sV + vs * C::kTile, &maps.v_tile, v_full + vs, t, prow0);
+        v_issued = t + 1;
+      }
+      // the block leaves only once every copy it started has landed
+      for (int t = max(0, k_issued - C::kKStages); t < k_issued; ++t)
+        mbar_wait(k_full + t % C::kKStages, (t / C::kKStages) & 1, kDrainLimitNs);
+      for (int t = max(0, v_issued - C::kVStages); t < v_issued; ++t)
+        mbar_wait(v_full + t % C::kVStages, (t / C::kVStages) & 1, kDrainLimitNs);
+      mbar_wait(q_full, 0, kDrainLimitNs);
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t id_sdp = instr_desc(128, 128, 1, 0, 0);   // Q K^T, dO V^T
+      constexpr uint32_t id_dq = instr_desc(128, D, 1, 0, 1);      // dS K (A in TMEM, B = K MN-major)
+      constexpr uint64_t kMn = (uint64_t)((16384 >> 4) - (16 >> 4)) << 16;
+      const uint64_t dq_k = smem_desc(smem_u32(sQ), 16, 1024), ddo_k = smem_desc(smem_u32(sDO), 16, 1024);
+      auto region = [&](int t) -> uint32_t { return tbase + ((t & 1) ? C::kColR1 : C::kColR0); };
+      auto issue_s = [&](int t) -> bool {   // S(t) = Q K(t)^T into the tile's region
+        const int ks = t % C::kKStages;
+        if (!mbar_wait(k_full + ks, (t / C::kKStages) & 1, prm.wait_ns)) return false;
+        tc_fence_after();
+        const uint64_t dk = smem_desc(smem_u32(sK + ks * C::kTile), 16, 1024);
+        const uint64_t dq = opaque(dq_k);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_f16_ss(region(t), desc_at(dq, off), desc_at(dk, off), id_sdp, kk > 0);
+        }
+        mma_commit(s_full + (t & 1));
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0, prm.wait_ns);
+      if (ok && nt > 0) ok = issue_s(0);
+      if (ok && nt > 1) ok = issue_s(1);
+      for (int t = 0; ok && t < nt; ++t) {
+        const int ks = t % C::kKStages, vs = t % C::kVStages;
+        // dP(t) = dO V(t)^T into the columns S(t) has left
+        if (!mbar_wait(s_free, t & 1, prm.wait_ns) ||
+            !mbar_wait(v_full + vs, (t / C::kVStages) & 1, prm.wait_ns)) { ok = false; break; }
+        tc_fence_after();
+        {
+          const uint64_t dv = smem_desc(smem_u32(sV + vs * C::kTile), 16, 1024);
+          const uint64_t ddo = opaque(ddo_k);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_f16_ss(region(t), desc_at(ddo, off), desc_at(dv, off), id_sdp, kk > 0);
+          }
+        }
+        mma_commit(dp_full);
+        mma_commit(v_empty + vs);
+        // dQ += dS(t) K(t), dS as bf16 pairs in the region's first 64 columns
+        if (!mbar_wait(ds_full, t & 1, prm.wait_ns)) { ok = false; break; }
+        tc_fence_after();
+        {
+          const uint64_t dk_m = smem_desc(smem_u32(sK + ks * C::kTile), 16, 1024) + kMn;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ts(tbase + C::kColDQ, region(t) + kk * 8, desc_at(dk_m, kk * 2048), id_dq,
+                       (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(k_empty + ks);
+        // S(t+2) into this region, after dQ(t) has read its dS (the MMAs run in issue order)
+        if (t + 2 < nt && !issue_s(t + 2)) { ok = false; break; }
+      }
+      if (ok) mma_commit(dq_done);
+      else raise_status(prm.status, DSV_ERR_TIMEOUT);
+      mma_commit(mma_drain);
+      mbar_wait(mma_drain, 0, kDrainLimitNs);
+    }
+  } else {
+    // ---------------------------------------------- P, dS, dQ rows (warps 0-3)
+    const int row = warp * 32 + lane;
+    const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+    const float sc = prm.scale_log2;
+    float lse2 = INFINITY, delta = 0.f;
+    int tok = 0;
+    if (row < G) {
+      tok = token_of(geo, g, row);
+      lse2 = prm.LSE[(int64_t)prow0 + tok] * 1.4426950408889634f;
+      delta = delta_all[(int64_t)prow0 + tok];
+    }
+    // dS pre-multiplied by the attention scale, so dQ = (scale dS) K needs no scaling afterwards
+    const float dsc = prm.scale, ndd = -delta * prm.scale;
+    bool ok = true;
+    for (int t = 0; ok && t < nt; ++t) {
+      const uint32_t rb = lane_addr + ((t & 1) ? C::kColR1 : C::kColR0);
+      ok = ok && mbar_wait_warp(s_full + (t & 1), (t >> 1) & 1, prm.wait_ns);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(rb + c * 32, sr[c]);
+      tmem_ld_wait(sr[0]);
+      reg_fence(sr[1]);
+      reg_fence(sr[2]);
+      reg_fence(sr[3]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);   // S(t) in registers: dP(t) may take its columns
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sr[c][e] = __float_as_uint(ex2_fast(fmaf(__uint_as_float(sr[c][e]), sc, -lse2)));
+      ok = ok && mbar_wait_warp(dp_full, t & 1, prm.wait_ns);
+      if (!ok) break;
+      tc_fence_after();
+      // dS of 32 columns at a time, written as 16 bf16-pair columns at 16c over dP values
+      // already read (chunks <= c), the next chunk's load in flight
+      uint32_t da[2][32];
+      tmem_ld32(rb, da[0]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int b = c & 1;
+        tmem_ld_wait(da[b]);
+        if (c + 1 < 4) tmem_ld32(rb + (c + 1) * 32, da[b ^ 1]);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          w[e >> 1] = pack_bf16x2(__uint_as_float(sr[c][e]) * fmaf(__uint_as_float(da[b][e]), dsc, ndd),
+                                  __uint_as_float(sr[c][e + 1]) * fmaf(__uint_as_float(da[b][e + 1]), dsc, ndd));
+        tmem_st16(rb + c * 16, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+    ok = ok && mbar_wait_warp(dq_done, 0, prm.wait_ns);
+    if (!ok) {
+      if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
+    } else {
+      tc_fence_after();
+      __nv_bfloat16* qrow = prm.out + ((int64_t)prow0 + tok) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(lane_addr + C::kColDQ + c * 32, o);
+        tmem_ld_wait(o);
+        if (row < G) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
+          uint4* dst = reinterpret_cast<uint4*>(qrow + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) tmem_dealloc(tbase, 512);
+}
+
 // Delta_i = sum_c dO_ic O_ic for every row of the listed problems. Each
 // thread takes one 16-byte chunk of a row (d / 8 threads per row, a divisor
 // of the warp), so the loads are coalesced; the row's threads then reduce in
@@ -1019,6 +1289,13 @@ static cudaError_t launch_bwd_q(const AttnMaps& maps, const CUtensorMap& do_cube
 }
 
 template <int D>
+static cudaError_t launch_bwd_dq(const AttnMaps& maps, const CUtensorMap& do_cube, const AttnParams& prm,
+                                const float* delta, const UnitTable& tab, int max_ng, cudaStream_t st) {
+  k_attn_bwd_dq<D><<<dim3(max_ng, tab.n), kBwdThreads, DqCfg<D>::kSmem, st>>>(maps, do_cube, prm, delta, tab);
+  return cudaGetLastError();
+}
+
+template <int D>
 static cudaError_t launch_bwd_kv(const AttnMaps& maps, const CUtensorMap& q_tile, const CUtensorMap& do_tile,
                                  const AttnParams& prm, const float* delta, const float* lse2, __nv_bfloat16* dK,
                                  __nv_bfloat16* dV, const ProblemTable& tab, int S, cudaStream_t st) {
@@ -1034,6 +1311,8 @@ static cudaError_t configure_bwd() {
   cudaError_t e = cudaFuncSetAttribute(k_attn_bwd_q<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_attn_bwd_kv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_attn_bwd_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmem);
   // The warpgroups' register shares add up to kBwdQLaunchRegs per thread; a
   // build that launched with any other count would never satisfy the softmax
   // warpgroup's increase, so it is refused here instead of launched.
@@ -1299,6 +1578,9 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
       ptab.k[i] = geo.S;
       ptab.off[i] = -1;
     }
+    k_bwd_delta<<<dim3((unsigned)(((int64_t)geo.S * (d / 8) + 255) / 256), ptab.n), 256, 0, st>>>(
+        prm.O, prm.dO, geo.S, d, w.delta, prm.LSE, w.lse2, ptab);
+    if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
     for (int c0 = 0; c0 < pl.dense.n; c0 += kMaxUnits) {
       UnitTable dt = pl.dense;
       dt.n = std::min(kMaxUnits, pl.dense.n - c0);
@@ -1309,15 +1591,10 @@ extern "C" dsv_status dsv_sparse_attn_bwd(const void* Q, const void* K, const vo
         dt.ng[i] = geo.n_groups;
         dt.off[i] = -1;
       }
-      CscParams none;
-      memset(&none, 0, sizeof(none));
-      cudaError_t e = d == 128 ? launch_bwd_q<128>(maps, do_cube, prm, none, dt, geo.n_groups, st)
-                               : launch_bwd_q<64>(maps, do_cube, prm, none, dt, geo.n_groups, st);
+      cudaError_t e = d == 128 ? launch_bwd_dq<128>(maps, do_cube, prm, w.delta, dt, geo.n_groups, st)
+                               : launch_bwd_dq<64>(maps, do_cube, prm, w.delta, dt, geo.n_groups, st);
       if (e != cudaSuccess) return DSV_ERR_CUDA;
     }
-    k_bwd_delta<<<dim3((unsigned)(((int64_t)geo.S * (d / 8) + 255) / 256), ptab.n), 256, 0, st>>>(
-        prm.O, prm.dO, geo.S, d, w.delta, prm.LSE, w.lse2, ptab);
-    if (cudaGetLastError() != cudaSuccess) return DSV_ERR_CUDA;
     const cudaError_t e =
         d == 128 ? launch_bwd_kv<128>(maps, q_tile, do_tile, prm, w.delta, w.lse2, csc.dK, csc.dV, ptab, geo.S, st)
                  : launch_bwd_kv<64>(maps, q_tile, do_tile, prm, w.delta, w.lse2, csc.dK, csc.dV, ptab, geo.S, st);
