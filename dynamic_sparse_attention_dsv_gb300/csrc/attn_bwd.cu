@@ -7,7 +7,7 @@
 // of the step. Recomputation from the saved LSE follows the usual
 // memory-efficient attention practice.
 //
-// Group-major kernel (every problem): one CTA per (query group, problem),
+// Group-major kernel (sparse problems): one CTA per (query group, problem),
 // looping over the group's 128-key tiles:
 //   S = Q K^T, dP = dO V^T                        tcgen05 (smem x smem) -> TMEM
 //   P = exp2(S*scale*log2e - LSE*log2e), dS' = scale P (dP - Delta)   registers
@@ -20,9 +20,10 @@
 // carries the count of the key's lower words), so the partials of one key
 // lie contiguously in ascending group order; a reduce kernel sums each key's
 // slots in that order in fp32. The result is the same bits on every run.
-// Key-major kernel (dense problems): one CTA per (128-key tile, problem),
-// looping over all 128-token query tiles with dV, dK accumulated in TMEM;
-// no cross-CTA reduction at all.
+// Dense problems: dQ by a group-major pass without partials (k_attn_bwd_dq,
+// dS kept in TMEM), dK/dV by a key-major kernel: one CTA per (128-key tile,
+// problem), looping over all 128-token query tiles with dV, dK accumulated in
+// TMEM; no cross-CTA reduction at all.
 #include <algorithm>
 #include <type_traits>
 #include <vector>
