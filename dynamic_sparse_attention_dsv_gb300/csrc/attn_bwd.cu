@@ -174,11 +174,10 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
   if ((int)blockIdx.x >= tab.ng[u]) return;   // units of a launch may hold fewer groups than the grid
   const int g = tab.g0[u] + blockIdx.x, p = tab.p[u];
   const Geometry& geo = prm.geo;
-  const bool dense = (prm.idx == nullptr) || (tab.off[u] < 0);
-  const bool partials = !dense && csc.part_v != nullptr;
-  const int k = dense ? geo.S : tab.k[u];
+  // every unit here is a sparse problem (dense ones take k_attn_bwd_dq and k_attn_bwd_kv)
+  const int k = tab.k[u];
   const int nt = (k + 127) / 128;
-  const int32_t* idx_row = dense ? nullptr : prm.idx + tab.off[u] + (int64_t)g * k;
+  const int32_t* idx_row = prm.idx + tab.off[u] + (int64_t)g * k;
   const int G = geo.G;
   constexpr int kProdWarp = 8, kMmaWarp = 8 + kBwdGatherWarps;
 
@@ -196,10 +195,9 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
   }
   if (tid == 0) {
     mbar_init(q_full, 1);
-    const uint32_t fills = dense ? 1u : 32u * kBwdGatherWarps;   // TMA tx arrival, or one per gathering lane
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(k_full + i, fills);
-      mbar_init(v_full + i, fills);
+    for (int i = 0; i < 2; ++i) {   // one arrival per gathering lane
+      mbar_init(k_full + i, 32u * kBwdGatherWarps);
+      mbar_init(v_full + i, 32u * kBwdGatherWarps);
       mbar_init(k_empty + i, 1);
       mbar_init(v_empty + i, 1);
     }
@@ -239,50 +237,28 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     }
     const int prow0 = p * geo.S;
     int rows[Gather<D, kBwdGatherWarps>::kIters], nxt[Gather<D, kBwdGatherWarps>::kIters];
-    if (idx_row) gather_rows<D, kBwdGatherWarps>(nxt, idx_row, k, 0, prow0, pw, lane);
-    int k_issued = 0, v_issued = 0;   // tiles whose K (V) copies this warp started
+    gather_rows<D, kBwdGatherWarps>(nxt, idx_row, k, 0, prow0, pw, lane);
     for (int t = 0; t < nt; ++t) {
       const int ks = t % C::kKStages, vs = t % C::kVStages;
-      if (idx_row) {
 #pragma unroll
-        for (int i = 0; i < Gather<D, kBwdGatherWarps>::kIters; ++i) rows[i] = nxt[i];
-        if (t + 1 < nt) gather_rows<D, kBwdGatherWarps>(nxt, idx_row, k, t + 1, prow0, pw, lane);
-      }
+      for (int i = 0; i < Gather<D, kBwdGatherWarps>::kIters; ++i) rows[i] = nxt[i];
+      if (t + 1 < nt) gather_rows<D, kBwdGatherWarps>(nxt, idx_row, k, t + 1, prow0, pw, lane);
       if (t >= C::kKStages && !mbar_wait_warp(k_empty + ks, ((t / C::kKStages) - 1) & 1, prm.wait_ns)) {
         if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
         break;
       }
-      if (idx_row) {
-        gather_tile<D, kBwdGatherWarps>(sK + ks * C::kTile, prm.K, rows, pw, lane);
-        cp_async_arrive_noinc(k_full + ks);
-      } else if (pw == 0 && lane == 0) {
-        mbar_arrive_expect_tx(k_full + ks, C::kTile);
-        load_dense_tile<D>(sK + ks * C::kTile, &maps.k_tile, k_full + ks, t, prow0);
-      }
-      k_issued = t + 1;
+      gather_tile<D, kBwdGatherWarps>(sK + ks * C::kTile, prm.K, rows, pw, lane);
+      cp_async_arrive_noinc(k_full + ks);
       if (t >= C::kVStages && !mbar_wait_warp(v_empty + vs, ((t / C::kVStages) - 1) & 1, prm.wait_ns)) {
         if (lane == 0) raise_status(prm.status, DSV_ERR_TIMEOUT);
         break;
       }
-      if (idx_row) {
-        gather_tile<D, kBwdGatherWarps>(sV + vs * C::kTile, prm.V, rows, pw, lane);
-        cp_async_arrive_noinc(v_full + vs);
-      } else if (pw == 0 && lane == 0) {
-        mbar_arrive_expect_tx(v_full + vs, C::kTile);
-        load_dense_tile<D>(sV + vs * C::kTile, &maps.v_tile, v_full + vs, t, prow0);
-      }
-      v_issued = t + 1;
+      gather_tile<D, kBwdGatherWarps>(sV + vs * C::kTile, prm.V, rows, pw, lane);
+      cp_async_arrive_noinc(v_full + vs);
     }
     // the warp leaves only once the copies it started have landed (a
     // timed-out pipeline may not have consumed them)
-    if (idx_row) {
-      asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (pw == 0 && lane == 0) {
-      for (int t = max(0, k_issued - C::kKStages); t < k_issued; ++t)
-        mbar_wait(k_full + t % C::kKStages, (t / C::kKStages) & 1, kDrainLimitNs);
-      for (int t = max(0, v_issued - C::kVStages); t < v_issued; ++t)
-        mbar_wait(v_full + t % C::kVStages, (t / C::kVStages) & 1, kDrainLimitNs);
-    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     if (pw == 0 && lane == 0) mbar_wait(q_full, 0, kDrainLimitNs);
    } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
@@ -330,18 +306,18 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
         }
         mma_commit(dp_full);
         mma_commit(v_empty + vs);
-        // dV(t) = P(t)^T dO (sparse problems only: dense ones take dK/dV key-major)
-        if (partials) {
-          if (!mbar_wait(p_full, t & 1, prm.wait_ns) ||
-              (t >= 1 && !mbar_wait(dv_free, (t - 1) & 1, prm.wait_ns))) { ok = false; break; }
-          tc_fence_after();
+        // dV(t) = P(t)^T dO
+        if (!mbar_wait(p_full, t & 1, prm.wait_ns) ||
+            (t >= 1 && !mbar_wait(dv_free, (t - 1) & 1, prm.wait_ns))) { ok = false; break; }
+        tc_fence_after();
+        {
           const uint64_t a = opaque(dp_k + kMn), b = opaque(ddo_k + kMn);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_f16_ss(tbase + C::kColDV, desc_at(a, kk * 2048), desc_at(b, kk * 2048), id_kv, kk > 0);
-          mma_commit(dv_full);
-          mma_commit(p_free);
         }
+        mma_commit(dv_full);
+        mma_commit(p_free);
         // S(t+1) into the columns dP(t) has left
         if (t + 1 < nt && (!mbar_wait(dp_free, t & 1, prm.wait_ns) || !issue_s(t + 1))) { ok = false; break; }
         // dQ += dS(t) K(t), then dK(t) = dS(t)^T Q
@@ -358,15 +334,15 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
           }
         }
         mma_commit(k_empty + ks);
-        if (partials) {
-          if (t >= 1 && !mbar_wait(dk_free, (t - 1) & 1, prm.wait_ns)) { ok = false; break; }
-          tc_fence_after();
+        if (t >= 1 && !mbar_wait(dk_free, (t - 1) & 1, prm.wait_ns)) { ok = false; break; }
+        tc_fence_after();
+        {
           const uint64_t a = opaque(dds_k + kMn), b = opaque(dq_k + kMn);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_f16_ss(tbase + C::kColDK, desc_at(a, kk * 2048), desc_at(b, kk * 2048), id_kv, kk > 0);
-          mma_commit(dk_full);
         }
+        mma_commit(dk_full);
         mma_commit(ds_free);
       }
       if (ok) mma_commit(dq_done);
@@ -436,22 +412,20 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (c * 32 + e >= nvalid) sr[c][e] = 0u;
       }
-      if (partials) {
-        // P(t-1) is free once its dV MMAs completed
-        if (t >= 1) ok = ok && mbar_wait_warp(p_free, (t - 1) & 1, prm.wait_ns);
+      // P(t-1) is free once its dV MMAs completed
+      if (t >= 1) ok = ok && mbar_wait_warp(p_free, (t - 1) & 1, prm.wait_ns);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const uint32_t* x = &sr[q >> 2][(q & 3) * 8];
-          st_sw128_chunk(sP, row, q,
-                         make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                                    pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                                    pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                                    pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7]))));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+      for (int q = 0; q < 16; ++q) {
+        const uint32_t* x = &sr[q >> 2][(q & 3) * 8];
+        st_sw128_chunk(sP, row, q,
+                       make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                                  pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                                  pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                                  pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7]))));
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
       // dS = P (scale dP - scale Delta), 32 columns at a time with the next
       // chunk's TMEM load in flight
       ok = ok && mbar_wait_warp(dp_full, t & 1, prm.wait_ns);
@@ -488,17 +462,17 @@ __global__ void __launch_bounds__(kBwdQThreads, 1)
     bool ok = true;
     // Slot of this key row for tile t: off[key] + groups below ours that chose it.
     const int gl = g - tab.g0[u];
-    const uint64_t* bits_u = partials ? csc.bits + tab.bits_base[u] : nullptr;
-    const int32_t* off_u = partials ? csc.off + (int64_t)u * (geo.S + 1) : nullptr;
-    const int32_t* bpre_u = partials ? csc.bpre + (int64_t)u * (kMaxBlocks + 1) : nullptr;
+    const uint64_t* bits_u = csc.bits + tab.bits_base[u];
+    const int32_t* off_u = csc.off + (int64_t)u * (geo.S + 1);
+    const int32_t* bpre_u = csc.bpre + (int64_t)u * (kMaxBlocks + 1);
     auto slot_of = [&](int j) -> int64_t {
       const uint64_t x = __ldg(bits_u + (int64_t)j * tab.nwords[u] + (gl >> 5));
       const int r = (int)(x >> 32) + __popc((uint32_t)x & ((1u << (gl & 31)) - 1u));
       return tab.part_base[u] + __ldg(bpre_u + (j >> 8)) + __ldg(off_u + j) + r;
     };
-    int j_next = (partials && row < k) ? __ldg(idx_row + row) : -1;
+    int j_next = row < k ? __ldg(idx_row + row) : -1;
     int64_t pos_next = j_next >= 0 ? slot_of(j_next) : 0;
-    for (int t = 0; partials && t < nt; ++t) {
+    for (int t = 0; t < nt; ++t) {
       // The drain reads 16 rows per TMEM load, each row's 64 columns split
       // over two threads (lane l and l + 16), so one store instruction covers
       // 16 rows x 64 bytes instead of 32 rows x 32: half the cache lines per
