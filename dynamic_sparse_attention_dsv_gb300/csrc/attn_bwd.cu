@@ -1200,7 +1200,7 @@ __global__ void __launch_bounds__(256) k_csc_reduce(const CscParams csc, int S, 
   }
   // slots are summed one after the other in ascending order; the rows of the
   // next kBatch slots are loaded first so that more of them are in flight
-  constexpr int kBatch = 4;
+  constexpr int kBatch = 8;
   auto add_row = [&](const uint32_t (&xv)[E / 2], const uint32_t (&xk)[E / 2]) {
 #pragma unroll
     for (int e = 0; e < E / 2; ++e) {
@@ -1227,19 +1227,25 @@ __global__ void __launch_bounds__(256) k_csc_reduce(const CscParams csc, int S, 
       xk[0] = __ldg(reinterpret_cast<const uint32_t*>(pk));
     }
   };
+  auto batch = [&](auto n, int64_t s) {   // n slots from s: all loads, then the adds in order
+    constexpr int N = decltype(n)::value;
+    uint32_t xv[N][E / 2], xk[N][E / 2];
+#pragma unroll
+    for (int i = 0; i < N; ++i) load_row(s + i, xv[i], xk[i]);
+#pragma unroll
+    for (int i = 0; i < N; ++i) add_row(xv[i], xk[i]);
+  };
   int64_t s = a;
-  for (; s + kBatch <= b; s += kBatch) {
-    uint32_t xv[kBatch][E / 2], xk[kBatch][E / 2];
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) load_row(s + i, xv[i], xk[i]);
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) add_row(xv[i], xk[i]);
+  for (; s + kBatch <= b; s += kBatch) batch(std::integral_constant<int, kBatch>{}, s);
+  if (s + 4 <= b) {   // the ragged end: at most one batch of four, one of two and one slot
+    batch(std::integral_constant<int, 4>{}, s);
+    s += 4;
   }
-  for (; s < b; ++s) {
-    uint32_t xv[E / 2], xk[E / 2];
-    load_row(s, xv, xk);
-    add_row(xv, xk);
+  if (s + 2 <= b) {
+    batch(std::integral_constant<int, 2>{}, s);
+    s += 2;
   }
+  if (s < b) batch(std::integral_constant<int, 1>{}, s);
   if (last) {
     const int64_t orow = ((int64_t)tab.p[u] * S + j) * D + lane * E;
 #pragma unroll
