@@ -497,7 +497,7 @@ def main():
     # DRAM bytes (read + write) per head of the phase's kernels from one ncu
     # capture of this workload at 2 heads (the per-head work is independent,
     # so traffic scales with the head count); null for other workloads
-    dram_per_head = {"attn_bwd": (291237632 + 3414094000 + 3436762624 + 70169856) / 2,   # k_attn_bwd_q, k_csc_reduce
+    dram_per_head = {"attn_bwd": (288039424 + 3413913088 + 3436769792 + 69537280) / 2,   # k_attn_bwd_q, k_csc_reduce
                      "attn_fwd": (101451264 + 17213696) / 2}                                # k_attn_fwd
     traffic = None
     if dom in dram_per_head and (w.S, w.d, w.k, w.gt, w.gy, w.gx) == (65536, 128, 6554, 2, 8, 8):
