@@ -8,8 +8,6 @@ namespace dsv {
 // Tensor maps used by one attention launch (all over bf16 [P*S][d] tensors).
 struct AttnMaps {
   CUtensorMap q_cube;   // 4D [P*T][Y][X][d], box (64, gx, gy, gt): one query group
-  CUtensorMap k_rows;   // 2D [P*S][d], box (64, 1): row gather of selected keys
-  CUtensorMap v_rows;
   CUtensorMap k_tile;   // 2D [P*S][d], box (64, 128): contiguous key tiles (dense)
   CUtensorMap v_tile;
 };
@@ -50,8 +48,6 @@ inline bool make_attn_maps(AttnMaps* m, const void* Q, const void* K, const void
                            int P) {
   const uint64_t rows = (uint64_t)P * geo.S;
   return make_cube_map(&m->q_cube, Q, geo, d, P) &&
-         make_map_2d(&m->k_rows, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, rows, 64, 1) &&
-         make_map_2d(&m->v_rows, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, rows, 64, 1) &&
          make_map_2d(&m->k_tile, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, rows, 64, 128) &&
          make_map_2d(&m->v_tile, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, rows, 64, 128);
 }
