@@ -1097,27 +1097,62 @@ __global__ void __launch_bounds__(256) k_csc_build(const int32_t* __restrict__ i
   const int nw = tab.nwords[u], ng = tab.ng[u], k = tab.k[u];
   for (int i = tid; i < kCscStride * nw; i += 256) sb[i] = 0u;
   __syncthreads();
-  for (int gl = tid; gl < ng; gl += 256) {
-    const int32_t* row = idx + tab.off[u] + (int64_t)(tab.g0[u] + gl) * k;
-    int lo = 0, hi = k;                            // first position whose key is >= j0
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(row + mid) < j0) lo = mid + 1;
-      else hi = mid;
+  // Each thread takes kPair groups (gl and gl + 256) at once, so the steps of
+  // their binary searches (and of their scans) have two loads in flight.
+  constexpr int kPair = 2;
+  for (int gb = tid; gb < ng; gb += 256 * kPair) {
+    const int32_t* row[kPair];
+    int lo[kPair], hi[kPair];                      // first position whose key is >= j0
+#pragma unroll
+    for (int e = 0; e < kPair; ++e) {
+      const int gl = gb + e * 256;
+      row[e] = idx + tab.off[u] + (int64_t)(tab.g0[u] + min(gl, ng - 1)) * k;
+      lo[e] = 0;
+      hi[e] = gl < ng ? k : 0;
     }
-    const uint32_t bit = 1u << (gl & 31);
-    uint32_t* col = sb + (gl >> 5) * kCscStride;
-    for (int s = lo; s < k; s += 4) {
-      int key[4];
+    while (lo[0] < hi[0] || lo[1] < hi[1]) {
+      int mid[kPair], v[kPair];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) key[e] = s + e < k ? __ldg(row + s + e) : j1;
-      bool done = false;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (key[e] >= j0 && key[e] < j1) atomicOr(col + (key[e] - j0), bit);
-        done = done || key[e] >= j1;
+      for (int e = 0; e < kPair; ++e) {
+        mid[e] = (lo[e] + hi[e]) >> 1;
+        v[e] = lo[e] < hi[e] ? __ldg(row[e] + mid[e]) : 0;
       }
-      if (done) break;
+#pragma unroll
+      for (int e = 0; e < kPair; ++e)
+        if (lo[e] < hi[e]) {
+          if (v[e] < j0) lo[e] = mid[e] + 1;
+          else hi[e] = mid[e];
+        }
+    }
+    // scan from there to the first key >= j1, eight keys of each row per step
+    int s[kPair];
+    bool live[kPair];
+#pragma unroll
+    for (int e = 0; e < kPair; ++e) {
+      s[e] = lo[e];
+      live[e] = gb + e * 256 < ng;
+    }
+    while (live[0] || live[1]) {
+      int key[kPair][8];
+#pragma unroll
+      for (int e = 0; e < kPair; ++e)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) key[e][i] = live[e] && s[e] + i < k ? __ldg(row[e] + s[e] + i) : j1;
+#pragma unroll
+      for (int e = 0; e < kPair; ++e) {
+        if (!live[e]) continue;
+        const int gl = gb + e * 256;
+        const uint32_t bit = 1u << (gl & 31);
+        uint32_t* col = sb + (gl >> 5) * kCscStride;
+        bool done = s[e] + 8 >= k;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (key[e][i] >= j0 && key[e][i] < j1) atomicOr(col + (key[e][i] - j0), bit);
+          done = done || key[e][i] >= j1;
+        }
+        s[e] += 8;
+        live[e] = !done;
+      }
     }
   }
   __syncthreads();
