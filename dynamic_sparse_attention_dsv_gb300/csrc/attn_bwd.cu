@@ -12,8 +12,8 @@
 //   S = Q K^T, dP = dO V^T                        tcgen05 (smem x smem) -> TMEM
 //   P = exp2(S*scale*log2e - LSE*log2e), dS' = scale P (dP - Delta)   registers
 //   dQ += dS' K                                   accumulated in TMEM, written once
-//   sparse problems only: dV_tile = P^T dO, dK_tile = dS'^T Q -> TMEM,
-//   written as bf16 partial rows, one per (group, selected key) pair.
+//   dV_tile = P^T dO, dK_tile = dS'^T Q -> TMEM, written as bf16 partial
+//   rows, one per (group, selected key) pair.
 // Ordered dK/dV reduction (no atomics on the data): a bitmap of which groups
 // selected each key gives every (key, group) pair a slot, off[key] + the
 // number of lower groups that selected the key (each 32-group bitmap word
@@ -97,8 +97,6 @@ struct BwdCfg {
 static_assert(BwdCfg<128>::kSmemUsed <= 232448, "group-major backward exceeds shared memory");
 static_assert(BwdCfg<128>::kColDK + 128 <= 512 && BwdCfg<64>::kColDK + 64 <= 512, "TMEM budget");
 
-__device__ __forceinline__ void compute_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
 // Writes 8 bf16 values (packed in 4 words) at 16-byte chunk `chunk` (0..15)
 // of row `row` of a [128][128] bf16 K-major tile with the 128-byte swizzle.
 __device__ __forceinline__ void st_sw128_chunk(uint8_t* tile, int row, int chunk, uint4 v) {
@@ -126,7 +124,7 @@ __device__ __forceinline__ void ds_chunk(uint8_t* sDS, int row, int c, const uin
 // ---------------------------------------------------------------------------
 // Group-major backward. Warps 0-3 turn S, dP into P, dS (shared memory);
 // warps 4-7 drain the dV/dK partial rows to their slots and write dQ at the
-// end; warps 8-10 load (cp.async row gather or TMA boxes); warp 11 issues
+// end; warps 8-10 gather the selected K/V rows (cp.async); warp 11 issues
 // the MMAs. Per 128-key tile t, in the order the MMAs are issued:
 //   dP(t) = dO V^T     once S(t) is in registers (same TMEM columns)
 //   dV(t) = P(t)^T dO  once P(t) is in shared memory and dV(t-1) drained
